@@ -1,0 +1,201 @@
+"""Pins of the oracle's attention skeleton, ExpCast step and repair step.
+
+* With the ExpCast byte replaced by an exact exp2 and no quantisation, the
+  online-softmax skeleton (mid-window traversal, lazy rescale, tail mask) must
+  reproduce brute-force softmax attention in double.
+* With ExpCast, every output row must lie within 2 * TV * max|v| of exact
+  attention on the same quantised inputs, TV being the 3.64 % bound the
+  VC-Attention summary proves ("ExpCast-FP8") plus the underflow tail.
+* The repair step must add exactly s_r * sum_t p_t dV_t / l over the selected
+  keys, leaving l and the reference unchanged ("Open VC Attention" catalogue
+  entry: prepare_v_repair / attention_v_repair).
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+GOLDEN = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "expcast_facts.json")))
+SM = 1.0 / math.sqrt(128.0)
+
+
+def _bits(t):
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _inputs(B, S, H, seed, bias=0.0, vdist="normal"):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((B, S, H, 128)) + bias * rng.standard_normal((1, 1, H, 128))
+    k = rng.standard_normal((B, S, H, 128)) + bias * rng.standard_normal((1, 1, H, 128))
+    v = rng.standard_t(3, (B, S, H, 128)) if vdist == "t3" else rng.standard_normal((B, S, H, 128))
+    return [torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16) for x in (q, k, v)]
+
+
+def _softmax_attention(q, k, v, sm=SM):
+    s = (q @ k.T) * sm
+    s -= s.max(axis=1, keepdims=True)
+    p = np.exp(s)
+    return (p @ v) / p.sum(axis=1, keepdims=True)
+
+
+@pytest.mark.parametrize("S", [1, 127, 128, 129, 300, 513])
+@pytest.mark.parametrize("mid,snap,tau", [(1, 1, 0.75), (0, 1, 0.75), (1, 0, 0.0), (1, 1, 50.0)])
+def test_exact_skeleton_equals_softmax_attention(S, mid, snap, tau):
+    rng = np.random.default_rng(S)
+    BH = 2
+    q = rng.standard_normal((BH, S, 128)) * 2
+    k = rng.standard_normal((BH, S, 128)) * 2
+    v = rng.standard_normal((BH, S, 128))
+    bh, s = np.meshgrid(np.arange(BH), np.arange(S), indexing="ij")
+    out, nres = oracle.attention_exact_rows(q, k, v, bh.ravel(), s.ravel(), tau=tau,
+                                            mid_window=mid, snap=snap)
+    for b in range(BH):
+        ref = _softmax_attention(q[b], k[b], v[b])
+        np.testing.assert_allclose(out[b * S:(b + 1) * S], ref, rtol=1e-10, atol=1e-12)
+    assert nres.min() >= 1
+    if tau == 50.0:
+        assert nres.max() == 1
+
+
+def test_rescale_count_with_zero_threshold_is_number_of_new_block_maxima():
+    rng = np.random.default_rng(21)
+    S = 1000
+    q = rng.standard_normal((1, S, 128))
+    k = rng.standard_normal((1, S, 128))
+    v = rng.standard_normal((1, S, 128))
+    rows = np.arange(0, S, 97)
+    _, nres = oracle.attention_exact_rows(q, k, v, np.zeros_like(rows), rows, tau=0.0,
+                                          mid_window=True, snap=False)
+    nb = (S + 127) // 128
+    order = [(nb // 2 + i) % nb for i in range(nb)]
+    for r, n in zip(rows, nres):
+        z = (k[0] @ q[0, r]) * SM
+        best, count = -np.inf, 0
+        for j in order:
+            bm = z[j * 128:(j + 1) * 128].max()
+            if bm > best:
+                best, count = bm, count + 1
+        assert n == count
+
+
+def _exact_on_quantised(prep, bh, s):
+    """Exact softmax attention of one row on the oracle's dequantised tensors."""
+    B, H = prep.B, prep.H
+    tab = oracle.e4m3_table()
+    S = prep.S
+    qc = prep.qc.reshape(B * H, -1, 128)[bh, s]
+    sq = prep.sq.reshape(B * H, -1)[bh, s // 128]
+    kc = prep.kc.reshape(B * H, -1, 128)[bh, :S]
+    sk = np.repeat(prep.sk.reshape(B * H, -1)[bh], 128)[:S]
+    vc = prep.vc.reshape(B * H, -1, 128)[bh, :S]
+    z = (tab[kc] @ tab[qc]) * sq * sk * SM * math.log2(math.e)    # log2 units
+    p = np.exp2(z - z.max())
+    vv = tab[vc] * prep.sv.reshape(-1)[bh]
+    return (p @ vv) / p.sum(), z, vv
+
+
+def test_expcast_rows_within_total_variation_bound():
+    q, k, v = _inputs(1, 700, 2, 31, bias=1.0, vdist="t3")
+    prep = oracle.Prepared(_bits(q), _bits(k), _bits(v))
+    rows_s = np.arange(0, 700, 23)
+    rows_bh = np.arange(rows_s.size) % 2
+    r = oracle.attention_rows(prep, rows_bh, rows_s)
+    tv = GOLDEN["tv_bound"]["value"]
+    for i, (bh, s) in enumerate(zip(rows_bh, rows_s)):
+        o_ref, z, vv = _exact_on_quantised(prep, bh, s)
+        Z = 8.0 * z
+        # mass whose stored value under the final reference falls below the
+        # normal range (an upper bound on the underflow/subnormal tail)
+        p = np.exp2((Z - Z.max()) / 8.0)
+        tail = p[(Z - r["m8"][i]) / 8.0 + 8.0 < -6.0].sum() / p.sum()
+        bound = 2.0 * (tv + tail) * np.abs(vv).max()
+        assert np.abs(r["out"][i] - o_ref).max() <= bound
+        assert abs((oracle.C0 + oracle.BETA - r["m8"][i]) - round(oracle.C0 + oracle.BETA - r["m8"][i])) < 1e-9
+
+
+def test_first_visited_block_is_the_middle_one():
+    q, k, v = _inputs(1, 1100, 1, 32)
+    prep = oracle.Prepared(_bits(q), _bits(k), _bits(v))
+    nb = prep.nb
+    rows = np.arange(0, 1100, 50)
+    r = oracle.attention_rows(prep, np.zeros_like(rows), rows, dump_block=nb // 2)
+    tab = oracle.e4m3_table()
+    for i, s in enumerate(rows):
+        j = nb // 2
+        kc = prep.kc[0, 0, j * 128:(j + 1) * 128]
+        z = (tab[kc] @ tab[prep.qc[0, 0, s]]) * prep.sq[0, 0, s // 128] * prep.sk[0, 0, j] * SM * math.log2(math.e)
+        bm = 8.0 * z.max()
+        frac = (oracle.C0 + oracle.BETA) % 1.0
+        assert r["dump_m8"][i] == pytest.approx(math.ceil(bm - frac) + frac, abs=1e-9)
+        assert np.array_equal(r["codes"][i], oracle.block_codes(prep, 0, s, j, r["dump_m8"][i]))
+
+
+def test_permuting_keys_within_blocks_leaves_output_unchanged():
+    q, k, v = _inputs(1, 300, 1, 33)
+    prep = oracle.Prepared(_bits(q), _bits(k), _bits(v))
+    rng = np.random.default_rng(34)
+    perm = np.concatenate([j * 128 + rng.permutation(min(128, 300 - j * 128)) for j in range(3)])
+    prep2 = oracle.Prepared(_bits(q), _bits(k[:, perm]), _bits(v[:, perm]))
+    rows = np.arange(0, 300, 7)
+    a = oracle.attention_rows(prep, np.zeros_like(rows), rows)
+    b = oracle.attention_rows(prep2, np.zeros_like(rows), rows)
+    np.testing.assert_allclose(a["out"], b["out"], rtol=1e-12, atol=1e-13)
+    assert np.array_equal(a["m8"], b["m8"]) and np.array_equal(a["nres"], b["nres"])
+
+
+def test_permuting_whole_sequence_changes_exact_result_not_at_all():
+    rng = np.random.default_rng(35)
+    S = 400
+    q, k, v = (rng.standard_normal((1, S, 128)) for _ in range(3))
+    perm = rng.permutation(S)
+    rows = np.arange(0, S, 11)
+    a, _ = oracle.attention_exact_rows(q, k, v, np.zeros_like(rows), rows)
+    b, _ = oracle.attention_exact_rows(q, k[:, perm], v[:, perm], np.zeros_like(rows), rows)
+    np.testing.assert_allclose(a, b, rtol=1e-11, atol=1e-13)
+
+
+@pytest.mark.parametrize("budget", [0.005, 0.05, 1.0])
+def test_repair_adds_residual_term_and_keeps_row_sum(budget):
+    q, k, v = _inputs(1, 600, 2, 36, bias=1.0, vdist="t3")
+    vb = v.clone()
+    vb[0, ::97, :, :8] *= 20
+    prep = oracle.Prepared(_bits(q), _bits(k), _bits(vb))
+    rep = oracle.Repair(prep, budget)
+    rows_s = np.arange(0, 600, 41)
+    rows_bh = np.arange(rows_s.size) % 2
+    plain = oracle.attention_rows(prep, rows_bh, rows_s)
+    fixed = oracle.attention_rows(prep, rows_bh, rows_s, repair=rep)
+    assert np.array_equal(plain["l"], fixed["l"]) and np.array_equal(plain["m8"], fixed["m8"])
+    assert fixed["nres"][:, 1].max() == 0
+    tab = oracle.e4m3_table()
+    for i, (bh, s) in enumerate(zip(rows_bh, rows_s)):
+        idx = rep.idx.reshape(2, -1)[bh]
+        extra = np.zeros(128)
+        for c, t in enumerate(idx):
+            codes = oracle.block_codes(prep, bh, s, t // 128, fixed["m8"][i])
+            extra += tab[codes[t % 128]] * tab[rep.dcodes.reshape(2, -1, 128)[bh, c]]
+        extra *= rep.sr.reshape(-1)[bh] / fixed["l"][i]
+        np.testing.assert_allclose(fixed["out"][i] - plain["out"][i], extra, rtol=1e-9, atol=1e-12)
+
+
+def test_repair_reduces_error_against_exact_attention():
+    q, k, v = _inputs(1, 1024, 2, 37, vdist="t3")
+    v[0, ::150, :, :8] *= 20
+    prep = oracle.Prepared(_bits(q), _bits(k), _bits(v))
+    rows_s = np.arange(0, 1024, 9)
+    rows_bh = np.arange(rows_s.size) % 2
+    qf, kf, vf = (x.to(torch.float64).numpy() for x in (q, k, v))
+    ref = np.stack([_softmax_attention(qf[0, :, bh], kf[0, :, bh], vf[0, :, bh])[s]
+                    for bh, s in zip(rows_bh, rows_s)])
+    errs = []
+    for budget in (None, 0.02, 1.0):
+        rep = None if budget is None else oracle.Repair(prep, budget)
+        out = oracle.attention_rows(prep, rows_bh, rows_s, repair=rep)["out"]
+        errs.append(np.linalg.norm(out - ref) / np.linalg.norm(ref))
+    assert errs[1] < errs[0] and errs[2] < errs[1]
+    assert 0.005 < errs[0] < 0.15

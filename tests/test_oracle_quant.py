@@ -1,0 +1,144 @@
+"""Pins of the oracle's FP32-defined quantisation and of the repair selection.
+
+The quantised codes are checked against torch's float8_e4m3fn cast of the
+FP32 product x * (448 / amax), the scales against numpy's amax, the residual
+energy against its defining sum in double, and the top-n selection against a
+brute-force sort.  ("Open VC Attention" catalogue entry: per-block Q/K scales,
+per-head V scale; prepare_v_repair(budget).)
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+
+def _bf16(x):
+    return torch.from_numpy(np.asarray(x, np.float32)).to(torch.bfloat16)
+
+
+def _bits(t):
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _cast(x32):
+    return torch.from_numpy(np.asarray(x32, np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def _f32(t):
+    return t.to(torch.float32).numpy()
+
+
+@pytest.mark.parametrize("S", [1, 127, 128, 129, 300])
+def test_quantize_blocks_scales_codes_and_tail(S):
+    rng = np.random.default_rng(S)
+    B, H = 2, 3
+    x = _bf16(rng.standard_normal((B, S, H, 128)) * 3 + rng.standard_normal((1, 1, H, 128)))
+    codes, scales = oracle.quantize_blocks(_bits(x))
+    nb = (S + 127) // 128
+    xf = _f32(x)
+    for b in range(B):
+        for h in range(H):
+            for j in range(nb):
+                blk = xf[b, j * 128:(j + 1) * 128, h, :]
+                amax = np.float32(np.abs(blk).max())
+                assert scales[b, h, j] == np.float32(amax / np.float32(448.0))
+                r = np.float32(448.0) / amax
+                want = _cast(blk * r)
+                got = codes[b, h, j * 128:j * 128 + blk.shape[0]]
+                assert np.array_equal(got, want)
+                assert not codes[b, h, j * 128 + blk.shape[0]:(j + 1) * 128].any()
+
+
+def test_quantize_blocks_zero_block_has_unit_scale():
+    x = torch.zeros((1, 256, 1, 128), dtype=torch.bfloat16)
+    x[0, 130, 0, 5] = 2.0
+    codes, scales = oracle.quantize_blocks(_bits(x))
+    assert scales[0, 0, 0] == 1.0 and not codes[0, 0, :128].any()
+    assert scales[0, 0, 1] == np.float32(2.0 / 448.0)
+    assert codes[0, 0, 130, 5] == 0x7E
+
+
+def test_quantize_v_per_head_scale_and_layout():
+    rng = np.random.default_rng(7)
+    B, S, H = 1, 200, 2
+    v = _bf16(rng.standard_t(3, (B, S, H, 128)))
+    codes, sv, energy = oracle.quantize_v(_bits(v))
+    vf = _f32(v)
+    for h in range(H):
+        amax = np.float32(np.abs(vf[0, :, h]).max())
+        assert sv[0, h] == np.float32(amax / np.float32(448.0))
+        assert np.array_equal(codes[0, h, :S], _cast(vf[0, :, h] * (np.float32(448.0) / amax)))
+        assert not codes[0, h, S:].any()
+
+
+def test_residual_energy_is_the_squared_residual_norm():
+    rng = np.random.default_rng(8)
+    B, S, H = 1, 64, 2
+    v = _bf16(rng.standard_normal((B, S, H, 128)))
+    codes, sv, energy = oracle.quantize_v(_bits(v))
+    vf = _f32(v).astype(np.float64)
+    dec = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    for h in range(H):
+        R = vf[0, :, h] - np.float64(sv[0, h]) * dec[0, h, :S]
+        e_ref = (R * R).sum(axis=1)
+        np.testing.assert_allclose(energy[0, h], e_ref, rtol=2e-5, atol=1e-30)
+
+
+def test_residual_energy_zero_for_representable_values():
+    # amax = 448 -> s_v = 1, and every value is an E4M3 (and BF16) value.
+    tab = oracle.e4m3_table()
+    vals = tab[np.r_[1:127, 129:255]]
+    rng = np.random.default_rng(9)
+    v = rng.choice(vals, (1, 40, 1, 128)).astype(np.float32)
+    v[0, 0, 0, 0] = 448.0
+    codes, sv, energy = oracle.quantize_v(_bits(_bf16(v)))
+    assert sv[0, 0] == 1.0
+    assert not energy.any()
+
+
+def test_residual_energy_order_and_nonnegativity():
+    rng = np.random.default_rng(10)
+    R = (rng.standard_normal(128) * 10.0 ** rng.uniform(-3, 3, 128)).astype(np.float32)
+    e = oracle.residual_energy(R)
+    assert e >= 0
+    assert e == pytest.approx(float((R.astype(np.float64) ** 2).sum()), rel=1e-5)
+    assert oracle.residual_energy(np.zeros(128, np.float32)) == 0.0
+
+
+@pytest.mark.parametrize("S,budget,n", [(73397, 0.005, 367), (73397, 0.01, 734),
+                                        (73397, 0.02, 1468), (1000, 0.0001, 1), (10, 1.0, 10)])
+def test_repair_count_is_ceil_budget_times_s(S, budget, n):
+    assert oracle.repair_count(S, budget) == n
+
+
+def test_repair_select_matches_brute_force_with_ties():
+    rng = np.random.default_rng(11)
+    B, H, S = 2, 3, 500
+    e = rng.integers(0, 40, (B, H, S)).astype(np.float32)      # many ties
+    for n in (1, 7, 64, 500):
+        idx = oracle.repair_select(e, n)
+        for b in range(B):
+            for h in range(H):
+                order = np.lexsort((np.arange(S), -e[b, h].astype(np.float64)))
+                assert np.array_equal(idx[b, h], np.sort(order[:n]))
+
+
+def test_repair_quantize_scale_and_codes():
+    rng = np.random.default_rng(12)
+    B, S, H = 1, 300, 2
+    v = _bf16(rng.standard_normal((B, S, H, 128)))
+    vc, sv, energy = oracle.quantize_v(_bits(v))
+    n = oracle.repair_count(S, 0.05)
+    idx = oracle.repair_select(energy, n)
+    dcodes, sr = oracle.repair_quantize(_bits(v), vc, sv, idx)
+    vf = _f32(v)
+    dec = torch.from_numpy(vc).view(torch.float8_e4m3fn).to(torch.float32).numpy()
+    for h in range(H):
+        t = idx[0, h]
+        R = vf[0, t, h] - (sv[0, h] * dec[0, h, t]).astype(np.float32)
+        amax = np.float32(np.abs(R).max())
+        assert sr[0, h] == np.float32(amax / np.float32(448.0))
+        assert np.array_equal(dcodes[0, h], _cast(R * (np.float32(448.0) / amax)))
+        # the selected tokens carry the largest energies
+        assert energy[0, h, t].min() >= np.delete(energy[0, h], t).max()
