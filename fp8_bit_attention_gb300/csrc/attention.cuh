@@ -1,0 +1,476 @@
+// attention.cuh -- ExpCast FP8 attention forward for sm_103a.
+//
+// Method ("Open-VC attention" news item, "Solution: ExpCast" and
+// "Architectural optimisations"; "Open VC Attention" catalogue entry;
+// VC-Attention summary, "ExpCast-FP8"):
+//   S = Q^ K^T on E4M3 tensor cores; online softmax with a running reference
+//   m8 (1/8-log2 units) and row sum l; the probabilities are written as E4M3
+//   bytes by one FMA on the log2-domain score,
+//       code = clamp(rint(Z - m8 + c0 + beta), 0, 126),  Z = 8 log2(e) sm sq sk S,
+//   with no exponent instruction and no FP32->FP8 conversion; O += P V^ on
+//   E4M3 tensor cores; key blocks are visited cyclically from the middle one.
+//
+// Kernel design (one CTA per SM, persistent over tiles):
+//   * a tile is two 128-row query blocks of one head (Q0, Q1);
+//   * warp 8 (one lane) streams Q tiles and K/V^T blocks with TMA into a
+//     kStages-deep ring of 128x128-byte tiles (128-byte swizzle);
+//   * warp 9 (one lane) issues tcgen05.mma: S_t = Q_t K_j^T into TMEM
+//     (kind::f8f6f4, M = N = 128, K = 32 per instruction), then
+//     O_t += P_t V_j^T with P_t read from TMEM (it overwrites S_t's first 32
+//     columns);
+//   * warps 0-3 and 4-7 are the softmax/ExpCast groups of Q0 and Q1: one
+//     thread per query row reads its 128 scores with tcgen05.ld, takes the
+//     block max, applies the lazy rescale, computes the 128 codes with one FMA
+//     each (the FMA adds 1.5*2^23 so that its rounding yields the integer
+//     code), clamps at 0, packs bytes, writes them back with tcgen05.st and
+//     adds the decoded bytes to l;
+//   * TMEM: S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512) columns.
+// Every mbarrier wait is bounded (wall-clock limit); on expiry the CTA
+// records a timeout, drains its own async copies and MMAs, frees TMEM and
+// exits.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace ovc {
+
+constexpr int kStages = 5;
+constexpr int kAttnThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr uint32_t kTile = 128 * 128;                       // bytes of one E4M3 tile
+constexpr uint32_t kIdesc = idesc_e4m3_f32(128, 128);
+constexpr float kMagic = 12582912.0f;                       // 1.5 * 2^23
+// ExpCast constants: c0 = 120 (stored value 2^8 p), beta = -0.35, tau = 0.75.
+constexpr float kCodeBase = 119.0f;                         // floor(c0 + beta)
+constexpr float kFrac = 0.65f;                              // frac(c0 + beta)
+constexpr float kLazy = 6.0f;                               // 8 * tau
+constexpr uint64_t kDrainNs = 4000000000ull;
+
+// Status bits recorded by kernels.
+constexpr unsigned kStatusTimeout = 1u;
+
+struct AttnParams {
+  int32_t B, S, H, nb, S_pad, npairs, ntiles;
+  const float* sq;
+  const float* sk;
+  const float* sv;
+  uint16_t* o;
+  int64_t os[3];          // output element strides (b, s, h)
+  float c8;               // 8 * log2(e) * softmax_scale
+  // repair set (rep_blocks == 0: none)
+  int32_t n_rep, n_rep_pad, rep_blocks;
+  const float* sk_sel;
+  const float* sr;
+  // probe
+  int64_t dump_bh, dump_qb, dump_kb;
+  uint8_t* dump_codes;
+  float* dump_m8;
+  uint64_t timeout_ns;
+  int32_t skip_mma;
+  unsigned int* status;
+};
+
+struct AttnSmem {
+  uint8_t q[2][kTile];
+  uint8_t k[kStages][kTile];
+  uint8_t v[kStages][kTile];
+  uint64_t q_full, q_empty;
+  uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
+  uint64_t s_full[2], p_full[2], o_full[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+constexpr size_t kAttnSmemBytes = sizeof(AttnSmem) + 1024;  // + alignment slack
+
+__device__ __forceinline__ void record_abort(AttnSmem& sm, const AttnParams& P) {
+  if (!*reinterpret_cast<volatile int*>(&sm.abort)) atomicOr(P.status, kStatusTimeout);
+  *reinterpret_cast<volatile int*>(&sm.abort) = 1;
+}
+
+struct TileCoord {
+  int bh, qb0, qb1, has1;
+};
+
+__device__ __forceinline__ TileCoord tile_coord(const AttnParams& P, int tile) {
+  TileCoord c;
+  c.bh = tile / P.npairs;
+  const int pair = tile - c.bh * P.npairs;
+  c.qb0 = 2 * pair;
+  c.has1 = (2 * pair + 1 < P.nb);
+  c.qb1 = c.has1 ? 2 * pair + 1 : c.qb0;
+  return c;
+}
+
+// Key block visited at step i: cyclic from the middle block.
+__device__ __forceinline__ int key_block(int i, int nb) {
+  const int j = nb / 2 + i;
+  return j >= nb ? j - nb : j;
+}
+
+// ---------------------------------------------------------------------------
+// The ExpCast step for one row and one block of 128 scores.
+//   s[c]  raw FP32 accumulator bits (masked columns already -inf)
+//   a     per-block multiplier (8 log2e sm sq sk)
+//   cterm (c0 + beta - m8) + 1.5*2^23, an exactly representable integer + magic
+// Produces 32 packed words of codes (bytes in key order) and returns the sum
+// of the decoded codes (accumulated as f16x2 pairs per block).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float expcast_block(const uint32_t* s, float a, float cterm, uint32_t* w) {
+  uint32_t acc[16];
+#pragma unroll
+  for (int g = 0; g < 32; ++g) {
+    const float u0 = fmaxf(fmaf(__uint_as_float(s[4 * g + 0]), a, cterm), kMagic);
+    const float u1 = fmaxf(fmaf(__uint_as_float(s[4 * g + 1]), a, cterm), kMagic);
+    const float u2 = fmaxf(fmaf(__uint_as_float(s[4 * g + 2]), a, cterm), kMagic);
+    const float u3 = fmaxf(fmaf(__uint_as_float(s[4 * g + 3]), a, cterm), kMagic);
+    const uint32_t t01 = __byte_perm(__float_as_uint(u0), __float_as_uint(u1), 0x0040);
+    const uint32_t t23 = __byte_perm(__float_as_uint(u2), __float_as_uint(u3), 0x0040);
+    w[g] = __byte_perm(t01, t23, 0x5410);
+    uint32_t h0, h1;
+    cvt_e4m3x4_to_f16x2x2(w[g], h0, h1);
+    const uint32_t h = hadd2(h0, h1);
+    if (g < 16) acc[g] = h;
+    else acc[g - 16] = hadd2(acc[g - 16], h);
+  }
+#pragma unroll
+  for (int width = 8; width >= 1; width >>= 1)
+#pragma unroll
+    for (int g = 0; g < width; ++g) acc[g] = hadd2(acc[g], acc[g + width]);
+  return f16x2_sum_to_f32(acc[0]);
+}
+
+// Same, with one multiplier per column (repair blocks: each selected key
+// keeps the scale of the block it came from) and no row sum.
+__device__ __forceinline__ void expcast_block_cols(const uint32_t* s, const float4* ksel, float c8sq,
+                                                   float cterm, uint32_t* w) {
+#pragma unroll
+  for (int g = 0; g < 32; ++g) {
+    const float4 k4 = __ldg(ksel + g);
+    const float u0 = fmaxf(fmaf(__uint_as_float(s[4 * g + 0]), c8sq * k4.x, cterm), kMagic);
+    const float u1 = fmaxf(fmaf(__uint_as_float(s[4 * g + 1]), c8sq * k4.y, cterm), kMagic);
+    const float u2 = fmaxf(fmaf(__uint_as_float(s[4 * g + 2]), c8sq * k4.z, cterm), kMagic);
+    const float u3 = fmaxf(fmaf(__uint_as_float(s[4 * g + 3]), c8sq * k4.w, cterm), kMagic);
+    const uint32_t t01 = __byte_perm(__float_as_uint(u0), __float_as_uint(u1), 0x0040);
+    const uint32_t t23 = __byte_perm(__float_as_uint(u2), __float_as_uint(u3), 0x0040);
+    w[g] = __byte_perm(t01, t23, 0x5410);
+  }
+}
+
+__device__ __forceinline__ void tmem_load_row128(uint32_t taddr, uint32_t* s) {
+  tmem_ld32(taddr + 0, s);
+  tmem_ld32(taddr + 32, s + 32);
+  tmem_ld32(taddr + 64, s + 64);
+  tmem_ld32(taddr + 96, s + 96);
+  tmem_wait_ld32(s);
+  tmem_wait_ld32(s + 32);
+  tmem_wait_ld32(s + 64);
+  tmem_wait_ld32(s + 96);
+}
+
+// O row *= f in tensor memory (one 128-column row per thread).
+__device__ __forceinline__ void tmem_scale_row128(uint32_t taddr, float f) {
+#pragma unroll 1
+  for (int c = 0; c < 128; c += 32) {
+    uint32_t r[32];
+    tmem_ld32(taddr + c, r);
+    tmem_wait_ld32(r);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * f);
+    tmem_st32(taddr + c, r);
+  }
+  tmem_wait_st();
+}
+
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_ks,
+                     const __grid_constant__ CUtensorMap tm_dv, const __grid_constant__ AttnParams P) {
+  extern __shared__ uint8_t smem_raw[];
+  AttnSmem& sm = *reinterpret_cast<AttnSmem*>(
+      smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const volatile int* abort_flag = &sm.abort;
+  const int nblk = P.nb + P.rep_blocks;
+  const uint64_t tmo = P.timeout_ns;
+
+  if (warp == kProducerWarp && lane == 0) {
+    mbar_init(smem_addr(&sm.q_full), 1);
+    mbar_init(smem_addr(&sm.q_empty), 1);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(smem_addr(&sm.k_full[i]), 1);
+      mbar_init(smem_addr(&sm.v_full[i]), 1);
+      mbar_init(smem_addr(&sm.kv_empty[i]), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(smem_addr(&sm.s_full[t]), 1);
+      mbar_init(smem_addr(&sm.p_full[t]), 128);
+      mbar_init(smem_addr(&sm.o_full[t]), 1);
+    }
+    mbar_init(smem_addr(&sm.drain), 1);
+    sm.abort = 0;
+    fence_mbar_init();
+    tma_prefetch_map(&tm_q);
+    tma_prefetch_map(&tm_k);
+    tma_prefetch_map(&tm_v);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_addr(&sm.tmem_base), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------------ TMA
+    if (lane == 0) {
+      uint32_t kv_iter = 0, q_iter = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < P.ntiles && ok; tile += gridDim.x) {
+        const TileCoord tc = tile_coord(P, tile);
+        if (q_iter > 0) ok = mbar_wait(smem_addr(&sm.q_empty), (q_iter - 1) & 1, tmo, abort_flag);
+        if (!ok) break;
+        const uint32_t qbar = smem_addr(&sm.q_full);
+        mbar_arrive_expect_tx(qbar, 2 * kTile);
+        tma_load_2d(smem_addr(sm.q[0]), &tm_q, qbar, 0, tc.bh * P.S_pad + tc.qb0 * 128);
+        tma_load_2d(smem_addr(sm.q[1]), &tm_q, qbar, 0, tc.bh * P.S_pad + tc.qb1 * 128);
+        ++q_iter;
+        for (int i = 0; i < nblk; ++i) {
+          const uint32_t stage = kv_iter % kStages, round = kv_iter / kStages;
+          if (kv_iter >= kStages) {
+            ok = mbar_wait(smem_addr(&sm.kv_empty[stage]), (round - 1) & 1, tmo, abort_flag);
+            if (!ok) break;
+          }
+          const uint32_t kbar = smem_addr(&sm.k_full[stage]), vbar = smem_addr(&sm.v_full[stage]);
+          mbar_arrive_expect_tx(kbar, kTile);
+          mbar_arrive_expect_tx(vbar, kTile);
+          if (i < P.nb) {
+            const int j = key_block(i, P.nb);
+            tma_load_2d(smem_addr(sm.k[stage]), &tm_k, kbar, 0, tc.bh * P.S_pad + j * 128);
+            tma_load_2d(smem_addr(sm.v[stage]), &tm_v, vbar, j * 128, tc.bh * 128);
+          } else {
+            const int r = i - P.nb;
+            tma_load_2d(smem_addr(sm.k[stage]), &tm_ks, kbar, 0, tc.bh * P.n_rep_pad + r * 128);
+            tma_load_2d(smem_addr(sm.v[stage]), &tm_dv, vbar, r * 128, tc.bh * 128);
+          }
+          ++kv_iter;
+        }
+      }
+      if (!ok) {
+        record_abort(sm, P);
+        // Drain: wait for the copies already issued (they always complete).
+        const volatile int never = 0;
+        for (uint32_t n = (kv_iter > kStages ? kv_iter - kStages : 0); n < kv_iter; ++n) {
+          const uint32_t stage = n % kStages, par = (n / kStages) & 1;
+          mbar_wait(smem_addr(&sm.k_full[stage]), par, kDrainNs, &never);
+          mbar_wait(smem_addr(&sm.v_full[stage]), par, kDrainNs, &never);
+        }
+        if (q_iter > 0) mbar_wait(smem_addr(&sm.q_full), (q_iter - 1) & 1, kDrainNs, &never);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------------ MMA
+    if (lane == 0 && !P.skip_mma) {
+      uint32_t kv_iter = 0, q_iter = 0, sp0 = 0, sp1 = 0;
+      bool ok = true, issued = false;
+      const uint32_t tS0 = tmem + 0, tS1 = tmem + 128;
+      const uint32_t tO0 = tmem + 256, tO1 = tmem + 384;
+      const uint64_t qd0 = sw128_desc(smem_addr(sm.q[0])), qd1 = sw128_desc(smem_addr(sm.q[1]));
+      for (int tile = blockIdx.x; tile < P.ntiles && ok; tile += gridDim.x) {
+        ok = mbar_wait(smem_addr(&sm.q_full), q_iter & 1, tmo, abort_flag);
+        if (!ok) break;
+        // Scores of the first block for both query tiles.
+        {
+          const uint32_t stage = kv_iter % kStages;
+          ok = mbar_wait(smem_addr(&sm.k_full[stage]), (kv_iter / kStages) & 1, tmo, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t kd = sw128_desc(smem_addr(sm.k[stage]));
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) mma_f8_ss(tS0, qd0 + 2 * kk, kd + 2 * kk, kIdesc, kk > 0);
+          tc_commit(smem_addr(&sm.s_full[0]));
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) mma_f8_ss(tS1, qd1 + 2 * kk, kd + 2 * kk, kIdesc, kk > 0);
+          tc_commit(smem_addr(&sm.s_full[1]));
+          issued = true;
+        }
+        for (int i = 0; i < nblk; ++i) {
+          const uint32_t stage = kv_iter % kStages;
+          ok = mbar_wait(smem_addr(&sm.v_full[stage]), (kv_iter / kStages) & 1, tmo, abort_flag);
+          if (!ok) break;
+          const uint64_t vd = sw128_desc(smem_addr(sm.v[stage]));
+          const bool last = (i + 1 == nblk);
+          const uint32_t nstage = (kv_iter + 1) % kStages;
+          // ---- query tile 0: O0 += P0 V, then the next block's S0
+          ok = mbar_wait(smem_addr(&sm.p_full[0]), sp0, tmo, abort_flag);
+          if (!ok) break;
+          sp0 ^= 1;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_f8_ts(tO0, tS0 + 8 * kk, vd + 2 * kk, kIdesc, (i > 0 || kk > 0) ? 1u : 0u);
+          uint64_t kd_next = 0;
+          if (!last) {
+            ok = mbar_wait(smem_addr(&sm.k_full[nstage]), ((kv_iter + 1) / kStages) & 1, tmo, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            kd_next = sw128_desc(smem_addr(sm.k[nstage]));
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) mma_f8_ss(tS0, qd0 + 2 * kk, kd_next + 2 * kk, kIdesc, kk > 0);
+            tc_commit(smem_addr(&sm.s_full[0]));
+          } else {
+            tc_commit(smem_addr(&sm.o_full[0]));
+          }
+          // ---- query tile 1
+          ok = mbar_wait(smem_addr(&sm.p_full[1]), sp1, tmo, abort_flag);
+          if (!ok) break;
+          sp1 ^= 1;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_f8_ts(tO1, tS1 + 8 * kk, vd + 2 * kk, kIdesc, (i > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(smem_addr(&sm.kv_empty[stage]));
+          if (!last) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) mma_f8_ss(tS1, qd1 + 2 * kk, kd_next + 2 * kk, kIdesc, kk > 0);
+            tc_commit(smem_addr(&sm.s_full[1]));
+          } else {
+            tc_commit(smem_addr(&sm.o_full[1]));
+            tc_commit(smem_addr(&sm.q_empty));
+          }
+          ++kv_iter;
+        }
+        ++q_iter;
+      }
+      if (!ok) record_abort(sm, P);
+      if (issued) {
+        // Every MMA issued so far has completed once this barrier flips.
+        const volatile int never = 0;
+        tc_commit(smem_addr(&sm.drain));
+        mbar_wait(smem_addr(&sm.drain), 0, kDrainNs, &never);
+      }
+    }
+  } else {
+    // ------------------------------------------------------- softmax/ExpCast
+    const int t = warp >> 2;                    // query tile 0 or 1
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_off + t * 128;
+    const uint32_t tO = tmem + lane_off + 256 + t * 128;
+    uint32_t blk_count = 0, tile_count = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < P.ntiles && ok; tile += gridDim.x) {
+      const TileCoord tc = tile_coord(P, tile);
+      const int qb = t ? tc.qb1 : tc.qb0;
+      const bool store = (t == 0) || tc.has1;
+      const float sq = P.sq[tc.bh * P.nb + qb];
+      const float c8sq = P.c8 * sq;
+      float kf = -INFINITY;                     // reference m8 = kf + frac(c0+beta)
+      float l = 0.0f;
+      const bool dump_tile = (P.dump_codes != nullptr) && tc.bh == P.dump_bh && qb == P.dump_qb && store;
+      for (int i = 0; i < nblk; ++i) {
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&sm.s_full[t]), blk_count & 1, tmo, abort_flag));
+        ++blk_count;
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t s[128];
+        uint32_t w[32];
+        tmem_load_row128(tS, s);
+        if (i < P.nb) {
+          const int j = key_block(i, P.nb);
+          const int valid = P.S - j * 128;
+          if (valid < 128) {
+#pragma unroll
+            for (int c = 0; c < 128; ++c)
+              if (c >= valid) s[c] = 0xFF800000u;  // -inf: excluded from max, code 0
+          }
+          float mx = __uint_as_float(s[0]);
+#pragma unroll
+          for (int c = 1; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
+          const float a = c8sq * P.sk[tc.bh * P.nb + j];
+          const float bm8 = mx * a;
+          const bool need = bm8 > kf + (kFrac + kLazy);
+          if (__any_sync(0xFFFFFFFFu, need)) {
+            const float kn = need ? ceilf(bm8 - kFrac) : kf;
+            const float f = need ? exp2f((kf - kn) * 0.125f) : 1.0f;
+            l *= f;
+            if (i > 0) tmem_scale_row128(tO, f);
+            kf = kn;
+          }
+          const float cterm = (kCodeBase - kf) + kMagic;
+          l += expcast_block(s, a, cterm, w);
+          if (dump_tile && j == P.dump_kb) {
+            uint4* d = reinterpret_cast<uint4*>(P.dump_codes + row * 128);
+#pragma unroll
+            for (int g = 0; g < 8; ++g) d[g] = make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
+            P.dump_m8[row] = kf + kFrac;
+          }
+        } else {
+          const int r = i - P.nb;
+          if (r == 0) tmem_scale_row128(tO, P.sv[tc.bh] / P.sr[tc.bh]);
+          const int valid = P.n_rep - r * 128;
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c >= valid) s[c] = 0xFF800000u;
+          const float4* ks = reinterpret_cast<const float4*>(
+              P.sk_sel + static_cast<int64_t>(tc.bh) * P.n_rep_pad + r * 128);
+          expcast_block_cols(s, ks, c8sq, (kCodeBase - kf) + kMagic, w);
+        }
+        tmem_st32(tS, w);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(smem_addr(&sm.p_full[t]));
+      }
+      if (!ok) break;
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&sm.o_full[t]), tile_count & 1, tmo, abort_flag));
+      ++tile_count;
+      if (!ok) break;
+      tc_fence_after();
+      // Epilogue: O = scale * O_acc / l, BF16, one 256-byte row per thread.
+      const float scale = (P.rep_blocks > 0 ? P.sr[tc.bh] : P.sv[tc.bh]) / l;
+      const int q_row = qb * 128 + row;
+      const int b = tc.bh / P.H, h = tc.bh - b * P.H;
+      uint16_t* orow = P.o + b * P.os[0] + static_cast<int64_t>(q_row) * P.os[1] + h * P.os[2];
+#pragma unroll 1
+      for (int c = 0; c < 128; c += 32) {
+        uint32_t r[32];
+        tmem_ld32(tO + c, r);
+        tmem_wait_ld32(r);
+        if (store && q_row < P.S) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            __nv_bfloat162 v2 = __floats2bfloat162_rn(__uint_as_float(r[2 * e]) * scale,
+                                                      __uint_as_float(r[2 * e + 1]) * scale);
+            pk[e] = *reinterpret_cast<uint32_t*>(&v2);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(orow + c);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+        }
+      }
+    }
+    if (!ok) record_abort(sm, P);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace ovc

@@ -1,0 +1,449 @@
+// ovc.cu -- libovc: the C ABI of ExpCast FP8 attention (see include/ovc.h).
+//
+// One translation unit: the kernels (prepare.cuh, attention.cuh, repair.cuh)
+// and the host entry points that validate arguments, carve caller workspace,
+// build TMA tensor maps and launch on the caller's stream.  Nothing here
+// allocates device memory.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "ovc.h"
+#include "attention.cuh"
+#include "prepare.cuh"
+#include "repair.cuh"
+
+namespace ovc {
+
+// Device-side status word: kernels OR in kStatusTimeout when a bounded wait
+// expires.  Read and cleared by ovc_get_device_status().
+__device__ unsigned int g_status;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kDefaultTimeoutNs = 4000000000ull;   // 4 s per wait
+
+struct DeviceState {
+  bool init = false;
+  bool supported = false;
+  int sms = 0;
+  unsigned int* status = nullptr;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+ovc_status device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return OVC_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& d = g_dev[dev];
+  if (!d.init) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return OVC_ERR_CUDA;
+    d.supported = (major == 10 && minor == 3);
+    d.sms = sms;
+    if (d.supported) {
+      if (cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(kAttnSmemBytes)) != cudaSuccess)
+        return OVC_ERR_CUDA;
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return OVC_ERR_CUDA;
+      d.status = static_cast<unsigned int*>(p);
+    }
+    d.init = true;
+  }
+  *out = &d;
+  return d.supported ? OVC_OK : OVC_ERR_UNSUPPORTED;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D byte tensor [rows][inner] (row pitch `pitch` bytes), 128x128 boxes,
+// 128-byte swizzle (the layout tcgen05 reads as K-major SW128).
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t pitch) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {pitch};
+  cuuint32_t box[2] = {128, 128};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool dims_ok(int64_t B, int64_t S, int64_t H) {
+  if (B < 1 || S < 1 || H < 1) return false;
+  const int64_t nb = (S + 127) / 128;
+  const int64_t BH = B * H;
+  if (BH > 65535 || nb > 65535) return false;               // grid limits
+  if (BH * nb * 128 > (int64_t{1} << 31) - 1) return false;  // 32-bit TMA row coordinates
+  return true;
+}
+
+struct PrepLayout {
+  size_t q, k, vt, sq, sk, sv, vamax, energy, total;
+};
+
+PrepLayout prep_layout(int64_t B, int64_t S, int64_t H) {
+  const int64_t nb = (S + 127) / 128, S_pad = nb * 128, BH = B * H;
+  PrepLayout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes, 256);
+    return at;
+  };
+  L.q = take(static_cast<size_t>(BH) * S_pad * 128);
+  L.k = take(static_cast<size_t>(BH) * S_pad * 128);
+  L.vt = take(static_cast<size_t>(BH) * S_pad * 128);
+  L.sq = take(static_cast<size_t>(BH) * nb * 4);
+  L.sk = take(static_cast<size_t>(BH) * nb * 4);
+  L.sv = take(static_cast<size_t>(BH) * 4);
+  L.vamax = take(static_cast<size_t>(BH) * 4);
+  L.energy = take(static_cast<size_t>(BH) * S * 4);
+  L.total = off;
+  return L;
+}
+
+int64_t repair_n(int64_t S, float budget) {
+  const double n = std::ceil(static_cast<double>(budget) * static_cast<double>(S));
+  int64_t k = static_cast<int64_t>(n);
+  if (k < 1) k = 1;
+  if (k > S) k = S;
+  return k;
+}
+
+struct RepLayout {
+  size_t idx, k_sel, dvt, sk_sel, sr, total;
+};
+
+RepLayout rep_layout(int64_t B, int64_t H, int64_t n) {
+  const int64_t n_pad = (n + 127) / 128 * 128, BH = B * H;
+  RepLayout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes, 256);
+    return at;
+  };
+  L.idx = take(static_cast<size_t>(BH) * n * 4);
+  L.k_sel = take(static_cast<size_t>(BH) * n_pad * 128);
+  L.dvt = take(static_cast<size_t>(BH) * n_pad * 128);
+  L.sk_sel = take(static_cast<size_t>(BH) * n_pad * 4);
+  L.sr = take(static_cast<size_t>(BH) * 4);
+  L.total = off;
+  return L;
+}
+
+bool tensor_ok(const ovc_tensor* t) {
+  if (!t || !t->ptr) return false;
+  if (t->dtype != OVC_BF16 && t->dtype != OVC_FP16) return false;
+  if (!aligned16(t->ptr)) return false;
+  if (t->stride_b % 8 || t->stride_s % 8 || t->stride_h % 8) return false;
+  if (t->stride_b < 0 || t->stride_s < 0 || t->stride_h < 0) return false;
+  return dims_ok(t->B, t->S, t->H);
+}
+
+bool prepared_ok(const ovc_prepared* p) {
+  if (!p || !p->q || !p->k || !p->vt || !p->sq || !p->sk || !p->sv || !p->vamax || !p->energy) return false;
+  if (!dims_ok(p->B, p->S, p->H)) return false;
+  return p->nb == (p->S + 127) / 128 && p->S_pad == p->nb * 128;
+}
+
+bool output_ok(const ovc_output* o) {
+  if (!o || !o->ptr || !aligned16(o->ptr)) return false;
+  if (o->stride_b % 8 || o->stride_s % 8 || o->stride_h % 8) return false;
+  return o->stride_b >= 0 && o->stride_s >= 0 && o->stride_h >= 0;
+}
+
+ovc_status launch_status() { return cudaGetLastError() == cudaSuccess ? OVC_OK : OVC_ERR_CUDA; }
+
+ovc_status run_attention(const ovc_prepared* p, const ovc_repair* r, float softmax_scale,
+                         const ovc_output* o, const ovc_probe* probe, void* stream) {
+  if (!prepared_ok(p) || !output_ok(o)) return OVC_ERR_INVALID_ARG;
+  if (r) {
+    if (!r->idx || !r->k_sel || !r->dvt || !r->sk_sel || !r->sr) return OVC_ERR_INVALID_ARG;
+    if (r->B != p->B || r->S != p->S || r->H != p->H) return OVC_ERR_INVALID_ARG;
+    if (r->n < 1 || r->n > p->S || r->n_pad != (r->n + 127) / 128 * 128) return OVC_ERR_INVALID_ARG;
+  }
+  if (probe && probe->dump_codes && !probe->dump_m8) return OVC_ERR_INVALID_ARG;
+  DeviceState* dev = nullptr;
+  ovc_status st = device_state(&dev);
+  if (st != OVC_OK) return st;
+
+  const int64_t BH = p->B * p->H;
+  CUtensorMap mq, mk, mv, mks, mdv;
+  if (!make_map(&mq, p->q, 128, BH * p->S_pad, 128) || !make_map(&mk, p->k, 128, BH * p->S_pad, 128) ||
+      !make_map(&mv, p->vt, p->S_pad, BH * 128, p->S_pad))
+    return OVC_ERR_CUDA;
+  if (r) {
+    if (!make_map(&mks, r->k_sel, 128, BH * r->n_pad, 128) || !make_map(&mdv, r->dvt, r->n_pad, BH * 128, r->n_pad))
+      return OVC_ERR_CUDA;
+  } else {
+    mks = mk;
+    mdv = mv;
+  }
+
+  AttnParams P{};
+  P.B = static_cast<int32_t>(p->B);
+  P.S = static_cast<int32_t>(p->S);
+  P.H = static_cast<int32_t>(p->H);
+  P.nb = static_cast<int32_t>(p->nb);
+  P.S_pad = static_cast<int32_t>(p->S_pad);
+  P.npairs = (P.nb + 1) / 2;
+  const int64_t ntiles = BH * P.npairs;
+  P.ntiles = static_cast<int32_t>(ntiles);
+  P.sq = p->sq;
+  P.sk = p->sk;
+  P.sv = p->sv;
+  P.o = static_cast<uint16_t*>(o->ptr);
+  P.os[0] = o->stride_b;
+  P.os[1] = o->stride_s;
+  P.os[2] = o->stride_h;
+  const double sm = softmax_scale > 0.0f ? static_cast<double>(softmax_scale) : 1.0 / std::sqrt(128.0);
+  P.c8 = static_cast<float>(8.0 * 1.4426950408889634074 * sm);
+  if (r) {
+    P.n_rep = static_cast<int32_t>(r->n);
+    P.n_rep_pad = static_cast<int32_t>(r->n_pad);
+    P.rep_blocks = static_cast<int32_t>(r->n_pad / 128);
+    P.sk_sel = r->sk_sel;
+    P.sr = r->sr;
+  }
+  P.dump_bh = -1;
+  P.timeout_ns = kDefaultTimeoutNs;
+  int force = 0;
+  if (probe) {
+    P.dump_bh = probe->dump_codes ? probe->dump_bh : -1;
+    P.dump_qb = probe->dump_qblock;
+    P.dump_kb = probe->dump_kblock;
+    P.dump_codes = probe->dump_codes;
+    P.dump_m8 = probe->dump_m8;
+    if (probe->wait_timeout_ns > 0) P.timeout_ns = probe->wait_timeout_ns;
+    P.skip_mma = probe->skip_mma;
+    force = probe->force_persistent;
+  }
+  P.status = dev->status;
+
+  // The packed long-sequence path (S >= 32768) is persistent: one CTA per SM
+  // looping over tiles.  Shorter sequences launch one CTA per tile.
+  const bool persistent = force > 0 || (force == 0 && p->S >= 32768);
+  const int64_t grid = persistent ? (ntiles < dev->sms ? ntiles : dev->sms) : ntiles;
+  attention_kernel<<<static_cast<unsigned>(grid), kAttnThreads, kAttnSmemBytes,
+                     static_cast<cudaStream_t>(stream)>>>(mq, mk, mv, mks, mdv, P);
+  return launch_status();
+}
+
+}  // namespace
+}  // namespace ovc
+
+using namespace ovc;
+
+extern "C" {
+
+size_t ovc_prepare_workspace_bytes(int64_t B, int64_t S, int64_t H, int64_t D) {
+  if (D != 128 || !dims_ok(B, S, H)) return 0;
+  return prep_layout(B, S, H).total;
+}
+
+ovc_status ovc_prepare(const ovc_tensor* q, const ovc_tensor* k, const ovc_tensor* v, void* workspace,
+                       size_t workspace_bytes, ovc_prepared* out, void* stream) {
+  if (!q || !k || !v || !out) return OVC_ERR_INVALID_ARG;
+  if (q->D != 128 || k->D != 128 || v->D != 128) return OVC_ERR_UNSUPPORTED;
+  if ((q->dtype != OVC_BF16 && q->dtype != OVC_FP16) || k->dtype != q->dtype || v->dtype != q->dtype)
+    return OVC_ERR_UNSUPPORTED;
+  if (!tensor_ok(q) || !tensor_ok(k) || !tensor_ok(v)) return OVC_ERR_INVALID_ARG;
+  if (k->B != q->B || k->S != q->S || k->H != q->H || v->B != q->B || v->S != q->S || v->H != q->H)
+    return OVC_ERR_INVALID_ARG;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return OVC_ERR_INVALID_ARG;
+  const PrepLayout L = prep_layout(q->B, q->S, q->H);
+  if (workspace_bytes < L.total) return OVC_ERR_WORKSPACE_TOO_SMALL;
+  DeviceState* dev = nullptr;
+  ovc_status st = device_state(&dev);
+  if (st != OVC_OK) return st;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  ovc_prepared p{};
+  p.B = q->B;
+  p.S = q->S;
+  p.H = q->H;
+  p.nb = (q->S + 127) / 128;
+  p.S_pad = p.nb * 128;
+  p.q = ws + L.q;
+  p.k = ws + L.k;
+  p.vt = ws + L.vt;
+  p.sq = reinterpret_cast<float*>(ws + L.sq);
+  p.sk = reinterpret_cast<float*>(ws + L.sk);
+  p.sv = reinterpret_cast<float*>(ws + L.sv);
+  p.vamax = reinterpret_cast<uint32_t*>(ws + L.vamax);
+  p.energy = reinterpret_cast<float*>(ws + L.energy);
+
+  PrepParams P{};
+  P.q = static_cast<const uint16_t*>(q->ptr);
+  P.k = static_cast<const uint16_t*>(k->ptr);
+  P.v = static_cast<const uint16_t*>(v->ptr);
+  const ovc_tensor* ts[3] = {q, k, v};
+  int64_t* ss[3] = {P.qs, P.ks, P.vs};
+  for (int i = 0; i < 3; ++i) {
+    ss[i][0] = ts[i]->stride_b;
+    ss[i][1] = ts[i]->stride_s;
+    ss[i][2] = ts[i]->stride_h;
+  }
+  P.B = static_cast<int32_t>(p.B);
+  P.S = static_cast<int32_t>(p.S);
+  P.H = static_cast<int32_t>(p.H);
+  P.nb = static_cast<int32_t>(p.nb);
+  P.S_pad = static_cast<int32_t>(p.S_pad);
+  P.fp16 = q->dtype == OVC_FP16;
+  P.qc = p.q;
+  P.kc = p.k;
+  P.vt = p.vt;
+  P.sq = p.sq;
+  P.sk = p.sk;
+  P.sv = p.sv;
+  P.vamax = p.vamax;
+  P.energy = p.energy;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(p.vamax, 0, static_cast<size_t>(p.B * p.H) * 4, s) != cudaSuccess) return OVC_ERR_CUDA;
+  const dim3 g1(static_cast<unsigned>(p.nb), static_cast<unsigned>(p.B * p.H), 3);
+  prepare_qk_kernel<<<g1, 256, 0, s>>>(P);
+  const dim3 g2(static_cast<unsigned>(p.nb), static_cast<unsigned>(p.B * p.H), 1);
+  prepare_v_kernel<<<g2, 512, 0, s>>>(P);
+  st = launch_status();
+  if (st == OVC_OK) *out = p;
+  return st;
+}
+
+ovc_status ovc_attention(const ovc_prepared* p, float softmax_scale, const ovc_output* o, void* stream) {
+  return run_attention(p, nullptr, softmax_scale, o, nullptr, stream);
+}
+
+size_t ovc_repair_workspace_bytes(int64_t B, int64_t S, int64_t H, float budget) {
+  if (!dims_ok(B, S, H) || !(budget > 0.0f) || budget > 1.0f) return 0;
+  return rep_layout(B, H, repair_n(S, budget)).total;
+}
+
+ovc_status ovc_prepare_v_repair(const ovc_tensor* v, const ovc_prepared* p, float budget, void* workspace,
+                                size_t workspace_bytes, ovc_repair* out, void* stream) {
+  if (!v || !p || !out) return OVC_ERR_INVALID_ARG;
+  if (v->D != 128) return OVC_ERR_UNSUPPORTED;
+  if (v->dtype != OVC_BF16 && v->dtype != OVC_FP16) return OVC_ERR_UNSUPPORTED;
+  if (!tensor_ok(v) || !prepared_ok(p)) return OVC_ERR_INVALID_ARG;
+  if (v->B != p->B || v->S != p->S || v->H != p->H) return OVC_ERR_INVALID_ARG;
+  if (!(budget > 0.0f) || budget > 1.0f) return OVC_ERR_INVALID_ARG;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return OVC_ERR_INVALID_ARG;
+  const int64_t n = repair_n(p->S, budget);
+  const RepLayout L = rep_layout(p->B, p->H, n);
+  if (workspace_bytes < L.total) return OVC_ERR_WORKSPACE_TOO_SMALL;
+  DeviceState* dev = nullptr;
+  ovc_status st = device_state(&dev);
+  if (st != OVC_OK) return st;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  ovc_repair r{};
+  r.B = p->B;
+  r.S = p->S;
+  r.H = p->H;
+  r.n = n;
+  r.n_pad = (n + 127) / 128 * 128;
+  r.idx = reinterpret_cast<int32_t*>(ws + L.idx);
+  r.k_sel = ws + L.k_sel;
+  r.dvt = ws + L.dvt;
+  r.sk_sel = reinterpret_cast<float*>(ws + L.sk_sel);
+  r.sr = reinterpret_cast<float*>(ws + L.sr);
+
+  RepairParams P{};
+  P.v = static_cast<const uint16_t*>(v->ptr);
+  P.vs[0] = v->stride_b;
+  P.vs[1] = v->stride_s;
+  P.vs[2] = v->stride_h;
+  P.B = static_cast<int32_t>(p->B);
+  P.S = static_cast<int32_t>(p->S);
+  P.H = static_cast<int32_t>(p->H);
+  P.nb = static_cast<int32_t>(p->nb);
+  P.S_pad = static_cast<int32_t>(p->S_pad);
+  P.fp16 = v->dtype == OVC_FP16;
+  P.kc = p->k;
+  P.sk = p->sk;
+  P.energy = p->energy;
+  P.vamax = p->vamax;
+  P.n = static_cast<int32_t>(r.n);
+  P.n_pad = static_cast<int32_t>(r.n_pad);
+  P.idx = r.idx;
+  P.k_sel = r.k_sel;
+  P.dvt = r.dvt;
+  P.sk_sel = r.sk_sel;
+  P.sr = r.sr;
+  repair_prepare_kernel<<<static_cast<unsigned>(p->B * p->H), kRepairThreads, 0,
+                          static_cast<cudaStream_t>(stream)>>>(P);
+  st = launch_status();
+  if (st == OVC_OK) *out = r;
+  return st;
+}
+
+ovc_status ovc_attention_v_repair(const ovc_prepared* p, const ovc_repair* r, float softmax_scale,
+                                  const ovc_output* o, void* stream) {
+  if (!r) return OVC_ERR_INVALID_ARG;
+  return run_attention(p, r, softmax_scale, o, nullptr, stream);
+}
+
+ovc_status ovc_attention_probe(const ovc_prepared* p, const ovc_repair* r, float softmax_scale,
+                               const ovc_output* o, const ovc_probe* probe, void* stream) {
+  return run_attention(p, r, softmax_scale, o, probe, stream);
+}
+
+ovc_status ovc_get_device_status(void* stream) {
+  DeviceState* dev = nullptr;
+  ovc_status st = device_state(&dev);
+  if (st != OVC_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return OVC_ERR_CUDA;
+  unsigned int word = 0;
+  if (cudaMemcpyFromSymbol(&word, g_status, sizeof(word)) != cudaSuccess) return OVC_ERR_CUDA;
+  if (word != 0) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(g_status, &zero, sizeof(zero)) != cudaSuccess) return OVC_ERR_CUDA;
+    return OVC_ERR_TIMEOUT;
+  }
+  return OVC_OK;
+}
+
+const char* ovc_status_string(ovc_status s) {
+  switch (s) {
+    case OVC_OK: return "ok";
+    case OVC_ERR_INVALID_ARG: return "invalid argument";
+    case OVC_ERR_UNSUPPORTED: return "unsupported (needs D = 128, BF16/FP16 inputs and an sm_103 GPU)";
+    case OVC_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case OVC_ERR_CUDA: return "CUDA runtime error";
+    case OVC_ERR_TIMEOUT: return "a device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

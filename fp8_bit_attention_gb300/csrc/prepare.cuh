@@ -1,0 +1,237 @@
+// prepare.cuh -- input preparation: BF16/FP16 Q, K, V -> E4M3 plus scales.
+//
+// "Open VC Attention" (catalogue entry): Q/K scales per block, V per head.
+// "Open-VC attention" (news item), "Architectural optimisations": the Q, K and
+// V quantisation is one fused preparation step.
+//
+// Quantisation is defined in FP32: s = amax/448, r = 448/amax (IEEE single
+// divisions; amax = 0 gives s = r = 1), code = E4M3_rn_satfinite(x * r).
+//
+// Two launches, both HBM-bound and coalesced:
+//   prepare_qk_kernel  grid (nb, B*H, 3): z = 0 quantises a 128-token block of
+//                      Q, z = 1 of K, z = 2 folds the block's amax|V| into the
+//                      head's running maximum.
+//   prepare_v_kernel   grid (nb, B*H): quantises a 128-token block of V with
+//                      the head scale, writes it transposed (keys contiguous)
+//                      and the per-token residual energy.
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace ovc {
+
+struct PrepParams {
+  const uint16_t* q;
+  const uint16_t* k;
+  const uint16_t* v;
+  int64_t qs[3], ks[3], vs[3];   // element strides (b, s, h)
+  int32_t B, S, H, nb, S_pad;
+  int32_t fp16;                  // 0: BF16 inputs, 1: FP16 inputs
+  uint8_t* qc;
+  uint8_t* kc;
+  uint8_t* vt;
+  float* sq;
+  float* sk;
+  float* sv;
+  uint32_t* vamax;
+  float* energy;
+};
+
+// |x| of two packed 16-bit floats, as ordered integers (sign bit cleared).
+__device__ __forceinline__ uint32_t abs2_bits(uint32_t w) { return w & 0x7FFF7FFFu; }
+
+__device__ __forceinline__ float half_bits_to_float(uint32_t bits16, int fp16) {
+  if (!fp16) return __uint_as_float(bits16 << 16);
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(bits16)));
+}
+
+__device__ __forceinline__ float2 unpack2(uint32_t w, int fp16) {
+  return make_float2(half_bits_to_float(w & 0xFFFFu, fp16), half_bits_to_float(w >> 16, fp16));
+}
+
+struct QScale {
+  float s, r;
+};
+
+__device__ __forceinline__ QScale scale_from_amax(float amax) {
+  if (amax == 0.0f) return {1.0f, 1.0f};
+  return {__fdiv_rn(amax, 448.0f), __fdiv_rn(448.0f, amax)};
+}
+
+// Four values -> four E4M3 bytes in one word (first value in bits 0..7).
+__device__ __forceinline__ uint32_t quant4(float a, float b, float c, float d, float r) {
+  const uint32_t lo = cvt_e4m3x2(__fmul_rn(a, r), __fmul_rn(b, r));
+  const uint32_t hi = cvt_e4m3x2(__fmul_rn(c, r), __fmul_rn(d, r));
+  return lo | (hi << 16);
+}
+
+// E4M3 bytes of a word -> four FP32 values (exact).
+__device__ __forceinline__ void dec4(uint32_t codes, float* out) {
+  uint32_t lo, hi;
+  cvt_e4m3x4_to_f16x2x2(codes, lo, hi);
+  const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+  const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+  out[0] = f0.x;
+  out[1] = f0.y;
+  out[2] = f1.x;
+  out[3] = f1.y;
+}
+
+// Maximum of a 32-bit value over the CTA (blockDim.x multiple of 32, <= 1024).
+__device__ __forceinline__ uint32_t block_max_u32(uint32_t m, uint32_t* red) {
+  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red[warp] = m;
+  __syncthreads();
+  if (warp == 0) {
+    m = (lane < static_cast<int>(blockDim.x >> 5)) ? red[lane] : 0u;
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if (lane == 0) red[0] = m;
+  }
+  __syncthreads();
+  const uint32_t r = red[0];
+  __syncthreads();
+  return r;
+}
+
+// One 128-token block of Q or K (z = 0, 1), or the amax of one block of V
+// (z = 2).  256 threads: two per token row, 64 channels each.
+__global__ void __launch_bounds__(256) prepare_qk_kernel(const __grid_constant__ PrepParams P) {
+  __shared__ uint32_t red[32];
+  const int j = blockIdx.x;
+  const int bh = blockIdx.y;
+  const int which = blockIdx.z;
+  const int b = bh / P.H, h = bh % P.H;
+  const int tid = threadIdx.x;
+  const int row = tid >> 1, half = tid & 1;
+  const int t = j * 128 + row;
+
+  const uint16_t* src = which == 0 ? P.q : (which == 1 ? P.k : P.v);
+  const int64_t* st = which == 0 ? P.qs : (which == 1 ? P.ks : P.vs);
+
+  uint4 x[8];
+  if (t < P.S) {
+    const uint4* p = reinterpret_cast<const uint4*>(src + b * st[0] + t * st[1] + h * st[2] + half * 64);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] = __ldg(p + i);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] = make_uint4(0, 0, 0, 0);
+  }
+
+  uint32_t m2 = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    m2 = __vmaxu2(m2, abs2_bits(x[i].x));
+    m2 = __vmaxu2(m2, abs2_bits(x[i].y));
+    m2 = __vmaxu2(m2, abs2_bits(x[i].z));
+    m2 = __vmaxu2(m2, abs2_bits(x[i].w));
+  }
+  const uint32_t mbits = block_max_u32(max(m2 & 0xFFFFu, m2 >> 16), red);
+  const float amax = half_bits_to_float(mbits, P.fp16);
+
+  if (which == 2) {
+    if (tid == 0) atomicMax(P.vamax + bh, __float_as_uint(amax));
+    return;
+  }
+
+  const QScale sc = scale_from_amax(amax);
+  if (tid == 0) (which == 0 ? P.sq : P.sk)[bh * P.nb + j] = sc.s;
+
+  uint32_t w[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float2 a = unpack2(x[i].x, P.fp16), b2 = unpack2(x[i].y, P.fp16);
+    const float2 c = unpack2(x[i].z, P.fp16), d = unpack2(x[i].w, P.fp16);
+    w[2 * i] = quant4(a.x, a.y, b2.x, b2.y, sc.r);
+    w[2 * i + 1] = quant4(c.x, c.y, d.x, d.y, sc.r);
+  }
+  uint8_t* dst = (which == 0 ? P.qc : P.kc) + (static_cast<int64_t>(bh) * P.S_pad + t) * 128 + half * 64;
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+}
+
+// One 128-token block of V.  512 threads: warp w owns channels 8w..8w+7,
+// lane l owns tokens 4l..4l+3 of the block.  Writes V^T (keys contiguous)
+// with coalesced 128-byte rows, and the residual energy of each token:
+// R = fl(v - fl(s_v * dec(code))), sixteen sequential partial sums over 8
+// channels, then the pairwise tree p_g += p_(g+w), w = 8, 4, 2, 1.
+__global__ void __launch_bounds__(512) prepare_v_kernel(const __grid_constant__ PrepParams P) {
+  __shared__ float part[16][128];
+  const int j = blockIdx.x;
+  const int bh = blockIdx.y;
+  const int b = bh / P.H, h = bh % P.H;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const float amax = __uint_as_float(P.vamax[bh]);
+  const QScale sc = scale_from_amax(amax);
+  if (j == 0 && threadIdx.x == 0) P.sv[bh] = sc.s;
+
+  uint32_t lo[4], hi[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int t = j * 128 + 4 * lane + k;
+    uint4 x = make_uint4(0, 0, 0, 0);
+    if (t < P.S)
+      x = __ldg(reinterpret_cast<const uint4*>(P.v + b * P.vs[0] + t * P.vs[1] + h * P.vs[2] + 8 * warp));
+    const float2 a = unpack2(x.x, P.fp16), c = unpack2(x.y, P.fp16);
+    const float2 d = unpack2(x.z, P.fp16), e = unpack2(x.w, P.fp16);
+    const float xv[8] = {a.x, a.y, c.x, c.y, d.x, d.y, e.x, e.y};
+    lo[k] = quant4(xv[0], xv[1], xv[2], xv[3], sc.r);
+    hi[k] = quant4(xv[4], xv[5], xv[6], xv[7], sc.r);
+    float dq[8];
+    dec4(lo[k], dq);
+    dec4(hi[k], dq + 4);
+    float acc = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float r = __fsub_rn(xv[i], __fmul_rn(sc.s, dq[i]));
+      const float sq = __fmul_rn(r, r);
+      acc = (i == 0) ? sq : __fadd_rn(acc, sq);
+    }
+    part[warp][k * 32 + lane] = acc;
+  }
+
+  // 4 tokens x 8 channels -> 8 words (one per channel) of 4 token bytes.
+  uint32_t out[8];
+  {
+    const uint32_t a01 = __byte_perm(lo[0], lo[1], 0x5140), a23 = __byte_perm(lo[2], lo[3], 0x5140);
+    const uint32_t b01 = __byte_perm(lo[0], lo[1], 0x7362), b23 = __byte_perm(lo[2], lo[3], 0x7362);
+    out[0] = __byte_perm(a01, a23, 0x5410);
+    out[1] = __byte_perm(a01, a23, 0x7632);
+    out[2] = __byte_perm(b01, b23, 0x5410);
+    out[3] = __byte_perm(b01, b23, 0x7632);
+    const uint32_t c01 = __byte_perm(hi[0], hi[1], 0x5140), c23 = __byte_perm(hi[2], hi[3], 0x5140);
+    const uint32_t d01 = __byte_perm(hi[0], hi[1], 0x7362), d23 = __byte_perm(hi[2], hi[3], 0x7362);
+    out[4] = __byte_perm(c01, c23, 0x5410);
+    out[5] = __byte_perm(c01, c23, 0x7632);
+    out[6] = __byte_perm(d01, d23, 0x5410);
+    out[7] = __byte_perm(d01, d23, 0x7632);
+  }
+  uint8_t* vt = P.vt + (static_cast<int64_t>(bh) * 128 + 8 * warp) * P.S_pad + j * 128 + 4 * lane;
+#pragma unroll
+  for (int d = 0; d < 8; ++d) *reinterpret_cast<uint32_t*>(vt + static_cast<int64_t>(d) * P.S_pad) = out[d];
+
+  __syncthreads();
+  if (threadIdx.x < 128) {
+    const int tok = threadIdx.x;
+    const int t = j * 128 + tok;
+    if (t < P.S) {
+      float p[16];
+#pragma unroll
+      for (int g = 0; g < 16; ++g) p[g] = part[g][(tok & 3) * 32 + (tok >> 2)];
+#pragma unroll
+      for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+        for (int g = 0; g < w; ++g) p[g] = __fadd_rn(p[g], p[g + w]);
+      P.energy[static_cast<int64_t>(bh) * P.S + t] = p[0];
+    }
+  }
+}
+
+}  // namespace ovc

@@ -1,0 +1,177 @@
+/*
+ * ovc.h -- C ABI of libovc: ExpCast FP8 attention for GB300 (sm_103a).
+ *
+ * Non-causal multi-head forward attention, head dim 128, long sequences, with
+ * Q/K/V quantised to FP8 E4M3 and the softmax probabilities written straight
+ * out as E4M3 bytes by one FMA on the log2-domain score ("ExpCast").
+ *
+ * What each call computes follows these pages (title, section):
+ *   "Open VC Attention" (catalogue entry): the API covers forward MHA with head
+ *     dim 128 on FP16/BF16 inputs shaped [S,H,128] or [B,S,H,128] and returns
+ *     BF16; per-block Q/K scales and per-head V scales; keys traversed from the
+ *     middle of the window; a packed fast path for non-causal S >= 32768;
+ *     V residual repair prepared with prepare_v_repair(budget) and applied by
+ *     attention_v_repair.
+ *   "Open-VC attention" (news item), "Solution: ExpCast": one FMA per score,
+ *     no MUFU exponent, no FP32->FP8 conversion; "Architectural
+ *     optimisations": mid-window traversal, warp-specialised pipeline, Q/K/V
+ *     quantisation fused into one preparation step.
+ *   VC-Attention summary, "ExpCast-FP8": an E4M3 byte read as an integer is
+ *     about 8*log2(v)+56; beta = -0.35.
+ *
+ * Conventions for every call:
+ *   - All pointers inside ovc_tensor / ovc_output / ovc_prepared / ovc_repair
+ *     are DEVICE pointers of the current CUDA device.  The caller owns every
+ *     buffer; the library never allocates or frees device memory.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
+ *     call is asynchronous on it; argument errors are returned synchronously
+ *     and nothing is launched.
+ *   - Input tensors must be 16-byte aligned with unit channel stride and
+ *     element strides that are multiples of 8.
+ *   - The library requires an sm_103 device (GB300); others get
+ *     OVC_ERR_UNSUPPORTED.
+ *   - Device-side waits are bounded: a kernel that waits too long records
+ *     OVC_ERR_TIMEOUT, which ovc_get_device_status() reports.
+ */
+#ifndef OVC_H_
+#define OVC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  OVC_OK = 0,
+  OVC_ERR_INVALID_ARG = 1,          /* null pointer, bad shape, stride or alignment */
+  OVC_ERR_UNSUPPORTED = 2,          /* D != 128, unknown dtype, device not sm_103 */
+  OVC_ERR_WORKSPACE_TOO_SMALL = 3,  /* workspace_bytes below the *_workspace_bytes() figure */
+  OVC_ERR_CUDA = 4,                 /* a CUDA runtime call failed */
+  OVC_ERR_TIMEOUT = 5               /* a device-side wait hit its limit */
+} ovc_status;
+
+enum { OVC_BF16 = 0, OVC_FP16 = 1 };
+
+/* A BF16/FP16 tensor [B,S,H,D] (use B = 1 for [S,H,D]); strides in elements,
+ * the channel stride is 1. */
+typedef struct {
+  const void* ptr;
+  int32_t dtype;                    /* OVC_BF16 or OVC_FP16 */
+  int64_t B, S, H, D;               /* D must be 128 */
+  int64_t stride_b, stride_s, stride_h;
+} ovc_tensor;
+
+/* The BF16 output O [B,S,H,128]; strides in elements, channel stride 1. */
+typedef struct {
+  void* ptr;
+  int64_t stride_b, stride_s, stride_h;
+} ovc_output;
+
+/* Quantised inputs written by ovc_prepare into caller workspace.  Layouts
+ * (nb = ceil(S/128), S_pad = 128*nb, E4M3 bytes, rows >= S are zero):
+ *   q, k  [B,H,S_pad,128]  head-major, 128-token blocks contiguous
+ *   vt    [B,H,128,S_pad]  V transposed: keys contiguous ("packed transposed V")
+ *   sq,sk [B,H,nb]         FP32 scale of each 128-token block, amax/448
+ *   sv    [B,H]            FP32 scale of each head of V, amax/448
+ *   vamax [B,H]            FP32 bits of each head's amax|V|
+ *   energy[B,H,S]          FP32 residual energy ||v_t - sv*dec(code_t)||^2 */
+typedef struct {
+  int64_t B, S, H, nb, S_pad;
+  uint8_t* q;
+  uint8_t* k;
+  uint8_t* vt;
+  float* sq;
+  float* sk;
+  float* sv;
+  uint32_t* vamax;
+  float* energy;
+} ovc_prepared;
+
+/* V residual repair set written by ovc_prepare_v_repair (n_pad = 128*ceil(n/128)):
+ *   idx    [B,H,n]         selected token indices, ascending
+ *   k_sel  [B,H,n_pad,128] their quantised keys (zero padded)
+ *   dvt    [B,H,128,n_pad] their quantised V residuals, transposed
+ *   sk_sel [B,H,n_pad]     the key scale of each selected token's block
+ *   sr     [B,H]           FP32 residual scale, amax|R_sel|/448 */
+typedef struct {
+  int64_t B, S, H, n, n_pad;
+  int32_t* idx;
+  uint8_t* k_sel;
+  uint8_t* dvt;
+  float* sk_sel;
+  float* sr;
+} ovc_repair;
+
+/* Bytes of workspace ovc_prepare needs for these dimensions (0 if invalid). */
+size_t ovc_prepare_workspace_bytes(int64_t B, int64_t S, int64_t H, int64_t D);
+
+/* Quantise Q, K (one scale per 128-token block) and V (one scale per head) to
+ * E4M3 and lay them out for the attention kernel; also computes the per-token
+ * V residual energy used by repair.  q, k, v must have identical shapes and
+ * dtypes.  `workspace` (>= ovc_prepare_workspace_bytes, 256-byte aligned)
+ * backs every buffer of *out; it must stay alive while *out is used.
+ * ("Open VC Attention": per-block Q/K and per-head V scales; "Open-VC
+ * attention", "Architectural optimisations": fused input preparation.) */
+ovc_status ovc_prepare(const ovc_tensor* q, const ovc_tensor* k, const ovc_tensor* v,
+                       void* workspace, size_t workspace_bytes, ovc_prepared* out, void* stream);
+
+/* O = softmax(Q K^T * softmax_scale) V with ExpCast probabilities, written as
+ * BF16 to *o.  softmax_scale <= 0 selects 1/sqrt(128).  Non-causal only.
+ * S >= 32768 runs the persistent (packed) schedule; shorter sequences run one
+ * CTA per pair of 128-row Q blocks.  Both give identical results. */
+ovc_status ovc_attention(const ovc_prepared* p, float softmax_scale, const ovc_output* o,
+                         void* stream);
+
+/* Bytes of workspace ovc_prepare_v_repair needs (0 if invalid).  budget in (0,1]. */
+size_t ovc_repair_workspace_bytes(int64_t B, int64_t S, int64_t H, float budget);
+
+/* Select, per head, the n = ceil(budget*S) V tokens with the largest residual
+ * energy (ties to the lower index), quantise their residuals with one scale
+ * per head and gather their keys.  `v` is the same tensor given to
+ * ovc_prepare for `p`.  ("Open VC Attention": prepare_v_repair with a budget
+ * such as 0.005; "MachGen opened the sources...", "What happened".) */
+ovc_status ovc_prepare_v_repair(const ovc_tensor* v, const ovc_prepared* p, float budget,
+                                void* workspace, size_t workspace_bytes, ovc_repair* out,
+                                void* stream);
+
+/* ovc_attention plus one more sparse P*dV term over the repair set: the
+ * selected keys are scored again with the row's final reference and their
+ * quantised residuals are accumulated into O; the row sum is unchanged. */
+ovc_status ovc_attention_v_repair(const ovc_prepared* p, const ovc_repair* r, float softmax_scale,
+                                  const ovc_output* o, void* stream);
+
+/* Synchronise `stream`, then report and clear the device-side status word:
+ * OVC_ERR_TIMEOUT if any kernel gave up on a wait since the last call. */
+ovc_status ovc_get_device_status(void* stream);
+
+/* A static English description of a status code. */
+const char* ovc_status_string(ovc_status s);
+
+/* Test hook (not part of the method): ovc_attention / ovc_attention_v_repair
+ * with extra controls.  For every row of 128-row query block `dump_qblock` of
+ * head `dump_bh` (= b*H + h), the P bytes written for key block `dump_kblock`
+ * go to dump_codes [128,128] (device, uint8) and the reference used for them
+ * (in 1/8-log2 units) to dump_m8 [128] (device, float).  wait_timeout_ns > 0
+ * overrides the device wait limit; skip_mma != 0 makes the MMA warp issue
+ * nothing so that every other wait runs into the limit (exercises the timeout
+ * path without faulting or hanging).  force_persistent: 1 = persistent
+ * schedule, -1 = one CTA per tile, 0 = automatic.  r may be NULL. */
+typedef struct {
+  int64_t dump_bh, dump_qblock, dump_kblock;
+  uint8_t* dump_codes;
+  float* dump_m8;
+  uint64_t wait_timeout_ns;
+  int32_t skip_mma;
+  int32_t force_persistent;
+} ovc_probe;
+
+ovc_status ovc_attention_probe(const ovc_prepared* p, const ovc_repair* r, float softmax_scale,
+                               const ovc_output* o, const ovc_probe* probe, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OVC_H_ */

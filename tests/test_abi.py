@@ -1,0 +1,103 @@
+"""CPU checks of the C ABI: the library loads, exports every function that
+include/ovc.h declares, sizes workspaces, and rejects bad arguments on the
+host before touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from fp8_bit_attention_gb300 import _abi, build
+    build.build()
+    return _abi.lib()
+
+
+def _declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names += re.findall(r"^\s*(?:size_t|ovc_status|const char\*)\s+(ovc_\w+)\s*\(", text, re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for required in ("ovc_prepare", "ovc_attention", "ovc_prepare_v_repair", "ovc_attention_v_repair"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from fp8_bit_attention_gb300 import _abi
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+        assert name in _abi.SIGNATURES, name
+
+
+def test_workspace_sizes(lib):
+    nb, S_pad = 574, 574 * 128
+    bh = 56
+    got = lib.ovc_prepare_workspace_bytes(1, 73397, 56, 128)
+    assert got >= 3 * bh * S_pad * 128 + 2 * bh * nb * 4 + bh * 73397 * 4
+    assert got % 256 == 0
+    assert lib.ovc_prepare_workspace_bytes(1, 73397, 56, 64) == 0      # D must be 128
+    assert lib.ovc_prepare_workspace_bytes(0, 10, 1, 128) == 0
+    assert lib.ovc_prepare_workspace_bytes(1, 0, 1, 128) == 0
+    r = lib.ovc_repair_workspace_bytes(1, 73397, 56, 0.005)
+    assert r >= bh * 367 * 4 + 2 * bh * 384 * 128
+    assert lib.ovc_repair_workspace_bytes(1, 73397, 56, 0.0) == 0
+    assert lib.ovc_repair_workspace_bytes(1, 73397, 56, 1.5) == 0
+
+
+def test_host_validation_rejects_bad_arguments(lib):
+    from fp8_bit_attention_gb300 import _abi
+    t = _abi.OvcTensor(0x1000, _abi.OVC_BF16, 1, 128, 1, 128, 128 * 128, 128, 128)
+    out = _abi.OvcPrepared()
+    ws = ctypes.c_void_p(0x100000)
+    # null output struct / null tensors
+    assert lib.ovc_prepare(None, ctypes.byref(t), ctypes.byref(t), ws, 1 << 30, ctypes.byref(out), None) == _abi.OVC_ERR_INVALID_ARG
+    # unsupported head dim and dtype
+    bad_d = _abi.OvcTensor(0x1000, _abi.OVC_BF16, 1, 128, 1, 64, 64 * 128, 64, 64)
+    assert lib.ovc_prepare(ctypes.byref(bad_d), ctypes.byref(bad_d), ctypes.byref(bad_d), ws, 1 << 30,
+                           ctypes.byref(out), None) == _abi.OVC_ERR_UNSUPPORTED
+    bad_t = _abi.OvcTensor(0x1000, 7, 1, 128, 1, 128, 128 * 128, 128, 128)
+    assert lib.ovc_prepare(ctypes.byref(bad_t), ctypes.byref(bad_t), ctypes.byref(bad_t), ws, 1 << 30,
+                           ctypes.byref(out), None) == _abi.OVC_ERR_UNSUPPORTED
+    # misaligned pointer, bad strides, shape mismatch
+    mis = _abi.OvcTensor(0x1002, _abi.OVC_BF16, 1, 128, 1, 128, 128 * 128, 128, 128)
+    assert lib.ovc_prepare(ctypes.byref(mis), ctypes.byref(t), ctypes.byref(t), ws, 1 << 30,
+                           ctypes.byref(out), None) == _abi.OVC_ERR_INVALID_ARG
+    strided = _abi.OvcTensor(0x1000, _abi.OVC_BF16, 1, 128, 1, 128, 128 * 128, 130, 128)
+    assert lib.ovc_prepare(ctypes.byref(strided), ctypes.byref(t), ctypes.byref(t), ws, 1 << 30,
+                           ctypes.byref(out), None) == _abi.OVC_ERR_INVALID_ARG
+    other = _abi.OvcTensor(0x1000, _abi.OVC_BF16, 1, 256, 1, 128, 256 * 128, 128, 128)
+    assert lib.ovc_prepare(ctypes.byref(t), ctypes.byref(other), ctypes.byref(t), ws, 1 << 30,
+                           ctypes.byref(out), None) == _abi.OVC_ERR_INVALID_ARG
+    # workspace: misaligned, too small
+    assert lib.ovc_prepare(ctypes.byref(t), ctypes.byref(t), ctypes.byref(t), ctypes.c_void_p(0x100010),
+                           1 << 30, ctypes.byref(out), None) == _abi.OVC_ERR_INVALID_ARG
+    assert lib.ovc_prepare(ctypes.byref(t), ctypes.byref(t), ctypes.byref(t), ws, 100, ctypes.byref(out),
+                           None) == _abi.OVC_ERR_WORKSPACE_TOO_SMALL
+    # attention with an empty prepared struct
+    o = _abi.OvcOutput(0x2000, 128 * 128, 128, 128)
+    assert lib.ovc_attention(ctypes.byref(_abi.OvcPrepared()), 0.0, ctypes.byref(o), None) == _abi.OVC_ERR_INVALID_ARG
+    assert lib.ovc_attention_v_repair(ctypes.byref(_abi.OvcPrepared()), None, 0.0, ctypes.byref(o), None) == _abi.OVC_ERR_INVALID_ARG
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert lib.ovc_status_string(s)
+    assert b"timed out" in lib.ovc_status_string(5)
+
+
+def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
+    from fp8_bit_attention_gb300 import _abi, build
+    monkeypatch.setattr(build, "LIB", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(_abi, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        _abi.lib()

@@ -1,0 +1,150 @@
+"""GPU parity: libovc (through the C ABI) against the CPU oracle.
+
+Bit-exact: quantised Q/K/V codes and scales, residual energies, repair
+indices and repair codes.  Floating point: O within relative L2 5e-3 of the
+oracle's double result; P bytes within one code of the oracle's recomputation
+under the device's own reference."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import fp8_bit_attention_gb300 as ovc
+from fp8_bit_attention_gb300 import workloads as W
+
+from gpu_util import TOL_REL_L2, inputs, oracle_prep, rel_l2, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _build():
+    import __graft_entry__
+    __graft_entry__.build()
+    assert torch.cuda.is_available()
+    yield
+    assert ovc.device_status() == 0
+
+
+SHAPES = [(1, 2, 1024), (1, 1, 1), (1, 1, 127), (1, 2, 129), (2, 3, 300), (1, 2, 1000), (1, 1, 640)]
+
+
+@pytest.mark.parametrize("B,H,S", SHAPES)
+def test_prepare_bit_exact(B, H, S):
+    q, k, v = inputs(B, H, S, seed=100 + S)
+    ref = oracle_prep(q, k, v)
+    prep = ovc.prepare(*to_dev(q, k, v))
+    torch.cuda.synchronize()
+    assert np.array_equal(prep.q_codes().cpu().numpy(), ref.qc)
+    assert np.array_equal(prep.k_codes().cpu().numpy(), ref.kc)
+    assert np.array_equal(prep.q_scales().cpu().numpy(), ref.sq)
+    assert np.array_equal(prep.k_scales().cpu().numpy(), ref.sk)
+    assert np.array_equal(prep.v_scales().cpu().numpy(), ref.sv)
+    vt = prep.vt_codes().cpu().numpy()
+    assert np.array_equal(vt.transpose(0, 1, 3, 2), ref.vc)
+    assert np.array_equal(prep.energy().cpu().numpy().view(np.uint32), ref.energy.view(np.uint32))
+
+
+@pytest.mark.parametrize("B,H,S", SHAPES)
+def test_attention_matches_oracle(B, H, S):
+    q, k, v = inputs(B, H, S, seed=200 + S)
+    ref, _ = oracle.attention_full(oracle_prep(q, k, v))
+    o = ovc.attention(*to_dev(q, k, v))
+    assert ovc.device_status() == 0
+    got = o.float().cpu().numpy()
+    assert np.isfinite(got).all()
+    assert rel_l2(got, ref) <= TOL_REL_L2
+
+
+def test_attention_3d_layout_and_strided_inputs():
+    q, k, v = inputs(1, 2, 700, seed=301)
+    ref, _ = oracle.attention_full(oracle_prep(q, k, v))
+    qd, kd, vd = to_dev(q, k, v)
+    o3 = ovc.attention(qd[0], kd[0], vd[0])                       # [S,H,128]
+    assert rel_l2(o3.float().cpu().numpy(), ref[0]) <= TOL_REL_L2
+    # inputs embedded in a wider buffer (head stride 256 elements)
+    big = torch.zeros((3, 1, 700, 2, 256), dtype=torch.bfloat16, device="cuda")
+    big[0, ..., :128], big[1, ..., :128], big[2, ..., :128] = qd, kd, vd
+    out = torch.zeros((1, 700, 2, 256), dtype=torch.bfloat16, device="cuda")
+    prep = ovc.prepare(big[0, ..., :128], big[1, ..., :128], big[2, ..., :128])
+    ovc.attention_prepared(prep, out=out[..., 128:])
+    assert rel_l2(out[..., 128:].float().cpu().numpy(), ref) <= TOL_REL_L2
+    assert not out[..., :128].any()
+
+
+def test_persistent_and_plain_schedules_agree_bitwise():
+    q, k, v = inputs(1, 3, 1500, seed=302)
+    prep = ovc.prepare(*to_dev(q, k, v))
+    a, _, _ = ovc.attention_probe(prep, force_persistent=1)
+    b, _, _ = ovc.attention_probe(prep, force_persistent=-1)
+    assert ovc.device_status() == 0
+    assert torch.equal(a, b)
+
+
+def test_softmax_scale_argument():
+    q, k, v = inputs(1, 1, 512, seed=303)
+    ref, _ = oracle.attention_full(oracle_prep(q, k, v), sm=0.05)
+    o = ovc.attention(*to_dev(q, k, v), softmax_scale=0.05)
+    assert rel_l2(o.float().cpu().numpy(), ref) <= TOL_REL_L2
+
+
+@pytest.mark.parametrize("S,qb,kb", [(1024, 3, 4), (1000, 7, 7), (1000, 0, 3), (300, 2, 1)])
+def test_p_codes_within_one_code_under_device_reference(S, qb, kb):
+    H = 2
+    q, k, v = inputs(1, H, S, seed=400 + S)
+    ref = oracle_prep(q, k, v)
+    prep = ovc.prepare(*to_dev(q, k, v))
+    bh = 1
+    _, codes, m8 = ovc.attention_probe(prep, dump=(bh, qb, kb))
+    codes = codes.cpu().numpy()
+    m8 = m8.cpu().numpy()
+    rows = [r for r in range(128) if qb * 128 + r < S]
+    diffs = []
+    for r in rows:
+        assert np.isfinite(m8[r])
+        want = oracle.block_codes(ref, bh, qb * 128 + r, kb, float(m8[r]))
+        d = np.abs(codes[r].astype(int) - want.astype(int))
+        assert d.max() <= 1, (r, d.max())
+        diffs.append(d)
+    frac_equal = float(np.mean(np.concatenate(diffs) == 0))
+    assert frac_equal > 0.99
+
+
+@pytest.mark.parametrize("budget", [0.005, 0.02, 0.3])
+def test_repair_selection_bit_exact_and_output(budget):
+    B, H, S = 1, 2, 1100
+    q, k, v = inputs(B, H, S, seed=500)
+    ref = oracle_prep(q, k, v)
+    rep_ref = oracle.Repair(ref, budget)
+    qd, kd, vd = to_dev(q, k, v)
+    prep = ovc.prepare(qd, kd, vd)
+    rep = ovc.prepare_v_repair(vd, prep, budget)
+    torch.cuda.synchronize()
+    assert rep.desc.n == rep_ref.n
+    assert np.array_equal(rep.idx().cpu().numpy(), rep_ref.idx)
+    assert np.array_equal(rep.sr().cpu().numpy(), rep_ref.sr)
+    n = rep_ref.n
+    dvt = rep.dvt().cpu().numpy()
+    assert np.array_equal(dvt[..., :n].transpose(0, 1, 3, 2), rep_ref.dcodes)
+    assert not dvt[..., n:].any()
+    ksel = rep.k_sel().cpu().numpy()
+    for h in range(H):
+        assert np.array_equal(ksel[0, h, :n], ref.kc[0, h, rep_ref.idx[0, h]])
+        assert np.array_equal(rep.sk_sel().cpu().numpy()[0, h, :n], ref.sk[0, h, rep_ref.idx[0, h] // 128])
+    want, _ = oracle.attention_full(ref, repair=rep_ref)
+    o = ovc.attention_v_repair(prep, rep)
+    assert ovc.device_status() == 0
+    assert rel_l2(o.float().cpu().numpy(), want) <= TOL_REL_L2
+
+
+def test_timeout_path_reports_and_recovers():
+    q, k, v = inputs(1, 1, 512, seed=600)
+    prep = ovc.prepare(*to_dev(q, k, v))
+    ovc.attention_probe(prep, skip_mma=True, wait_timeout_ns=20_000_000)
+    assert ovc.device_status() == 5          # OVC_ERR_TIMEOUT, context still usable
+    ref, _ = oracle.attention_full(oracle_prep(q, k, v))
+    o = ovc.attention_prepared(prep)
+    assert ovc.device_status() == 0
+    assert rel_l2(o.float().cpu().numpy(), ref) <= TOL_REL_L2
