@@ -1,0 +1,363 @@
+"""Benchmark: ExpCast FP8 attention full call on one GB300 (or N, weak scaling).
+
+One step = ovc_prepare (Q/K/V -> E4M3) + ovc_attention on the h56_s73397
+workload (B=1, H=56, S=73397, D=128, seeded synthetic BF16 inputs shaped like
+the pages' MiniMax-H3 capture).  Metric: TFLOP/s counted as 4*B*H*S^2*D / t.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  --impl reference times the CPU oracle on the
+host cores instead (each step a bounded sample of the same workload).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "FP8 ExpCast attn TFLOP/s (4·H·S²·D/t) at S=73397,H=56,D=128; % of FP8 peak"
+WORKLOAD = "h56_s73397"
+FP8_PER_BF16 = 2.0          # nominal dense FP8 / BF16 tensor throughput ratio on GB300
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--repair-budget", type=float, default=0.005)
+    return ap.parse_args()
+
+
+def _dist():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return p, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.uuid:
+            cmd += ["-i", self.uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.file.flush()
+
+    def summary(self):
+        rows = []
+        try:
+            with open(self.file.name) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) >= 8:
+                        rows.append(parts)
+            os.unlink(self.file.name)
+        except OSError:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
+        mx = [num(r[1]) for r in rows if num(r[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[4:8]) if v.lower().startswith("active")})
+        loaded = [s for s in sm if mx and s > 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows),
+                "power_w_max": max((num(r[2]) or 0.0) for r in rows)}
+
+
+def _gpu_uuid(torch):
+    try:
+        u = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+def cpu_baseline(w, q, k, v, *, rows: int, seconds_hint: float | None = None):
+    """The oracle, as it stands, on a bounded sample of the workload: head 0
+    quantised in full, then `rows` query rows (half from the middle query
+    block, half from the last, ragged one) against all keys.  Returns TFLOP/s
+    of the sample (4 * rows * S * D flops) and the wall time."""
+    import numpy as np
+
+    import oracle
+    from fp8_bit_attention_gb300 import workloads as W
+
+    S = w.S
+    qb, kb, vb = (W.bf16_bits(x)[:1, :, :1, :] for x in (q, k, v))
+    nb = (S + 127) // 128
+    mid = (nb // 2) * 128
+    tail0 = (nb - 1) * 128
+    ntail = min(S - tail0, rows // 2)
+    sel = np.concatenate([mid + np.arange(rows - ntail), tail0 + np.arange(ntail)]) % S
+    threads = oracle.default_threads()
+    t0 = time.perf_counter()
+    prep = oracle.Prepared(qb, kb, vb)
+    oracle.attention_rows(prep, np.zeros_like(sel), sel, nthreads=threads)
+    dt = time.perf_counter() - t0
+    flop = 4.0 * rows * S * 128
+    return {"value": flop / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"head 0 of {w.name}: Q/K/V quantised in full, then {rows} query rows "
+                      f"(from the middle query block on, plus the ragged tail block) against all {S} keys; "
+                      f"{dt:.2f} s wall; value = 4*rows*S*D / t"}
+
+
+def run_reference(a):
+    """--impl reference: the CPU oracle as it stands, on the host cores."""
+    import torch  # noqa: F401  (input generation)
+
+    from fp8_bit_attention_gb300 import workloads as W
+
+    rank, world, _ = _dist()
+    if rank != 0:
+        return
+    w = W.WORKLOADS[a.workload]
+    q, k, v = W.generate(w)
+    rows = 64
+    for _ in range(a.warmup):
+        cpu_baseline(w, q, k, v, rows=rows)
+    vals, times = [], []
+    for _ in range(a.steps):
+        r = cpu_baseline(w, q, k, v, rows=rows)
+        vals.append(r["value"])
+        times.append(4.0 * rows * w.S * 128 / (r["value"] * 1e12))
+    value = sum(4.0 * rows * w.S * 128 for _ in vals) / sum(times) / 1e12
+    cb = dict(r)
+    cb["value"] = value
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": a.steps,
+            "warmup": a.warmup, "ms_per_step": 1e3 * statistics.mean(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "S": w.S, "D": 128,
+                       "step": f"oracle sample: {rows} query rows of head 0 against all keys"},
+            "cpu_baseline": cb,
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(a):
+    import torch
+
+    import fp8_bit_attention_gb300 as ovc
+    from fp8_bit_attention_gb300 import build as libbuild
+    from fp8_bit_attention_gb300 import workloads as W
+
+    rank, world, local = _dist()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    libbuild.build()
+    w = W.WORKLOADS[a.workload]
+    # Weak scaling: every rank runs its own full problem (independent batch).
+    if rank:
+        w = W.custom(w.B, w.H, w.S, seed=w.seed + 1000 * rank, name=w.name,
+                     qk_bias=w.qk_bias, v_dist=w.v_dist, v_outliers=w.v_outliers)
+    q, k, v = W.generate(w, pin=True)
+    dev = torch.device("cuda", local)
+    qd, kd, vd = (x.to(dev) for x in (q, k, v))
+    ws = torch.empty(ovc.prepare_workspace_bytes(w.B, w.S, w.H), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(qd)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        prep = ovc.prepare(qd, kd, vd, workspace=ws)
+        if ev is not None:
+            ev[1].record(stream)
+        ovc.attention_prepared(prep, out=out)
+        if ev is not None:
+            ev[2].record(stream)
+        return prep
+
+    for _ in range(a.warmup):
+        step()
+    torch.cuda.synchronize()
+    if ovc.device_status() != 0:
+        raise RuntimeError("device-side timeout during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(a.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(_gpu_uuid(torch)) as clk:
+        start.record(stream)
+        for i in range(a.steps):
+            step(evs[i])
+        stop.record(stream)
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = clk.summary()
+    total_ms = start.elapsed_time(stop)
+    t_prep = [e[0].elapsed_time(e[1]) for e in evs]
+    t_attn = [e[1].elapsed_time(e[2]) for e in evs]
+    if ovc.device_status() != 0:
+        raise RuntimeError("device-side timeout during the timed region")
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    flop = ovc.flops(w.B, w.S, w.H)
+    ms_per_step = total_ms / a.steps
+    value = world * flop * a.steps / (total_ms / 1e3) / 1e12
+
+    # Repair variant (same step + ovc_prepare_v_repair + ovc_attention_v_repair).
+    repair = None
+    if a.repair_budget > 0:
+        rws = torch.empty(ovc.repair_workspace_bytes(w.B, w.S, w.H, a.repair_budget), dtype=torch.uint8, device=dev)
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        for it in range(2):
+            if it == 1:
+                e[0].record(stream)
+            prep = ovc.prepare(qd, kd, vd, workspace=ws)
+            rep = ovc.prepare_v_repair(vd, prep, a.repair_budget, workspace=rws)
+            ovc.attention_v_repair(prep, rep, out=out)
+        e[1].record(stream)
+        torch.cuda.synchronize()
+        tr = e[0].elapsed_time(e[1])
+        repair = {"budget": a.repair_budget, "ms_per_step": tr, "value": flop / (tr / 1e3) / 1e12,
+                  "unit": "TFLOP/s", "n_repaired_per_head": int(rep.desc.n)}
+        del rws
+
+    # End to end through the public API with host buffers.
+    e2e = None
+    if not a.no_e2e:
+        o_host = torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=True)
+        ovc.attention(q, k, v, out=o_host)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        t0 = time.perf_counter()
+        n_e2e = max(1, min(a.steps, 3))
+        for _ in range(n_e2e):
+            ovc.attention(q, k, v, out=o_host)
+        torch.cuda.synchronize()
+        te = (time.perf_counter() - t0) / n_e2e
+        if dist:
+            t = torch.tensor([te], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            te = float(t.item())
+        e2e = {"value": world * flop / te / 1e12, "unit": "TFLOP/s", "ms_per_step": te * 1e3,
+               "h2d_bytes_per_step": 3 * q.numel() * q.element_size(),
+               "d2h_bytes_per_step": o_host.numel() * o_host.element_size()}
+
+    peaks, which = _peaks()
+    bf16 = peaks.get("bf16_tflops_sustained") or peaks.get("bf16_tflops")
+    peak = bf16 * FP8_PER_BF16
+    attn_ms = statistics.mean(t_attn)
+    achieved = flop / (attn_ms / 1e3) / 1e12
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "attention_traffic.json")
+    if os.path.exists(tpath):
+        tr_rec = json.load(open(tpath))
+        if tr_rec.get("workload") == w.name and tr_rec.get("source_sha") == _kernel_sha():
+            traffic = tr_rec.get("bytes_per_launch")
+    hbm = peaks.get("hbm_gbs")
+    # algorithmic bytes of ovc_prepare: read BF16 Q/K/V once, write E4M3 Q/K/V^T
+    # and one FP32 energy per (head, token); scales are negligible
+    prep_bytes = 3 * 2 * q.numel() + 3 * q.numel() + 4 * w.B * w.H * w.S
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": a.steps,
+        "warmup": a.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "S": w.S, "D": 128,
+                   "step": "ovc_prepare + ovc_attention (no repair)",
+                   "l2": "inputs larger than L2 (1.05 GB BF16 per tensor); no flush",
+                   "parallelism": f"weak: {world} independent problem(s), one per GPU"},
+        "pct_of_fp8_peak": 100.0 * value / world / peak,
+        "breakdown_ms": {"prepare": statistics.mean(t_prep), "attention": attn_ms},
+        "prepare_gbs": prep_bytes / (statistics.mean(t_prep) / 1e3) / 1e9,
+        "prepare_frac_of_hbm": (prep_bytes / (statistics.mean(t_prep) / 1e3) / 1e9) / hbm if hbm else None,
+        "roofline": {"kernel": "attention_kernel", "bound": "tensor", "achieved": achieved, "peak": peak,
+                     "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{which} bf16 sustained x {FP8_PER_BF16:g} (FP8/BF16 nominal)"},
+        "repair": repair,
+        "e2e": e2e,
+        "gpu_launches": 3 * a.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and not a.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, q, k, v, rows=2048)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def _kernel_sha():
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("ptx.cuh", "attention.cuh"):
+        h.update(open(os.path.join(ROOT, "fp8_bit_attention_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def main():
+    a = _args()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_ours(a)
+
+
+if __name__ == "__main__":
+    main()
