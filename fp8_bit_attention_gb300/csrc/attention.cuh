@@ -18,6 +18,7 @@
 //     (kind::f8f6f4, M = N = 128, K = 32 per instruction), then
 //     O_t += P_t V_j^T with P_t read from TMEM (it overwrites S_t's first 32
 //     columns);
+//   * warps 10-11 idle; warps 8-11 give registers to warps 0-7 (setmaxnreg);
 //   * warps 0-3 and 4-7 are the softmax/ExpCast groups of Q0 and Q1: one
 //     thread per query row reads its 128 scores with tcgen05.ld, takes the
 //     block max, applies the lazy rescale, computes the 128 codes with one FMA
@@ -40,7 +41,13 @@
 namespace ovc {
 
 constexpr int kStages = 5;
-constexpr int kAttnThreads = 320;
+constexpr int kAttnThreads = 384;                          // 3 warpgroups
+// Register split: 168 per thread at launch (384 x 168 = 64512 <= 65536);
+// the producer/MMA warpgroup drops to 64 so that the two softmax warpgroups
+// can hold 216 each: 256 x 216 + 128 x 64 = 63488 <= 64512.
+constexpr int kSoftmaxRegs = 216;
+constexpr int kControlRegs = 64;
+static_assert(256 * kSoftmaxRegs + 128 * kControlRegs <= kAttnThreads * 168, "register split");
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr uint32_t kTile = 128 * 128;                       // bytes of one E4M3 tile
@@ -86,6 +93,7 @@ struct AttnSmem {
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
+  int zero;               // always 0: the "never abort" flag of drain waits
 };
 
 constexpr size_t kAttnSmemBytes = sizeof(AttnSmem) + 1024;  // + alignment slack
@@ -164,6 +172,18 @@ __device__ __forceinline__ void expcast_block_cols(const uint32_t* s, const floa
   }
 }
 
+// Maximum of 128 FP32 values: eight independent 3-input chains, then a tree.
+__device__ __forceinline__ float rowmax128(const uint32_t* s) {
+  float m[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) m[k] = fmaxf(__uint_as_float(s[k]), __uint_as_float(s[k + 8]));
+#pragma unroll
+  for (int c = 16; c < 128; c += 16)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) m[k] = fmax3(m[k], __uint_as_float(s[c + k]), __uint_as_float(s[c + 8 + k]));
+  return fmax3(fmax3(m[0], m[1], m[2]), fmax3(m[3], m[4], m[5]), fmaxf(m[6], m[7]));
+}
+
 __device__ __forceinline__ void tmem_load_row128(uint32_t taddr, uint32_t* s) {
   tmem_ld32(taddr + 0, s);
   tmem_ld32(taddr + 32, s + 32);
@@ -217,6 +237,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
     mbar_init(smem_addr(&sm.drain), 1);
     sm.abort = 0;
+    sm.zero = 0;
     fence_mbar_init();
     tma_prefetch_map(&tm_q);
     tma_prefetch_map(&tm_k);
@@ -230,7 +251,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
-
+  if (warp >= 8) {
+    regs_dec<kControlRegs>();
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------------ TMA
     if (lane == 0) {
@@ -269,13 +291,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (!ok) {
         record_abort(sm, P);
         // Drain: wait for the copies already issued (they always complete).
-        const volatile int never = 0;
+        const volatile int* never = &sm.zero;
         for (uint32_t n = (kv_iter > kStages ? kv_iter - kStages : 0); n < kv_iter; ++n) {
           const uint32_t stage = n % kStages, par = (n / kStages) & 1;
-          mbar_wait(smem_addr(&sm.k_full[stage]), par, kDrainNs, &never);
-          mbar_wait(smem_addr(&sm.v_full[stage]), par, kDrainNs, &never);
+          mbar_wait(smem_addr(&sm.k_full[stage]), par, kDrainNs, never);
+          mbar_wait(smem_addr(&sm.v_full[stage]), par, kDrainNs, never);
         }
-        if (q_iter > 0) mbar_wait(smem_addr(&sm.q_full), (q_iter - 1) & 1, kDrainNs, &never);
+        if (q_iter > 0) mbar_wait(smem_addr(&sm.q_full), (q_iter - 1) & 1, kDrainNs, never);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -355,12 +377,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (!ok) record_abort(sm, P);
       if (issued) {
         // Every MMA issued so far has completed once this barrier flips.
-        const volatile int never = 0;
         tc_commit(smem_addr(&sm.drain));
-        mbar_wait(smem_addr(&sm.drain), 0, kDrainNs, &never);
+        mbar_wait(smem_addr(&sm.drain), 0, kDrainNs, &sm.zero);
       }
     }
+  }
   } else {
+    regs_inc<kSoftmaxRegs>();
     // ------------------------------------------------------- softmax/ExpCast
     const int t = warp >> 2;                    // query tile 0 or 1
     const int wq = warp & 3;
@@ -380,6 +403,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       float l = 0.0f;
       const bool dump_tile = (P.dump_codes != nullptr) && tc.bh == P.dump_bh && qb == P.dump_qb && store;
       for (int i = 0; i < nblk; ++i) {
+        const bool main_blk = i < P.nb;
+        const int j = main_blk ? key_block(i, P.nb) : 0;
+        // Issued before the wait so that its latency hides behind it.
+        const float skj = main_blk ? __ldg(P.sk + tc.bh * P.nb + j) : 0.0f;
         ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&sm.s_full[t]), blk_count & 1, tmo, abort_flag));
         ++blk_count;
         if (!ok) break;
@@ -387,29 +414,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         uint32_t s[128];
         uint32_t w[32];
         tmem_load_row128(tS, s);
-        if (i < P.nb) {
-          const int j = key_block(i, P.nb);
+        float f = 1.0f;
+        bool rescale = false;
+        if (main_blk) {
           const int valid = P.S - j * 128;
           if (valid < 128) {
 #pragma unroll
             for (int c = 0; c < 128; ++c)
               if (c >= valid) s[c] = 0xFF800000u;  // -inf: excluded from max, code 0
           }
-          float mx = __uint_as_float(s[0]);
-#pragma unroll
-          for (int c = 1; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
-          const float a = c8sq * P.sk[tc.bh * P.nb + j];
-          const float bm8 = mx * a;
+          const float a = c8sq * skj;
+          const float bm8 = rowmax128(s) * a;
           const bool need = bm8 > kf + (kFrac + kLazy);
           if (__any_sync(0xFFFFFFFFu, need)) {
             const float kn = need ? ceilf(bm8 - kFrac) : kf;
-            const float f = need ? exp2f((kf - kn) * 0.125f) : 1.0f;
+            f = need ? exp2f((kf - kn) * 0.125f) : 1.0f;
             l *= f;
-            if (i > 0) tmem_scale_row128(tO, f);
             kf = kn;
+            rescale = i > 0;
           }
-          const float cterm = (kCodeBase - kf) + kMagic;
-          l += expcast_block(s, a, cterm, w);
+          l += expcast_block(s, a, (kCodeBase - kf) + kMagic, w);
           if (dump_tile && j == P.dump_kb) {
             uint4* d = reinterpret_cast<uint4*>(P.dump_codes + row * 128);
 #pragma unroll
@@ -418,7 +442,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           }
         } else {
           const int r = i - P.nb;
-          if (r == 0) tmem_scale_row128(tO, P.sv[tc.bh] / P.sr[tc.bh]);
           const int valid = P.n_rep - r * 128;
 #pragma unroll
           for (int c = 0; c < 128; ++c)
@@ -426,8 +449,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           const float4* ks = reinterpret_cast<const float4*>(
               P.sk_sel + static_cast<int64_t>(tc.bh) * P.n_rep_pad + r * 128);
           expcast_block_cols(s, ks, c8sq, (kCodeBase - kf) + kMagic, w);
+          if (r == 0) {
+            f = P.sv[tc.bh] / P.sr[tc.bh];
+            rescale = true;
+          }
         }
         tmem_st32(tS, w);
+        // O is stable here (every earlier MMA of this tile has completed) and
+        // the next P.V waits for this thread's arrival below.
+        if (rescale) tmem_scale_row128(tO, f);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(smem_addr(&sm.p_full[t]));

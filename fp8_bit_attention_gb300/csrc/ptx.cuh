@@ -195,6 +195,17 @@ __device__ __forceinline__ void tmem_wait_st() {
 #undef OVC_W8
 #undef OVC_U8
 
+// Per-warpgroup register reallocation (all four warps of a warpgroup execute
+// it).  The counts must fit the registers the CTA was launched with.
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ---------------------------------------------------------------------------
 // Conversions
 // ---------------------------------------------------------------------------
@@ -212,6 +223,13 @@ __device__ __forceinline__ void cvt_e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, 
       "cvt.rn.f16x2.e4m3x2 %0, x;\n\tcvt.rn.f16x2.e4m3x2 %1, y;\n\t}"
       : "=r"(lo), "=r"(hi)
       : "r"(w));
+}
+
+// Three-input FP32 maximum (one instruction on sm_100+).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
 
 __device__ __forceinline__ uint32_t hadd2(uint32_t a, uint32_t b) {
