@@ -44,7 +44,7 @@ class OvcRepair(ctypes.Structure):
 class OvcProbe(ctypes.Structure):
     _fields_ = [("dump_bh", c_i64), ("dump_qblock", c_i64), ("dump_kblock", c_i64),
                 ("dump_codes", c_ptr), ("dump_m8", c_ptr), ("wait_timeout_ns", ctypes.c_uint64),
-                ("skip_mma", c_i32), ("force_persistent", c_i32)]
+                ("skip_mma", c_i32), ("force_persistent", c_i32), ("trace", c_ptr)]
 
 
 P = ctypes.POINTER

@@ -207,7 +207,7 @@ def attention_v_repair(prep: Prepared, rep: Repair, *, softmax_scale: float | No
 
 def attention_probe(prep: Prepared, rep: Repair | None = None, *, softmax_scale=None, out=None,
                     dump=None, wait_timeout_ns: int = 0, skip_mma: bool = False,
-                    force_persistent: int = 0, stream=None):
+                    force_persistent: int = 0, trace: torch.Tensor | None = None, stream=None):
     """Test hook: attention with P-byte dumps / wait-limit controls.
 
     dump = (bh, qblock, kblock) returns (out, codes [128,128] uint8, m8 [128])."""
@@ -218,6 +218,9 @@ def attention_probe(prep: Prepared, rep: Repair | None = None, *, softmax_scale=
     probe.wait_timeout_ns = int(wait_timeout_ns)
     probe.skip_mma = int(skip_mma)
     probe.force_persistent = int(force_persistent)
+    if trace is not None:
+        assert trace.dtype == torch.int64 and trace.is_cuda and trace.numel() >= 4 * 64 * 8
+        probe.trace = trace.data_ptr()
     codes = m8 = None
     if dump is not None:
         dev = prep.workspace.device

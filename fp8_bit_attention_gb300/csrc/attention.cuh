@@ -20,10 +20,11 @@
 //     columns);
 //   * warps 10-11 idle; warps 8-11 give registers to warps 0-7 (setmaxnreg);
 //   * warps 0-3 and 4-7 are the softmax/ExpCast groups of Q0 and Q1: one
-//     thread per query row reads its 128 scores with tcgen05.ld, takes the
-//     block max, applies the lazy rescale, computes the 128 codes with one FMA
-//     each (the FMA adds 1.5*2^23 so that its rounding yields the integer
-//     code), clamps at 0, packs bytes, writes them back with tcgen05.st and
+//     thread per query row reads its 128 scores with the max-reducing form of
+//     tcgen05.ld (sm_103a), so the block max costs no instruction; applies the
+//     lazy rescale; computes each code with one saturating FMA (clamp at 0)
+//     and one FMA that adds 1.5*2^23 so that its rounding yields the integer
+//     code in the low byte; packs bytes, writes them back with tcgen05.st and
 //     adds the decoded bytes to l;
 //   * TMEM: S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512) columns.
 // Every mbarrier wait is bounded (wall-clock limit); on expiry the CTA
@@ -81,7 +82,25 @@ struct AttnParams {
   uint64_t timeout_ns;
   int32_t skip_mma;
   unsigned int* status;
+  // timeline trace (test hook, builds with -DOVC_TRACE=1 only): CTA 0 records clock64() stamps of the first
+  // kTraceBlocks blocks: [role][block][event], roles 0 = softmax warp 0,
+  // 1 = softmax warp 4, 2 = MMA lane, 3 = producer lane.
+  long long* trace;
 };
+
+constexpr int kTraceBlocks = 64, kTraceEvents = 8;
+
+// Compiled in only with -DOVC_TRACE=1: clock reads are scheduling barriers,
+// so the stamps would slow the loop they measure.
+__device__ __forceinline__ void trace_mark(const AttnParams& P, int role, uint32_t blk, int ev) {
+#if defined(OVC_TRACE) && OVC_TRACE
+  if (P.trace != nullptr && blockIdx.x == 0 && blk < static_cast<uint32_t>(kTraceBlocks) &&
+      (threadIdx.x & 31) == 0)
+    P.trace[(role * kTraceBlocks + blk) * kTraceEvents + ev] = clock64();
+#else
+  (void)P, (void)role, (void)blk, (void)ev;
+#endif
+}
 
 struct AttnSmem {
   uint8_t q[2][kTile];
@@ -131,17 +150,41 @@ __device__ __forceinline__ int key_block(int i, int nb) {
 // Produces 32 packed words of codes (bytes in key order) and returns the sum
 // of the decoded codes (accumulated as f16x2 pairs per block).
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float expcast_block(const uint32_t* s, float a, float cterm, uint32_t* w) {
+#ifndef OVC_EXPCAST_SAT
+#define OVC_EXPCAST_SAT 1
+#endif
+#ifndef OVC_LDRED
+#define OVC_LDRED 1
+#endif
+
+// One ExpCast code in the low byte of the result.  With OVC_EXPCAST_SAT the
+// inputs are scaled by 1/256 (as = a/256, cs = (c0+beta-m8)/256): a saturating
+// FMA clamps at 0 and a second FMA rounds; otherwise (as = a, cs =
+// c0+beta-m8+1.5*2^23) one FMA rounds and a max clamps.
+__device__ __forceinline__ uint32_t expcast_code(uint32_t s, float as, float cs) {
+#if OVC_EXPCAST_SAT
+  return __float_as_uint(fmaf(fma_sat(__uint_as_float(s), as, cs), 256.0f, kMagic));
+#else
+  return __float_as_uint(fmaxf(fmaf(__uint_as_float(s), as, cs), kMagic));
+#endif
+}
+
+__device__ __forceinline__ float expcast_scale_a(float a) {
+  return OVC_EXPCAST_SAT ? a * (1.0f / 256.0f) : a;
+}
+__device__ __forceinline__ float expcast_scale_c(float c) {   // c = c0 + beta - m8 (an integer)
+  return OVC_EXPCAST_SAT ? c * (1.0f / 256.0f) : c + kMagic;
+}
+
+__device__ __forceinline__ float expcast_block(const uint32_t* s, float as, float cs, uint32_t* w) {
   uint32_t acc[16];
 #pragma unroll
   for (int g = 0; g < 32; ++g) {
-    const float u0 = fmaxf(fmaf(__uint_as_float(s[4 * g + 0]), a, cterm), kMagic);
-    const float u1 = fmaxf(fmaf(__uint_as_float(s[4 * g + 1]), a, cterm), kMagic);
-    const float u2 = fmaxf(fmaf(__uint_as_float(s[4 * g + 2]), a, cterm), kMagic);
-    const float u3 = fmaxf(fmaf(__uint_as_float(s[4 * g + 3]), a, cterm), kMagic);
-    const uint32_t t01 = __byte_perm(__float_as_uint(u0), __float_as_uint(u1), 0x0040);
-    const uint32_t t23 = __byte_perm(__float_as_uint(u2), __float_as_uint(u3), 0x0040);
-    w[g] = __byte_perm(t01, t23, 0x5410);
+    const uint32_t u0 = expcast_code(s[4 * g + 0], as, cs);
+    const uint32_t u1 = expcast_code(s[4 * g + 1], as, cs);
+    const uint32_t u2 = expcast_code(s[4 * g + 2], as, cs);
+    const uint32_t u3 = expcast_code(s[4 * g + 3], as, cs);
+    w[g] = __byte_perm(__byte_perm(u0, u1, 0x0040), __byte_perm(u2, u3, 0x0040), 0x5410);
     uint32_t h0, h1;
     cvt_e4m3x4_to_f16x2x2(w[g], h0, h1);
     const uint32_t h = hadd2(h0, h1);
@@ -157,18 +200,16 @@ __device__ __forceinline__ float expcast_block(const uint32_t* s, float a, float
 
 // Same, with one multiplier per column (repair blocks: each selected key
 // keeps the scale of the block it came from) and no row sum.
-__device__ __forceinline__ void expcast_block_cols(const uint32_t* s, const float4* ksel, float c8sq,
-                                                   float cterm, uint32_t* w) {
+__device__ __forceinline__ void expcast_block_cols(const uint32_t* s, const float4* ksel, float c8sq256,
+                                                   float cs, uint32_t* w) {
 #pragma unroll
   for (int g = 0; g < 32; ++g) {
     const float4 k4 = __ldg(ksel + g);
-    const float u0 = fmaxf(fmaf(__uint_as_float(s[4 * g + 0]), c8sq * k4.x, cterm), kMagic);
-    const float u1 = fmaxf(fmaf(__uint_as_float(s[4 * g + 1]), c8sq * k4.y, cterm), kMagic);
-    const float u2 = fmaxf(fmaf(__uint_as_float(s[4 * g + 2]), c8sq * k4.z, cterm), kMagic);
-    const float u3 = fmaxf(fmaf(__uint_as_float(s[4 * g + 3]), c8sq * k4.w, cterm), kMagic);
-    const uint32_t t01 = __byte_perm(__float_as_uint(u0), __float_as_uint(u1), 0x0040);
-    const uint32_t t23 = __byte_perm(__float_as_uint(u2), __float_as_uint(u3), 0x0040);
-    w[g] = __byte_perm(t01, t23, 0x5410);
+    const uint32_t u0 = expcast_code(s[4 * g + 0], c8sq256 * k4.x, cs);
+    const uint32_t u1 = expcast_code(s[4 * g + 1], c8sq256 * k4.y, cs);
+    const uint32_t u2 = expcast_code(s[4 * g + 2], c8sq256 * k4.z, cs);
+    const uint32_t u3 = expcast_code(s[4 * g + 3], c8sq256 * k4.w, cs);
+    w[g] = __byte_perm(__byte_perm(u0, u1, 0x0040), __byte_perm(u2, u3, 0x0040), 0x5410);
   }
 }
 
@@ -182,6 +223,20 @@ __device__ __forceinline__ float rowmax128(const uint32_t* s) {
 #pragma unroll
     for (int k = 0; k < 8; ++k) m[k] = fmax3(m[k], __uint_as_float(s[c + k]), __uint_as_float(s[c + 8 + k]));
   return fmax3(fmax3(m[0], m[1], m[2]), fmax3(m[3], m[4], m[5]), fmaxf(m[6], m[7]));
+}
+
+// 128 scores and their maximum (four max-reducing loads).
+__device__ __forceinline__ float tmem_load_row128_max(uint32_t taddr, uint32_t* s) {
+  float m0, m1, m2, m3;
+  tmem_ld32_max(taddr + 0, s, m0);
+  tmem_ld32_max(taddr + 32, s + 32, m1);
+  tmem_ld32_max(taddr + 64, s + 64, m2);
+  tmem_ld32_max(taddr + 96, s + 96, m3);
+  tmem_wait_ld32_max(s, m0);
+  tmem_wait_ld32_max(s + 32, m1);
+  tmem_wait_ld32_max(s + 64, m2);
+  tmem_wait_ld32_max(s + 96, m3);
+  return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
 }
 
 __device__ __forceinline__ void tmem_load_row128(uint32_t taddr, uint32_t* s) {
@@ -328,6 +383,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         for (int i = 0; i < nblk; ++i) {
           const uint32_t stage = kv_iter % kStages;
+          trace_mark(P, 2, kv_iter, 0);
           ok = mbar_wait(smem_addr(&sm.v_full[stage]), (kv_iter / kStages) & 1, tmo, abort_flag);
           if (!ok) break;
           const uint64_t vd = sw128_desc(smem_addr(sm.v[stage]));
@@ -336,6 +392,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           // ---- query tile 0: O0 += P0 V, then the next block's S0
           ok = mbar_wait(smem_addr(&sm.p_full[0]), sp0, tmo, abort_flag);
           if (!ok) break;
+          trace_mark(P, 2, kv_iter, 1);
           sp0 ^= 1;
           tc_fence_after();
 #pragma unroll
@@ -354,8 +411,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             tc_commit(smem_addr(&sm.o_full[0]));
           }
           // ---- query tile 1
+          trace_mark(P, 2, kv_iter, 2);
           ok = mbar_wait(smem_addr(&sm.p_full[1]), sp1, tmo, abort_flag);
           if (!ok) break;
+          trace_mark(P, 2, kv_iter, 3);
           sp1 ^= 1;
           tc_fence_after();
 #pragma unroll
@@ -392,6 +451,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const uint32_t tS = tmem + lane_off + t * 128;
     const uint32_t tO = tmem + lane_off + 256 + t * 128;
     uint32_t blk_count = 0, tile_count = 0;
+    const int trole = (wq == 0) ? t : -1;
     bool ok = true;
     for (int tile = blockIdx.x; tile < P.ntiles && ok; tile += gridDim.x) {
       const TileCoord tc = tile_coord(P, tile);
@@ -402,29 +462,41 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       float kf = -INFINITY;                     // reference m8 = kf + frac(c0+beta)
       float l = 0.0f;
       const bool dump_tile = (P.dump_codes != nullptr) && tc.bh == P.dump_bh && qb == P.dump_qb && store;
+      // Key scale of the current block, loaded one block ahead.
+      float sk_next = __ldg(P.sk + tc.bh * P.nb + key_block(0, P.nb));
       for (int i = 0; i < nblk; ++i) {
         const bool main_blk = i < P.nb;
         const int j = main_blk ? key_block(i, P.nb) : 0;
-        // Issued before the wait so that its latency hides behind it.
-        const float skj = main_blk ? __ldg(P.sk + tc.bh * P.nb + j) : 0.0f;
+        const float skj = sk_next;
+        if (i + 1 < P.nb) sk_next = __ldg(P.sk + tc.bh * P.nb + key_block(i + 1, P.nb));
+        const uint32_t gi = blk_count;
+        if (trole >= 0) trace_mark(P, trole, gi, 0);
         ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&sm.s_full[t]), blk_count & 1, tmo, abort_flag));
         ++blk_count;
         if (!ok) break;
+        if (trole >= 0) trace_mark(P, trole, gi, 1);
         tc_fence_after();
         uint32_t s[128];
         uint32_t w[32];
+#if OVC_LDRED
+        float mx = tmem_load_row128_max(tS, s);
+#else
         tmem_load_row128(tS, s);
+        float mx = rowmax128(s);
+#endif
+        if (trole >= 0) trace_mark(P, trole, gi, 2);
         float f = 1.0f;
         bool rescale = false;
         if (main_blk) {
           const int valid = P.S - j * 128;
-          if (valid < 128) {
+          if (valid < 128) {       // ragged tail block: mask, then a software max
 #pragma unroll
             for (int c = 0; c < 128; ++c)
               if (c >= valid) s[c] = 0xFF800000u;  // -inf: excluded from max, code 0
+            mx = rowmax128(s);
           }
           const float a = c8sq * skj;
-          const float bm8 = rowmax128(s) * a;
+          const float bm8 = mx * a;
           const bool need = bm8 > kf + (kFrac + kLazy);
           if (__any_sync(0xFFFFFFFFu, need)) {
             const float kn = need ? ceilf(bm8 - kFrac) : kf;
@@ -433,7 +505,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             kf = kn;
             rescale = i > 0;
           }
-          l += expcast_block(s, a, (kCodeBase - kf) + kMagic, w);
+          if (trole >= 0) trace_mark(P, trole, gi, 3);
+          l += expcast_block(s, expcast_scale_a(a), expcast_scale_c(kCodeBase - kf), w);
           if (dump_tile && j == P.dump_kb) {
             uint4* d = reinterpret_cast<uint4*>(P.dump_codes + row * 128);
 #pragma unroll
@@ -448,12 +521,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (c >= valid) s[c] = 0xFF800000u;
           const float4* ks = reinterpret_cast<const float4*>(
               P.sk_sel + static_cast<int64_t>(tc.bh) * P.n_rep_pad + r * 128);
-          expcast_block_cols(s, ks, c8sq, (kCodeBase - kf) + kMagic, w);
+          expcast_block_cols(s, ks, expcast_scale_a(c8sq), expcast_scale_c(kCodeBase - kf), w);
           if (r == 0) {
             f = P.sv[tc.bh] / P.sr[tc.bh];
             rescale = true;
           }
         }
+        if (trole >= 0) trace_mark(P, trole, gi, 4);
         tmem_st32(tS, w);
         // O is stable here (every earlier MMA of this tile has completed) and
         // the next P.V waits for this thread's arrival below.
@@ -461,6 +535,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(smem_addr(&sm.p_full[t]));
+        if (trole >= 0) trace_mark(P, trole, gi, 6);
       }
       if (!ok) break;
       ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&sm.o_full[t]), tile_count & 1, tmo, abort_flag));

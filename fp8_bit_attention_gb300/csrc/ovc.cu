@@ -217,7 +217,7 @@ ovc_status run_attention(const ovc_prepared* p, const ovc_repair* r, float softm
   P.nb = static_cast<int32_t>(p->nb);
   P.S_pad = static_cast<int32_t>(p->S_pad);
   P.npairs = (P.nb + 1) / 2;
-  const int64_t ntiles = BH * P.npairs;
+  const int64_t ntiles = BH * P.npairs;   // a tile is a pair of 128-row query blocks
   P.ntiles = static_cast<int32_t>(ntiles);
   P.sq = p->sq;
   P.sk = p->sk;
@@ -247,6 +247,7 @@ ovc_status run_attention(const ovc_prepared* p, const ovc_repair* r, float softm
     if (probe->wait_timeout_ns > 0) P.timeout_ns = probe->wait_timeout_ns;
     P.skip_mma = probe->skip_mma;
     force = probe->force_persistent;
+    P.trace = reinterpret_cast<long long*>(probe->trace);
   }
   P.status = dev->status;
 

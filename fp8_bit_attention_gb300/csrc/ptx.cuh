@@ -169,11 +169,29 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
       : "r"(taddr));
 }
 
+// Same load, plus the maximum of the 32 loaded values (sm_103a reduction
+// form of tcgen05.ld).  `mx` is valid after tmem_wait_ld32_max().
+__device__ __forceinline__ void tmem_ld32_max(uint32_t taddr, uint32_t* r, float& mx) {
+  asm volatile(
+      "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, %32, [%33];"
+      : OVC_R8(0), OVC_R8(8), OVC_R8(16), OVC_R8(24), "=f"(mx)
+      : "r"(taddr));
+}
+
 // Wait for outstanding tcgen05.ld; the registers are named so that the
 // compiler cannot move their uses above the wait.
 __device__ __forceinline__ void tmem_wait_ld32(uint32_t* r) {
   asm volatile("tcgen05.wait::ld.sync.aligned;"
                : OVC_U8(0), OVC_U8(8), OVC_U8(16), OVC_U8(24)
+               :
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld32_max(uint32_t* r, float& mx) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : OVC_U8(0), OVC_U8(8), OVC_U8(16), OVC_U8(24), "+f"(mx)
                :
                : "memory");
 }
@@ -185,6 +203,27 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
       "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
       OVC_W8(0), OVC_W8(8), OVC_W8(16), OVC_W8(24)
       : "memory");
+}
+
+// 16 and 1 consecutive columns (same lane rules as tmem_ld32).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t tmem_ld1_sync(uint32_t taddr) {
+  uint32_t r;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r)::"memory");
+  return r;
+}
+
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ void tmem_wait_st() {
@@ -223,6 +262,17 @@ __device__ __forceinline__ void cvt_e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, 
       "cvt.rn.f16x2.e4m3x2 %0, x;\n\tcvt.rn.f16x2.e4m3x2 %1, y;\n\t}"
       : "=r"(lo), "=r"(hi)
       : "r"(w));
+}
+
+// fma with the result saturated to [0, 1].
+__device__ __forceinline__ float fma_sat(float a, float b, float c) {
+  float r;
+  asm("fma.rn.sat.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // Three-input FP32 maximum (one instruction on sm_100+).

@@ -157,7 +157,10 @@ const char* ovc_status_string(ovc_status s);
  * overrides the device wait limit; skip_mma != 0 makes the MMA warp issue
  * nothing so that every other wait runs into the limit (exercises the timeout
  * path without faulting or hanging).  force_persistent: 1 = persistent
- * schedule, -1 = one CTA per tile, 0 = automatic.  r may be NULL. */
+ * schedule, -1 = one CTA per tile, 0 = automatic.  trace, if not NULL and
+ * the library was built with -DOVC_TRACE=1, receives per-role SM clock
+ * stamps of the first 64 blocks of CTA 0 (pipeline analysis; ignored
+ * otherwise).  r may be NULL. */
 typedef struct {
   int64_t dump_bh, dump_qblock, dump_kblock;
   uint8_t* dump_codes;
@@ -165,6 +168,7 @@ typedef struct {
   uint64_t wait_timeout_ns;
   int32_t skip_mma;
   int32_t force_persistent;
+  int64_t* trace;   /* device [4][64][8] int64 clock64() stamps of CTA 0, or NULL */
 } ovc_probe;
 
 ovc_status ovc_attention_probe(const ovc_prepared* p, const ovc_repair* r, float softmax_scale,

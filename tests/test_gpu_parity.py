@@ -148,3 +148,16 @@ def test_timeout_path_reports_and_recovers():
     o = ovc.attention_prepared(prep)
     assert ovc.device_status() == 0
     assert rel_l2(o.float().cpu().numpy(), ref) <= TOL_REL_L2
+
+
+def test_repair_persistent_and_plain_schedules_agree_bitwise():
+    q, k, v = inputs(1, 3, 1300, seed=303)
+    qd, kd, vd = to_dev(q, k, v)
+    prep = ovc.prepare(qd, kd, vd)
+    rep = ovc.prepare_v_repair(vd, prep, 0.05)
+    a, _, _ = ovc.attention_probe(prep, rep, force_persistent=1)
+    b, _, _ = ovc.attention_probe(prep, rep, force_persistent=-1)
+    assert ovc.device_status() == 0
+    assert torch.equal(a, b)
+    want, _ = oracle.attention_full(oracle_prep(q, k, v), repair=oracle.Repair(oracle_prep(q, k, v), 0.05))
+    assert rel_l2(a.float().cpu().numpy(), want) <= TOL_REL_L2
