@@ -17,6 +17,8 @@ OVC_ERR_UNSUPPORTED = 2
 OVC_ERR_WORKSPACE_TOO_SMALL = 3
 OVC_ERR_CUDA = 4
 OVC_ERR_TIMEOUT = 5
+OVC_ERR_SCRATCH_LIMIT = 6
+OVC_NOALLOC_MAX_HEADS = 4096
 OVC_BF16 = 0
 OVC_FP16 = 1
 
@@ -62,6 +64,7 @@ SIGNATURES = {
     "ovc_status_string": (ctypes.c_char_p, [c_i32]),
     "ovc_attention_probe": (c_i32, [P(OvcPrepared), P(OvcRepair), ctypes.c_float, P(OvcOutput),
                                     P(OvcProbe), c_ptr]),
+    "ovc_prepare_noalloc": (c_i32, [P(OvcTensor), P(OvcTensor), P(OvcTensor), P(OvcPrepared), c_ptr]),
 }
 
 _lock = threading.Lock()

@@ -443,8 +443,111 @@ const char* ovc_status_string(ovc_status s) {
     case OVC_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
     case OVC_ERR_CUDA: return "CUDA runtime error";
     case OVC_ERR_TIMEOUT: return "a device-side wait timed out";
+    case OVC_ERR_SCRATCH_LIMIT: return "B*H exceeds the fixed scratch of ovc_prepare_noalloc (OVC_NOALLOC_MAX_HEADS)";
   }
   return "unknown status";
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// ovc_prepare_noalloc: ovc_prepare without any caller workspace for scratch.
+// The per-head amax accumulators live in this fixed array instead.
+// ---------------------------------------------------------------------------
+namespace ovc {
+namespace {
+
+static __device__ __align__(256) uint32_t g_noalloc_amax[OVC_NOALLOC_MAX_HEADS];
+
+uint32_t* g_noalloc_ptr[kMaxDevices] = {};
+std::mutex g_noalloc_mu;
+
+// Device address of g_noalloc_amax for the current device, looked up once.
+ovc_status noalloc_scratch(uint32_t** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return OVC_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_amax) != cudaSuccess || p == nullptr) return OVC_ERR_CUDA;
+    g_noalloc_ptr[dev] = static_cast<uint32_t*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return OVC_OK;
+}
+
+__global__ void noalloc_clear_kernel(uint32_t* scratch, int n) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) scratch[i] = 0u;
+}
+
+__global__ void noalloc_copy_kernel(const uint32_t* scratch, uint32_t* dst, int n) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) dst[i] = scratch[i];
+}
+
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+}  // namespace
+}  // namespace ovc
+
+extern "C" ovc_status ovc_prepare_noalloc(const ovc_tensor* q, const ovc_tensor* k, const ovc_tensor* v,
+                                          const ovc_prepared* out, void* stream) {
+  if (!q || !k || !v || !out) return OVC_ERR_INVALID_ARG;
+  if (q->D != 128 || k->D != 128 || v->D != 128) return OVC_ERR_UNSUPPORTED;
+  if ((q->dtype != OVC_BF16 && q->dtype != OVC_FP16) || k->dtype != q->dtype || v->dtype != q->dtype)
+    return OVC_ERR_UNSUPPORTED;
+  if (!tensor_ok(q) || !tensor_ok(k) || !tensor_ok(v)) return OVC_ERR_INVALID_ARG;
+  if (k->B != q->B || k->S != q->S || k->H != q->H || v->B != q->B || v->S != q->S || v->H != q->H)
+    return OVC_ERR_INVALID_ARG;
+  const int64_t nb = (q->S + 127) / 128;
+  if (out->B != q->B || out->S != q->S || out->H != q->H || out->nb != nb || out->S_pad != nb * 128)
+    return OVC_ERR_INVALID_ARG;
+  if (!out->q || !out->k || !out->vt || !out->sq || !out->sk || !out->sv || !out->energy) return OVC_ERR_INVALID_ARG;
+  if (!aligned16(out->q) || !aligned16(out->k) || !aligned16(out->vt)) return OVC_ERR_INVALID_ARG;
+  if (!aligned4(out->sq) || !aligned4(out->sk) || !aligned4(out->sv) || !aligned4(out->energy) ||
+      (out->vamax && !aligned4(out->vamax)))
+    return OVC_ERR_INVALID_ARG;
+  const int64_t BH = q->B * q->H;
+  if (BH > OVC_NOALLOC_MAX_HEADS) return OVC_ERR_SCRATCH_LIMIT;
+  DeviceState* dev = nullptr;
+  ovc_status st = device_state(&dev);
+  if (st != OVC_OK) return st;
+  uint32_t* scratch = nullptr;
+  st = noalloc_scratch(&scratch);
+  if (st != OVC_OK) return st;
+
+  PrepParams P{};
+  P.q = static_cast<const uint16_t*>(q->ptr);
+  P.k = static_cast<const uint16_t*>(k->ptr);
+  P.v = static_cast<const uint16_t*>(v->ptr);
+  const ovc_tensor* ts[3] = {q, k, v};
+  int64_t* ss[3] = {P.qs, P.ks, P.vs};
+  for (int i = 0; i < 3; ++i) {
+    ss[i][0] = ts[i]->stride_b;
+    ss[i][1] = ts[i]->stride_s;
+    ss[i][2] = ts[i]->stride_h;
+  }
+  P.B = static_cast<int32_t>(q->B);
+  P.S = static_cast<int32_t>(q->S);
+  P.H = static_cast<int32_t>(q->H);
+  P.nb = static_cast<int32_t>(nb);
+  P.S_pad = static_cast<int32_t>(nb * 128);
+  P.fp16 = q->dtype == OVC_FP16;
+  P.qc = out->q;
+  P.kc = out->k;
+  P.vt = out->vt;
+  P.sq = out->sq;
+  P.sk = out->sk;
+  P.sv = out->sv;
+  P.vamax = scratch;          // the fixed array instead of caller workspace
+  P.energy = out->energy;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int n = static_cast<int>(BH);
+  noalloc_clear_kernel<<<(n + 255) / 256, 256, 0, s>>>(scratch, n);
+  const dim3 g1(static_cast<unsigned>(nb), static_cast<unsigned>(BH), 3);
+  prepare_qk_kernel<<<g1, 256, 0, s>>>(P);
+  const dim3 g2(static_cast<unsigned>(nb), static_cast<unsigned>(BH), 1);
+  prepare_v_kernel<<<g2, 512, 0, s>>>(P);
+  if (out->vamax) noalloc_copy_kernel<<<(n + 255) / 256, 256, 0, s>>>(scratch, out->vamax, n);
+  return launch_status();
+}
