@@ -49,6 +49,31 @@ def _dist():
     return rank, world, local
 
 
+def rank_workload(w, rank: int):
+    """Weak scaling: rank r runs its own full problem of the same shape; rank 0
+    keeps the named workload's seed, the others draw from distinct seeds."""
+    if rank == 0:
+        return w
+    from fp8_bit_attention_gb300 import workloads as W
+    return W.custom(w.B, w.H, w.S, seed=w.seed + 1000 * rank, name=w.name,
+                    qk_bias=w.qk_bias, v_dist=w.v_dist, v_outliers=w.v_outliers)
+
+
+def max_over_ranks(value: float, dist=None, device=None) -> float:
+    """The slowest rank's time (all ranks receive it)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flop_per_rank: float, world: int, steps: int, total_ms: float) -> float:
+    """Aggregate throughput: every rank's flops over the slowest rank's time."""
+    return world * flop_per_rank * steps / (total_ms / 1e3) / 1e12
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -205,9 +230,7 @@ def run_ours(a):
     libbuild.build()
     w = W.WORKLOADS[a.workload]
     # Weak scaling: every rank runs its own full problem (independent batch).
-    if rank:
-        w = W.custom(w.B, w.H, w.S, seed=w.seed + 1000 * rank, name=w.name,
-                     qk_bias=w.qk_bias, v_dist=w.v_dist, v_outliers=w.v_outliers)
+    w = rank_workload(w, rank)
     q, k, v = W.generate(w, pin=True)
     dev = torch.device("cuda", local)
     qd, kd, vd = (x.to(dev) for x in (q, k, v))
@@ -252,13 +275,10 @@ def run_ours(a):
     t_attn = [e[1].elapsed_time(e[2]) for e in evs]
     if ovc.device_status() != 0:
         raise RuntimeError("device-side timeout during the timed region")
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dist, dev)
     flop = ovc.flops(w.B, w.S, w.H)
     ms_per_step = total_ms / a.steps
-    value = world * flop * a.steps / (total_ms / 1e3) / 1e12
+    value = whole_job_tflops(flop, world, a.steps, total_ms)
 
     # Repair variant (same step + ovc_prepare_v_repair + ovc_attention_v_repair).
     repair = None
@@ -292,10 +312,7 @@ def run_ours(a):
             ovc.attention(q, k, v, out=o_host)
         torch.cuda.synchronize()
         te = (time.perf_counter() - t0) / n_e2e
-        if dist:
-            t = torch.tensor([te], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            te = float(t.item())
+        te = max_over_ranks(te, dist, dev)
         e2e = {"value": world * flop / te / 1e12, "unit": "TFLOP/s", "ms_per_step": te * 1e3,
                "h2d_bytes_per_step": 3 * q.numel() * q.element_size(),
                "d2h_bytes_per_step": o_host.numel() * o_host.element_size()}

@@ -1,0 +1,54 @@
+"""CPU (gloo, world size 2) test of bench.py's multi-rank host logic: each rank
+gets its own problem, the timing is the maximum over ranks, and the reported
+value is the whole job's throughput."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+from fp8_bit_attention_gb300 import workloads as W
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, out):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        w = bench.rank_workload(W.WORKLOADS["small"], rank)
+        my_ms = 100.0 + 50.0 * rank                    # rank 1 is the slow one
+        slowest = bench.max_over_ranks(my_ms, dist, torch.device("cpu"))
+        value = bench.whole_job_tflops(1e12, world, 4, slowest * 4)
+        out[rank] = (w.seed, slowest, value)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_ranks_gloo():
+    world = 2
+    with mp.Manager() as m:
+        out = m.dict()
+        mp.spawn(_worker, args=(world, _free_port(), out), nprocs=world, join=True)
+        res = dict(out)
+    seeds = {r: res[r][0] for r in range(world)}
+    assert seeds[0] == W.WORKLOADS["small"].seed and seeds[1] != seeds[0]
+    assert res[0][1] == res[1][1] == 150.0               # max over ranks, seen by both
+    # 2 ranks x 1e12 flop per step, 4 steps in 600 ms -> 13.33 TFLOP/s
+    assert res[0][2] == pytest.approx(2 * 1e12 * 4 / 0.6 / 1e12)
+
+
+def test_single_process_defaults():
+    w = W.WORKLOADS["small"]
+    assert bench.rank_workload(w, 0) is w
+    assert bench.max_over_ranks(3.5) == 3.5
