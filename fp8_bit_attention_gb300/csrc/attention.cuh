@@ -24,8 +24,10 @@
 //     tcgen05.ld (sm_103a), so the block max costs no instruction; applies the
 //     lazy rescale; computes each code with one saturating FMA (clamp at 0)
 //     and one FMA that adds 1.5*2^23 so that its rounding yields the integer
-//     code in the low byte; packs bytes, writes them back with tcgen05.st and
-//     adds the decoded bytes to l;
+//     code in the low byte; packs bytes and writes them back with
+//     tcgen05.st; only after handing P to the MMA warp does it add the
+//     decoded bytes to l (f16x2 pairs), so the row sum runs while the tensor
+//     core computes P.V and the next S instead of delaying them;
 //   * TMEM: S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512) columns.
 // Every mbarrier wait is bounded (wall-clock limit); on expiry the CTA
 // records a timeout, drains its own async copies and MMAs, frees TMEM and
@@ -153,9 +155,6 @@ __device__ __forceinline__ int key_block(int i, int nb) {
 #ifndef OVC_EXPCAST_SAT
 #define OVC_EXPCAST_SAT 1
 #endif
-#ifndef OVC_LDRED
-#define OVC_LDRED 1
-#endif
 
 // One ExpCast code in the low byte of the result.  With OVC_EXPCAST_SAT the
 // inputs are scaled by 1/256 (as = a/256, cs = (c0+beta-m8)/256): a saturating
@@ -176,15 +175,24 @@ __device__ __forceinline__ float expcast_scale_c(float c) {   // c = c0 + beta -
   return OVC_EXPCAST_SAT ? c * (1.0f / 256.0f) : c + kMagic;
 }
 
-__device__ __forceinline__ float expcast_block(const uint32_t* s, float as, float cs, uint32_t* w) {
-  uint32_t acc[16];
+// Codes of the scores s[4 G0 .. 4 (G0 + NG)) into the words w[G0 .. G0 + NG).
+template <int G0, int NG>
+__device__ __forceinline__ void expcast_words(const uint32_t* s, float as, float cs, uint32_t* w) {
 #pragma unroll
-  for (int g = 0; g < 32; ++g) {
+  for (int g = G0; g < G0 + NG; ++g) {
     const uint32_t u0 = expcast_code(s[4 * g + 0], as, cs);
     const uint32_t u1 = expcast_code(s[4 * g + 1], as, cs);
     const uint32_t u2 = expcast_code(s[4 * g + 2], as, cs);
     const uint32_t u3 = expcast_code(s[4 * g + 3], as, cs);
     w[g] = __byte_perm(__byte_perm(u0, u1, 0x0040), __byte_perm(u2, u3, 0x0040), 0x5410);
+  }
+}
+
+// Sum of the decoded E4M3 codes of 32 packed words (f16x2 pairs, then FP32).
+__device__ __forceinline__ float codes_sum(const uint32_t* w) {
+  uint32_t acc[16];
+#pragma unroll
+  for (int g = 0; g < 32; ++g) {
     uint32_t h0, h1;
     cvt_e4m3x4_to_f16x2x2(w[g], h0, h1);
     const uint32_t h = hadd2(h0, h1);
@@ -478,24 +486,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tc_fence_after();
         uint32_t s[128];
         uint32_t w[32];
-#if OVC_LDRED
-        float mx = tmem_load_row128_max(tS, s);
-#else
-        tmem_load_row128(tS, s);
-        float mx = rowmax128(s);
-#endif
-        if (trole >= 0) trace_mark(P, trole, gi, 2);
         float f = 1.0f;
         bool rescale = false;
         if (main_blk) {
           const int valid = P.S - j * 128;
+          const float a = c8sq * skj;
+          const float as = expcast_scale_a(a);
+          float mx = tmem_load_row128_max(tS, s);
           if (valid < 128) {       // ragged tail block: mask, then a software max
 #pragma unroll
             for (int c = 0; c < 128; ++c)
               if (c >= valid) s[c] = 0xFF800000u;  // -inf: excluded from max, code 0
             mx = rowmax128(s);
           }
-          const float a = c8sq * skj;
           const float bm8 = mx * a;
           const bool need = bm8 > kf + (kFrac + kLazy);
           if (__any_sync(0xFFFFFFFFu, need)) {
@@ -506,7 +509,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             rescale = i > 0;
           }
           if (trole >= 0) trace_mark(P, trole, gi, 3);
-          l += expcast_block(s, expcast_scale_a(a), expcast_scale_c(kCodeBase - kf), w);
+          expcast_words<0, 32>(s, as, expcast_scale_c(kCodeBase - kf), w);
           if (dump_tile && j == P.dump_kb) {
             uint4* d = reinterpret_cast<uint4*>(P.dump_codes + row * 128);
 #pragma unroll
@@ -514,6 +517,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             P.dump_m8[row] = kf + kFrac;
           }
         } else {
+          tmem_load_row128(tS, s);
           const int r = i - P.nb;
           const int valid = P.n_rep - r * 128;
 #pragma unroll
@@ -535,6 +539,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(smem_addr(&sm.p_full[t]));
+        // The row sum waits until the codes are on their way to the tensor core.
+        if (main_blk) l += codes_sum(w);
         if (trole >= 0) trace_mark(P, trole, gi, 6);
       }
       if (!ok) break;
