@@ -65,6 +65,8 @@ SIGNATURES = {
     "ovc_attention_probe": (c_i32, [P(OvcPrepared), P(OvcRepair), ctypes.c_float, P(OvcOutput),
                                     P(OvcProbe), c_ptr]),
     "ovc_prepare_noalloc": (c_i32, [P(OvcTensor), P(OvcTensor), P(OvcTensor), P(OvcPrepared), c_ptr]),
+    "ovc_memcpy2d": (c_i32, [c_ptr, ctypes.c_size_t, c_ptr, ctypes.c_size_t, ctypes.c_size_t,
+                             ctypes.c_size_t, c_ptr]),
 }
 
 _lock = threading.Lock()

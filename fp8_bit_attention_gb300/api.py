@@ -242,32 +242,121 @@ def device_status(stream=None) -> int:
     return int(lib().ovc_get_device_status(ctypes.c_void_p(_stream_handle(stream))))
 
 
-def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, softmax_scale: float | None = None,
-              repair_budget: float | None = None, out: torch.Tensor | None = None,
-              device=None) -> torch.Tensor:
-    """Full call: prepare + ExpCast attention (+ optional V residual repair).
+def memcpy2d(dst_ptr: int, dpitch: int, src_ptr: int, spitch: int, width: int, height: int,
+             stream=None) -> None:
+    """Strided asynchronous copy (``ovc_memcpy2d``) on ``stream`` (default: current)."""
+    check(lib().ovc_memcpy2d(dst_ptr, dpitch, src_ptr, spitch, width, height, _stream_handle(stream)),
+          "ovc_memcpy2d")
 
-    CUDA inputs give a CUDA output.  CPU inputs (pinned for speed) are copied
-    to `device` (default: the current CUDA device), computed there, and O is
-    copied back into `out` (or a new pinned tensor)."""
-    host = not q.is_cuda
-    if host:
-        dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
-        q, k, v = (x.to(dev, non_blocking=True) for x in (q, k, v))
+
+def head_chunks(H: int, chunk_heads: int | None = None) -> list[tuple[int, int]]:
+    """Head ranges of the host-buffer path: about four equal chunks by default."""
+    n = chunk_heads if chunk_heads else max(1, -(-H // 4))
+    return [(h0, min(H, h0 + n)) for h0 in range(0, H, n)]
+
+
+def _attention_device(q, k, v, softmax_scale, repair_budget, out):
     prep = prepare(q, k, v)
-    o = None if host else out
     if repair_budget:
         rep = prepare_v_repair(v, prep, repair_budget)
-        o = attention_v_repair(prep, rep, softmax_scale=softmax_scale, out=o)
-    else:
-        o = attention_prepared(prep, softmax_scale=softmax_scale, out=o)
-    if host:
-        if out is None:
-            out = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-        out.copy_(o, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
-        return out
-    return o
+        return attention_v_repair(prep, rep, softmax_scale=softmax_scale, out=out)
+    return attention_prepared(prep, softmax_scale=softmax_scale, out=out)
+
+
+def _attention_host(q, k, v, softmax_scale, repair_budget, out, dev, chunk_heads):
+    """Host-resident inputs streamed through the GPU in head chunks.
+
+    Every head is computed independently (its V scale, residual ranking and
+    attention involve that head alone), so the result equals a single
+    whole-tensor call bit for bit.  Chunk c+1 is copied in while chunk c is
+    prepared and attended, and chunk c-1's output is copied out meanwhile:
+    the copies (bound by the host link) hide behind the attention kernels."""
+    q4, k4, v4 = (_as4d(x) for x in (q, k, v))
+    if k4.shape != q4.shape or v4.shape != q4.shape:
+        raise ValueError("q, k and v must have the same shape")
+    if q4.dtype not in _DTYPES or k4.dtype != q4.dtype or v4.dtype != q4.dtype:
+        raise TypeError("inputs must all be bfloat16 or all float16")
+    for x in (q4, k4, v4):
+        if x.is_cuda or not x.is_contiguous():
+            raise ValueError("host inputs must be contiguous CPU tensors (pinned for speed)")
+    B, S, H, D = q4.shape
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=True)
+    o4 = _as4d(out)
+    if o4.shape != q4.shape or o4.dtype != torch.bfloat16 or o4.is_cuda or not o4.is_contiguous():
+        raise ValueError("out must be a contiguous CPU bfloat16 tensor shaped like q")
+    chunks = head_chunks(H, chunk_heads)
+    hmax = max(h1 - h0 for h0, h1 in chunks)
+    comp = torch.cuda.current_stream(dev)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    # Two sets of staging buffers: chunk c uses set c % 2.
+    n_el = B * S * hmax * D
+    stage_in = [[torch.empty(n_el, dtype=q4.dtype, device=dev) for _ in range(3)] for _ in range(2)]
+    stage_out = [torch.empty(n_el, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    in_free = [None, None]      # compute has consumed the set's inputs
+    out_free = [None, None]     # the set's output has been copied out
+    try:
+        _stream_chunks(q4, k4, v4, o4, chunks, stage_in, stage_out, in_free, out_free, comp, s_in, s_out,
+                       softmax_scale, repair_budget)
+    finally:
+        # The staging buffers die with this frame: let every stream finish with them.
+        s_out.synchronize()
+        s_in.synchronize()
+        comp.synchronize()
+    return out
+
+
+def _stream_chunks(q4, k4, v4, o4, chunks, stage_in, stage_out, in_free, out_free, comp, s_in, s_out,
+                   softmax_scale, repair_budget):
+    B, S, H, D = q4.shape
+    el = q4.element_size()
+    for c, (h0, h1) in enumerate(chunks):
+        hc, st = h1 - h0, c % 2
+        ins = [buf[:B * S * hc * D].view(B, S, hc, D) for buf in stage_in[st]]
+        with torch.cuda.stream(s_in):
+            if in_free[st] is not None:
+                s_in.wait_event(in_free[st])
+            for src, dst in zip((q4, k4, v4), ins):
+                memcpy2d(dst.data_ptr(), hc * D * el, src.data_ptr() + h0 * D * el, H * D * el,
+                         hc * D * el, B * S, s_in)
+            ready = torch.cuda.Event()
+            ready.record(s_in)
+        comp.wait_event(ready)
+        prep = prepare(*ins)
+        rep = prepare_v_repair(ins[2], prep, repair_budget) if repair_budget else None
+        in_free[st] = torch.cuda.Event()
+        in_free[st].record(comp)
+        if out_free[st] is not None:
+            comp.wait_event(out_free[st])
+        ob = stage_out[st][:B * S * hc * D].view(B, S, hc, D)
+        if rep is not None:
+            attention_v_repair(prep, rep, softmax_scale=softmax_scale, out=ob)
+        else:
+            attention_prepared(prep, softmax_scale=softmax_scale, out=ob)
+        done = torch.cuda.Event()
+        done.record(comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(done)
+            memcpy2d(o4.data_ptr() + h0 * D * 2, H * D * 2, ob.data_ptr(), hc * D * 2, hc * D * 2,
+                     B * S, s_out)
+            out_free[st] = torch.cuda.Event()
+            out_free[st].record(s_out)
+
+
+def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, softmax_scale: float | None = None,
+              repair_budget: float | None = None, out: torch.Tensor | None = None,
+              device=None, chunk_heads: int | None = None) -> torch.Tensor:
+    """Full call: prepare + ExpCast attention (+ optional V residual repair).
+
+    CUDA inputs give a CUDA output (asynchronous on the current stream).  CPU
+    inputs (pinned for speed) are streamed through `device` (default: the
+    current CUDA device) in head chunks of `chunk_heads` heads (default: about
+    a quarter of H), so that host<->device copies overlap the computation; O
+    lands in `out` (or a new pinned tensor), complete when the call returns."""
+    if q.is_cuda:
+        return _attention_device(q, k, v, softmax_scale, repair_budget, out)
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    return _attention_host(q, k, v, softmax_scale, repair_budget, out, dev, chunk_heads)
 
 
 def flops(B: int, S: int, H: int, D: int = 128) -> float:
@@ -276,5 +365,5 @@ def flops(B: int, S: int, H: int, D: int = 128) -> float:
 
 
 __all__ = ["Prepared", "Repair", "OvcError", "prepare", "attention_prepared", "prepare_v_repair",
-           "attention_v_repair", "attention_probe", "device_status", "attention",
-           "prepare_workspace_bytes", "repair_workspace_bytes", "flops"]
+           "attention_v_repair", "attention_probe", "device_status", "attention", "memcpy2d",
+           "head_chunks", "prepare_workspace_bytes", "repair_workspace_bytes", "flops"]

@@ -200,6 +200,22 @@ ovc_status ovc_attention_probe(const ovc_prepared* p, const ovc_repair* r, float
 ovc_status ovc_prepare_noalloc(const ovc_tensor* q, const ovc_tensor* k, const ovc_tensor* v,
                                const ovc_prepared* out, void* stream);
 
+/* Strided asynchronous copy (cudaMemcpy2DAsync, direction inferred from the
+ * pointers) -- no counterpart in the pages; infrastructure for the host-buffer
+ * path of the Python binding, which streams host-resident [B,S,H,128] inputs
+ * through the GPU in head chunks so that the copies overlap the previous
+ * chunk's attention.  A head range [h0,h1) of such a tensor is height = B*S
+ * rows of width = (h1-h0)*128*elem_bytes bytes, spitch = H*128*elem_bytes
+ * apart.
+ *   dst, src: host or device pointers; host memory must be pinned for the
+ *             copy to be asynchronous (pageable memory still copies
+ *             correctly, synchronously).  width <= dpitch and width <= spitch.
+ *   stream:   a cudaStream_t (NULL: the legacy default stream).
+ * Returns OVC_OK (also when width or height is 0), OVC_ERR_INVALID_ARG, or
+ * OVC_ERR_CUDA if the copy could not be enqueued. */
+ovc_status ovc_memcpy2d(void* dst, size_t dpitch, const void* src, size_t spitch, size_t width,
+                        size_t height, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -101,3 +101,23 @@ def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_abi, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         _abi.lib()
+
+
+def test_memcpy2d_validates_on_the_host(lib):
+    from fp8_bit_attention_gb300 import _abi
+    assert lib.ovc_memcpy2d(0x1000, 64, 0x2000, 64, 0, 10, None) == _abi.OVC_OK        # nothing to copy
+    assert lib.ovc_memcpy2d(0x1000, 64, 0x2000, 64, 16, 0, None) == _abi.OVC_OK
+    assert lib.ovc_memcpy2d(0x1000, 32, 0x2000, 64, 64, 1, None) == _abi.OVC_ERR_INVALID_ARG  # width > dpitch
+    assert lib.ovc_memcpy2d(0x1000, 64, 0x2000, 32, 64, 1, None) == _abi.OVC_ERR_INVALID_ARG  # width > spitch
+    assert lib.ovc_memcpy2d(None, 64, 0x2000, 64, 64, 1, None) == _abi.OVC_ERR_INVALID_ARG
+
+
+def test_head_chunks_cover_every_head_once():
+    from fp8_bit_attention_gb300.api import head_chunks
+    for H in (1, 2, 3, 7, 14, 56, 57):
+        for n in (None, 1, 3, 64):
+            ch = head_chunks(H, n)
+            assert ch[0][0] == 0 and ch[-1][1] == H
+            assert all(a1 == b0 for (_, a1), (b0, _) in zip(ch, ch[1:]))
+            assert all(h1 > h0 for h0, h1 in ch)
+    assert len(head_chunks(56)) == 4

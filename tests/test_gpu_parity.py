@@ -161,3 +161,26 @@ def test_repair_persistent_and_plain_schedules_agree_bitwise():
     assert torch.equal(a, b)
     want, _ = oracle.attention_full(oracle_prep(q, k, v), repair=oracle.Repair(oracle_prep(q, k, v), 0.05))
     assert rel_l2(a.float().cpu().numpy(), want) <= TOL_REL_L2
+
+
+@pytest.mark.parametrize("B,H,S,chunk,budget", [(1, 7, 1000, 3, None), (2, 5, 700, 2, 0.02),
+                                                 (1, 4, 300, None, None)])
+def test_host_buffer_path_streams_head_chunks_bit_exactly(B, H, S, chunk, budget):
+    """CPU inputs go through the GPU in head chunks (copies overlapping the
+    previous chunk's attention); every head is independent, so the result
+    must equal the whole-tensor device call bit for bit."""
+    q, k, v = inputs(B, H, S, seed=31 + H)
+    qd, kd, vd = to_dev(q, k, v)
+    want = ovc.attention(qd, kd, vd, repair_budget=budget).cpu()
+    qp, kp, vp = (x.pin_memory() for x in (q, k, v))
+    got = ovc.attention(qp, kp, vp, repair_budget=budget, chunk_heads=chunk)
+    assert not got.is_cuda
+    assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+    # [S,H,128] host inputs, pageable memory (synchronous copies), caller's out
+    if B == 1:
+        out = torch.empty(q[0].shape, dtype=torch.bfloat16)
+        got3 = ovc.attention(q[0].contiguous(), k[0].contiguous(), v[0].contiguous(),
+                             repair_budget=budget, chunk_heads=chunk, out=out)
+        assert got3 is out
+        assert torch.equal(got3.view(torch.int16), want[0].view(torch.int16))
+    assert ovc.device_status() == 0
