@@ -64,18 +64,20 @@ def lib():
             L.ovc_oracle_bf16_from_double.argtypes = [d]
             L.ovc_oracle_residual_energy.restype = ctypes.c_float
             L.ovc_oracle_residual_energy.argtypes = [P]
+            L.ovc_oracle_half_bits_to_float.restype = ctypes.c_float
+            L.ovc_oracle_half_bits_to_float.argtypes = [ctypes.c_uint16]
             L.ovc_oracle_expcast_code.restype = ctypes.c_uint8
             L.ovc_oracle_expcast_code.argtypes = [d, d, d, d]
             L.ovc_oracle_quantize_blocks.restype = None
-            L.ovc_oracle_quantize_blocks.argtypes = [P, i64, i64, i64, i64, i64, i64, P, P]
+            L.ovc_oracle_quantize_blocks.argtypes = [P, ctypes.c_int, i64, i64, i64, i64, i64, i64, P, P]
             L.ovc_oracle_quantize_v.restype = None
-            L.ovc_oracle_quantize_v.argtypes = [P, i64, i64, i64, i64, i64, i64, P, P, P]
+            L.ovc_oracle_quantize_v.argtypes = [P, ctypes.c_int, i64, i64, i64, i64, i64, i64, P, P, P]
             L.ovc_oracle_repair_count.restype = i64
             L.ovc_oracle_repair_count.argtypes = [i64, ctypes.c_float]
             L.ovc_oracle_repair_select.restype = None
             L.ovc_oracle_repair_select.argtypes = [P, i64, i64, i64, P]
             L.ovc_oracle_repair_quantize.restype = None
-            L.ovc_oracle_repair_quantize.argtypes = [P, i64, i64, i64, i64, i64, i64, P, P, P,
+            L.ovc_oracle_repair_quantize.argtypes = [P, ctypes.c_int, i64, i64, i64, i64, i64, i64, P, P, P,
                                                      i64, P, P]
             L.ovc_oracle_block_codes.restype = None
             L.ovc_oracle_block_codes.argtypes = [P, ctypes.c_float, P, P, i64, i64, d, d, d, d, P]
@@ -147,26 +149,32 @@ def residual_energy(R: np.ndarray) -> np.float32:
 # --------------------------------------------------------------------------
 # Quantisation (FP32-defined)
 # --------------------------------------------------------------------------
+def half_bits_to_float(bits: int) -> float:
+    """IEEE binary16 bits -> value (the oracle's own decoder)."""
+    return float(lib().ovc_oracle_half_bits_to_float(int(bits)))
+
+
 def _bf16_view(x: np.ndarray):
-    """x: uint16 array of BF16 bits shaped [B,S,H,128] (any strides, unit last)."""
+    """x: uint16 array of BF16 (or FP16) bits shaped [B,S,H,128] (any strides, unit last)."""
     assert x.dtype == np.uint16 and x.ndim == 4 and x.shape[3] == 128
     assert x.strides[3] == 2
     sb, ss, sh = (s // 2 for s in x.strides[:3])
     return x, sb, ss, sh
 
 
-def quantize_blocks(x: np.ndarray):
-    """Q or K -> (codes [B,H,S_pad,128] uint8, scales [B,H,nb] float32)."""
+def quantize_blocks(x: np.ndarray, fp16: bool = False):
+    """Q or K (BF16 bits, or FP16 bits if fp16) -> (codes [B,H,S_pad,128] uint8,
+    scales [B,H,nb] float32)."""
     x, sb, ss, sh = _bf16_view(x)
     B, S, H, _ = x.shape
     nb = (S + 127) // 128
     codes = np.zeros((B, H, nb * 128, 128), np.uint8)
     scales = np.zeros((B, H, nb), np.float32)
-    lib().ovc_oracle_quantize_blocks(_ptr(x), B, S, H, sb, ss, sh, _ptr(codes), _ptr(scales))
+    lib().ovc_oracle_quantize_blocks(_ptr(x), int(fp16), B, S, H, sb, ss, sh, _ptr(codes), _ptr(scales))
     return codes, scales
 
 
-def quantize_v(v: np.ndarray):
+def quantize_v(v: np.ndarray, fp16: bool = False):
     """V -> (codes token-major [B,H,S_pad,128], sv [B,H], energy [B,H,S])."""
     v, sb, ss, sh = _bf16_view(v)
     B, S, H, _ = v.shape
@@ -174,7 +182,7 @@ def quantize_v(v: np.ndarray):
     codes = np.zeros((B, H, nb * 128, 128), np.uint8)
     sv = np.zeros((B, H), np.float32)
     energy = np.zeros((B, H, S), np.float32)
-    lib().ovc_oracle_quantize_v(_ptr(v), B, S, H, sb, ss, sh, _ptr(codes), _ptr(sv), _ptr(energy))
+    lib().ovc_oracle_quantize_v(_ptr(v), int(fp16), B, S, H, sb, ss, sh, _ptr(codes), _ptr(sv), _ptr(energy))
     return codes, sv, energy
 
 
@@ -191,7 +199,7 @@ def repair_select(energy: np.ndarray, n: int) -> np.ndarray:
     return idx
 
 
-def repair_quantize(v: np.ndarray, vcodes: np.ndarray, sv: np.ndarray, idx: np.ndarray):
+def repair_quantize(v: np.ndarray, vcodes: np.ndarray, sv: np.ndarray, idx: np.ndarray, fp16: bool = False):
     """-> (dcodes [B,H,n,128] uint8, sr [B,H] float32)."""
     v, sb, ss, sh = _bf16_view(v)
     B, S, H, _ = v.shape
@@ -200,7 +208,7 @@ def repair_quantize(v: np.ndarray, vcodes: np.ndarray, sv: np.ndarray, idx: np.n
     idx = np.ascontiguousarray(idx, dtype=np.int32)
     dcodes = np.zeros((B, H, n, 128), np.uint8)
     sr = np.zeros((B, H), np.float32)
-    lib().ovc_oracle_repair_quantize(_ptr(v), B, S, H, sb, ss, sh, _ptr(vcodes),
+    lib().ovc_oracle_repair_quantize(_ptr(v), int(fp16), B, S, H, sb, ss, sh, _ptr(vcodes),
                                      _ptr(np.ascontiguousarray(sv, dtype=np.float32)),
                                      _ptr(idx), n, _ptr(dcodes), _ptr(sr))
     return dcodes, sr
@@ -212,12 +220,14 @@ def repair_quantize(v: np.ndarray, vcodes: np.ndarray, sv: np.ndarray, idx: np.n
 class Prepared:
     """The oracle's own quantised tensors for one (Q, K, V) triple."""
 
-    def __init__(self, q, k, v):
+    def __init__(self, q, k, v, fp16: bool = False):
+        """q, k, v: uint16 bits [B,S,H,128] of BF16 inputs, or of FP16 ones if fp16."""
         self.B, self.S, self.H, _ = q.shape
         self.nb = (self.S + 127) // 128
-        self.qc, self.sq = quantize_blocks(q)
-        self.kc, self.sk = quantize_blocks(k)
-        self.vc, self.sv, self.energy = quantize_v(v)
+        self.fp16 = bool(fp16)
+        self.qc, self.sq = quantize_blocks(q, fp16)
+        self.kc, self.sk = quantize_blocks(k, fp16)
+        self.vc, self.sv, self.energy = quantize_v(v, fp16)
         self.v = v
 
 
@@ -225,7 +235,7 @@ class Repair:
     def __init__(self, prep: Prepared, budget: float):
         self.n = repair_count(prep.S, budget)
         self.idx = repair_select(prep.energy, self.n)
-        self.dcodes, self.sr = repair_quantize(prep.v, prep.vc, prep.sv, self.idx)
+        self.dcodes, self.sr = repair_quantize(prep.v, prep.vc, prep.sv, self.idx, prep.fp16)
 
 
 def attention_rows(prep: Prepared, rows_bh, rows_s, *, sm=None, repair: Repair | None = None,

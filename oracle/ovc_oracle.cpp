@@ -104,6 +104,22 @@ float bf16_bits_to_float(uint16_t b) {
   return f;
 }
 
+// IEEE binary16 bits -> value, from the format definition: 1 sign bit, 5
+// exponent bits (bias 15), 10 fraction bits; exponent 0 is subnormal
+// (f * 2^-24), exponent 31 is Inf/NaN.  Every binary16 value is exact in FP32.
+float half_bits_to_float(uint16_t h) {
+  const int sign = h >> 15, e = (h >> 10) & 31, f = h & 1023;
+  double v;
+  if (e == 0) v = std::ldexp(static_cast<double>(f), -24);
+  else if (e == 31) v = f ? NAN : INFINITY;
+  else v = std::ldexp(1.0 + f / 1024.0, e - 15);
+  return static_cast<float>(sign ? -v : v);
+}
+
+// Input element (BF16 or FP16 bits, the two input types of the API
+// ["Open VC Attention" catalogue entry: FP16 or BF16 inputs]) -> FP32.
+float input_bits_to_float(uint16_t b, int fp16) { return fp16 ? half_bits_to_float(b) : bf16_bits_to_float(b); }
+
 // double -> BF16 with a single round to nearest even.
 uint16_t bf16_from_double(double x) {
   if (std::isnan(x)) return 0x7FC0;
@@ -356,6 +372,7 @@ double ovc_oracle_e4m3_value(uint8_t code) { return e4m3_value(code); }
 uint8_t ovc_oracle_e4m3_from_float(float x) { return e4m3_from_float(x); }
 uint16_t ovc_oracle_bf16_from_double(double x) { return bf16_from_double(x); }
 float ovc_oracle_residual_energy(const float* R) { return residual_energy(R); }
+float ovc_oracle_half_bits_to_float(uint16_t h) { return half_bits_to_float(h); }
 
 // ExpCast code of one score: clamp(rint(Z - m8 + c0 + beta), 0, 126).
 uint8_t ovc_oracle_expcast_code(double Z, double m8, double c0, double beta) {
@@ -365,10 +382,10 @@ uint8_t ovc_oracle_expcast_code(double Z, double m8, double c0, double beta) {
   return code;
 }
 
-// Q or K quantisation.  x: BF16 bits of a [B,S,H,128] tensor with element
+// Q or K quantisation.  x: BF16 (fp16 = 0) or FP16 bits of a [B,S,H,128] tensor with element
 // strides (sb, ss, sh) and unit channel stride.  codes: [B,H,S_pad,128], rows
 // >= S are zero.  scales: [B,H,nb].
-void ovc_oracle_quantize_blocks(const uint16_t* x, int64_t B, int64_t S, int64_t H, int64_t sb,
+void ovc_oracle_quantize_blocks(const uint16_t* x, int fp16, int64_t B, int64_t S, int64_t H, int64_t sb,
                                 int64_t ss, int64_t sh, uint8_t* codes, float* scales) {
   const Dims dm = make_dims(B, S, H);
   for (int64_t b = 0; b < B; ++b)
@@ -378,20 +395,20 @@ void ovc_oracle_quantize_blocks(const uint16_t* x, int64_t B, int64_t S, int64_t
         float amax = 0.0f;
         for (int64_t t = t0; t < t1; ++t)
           for (int d = 0; d < 128; ++d)
-            amax = std::max(amax, std::fabs(bf16_bits_to_float(x[b * sb + t * ss + h * sh + d])));
+            amax = std::max(amax, std::fabs(input_bits_to_float(x[b * sb + t * ss + h * sh + d], fp16)));
         const Scale sc = scale_from_amax(amax);
         scales[(b * H + h) * dm.nb + j] = sc.s;
         uint8_t* out = codes + ((b * H + h) * dm.S_pad + t0) * 128;
         for (int64_t t = t0; t < t0 + 128; ++t)
           for (int d = 0; d < 128; ++d)
             out[(t - t0) * 128 + d] =
-                (t < S) ? quantize_value(bf16_bits_to_float(x[b * sb + t * ss + h * sh + d]), sc.r) : 0;
+                (t < S) ? quantize_value(input_bits_to_float(x[b * sb + t * ss + h * sh + d], fp16), sc.r) : 0;
       }
 }
 
 // V quantisation with one scale per head.  codes: token-major [B,H,S_pad,128]
 // (rows >= S zero); sv: [B,H]; energy: [B,H,S] residual energy per token.
-void ovc_oracle_quantize_v(const uint16_t* v, int64_t B, int64_t S, int64_t H, int64_t sb,
+void ovc_oracle_quantize_v(const uint16_t* v, int fp16, int64_t B, int64_t S, int64_t H, int64_t sb,
                            int64_t ss, int64_t sh, uint8_t* codes, float* sv, float* energy) {
   const Dims dm = make_dims(B, S, H);
   for (int64_t b = 0; b < B; ++b)
@@ -399,7 +416,7 @@ void ovc_oracle_quantize_v(const uint16_t* v, int64_t B, int64_t S, int64_t H, i
       float amax = 0.0f;
       for (int64_t t = 0; t < S; ++t)
         for (int d = 0; d < 128; ++d)
-          amax = std::max(amax, std::fabs(bf16_bits_to_float(v[b * sb + t * ss + h * sh + d])));
+          amax = std::max(amax, std::fabs(input_bits_to_float(v[b * sb + t * ss + h * sh + d], fp16)));
       const Scale sc = scale_from_amax(amax);
       sv[b * H + h] = sc.s;
       uint8_t* out = codes + (b * H + h) * dm.S_pad * 128;
@@ -407,7 +424,7 @@ void ovc_oracle_quantize_v(const uint16_t* v, int64_t B, int64_t S, int64_t H, i
         float R[128];
         for (int d = 0; d < 128; ++d) {
           if (t < S) {
-            const float x = bf16_bits_to_float(v[b * sb + t * ss + h * sh + d]);
+            const float x = input_bits_to_float(v[b * sb + t * ss + h * sh + d], fp16);
             const uint8_t c = quantize_value(x, sc.r);
             out[t * 128 + d] = c;
             R[d] = v_residual(x, c, sc.s);
@@ -445,7 +462,7 @@ void ovc_oracle_repair_select(const float* energy, int64_t BH, int64_t S, int64_
 // Repair quantisation: residuals of the selected tokens, one scale per head
 // s_r = amax|R_sel| / 448, codes E4M3(fl(R * r_r)).  vcodes: token-major
 // [B,H,S_pad,128]; idx: [B,H,n]; dcodes: [B,H,n,128]; sr: [B,H].
-void ovc_oracle_repair_quantize(const uint16_t* v, int64_t B, int64_t S, int64_t H, int64_t sb,
+void ovc_oracle_repair_quantize(const uint16_t* v, int fp16, int64_t B, int64_t S, int64_t H, int64_t sb,
                                 int64_t ss, int64_t sh, const uint8_t* vcodes, const float* sv,
                                 const int32_t* idx, int64_t n, uint8_t* dcodes, float* sr) {
   const Dims dm = make_dims(B, S, H);
@@ -457,7 +474,7 @@ void ovc_oracle_repair_quantize(const uint16_t* v, int64_t B, int64_t S, int64_t
       for (int64_t i = 0; i < n; ++i) {
         const int64_t t = idx[bh * n + i];
         for (int d = 0; d < 128; ++d) {
-          const float x = bf16_bits_to_float(v[b * sb + t * ss + h * sh + d]);
+          const float x = input_bits_to_float(v[b * sb + t * ss + h * sh + d], fp16);
           R[i * 128 + d] = v_residual(x, vcodes[(bh * dm.S_pad + t) * 128 + d], sv[bh]);
           amax = std::max(amax, std::fabs(R[i * 128 + d]));
         }

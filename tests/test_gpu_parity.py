@@ -184,3 +184,34 @@ def test_host_buffer_path_streams_head_chunks_bit_exactly(B, H, S, chunk, budget
         assert got3 is out
         assert torch.equal(got3.view(torch.int16), want[0].view(torch.int16))
     assert ovc.device_status() == 0
+
+
+@pytest.mark.parametrize("B,H,S", [(1, 2, 1000), (2, 1, 300)])
+def test_fp16_inputs_match_oracle(B, H, S):
+    """FP16 inputs ("Open VC Attention" catalogue entry: FP16 or BF16):
+    quantised codes, scales, energies and repair indices bit-exact against
+    the oracle's FP16 path; O within relative L2 5e-3."""
+    q, k, v = (x.to(torch.float16) for x in inputs(B, H, S, seed=57 + S))
+    bits = [x.contiguous().view(torch.int16).numpy().view(np.uint16) for x in (q, k, v)]
+    ref = oracle.Prepared(*bits, fp16=True)
+    qd, kd, vd = to_dev(q, k, v)
+    prep = ovc.prepare(qd, kd, vd)
+    assert np.array_equal(prep.q_codes().cpu().numpy(), ref.qc[:, :, :, :])
+    assert np.array_equal(prep.k_codes().cpu().numpy(), ref.kc)
+    assert np.array_equal(prep.vt_codes().cpu().numpy().transpose(0, 1, 3, 2), ref.vc)
+    assert np.array_equal(prep.q_scales().cpu().numpy(), ref.sq)
+    assert np.array_equal(prep.k_scales().cpu().numpy(), ref.sk)
+    assert np.array_equal(prep.v_scales().cpu().numpy(), ref.sv)
+    assert np.array_equal(prep.energy().cpu().numpy().view(np.uint32), ref.energy.view(np.uint32))
+    o = ovc.attention_prepared(prep).float().cpu().numpy()
+    bh = np.repeat(np.arange(B * H), S)
+    ss = np.tile(np.arange(S), B * H)
+    r = oracle.attention_rows(ref, bh, ss)["out"].reshape(B, H, S, 128).transpose(0, 2, 1, 3)
+    assert rel_l2(o, r) <= TOL_REL_L2
+    rep = ovc.prepare_v_repair(vd, prep, 0.02)
+    rr = oracle.Repair(ref, 0.02)
+    assert np.array_equal(rep.idx().cpu().numpy(), rr.idx)
+    assert np.array_equal(rep.sr().cpu().numpy(), rr.sr)
+    orep = ovc.attention_v_repair(prep, rep).float().cpu().numpy()
+    rrep = oracle.attention_rows(ref, bh, ss, repair=rr)["out"].reshape(B, H, S, 128).transpose(0, 2, 1, 3)
+    assert rel_l2(orep, rrep) <= TOL_REL_L2

@@ -142,3 +142,39 @@ def test_repair_quantize_scale_and_codes():
         assert np.array_equal(dcodes[0, h], _cast(R * (np.float32(448.0) / amax)))
         # the selected tokens carry the largest energies
         assert energy[0, h, t].min() >= np.delete(energy[0, h], t).max()
+
+
+def test_half_decoder_matches_ieee_binary16_on_every_pattern():
+    """The oracle's FP16 decoder (written from the format definition) against
+    numpy's binary16 on all 65536 bit patterns; NaNs as NaNs."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    want = bits.view(np.float16).astype(np.float32)
+    got = np.array([oracle.half_bits_to_float(int(b)) for b in bits], np.float32)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan].view(np.uint32), want[~nan].view(np.uint32))
+
+
+def test_fp16_and_bf16_inputs_quantise_alike_on_shared_values():
+    """Values exact in both formats give the same codes, scales and energies
+    through the FP16 and the BF16 paths ("Open VC Attention" catalogue entry:
+    FP16 or BF16 inputs)."""
+    rng = np.random.default_rng(11)
+    # m * 2^e with |m| < 128, -6 <= e <= 2: at most 8 significant bits (exact
+    # in BF16) and inside FP16's normal range
+    m = rng.integers(-127, 128, (1, 200, 2, 128)).astype(np.float64)
+    e = rng.integers(-6, 3, (1, 200, 2, 128))
+    x = np.ldexp(m, e).astype(np.float32)
+    xb = torch.from_numpy(x).to(torch.bfloat16)
+    xh = torch.from_numpy(x).to(torch.float16)
+    assert np.array_equal(xb.float().numpy(), x) and np.array_equal(xh.float().numpy(), x)
+    cb, sb = oracle.quantize_blocks(_bits(xb))
+    ch, sh = oracle.quantize_blocks(_bits(xh), fp16=True)
+    assert np.array_equal(cb, ch) and np.array_equal(sb, sh)
+    vb = oracle.quantize_v(_bits(xb))
+    vh = oracle.quantize_v(_bits(xh), fp16=True)
+    for a, b in zip(vb, vh):
+        assert np.array_equal(a, b)
+    # and they differ once the bits are misread: the flag is honoured
+    cx, _ = oracle.quantize_blocks(_bits(xh))
+    assert not np.array_equal(cx, ch)
