@@ -69,7 +69,9 @@ def lib():
             L.ovc_oracle_expcast_code.restype = ctypes.c_uint8
             L.ovc_oracle_expcast_code.argtypes = [d, d, d, d]
             L.ovc_oracle_quantize_blocks.restype = None
-            L.ovc_oracle_quantize_blocks.argtypes = [P, ctypes.c_int, i64, i64, i64, i64, i64, i64, P, P]
+            L.ovc_oracle_quantize_blocks.argtypes = [P, ctypes.c_int, i64, i64, i64, i64, i64, i64, P, P, P]
+            L.ovc_oracle_k_mean.restype = None
+            L.ovc_oracle_k_mean.argtypes = [P, ctypes.c_int, i64, i64, i64, i64, i64, i64, P]
             L.ovc_oracle_quantize_v.restype = None
             L.ovc_oracle_quantize_v.argtypes = [P, ctypes.c_int, i64, i64, i64, i64, i64, i64, P, P, P]
             L.ovc_oracle_repair_count.restype = i64
@@ -162,15 +164,30 @@ def _bf16_view(x: np.ndarray):
     return x, sb, ss, sh
 
 
-def quantize_blocks(x: np.ndarray, fp16: bool = False):
-    """Q or K (BF16 bits, or FP16 bits if fp16) -> (codes [B,H,S_pad,128] uint8,
-    scales [B,H,nb] float32)."""
+def k_mean(x: np.ndarray, fp16: bool = False) -> np.ndarray:
+    """Channel means of K over the sequence, [B,H,128] float32 (K smoothing;
+    FP32 block sums in token order, then over blocks, then / S)."""
+    x, sb, ss, sh = _bf16_view(x)
+    B, S, H, _ = x.shape
+    mean = np.zeros((B, H, 128), np.float32)
+    lib().ovc_oracle_k_mean(_ptr(x), int(fp16), B, S, H, sb, ss, sh, _ptr(mean))
+    return mean
+
+
+def quantize_blocks(x: np.ndarray, fp16: bool = False, mean: np.ndarray | None = None):
+    """Q or K (BF16 bits, or FP16 bits if fp16; minus `mean` [B,H,128] if given)
+    -> (codes [B,H,S_pad,128] uint8, scales [B,H,nb] float32)."""
     x, sb, ss, sh = _bf16_view(x)
     B, S, H, _ = x.shape
     nb = (S + 127) // 128
     codes = np.zeros((B, H, nb * 128, 128), np.uint8)
     scales = np.zeros((B, H, nb), np.float32)
-    lib().ovc_oracle_quantize_blocks(_ptr(x), int(fp16), B, S, H, sb, ss, sh, _ptr(codes), _ptr(scales))
+    mp = None
+    if mean is not None:
+        mean = np.ascontiguousarray(mean, dtype=np.float32)
+        assert mean.shape == (B, H, 128)
+        mp = _ptr(mean)
+    lib().ovc_oracle_quantize_blocks(_ptr(x), int(fp16), B, S, H, sb, ss, sh, mp, _ptr(codes), _ptr(scales))
     return codes, scales
 
 
@@ -220,13 +237,15 @@ def repair_quantize(v: np.ndarray, vcodes: np.ndarray, sv: np.ndarray, idx: np.n
 class Prepared:
     """The oracle's own quantised tensors for one (Q, K, V) triple."""
 
-    def __init__(self, q, k, v, fp16: bool = False):
-        """q, k, v: uint16 bits [B,S,H,128] of BF16 inputs, or of FP16 ones if fp16."""
+    def __init__(self, q, k, v, fp16: bool = False, smooth_k: bool = False):
+        """q, k, v: uint16 bits [B,S,H,128] of BF16 inputs, or of FP16 ones if
+        fp16.  smooth_k: subtract K's channel means before quantising K."""
         self.B, self.S, self.H, _ = q.shape
         self.nb = (self.S + 127) // 128
         self.fp16 = bool(fp16)
+        self.kmean = k_mean(k, fp16) if smooth_k else None
         self.qc, self.sq = quantize_blocks(q, fp16)
-        self.kc, self.sk = quantize_blocks(k, fp16)
+        self.kc, self.sk = quantize_blocks(k, fp16, self.kmean)
         self.vc, self.sv, self.energy = quantize_v(v, fp16)
         self.v = v
 

@@ -382,27 +382,59 @@ uint8_t ovc_oracle_expcast_code(double Z, double m8, double c0, double beta) {
   return code;
 }
 
+// K smoothing (optional; prior art the VC-Attention summary names in "Why
+// attention is the video bottleneck": earlier low-bit kernels smooth Q and K).
+// For non-causal attention, subtracting a per-channel constant mu from every
+// key changes each score row by the constant q.mu, so the softmax is
+// unchanged; what changes is the quantisation, whose per-block amax no
+// longer carries the channel offset.  mu is defined in FP32 with a fixed
+// order: per 128-token block a sequential sum over its tokens, then a
+// sequential sum of the block sums, then one division by S.
+//   mean: [B,H,128]
+void ovc_oracle_k_mean(const uint16_t* x, int fp16, int64_t B, int64_t S, int64_t H, int64_t sb,
+                       int64_t ss, int64_t sh, float* mean) {
+  const Dims dm = make_dims(B, S, H);
+  for (int64_t b = 0; b < B; ++b)
+    for (int64_t h = 0; h < H; ++h)
+      for (int d = 0; d < 128; ++d) {
+        volatile float total = 0.0f;
+        for (int64_t j = 0; j < dm.nb; ++j) {
+          volatile float part = 0.0f;
+          for (int64_t t = j * 128; t < std::min(S, j * 128 + 128); ++t)
+            part = part + input_bits_to_float(x[b * sb + t * ss + h * sh + d], fp16);
+          total = total + part;
+        }
+        volatile float m = total / static_cast<float>(S);
+        mean[(b * H + h) * 128 + d] = m;
+      }
+}
+
 // Q or K quantisation.  x: BF16 (fp16 = 0) or FP16 bits of a [B,S,H,128] tensor with element
-// strides (sb, ss, sh) and unit channel stride.  codes: [B,H,S_pad,128], rows
-// >= S are zero.  scales: [B,H,nb].
+// strides (sb, ss, sh) and unit channel stride; mean: NULL, or [B,H,128]
+// channel means subtracted (in FP32) before quantising (K smoothing).
+// codes: [B,H,S_pad,128], rows >= S are zero.  scales: [B,H,nb].
 void ovc_oracle_quantize_blocks(const uint16_t* x, int fp16, int64_t B, int64_t S, int64_t H, int64_t sb,
-                                int64_t ss, int64_t sh, uint8_t* codes, float* scales) {
+                                int64_t ss, int64_t sh, const float* mean, uint8_t* codes, float* scales) {
   const Dims dm = make_dims(B, S, H);
   for (int64_t b = 0; b < B; ++b)
     for (int64_t h = 0; h < H; ++h)
       for (int64_t j = 0; j < dm.nb; ++j) {
         const int64_t t0 = j * 128, t1 = std::min(S, t0 + 128);
+        const float* mu = mean ? mean + (b * H + h) * 128 : nullptr;
+        auto value = [&](int64_t t, int d) {
+          const float v = input_bits_to_float(x[b * sb + t * ss + h * sh + d], fp16);
+          if (!mu) return v;
+          volatile float r = v - mu[d];
+          return static_cast<float>(r);
+        };
         float amax = 0.0f;
         for (int64_t t = t0; t < t1; ++t)
-          for (int d = 0; d < 128; ++d)
-            amax = std::max(amax, std::fabs(input_bits_to_float(x[b * sb + t * ss + h * sh + d], fp16)));
+          for (int d = 0; d < 128; ++d) amax = std::max(amax, std::fabs(value(t, d)));
         const Scale sc = scale_from_amax(amax);
         scales[(b * H + h) * dm.nb + j] = sc.s;
         uint8_t* out = codes + ((b * H + h) * dm.S_pad + t0) * 128;
         for (int64_t t = t0; t < t0 + 128; ++t)
-          for (int d = 0; d < 128; ++d)
-            out[(t - t0) * 128 + d] =
-                (t < S) ? quantize_value(input_bits_to_float(x[b * sb + t * ss + h * sh + d], fp16), sc.r) : 0;
+          for (int d = 0; d < 128; ++d) out[(t - t0) * 128 + d] = (t < S) ? quantize_value(value(t, d), sc.r) : 0;
       }
 }
 

@@ -199,3 +199,35 @@ def test_repair_reduces_error_against_exact_attention():
         errs.append(np.linalg.norm(out - ref) / np.linalg.norm(ref))
     assert errs[1] < errs[0] and errs[2] < errs[1]
     assert 0.005 < errs[0] < 0.15
+
+
+def test_k_smoothing_leaves_exact_attention_unchanged():
+    """Subtracting a per-channel constant from every key shifts each score
+    row by a constant, so exact softmax attention is unchanged (the reason K
+    smoothing is admissible for non-causal attention)."""
+    q, k, v = _inputs(1, 300, 2, 41, bias=3.0)
+    mean = oracle.k_mean(_bits(k))
+    qf, kf, vf = (x.to(torch.float64).numpy()[0].transpose(1, 0, 2) for x in (q, k, v))
+    kc = kf - mean[0][:, None, :].astype(np.float64)
+    rows_s = np.arange(0, 300, 7)
+    rows_bh = np.arange(rows_s.size) % 2
+    a = oracle.attention_exact_rows(qf, kf, vf, rows_bh, rows_s)[0]
+    b = oracle.attention_exact_rows(qf, kc, vf, rows_bh, rows_s)[0]
+    assert np.abs(a - b).max() <= 1e-10 * np.abs(a).max()
+
+
+def test_k_smoothing_reduces_error_on_biased_keys():
+    """With a per-channel key offset (the workloads' bias N(0, var 2)),
+    smoothing K before quantisation lowers the error against exact attention."""
+    q, k, v = _inputs(1, 1024, 2, 43, bias=np.sqrt(2.0))
+    qf, kf, vf = (x.to(torch.float64).numpy() for x in (q, k, v))
+    rows_s = np.arange(0, 1024, 11)
+    rows_bh = np.arange(rows_s.size) % 2
+    ref = np.stack([_softmax_attention(qf[0, :, bh], kf[0, :, bh], vf[0, :, bh])[s]
+                    for bh, s in zip(rows_bh, rows_s)])
+    errs = []
+    for smooth in (False, True):
+        prep = oracle.Prepared(_bits(q), _bits(k), _bits(v), smooth_k=smooth)
+        out = oracle.attention_rows(prep, rows_bh, rows_s)["out"]
+        errs.append(np.linalg.norm(out - ref) / np.linalg.norm(ref))
+    assert errs[1] < 0.9 * errs[0]

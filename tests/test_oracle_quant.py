@@ -178,3 +178,38 @@ def test_fp16_and_bf16_inputs_quantise_alike_on_shared_values():
     # and they differ once the bits are misread: the flag is honoured
     cx, _ = oracle.quantize_blocks(_bits(xh))
     assert not np.array_equal(cx, ch)
+
+
+def test_k_mean_is_the_channel_mean_to_fp32_rounding():
+    """K smoothing's channel means against float64 means (sum of S terms in
+    FP32: error below S * 2^-23 * max|partial|), and exact on tiny inputs."""
+    rng = np.random.default_rng(5)
+    for S in (1, 2, 3, 129, 1000):
+        x = _bf16(rng.standard_normal((2, S, 3, 128)) + 4.0 * rng.standard_normal((1, 1, 3, 128)))
+        mean = oracle.k_mean(_bits(x))
+        xf = _f32(x).astype(np.float64)
+        ref = xf.mean(axis=1)                           # [B, H, 128]
+        bound = S * 2.0 ** -23 * (np.abs(xf).sum(axis=1) / S + 1e-30) * 2
+        assert np.all(np.abs(mean - ref) <= bound + 1e-12)
+        if S <= 2:       # a sum of at most 2 BF16 values is exact in FP32, and so is /1 or /2
+            assert np.array_equal(mean, ref.astype(np.float32))
+
+
+def test_smoothed_k_codes_are_casts_of_the_centred_values():
+    """quantize_blocks(x, mean): codes equal torch's E4M3 casts of
+    fl(fl(x - mean) * 448/amax) with amax over the centred block."""
+    rng = np.random.default_rng(8)
+    S, H = 300, 2
+    x = _bf16(rng.standard_normal((1, S, H, 128)) + 5.0 * rng.standard_normal((1, 1, H, 128)))
+    mean = oracle.k_mean(_bits(x))
+    codes, scales = oracle.quantize_blocks(_bits(x), mean=mean)
+    xc = (_f32(x) - mean[:, None, :, :]).astype(np.float32)
+    for h in range(H):
+        for j in range(3):
+            blk = xc[0, j * 128:(j + 1) * 128, h, :]
+            amax = np.float32(np.abs(blk).max())
+            assert scales[0, h, j] == np.float32(amax / np.float32(448.0))
+            assert np.array_equal(codes[0, h, j * 128:j * 128 + blk.shape[0]], _cast(blk * (np.float32(448.0) / amax)))
+    # the offset no longer sets the scale: centred blocks use finer steps
+    _, raw_scales = oracle.quantize_blocks(_bits(x))
+    assert np.all(scales < raw_scales)
