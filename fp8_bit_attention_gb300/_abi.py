@@ -19,6 +19,7 @@ OVC_ERR_CUDA = 4
 OVC_ERR_TIMEOUT = 5
 OVC_ERR_SCRATCH_LIMIT = 6
 OVC_NOALLOC_MAX_HEADS = 4096
+OVC_PREPARE_SMOOTH_K = 1
 OVC_BF16 = 0
 OVC_FP16 = 1
 
@@ -65,6 +66,9 @@ SIGNATURES = {
     "ovc_attention_probe": (c_i32, [P(OvcPrepared), P(OvcRepair), ctypes.c_float, P(OvcOutput),
                                     P(OvcProbe), c_ptr]),
     "ovc_prepare_noalloc": (c_i32, [P(OvcTensor), P(OvcTensor), P(OvcTensor), P(OvcPrepared), c_ptr]),
+    "ovc_prepare_workspace_bytes_ex": (ctypes.c_size_t, [c_i64, c_i64, c_i64, c_i64, ctypes.c_uint32]),
+    "ovc_prepare_ex": (c_i32, [P(OvcTensor), P(OvcTensor), P(OvcTensor), ctypes.c_uint32, c_ptr,
+                               ctypes.c_size_t, P(OvcPrepared), c_ptr]),
     "ovc_memcpy2d": (c_i32, [c_ptr, ctypes.c_size_t, c_ptr, ctypes.c_size_t, ctypes.c_size_t,
                              ctypes.c_size_t, c_ptr]),
 }

@@ -134,24 +134,31 @@ class Repair:
         return _view(self.workspace, d.sr, 4 * d.B * d.H).view(torch.float32).view(d.B, d.H)
 
 
-def prepare_workspace_bytes(B: int, S: int, H: int) -> int:
-    return int(lib().ovc_prepare_workspace_bytes(B, S, H, 128))
+def prepare_workspace_bytes(B: int, S: int, H: int, *, smooth_k: bool = False) -> int:
+    return int(lib().ovc_prepare_workspace_bytes_ex(B, S, H, 128, _prep_flags(smooth_k)))
 
 
-def prepare(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, workspace: torch.Tensor | None = None,
-            stream=None) -> Prepared:
-    """Quantise Q/K (per 128-token block) and V (per head) to E4M3 (ovc_prepare)."""
+def _prep_flags(smooth_k: bool) -> int:
+    return _abi.OVC_PREPARE_SMOOTH_K if smooth_k else 0
+
+
+def prepare(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, smooth_k: bool = False,
+            workspace: torch.Tensor | None = None, stream=None) -> Prepared:
+    """Quantise Q/K (per 128-token block) and V (per head) to E4M3
+    (ovc_prepare_ex).  smooth_k subtracts K's channel means first (optional
+    K smoothing; exact non-causal attention is unchanged by it)."""
     tq, tk, tv = _tensor_desc(q), _tensor_desc(k), _tensor_desc(v)
-    nbytes = prepare_workspace_bytes(tq.B, tq.S, tq.H)
+    flags = _prep_flags(smooth_k)
+    nbytes = prepare_workspace_bytes(tq.B, tq.S, tq.H, smooth_k=smooth_k)
     if nbytes == 0:
         raise ValueError(f"unsupported shape {tuple(q.shape)}")
     if workspace is None:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
     desc = _abi.OvcPrepared()
-    st = lib().ovc_prepare(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv),
-                           ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
-                           ctypes.byref(desc), ctypes.c_void_p(_stream_handle(stream)))
-    check(st, "ovc_prepare")
+    st = lib().ovc_prepare_ex(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv), flags,
+                              ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
+                              ctypes.byref(desc), ctypes.c_void_p(_stream_handle(stream)))
+    check(st, "ovc_prepare_ex")
     return Prepared(desc, workspace, tuple(q.shape), q.dtype)
 
 
@@ -255,15 +262,15 @@ def head_chunks(H: int, chunk_heads: int | None = None) -> list[tuple[int, int]]
     return [(h0, min(H, h0 + n)) for h0 in range(0, H, n)]
 
 
-def _attention_device(q, k, v, softmax_scale, repair_budget, out):
-    prep = prepare(q, k, v)
+def _attention_device(q, k, v, softmax_scale, repair_budget, out, smooth_k=False):
+    prep = prepare(q, k, v, smooth_k=smooth_k)
     if repair_budget:
         rep = prepare_v_repair(v, prep, repair_budget)
         return attention_v_repair(prep, rep, softmax_scale=softmax_scale, out=out)
     return attention_prepared(prep, softmax_scale=softmax_scale, out=out)
 
 
-def _attention_host(q, k, v, softmax_scale, repair_budget, out, dev, chunk_heads):
+def _attention_host(q, k, v, softmax_scale, repair_budget, out, dev, chunk_heads, smooth_k=False):
     """Host-resident inputs streamed through the GPU in head chunks.
 
     Every head is computed independently (its V scale, residual ranking and
@@ -297,7 +304,7 @@ def _attention_host(q, k, v, softmax_scale, repair_budget, out, dev, chunk_heads
     out_free = [None, None]     # the set's output has been copied out
     try:
         _stream_chunks(q4, k4, v4, o4, chunks, stage_in, stage_out, in_free, out_free, comp, s_in, s_out,
-                       softmax_scale, repair_budget)
+                       softmax_scale, repair_budget, smooth_k)
     finally:
         # The staging buffers die with this frame: let every stream finish with them.
         s_out.synchronize()
@@ -307,7 +314,7 @@ def _attention_host(q, k, v, softmax_scale, repair_budget, out, dev, chunk_heads
 
 
 def _stream_chunks(q4, k4, v4, o4, chunks, stage_in, stage_out, in_free, out_free, comp, s_in, s_out,
-                   softmax_scale, repair_budget):
+                   softmax_scale, repair_budget, smooth_k):
     B, S, H, D = q4.shape
     el = q4.element_size()
     for c, (h0, h1) in enumerate(chunks):
@@ -322,7 +329,7 @@ def _stream_chunks(q4, k4, v4, o4, chunks, stage_in, stage_out, in_free, out_fre
             ready = torch.cuda.Event()
             ready.record(s_in)
         comp.wait_event(ready)
-        prep = prepare(*ins)
+        prep = prepare(*ins, smooth_k=smooth_k)
         rep = prepare_v_repair(ins[2], prep, repair_budget) if repair_budget else None
         in_free[st] = torch.cuda.Event()
         in_free[st].record(comp)
@@ -345,18 +352,19 @@ def _stream_chunks(q4, k4, v4, o4, chunks, stage_in, stage_out, in_free, out_fre
 
 def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, softmax_scale: float | None = None,
               repair_budget: float | None = None, out: torch.Tensor | None = None,
-              device=None, chunk_heads: int | None = None) -> torch.Tensor:
+              device=None, chunk_heads: int | None = None, smooth_k: bool = False) -> torch.Tensor:
     """Full call: prepare + ExpCast attention (+ optional V residual repair).
 
     CUDA inputs give a CUDA output (asynchronous on the current stream).  CPU
     inputs (pinned for speed) are streamed through `device` (default: the
     current CUDA device) in head chunks of `chunk_heads` heads (default: about
     a quarter of H), so that host<->device copies overlap the computation; O
-    lands in `out` (or a new pinned tensor), complete when the call returns."""
+    lands in `out` (or a new pinned tensor), complete when the call returns.
+    smooth_k: optional K smoothing in prepare (see `prepare`)."""
     if q.is_cuda:
-        return _attention_device(q, k, v, softmax_scale, repair_budget, out)
+        return _attention_device(q, k, v, softmax_scale, repair_budget, out, smooth_k)
     dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
-    return _attention_host(q, k, v, softmax_scale, repair_budget, out, dev, chunk_heads)
+    return _attention_host(q, k, v, softmax_scale, repair_budget, out, dev, chunk_heads, smooth_k)
 
 
 def flops(B: int, S: int, H: int, D: int = 128) -> float:

@@ -107,10 +107,10 @@ bool dims_ok(int64_t B, int64_t S, int64_t H) {
 }
 
 struct PrepLayout {
-  size_t q, k, vt, sq, sk, sv, vamax, energy, total;
+  size_t q, k, vt, sq, sk, sv, vamax, energy, kpart, kmean, total;
 };
 
-PrepLayout prep_layout(int64_t B, int64_t S, int64_t H) {
+PrepLayout prep_layout(int64_t B, int64_t S, int64_t H, uint32_t flags = 0) {
   const int64_t nb = (S + 127) / 128, S_pad = nb * 128, BH = B * H;
   PrepLayout L{};
   size_t off = 0;
@@ -127,6 +127,10 @@ PrepLayout prep_layout(int64_t B, int64_t S, int64_t H) {
   L.sv = take(static_cast<size_t>(BH) * 4);
   L.vamax = take(static_cast<size_t>(BH) * 4);
   L.energy = take(static_cast<size_t>(BH) * S * 4);
+  if (flags & OVC_PREPARE_SMOOTH_K) {
+    L.kpart = take(static_cast<size_t>(BH) * nb * 128 * 4);
+    L.kmean = take(static_cast<size_t>(BH) * 128 * 4);
+  }
   L.total = off;
   return L;
 }
@@ -268,12 +272,22 @@ using namespace ovc;
 extern "C" {
 
 size_t ovc_prepare_workspace_bytes(int64_t B, int64_t S, int64_t H, int64_t D) {
-  if (D != 128 || !dims_ok(B, S, H)) return 0;
-  return prep_layout(B, S, H).total;
+  return ovc_prepare_workspace_bytes_ex(B, S, H, D, 0);
+}
+
+size_t ovc_prepare_workspace_bytes_ex(int64_t B, int64_t S, int64_t H, int64_t D, uint32_t flags) {
+  if (D != 128 || !dims_ok(B, S, H) || (flags & ~OVC_PREPARE_SMOOTH_K)) return 0;
+  return prep_layout(B, S, H, flags).total;
 }
 
 ovc_status ovc_prepare(const ovc_tensor* q, const ovc_tensor* k, const ovc_tensor* v, void* workspace,
                        size_t workspace_bytes, ovc_prepared* out, void* stream) {
+  return ovc_prepare_ex(q, k, v, 0, workspace, workspace_bytes, out, stream);
+}
+
+ovc_status ovc_prepare_ex(const ovc_tensor* q, const ovc_tensor* k, const ovc_tensor* v, uint32_t flags,
+                          void* workspace, size_t workspace_bytes, ovc_prepared* out, void* stream) {
+  if (flags & ~OVC_PREPARE_SMOOTH_K) return OVC_ERR_INVALID_ARG;
   if (!q || !k || !v || !out) return OVC_ERR_INVALID_ARG;
   if (q->D != 128 || k->D != 128 || v->D != 128) return OVC_ERR_UNSUPPORTED;
   if ((q->dtype != OVC_BF16 && q->dtype != OVC_FP16) || k->dtype != q->dtype || v->dtype != q->dtype)
@@ -282,7 +296,7 @@ ovc_status ovc_prepare(const ovc_tensor* q, const ovc_tensor* k, const ovc_tenso
   if (k->B != q->B || k->S != q->S || k->H != q->H || v->B != q->B || v->S != q->S || v->H != q->H)
     return OVC_ERR_INVALID_ARG;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return OVC_ERR_INVALID_ARG;
-  const PrepLayout L = prep_layout(q->B, q->S, q->H);
+  const PrepLayout L = prep_layout(q->B, q->S, q->H, flags);
   if (workspace_bytes < L.total) return OVC_ERR_WORKSPACE_TOO_SMALL;
   DeviceState* dev = nullptr;
   ovc_status st = device_state(&dev);
@@ -332,6 +346,12 @@ ovc_status ovc_prepare(const ovc_tensor* q, const ovc_tensor* k, const ovc_tenso
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(p.vamax, 0, static_cast<size_t>(p.B * p.H) * 4, s) != cudaSuccess) return OVC_ERR_CUDA;
+  if (flags & OVC_PREPARE_SMOOTH_K) {
+    P.kpart = reinterpret_cast<float*>(ws + L.kpart);
+    P.kmean = reinterpret_cast<float*>(ws + L.kmean);
+    k_mean_partial_kernel<<<dim3(static_cast<unsigned>(p.nb), static_cast<unsigned>(p.B * p.H)), 128, 0, s>>>(P);
+    k_mean_final_kernel<<<static_cast<unsigned>(p.B * p.H), 128, 0, s>>>(P);
+  }
   const dim3 g1(static_cast<unsigned>(p.nb), static_cast<unsigned>(p.B * p.H), 3);
   prepare_qk_kernel<<<g1, 256, 0, s>>>(P);
   const dim3 g2(static_cast<unsigned>(p.nb), static_cast<unsigned>(p.B * p.H), 1);

@@ -7,6 +7,16 @@
 // Quantisation is defined in FP32: s = amax/448, r = 448/amax (IEEE single
 // divisions; amax = 0 gives s = r = 1), code = E4M3_rn_satfinite(x * r).
 //
+// K smoothing (optional; the VC-Attention summary, "Why attention is the
+// video bottleneck", names Q/K smoothing as the prior art): K's per-channel
+// means over the sequence are subtracted (FP32) before K is quantised, which
+// leaves non-causal softmax unchanged and takes the channel offset out of
+// K's block scales.  The mean is summed in a fixed order -- per 128-token
+// block in token order, then the block sums in block order, then / S -- so
+// that it is reproducible bit for bit:
+//   k_mean_partial_kernel  grid (nb, B*H) x 128: one thread per channel.
+//   k_mean_final_kernel    grid (B*H) x 128.
+//
 // Two launches, both HBM-bound and coalesced:
 //   prepare_qk_kernel  grid (nb, B*H, 3): z = 0 quantises a 128-token block of
 //                      Q, z = 1 of K, z = 2 folds the block's amax|V| into the
@@ -39,6 +49,10 @@ struct PrepParams {
   float* sv;
   uint32_t* vamax;
   float* energy;
+  // K smoothing (both NULL when off): kpart [B*H][nb][128] block sums,
+  // kmean [B*H][128] channel means subtracted from K before quantising.
+  float* kpart;
+  float* kmean;
 };
 
 // |x| of two packed 16-bit floats, as ordered integers (sign bit cleared).
@@ -98,6 +112,29 @@ __device__ __forceinline__ uint32_t block_max_u32(uint32_t m, uint32_t* red) {
   return r;
 }
 
+// Channel sums of one 128-token block of K, in token order.
+__global__ void __launch_bounds__(128) k_mean_partial_kernel(const __grid_constant__ PrepParams P) {
+  const int j = blockIdx.x, bh = blockIdx.y, d = threadIdx.x;
+  const int b = bh / P.H, h = bh % P.H;
+  const int t1 = min(P.S, j * 128 + 128);
+  const uint16_t* src = P.k + b * P.ks[0] + h * P.ks[2] + d;
+  float part = 0.0f;
+  // The loads are independent and can be in flight together; the additions
+  // stay in token order.
+#pragma unroll 16
+  for (int t = j * 128; t < t1; ++t) part = __fadd_rn(part, half_bits_to_float(__ldg(src + t * P.ks[1]), P.fp16));
+  P.kpart[(static_cast<int64_t>(bh) * P.nb + j) * 128 + d] = part;
+}
+
+// Channel means: the block sums in block order, then one division by S.
+__global__ void __launch_bounds__(128) k_mean_final_kernel(const __grid_constant__ PrepParams P) {
+  const int bh = blockIdx.x, d = threadIdx.x;
+  const float* part = P.kpart + static_cast<int64_t>(bh) * P.nb * 128 + d;
+  float total = 0.0f;
+  for (int j = 0; j < P.nb; ++j) total = __fadd_rn(total, part[j * 128]);
+  P.kmean[bh * 128 + d] = __fdiv_rn(total, static_cast<float>(P.S));
+}
+
 // One 128-token block of Q or K (z = 0, 1), or the amax of one block of V
 // (z = 2).  256 threads: two per token row, 64 channels each.
 __global__ void __launch_bounds__(256) prepare_qk_kernel(const __grid_constant__ PrepParams P) {
@@ -121,6 +158,36 @@ __global__ void __launch_bounds__(256) prepare_qk_kernel(const __grid_constant__
   } else {
 #pragma unroll
     for (int i = 0; i < 8; ++i) x[i] = make_uint4(0, 0, 0, 0);
+  }
+
+  if (which == 1 && P.kmean != nullptr) {
+    // Smoothed K: the centred values fl(x - mean) set the block amax and are
+    // quantised; rows past S stay zero (no code, no part of the amax).
+    const float* mu = P.kmean + bh * 128 + half * 64;
+    float c[64];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t wd[4] = {x[i].x, x[i].y, x[i].z, x[i].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = unpack2(wd[e], P.fp16);
+        c[8 * i + 2 * e] = t < P.S ? __fsub_rn(f.x, __ldg(mu + 8 * i + 2 * e)) : 0.0f;
+        c[8 * i + 2 * e + 1] = t < P.S ? __fsub_rn(f.y, __ldg(mu + 8 * i + 2 * e + 1)) : 0.0f;
+      }
+    }
+    float m = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 64; ++e) m = fmaxf(m, fabsf(c[e]));
+    const float amax = __uint_as_float(block_max_u32(__float_as_uint(m), red));
+    const QScale sc = scale_from_amax(amax);
+    if (tid == 0) P.sk[bh * P.nb + j] = sc.s;
+    uint32_t w[16];
+#pragma unroll
+    for (int g = 0; g < 16; ++g) w[g] = quant4(c[4 * g], c[4 * g + 1], c[4 * g + 2], c[4 * g + 3], sc.r);
+    uint4* d4 = reinterpret_cast<uint4*>(P.kc + (static_cast<int64_t>(bh) * P.S_pad + t) * 128 + half * 64);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    return;
   }
 
   uint32_t m2 = 0;

@@ -200,6 +200,26 @@ ovc_status ovc_attention_probe(const ovc_prepared* p, const ovc_repair* r, float
 ovc_status ovc_prepare_noalloc(const ovc_tensor* q, const ovc_tensor* k, const ovc_tensor* v,
                                const ovc_prepared* out, void* stream);
 
+/* ovc_prepare with options.  flags (OR of):
+ *   OVC_PREPARE_SMOOTH_K  K smoothing -- optional, off in ovc_prepare.  The
+ *     VC-Attention summary ("Why attention is the video bottleneck") names
+ *     Q/K smoothing as the prior art of low-bit attention.  Per (b,h) the
+ *     channel means of K over the sequence are subtracted (FP32) before K is
+ *     quantised.  Exact non-causal softmax attention is unchanged (every
+ *     score of a row moves by q.mean); K's block scales lose the channel
+ *     offset, which lowers the quantisation error when keys carry a common
+ *     per-channel bias.  The mean is summed in a fixed order (per 128-token
+ *     block in token order, the block sums in block order, then one FP32
+ *     division by S) so that it reproduces bit for bit.  The means themselves
+ *     are not part of ovc_prepared (attention does not need them).
+ * ovc_prepare_workspace_bytes_ex gives the workspace for the same flags
+ * (0 for unknown flags or unsupported shapes); unknown flags make
+ * ovc_prepare_ex return OVC_ERR_INVALID_ARG.  Otherwise as ovc_prepare. */
+#define OVC_PREPARE_SMOOTH_K 1u
+size_t ovc_prepare_workspace_bytes_ex(int64_t B, int64_t S, int64_t H, int64_t D, uint32_t flags);
+ovc_status ovc_prepare_ex(const ovc_tensor* q, const ovc_tensor* k, const ovc_tensor* v, uint32_t flags,
+                          void* workspace, size_t workspace_bytes, ovc_prepared* out, void* stream);
+
 /* Strided asynchronous copy (cudaMemcpy2DAsync, direction inferred from the
  * pointers) -- no counterpart in the pages; infrastructure for the host-buffer
  * path of the Python binding, which streams host-resident [B,S,H,128] inputs

@@ -121,3 +121,17 @@ def test_head_chunks_cover_every_head_once():
             assert all(a1 == b0 for (_, a1), (b0, _) in zip(ch, ch[1:]))
             assert all(h1 > h0 for h0, h1 in ch)
     assert len(head_chunks(56)) == 4
+
+
+def test_prepare_options_on_the_host(lib):
+    from fp8_bit_attention_gb300 import _abi
+    base = lib.ovc_prepare_workspace_bytes(1, 73397, 56, 128)
+    assert lib.ovc_prepare_workspace_bytes_ex(1, 73397, 56, 128, 0) == base
+    smooth = lib.ovc_prepare_workspace_bytes_ex(1, 73397, 56, 128, _abi.OVC_PREPARE_SMOOTH_K)
+    assert smooth >= base + 56 * 574 * 128 * 4 + 56 * 128 * 4
+    assert lib.ovc_prepare_workspace_bytes_ex(1, 73397, 56, 128, 2) == 0        # unknown flag
+    t = _abi.OvcTensor(0x1000, _abi.OVC_BF16, 1, 128, 1, 128, 128 * 128, 128, 128)
+    out = _abi.OvcPrepared()
+    st = lib.ovc_prepare_ex(ctypes.byref(t), ctypes.byref(t), ctypes.byref(t), 6, ctypes.c_void_p(0x100000),
+                            1 << 30, ctypes.byref(out), None)
+    assert st == _abi.OVC_ERR_INVALID_ARG

@@ -215,3 +215,50 @@ def test_fp16_inputs_match_oracle(B, H, S):
     orep = ovc.attention_v_repair(prep, rep).float().cpu().numpy()
     rrep = oracle.attention_rows(ref, bh, ss, repair=rr)["out"].reshape(B, H, S, 128).transpose(0, 2, 1, 3)
     assert rel_l2(orep, rrep) <= TOL_REL_L2
+
+
+@pytest.mark.parametrize("B,H,S,fp16", [(1, 2, 1000, False), (2, 1, 300, True), (1, 1, 1, False)])
+def test_k_smoothing_matches_oracle(B, H, S, fp16):
+    """prepare(smooth_k=True): K codes and scales bit-exact against the
+    oracle's smoothed quantisation (which pins the channel means' FP32 sums);
+    O within 5e-3; the host-buffer path agrees bit for bit."""
+    q, k, v = inputs(B, H, S, seed=71 + S)
+    if fp16:
+        q, k, v = (x.to(torch.float16) for x in (q, k, v))
+    bits = [x.contiguous().view(torch.int16).numpy().view(np.uint16) for x in (q, k, v)]
+    ref = oracle.Prepared(*bits, fp16=fp16, smooth_k=True)
+    qd, kd, vd = to_dev(q, k, v)
+    prep = ovc.prepare(qd, kd, vd, smooth_k=True)
+    assert np.array_equal(prep.k_codes().cpu().numpy(), ref.kc)
+    assert np.array_equal(prep.k_scales().cpu().numpy(), ref.sk)
+    assert np.array_equal(prep.q_codes().cpu().numpy(), ref.qc)
+    assert np.array_equal(prep.vt_codes().cpu().numpy().transpose(0, 1, 3, 2), ref.vc)
+    o = ovc.attention_prepared(prep).float().cpu().numpy()
+    bh = np.repeat(np.arange(B * H), S)
+    ss = np.tile(np.arange(S), B * H)
+    r = oracle.attention_rows(ref, bh, ss)["out"].reshape(B, H, S, 128).transpose(0, 2, 1, 3)
+    assert rel_l2(o, r) <= TOL_REL_L2
+    dev = ovc.attention(qd, kd, vd, smooth_k=True).cpu()
+    host = ovc.attention(q.pin_memory(), k.pin_memory(), v.pin_memory(), smooth_k=True)
+    assert torch.equal(host.view(torch.int16), dev.view(torch.int16))
+    assert ovc.device_status() == 0
+
+
+def test_k_smoothing_lowers_error_on_biased_keys():
+    """On the workloads' per-channel key bias, smoothing lowers the GPU
+    output's error against exact softmax attention."""
+    B, H, S = 1, 2, 1024
+    q, k, v = inputs(B, H, S, seed=77)
+    qf, kf, vf = (x.to(torch.float64).numpy() for x in (q, k, v))
+    errs = []
+    for smooth in (False, True):
+        o = ovc.attention(*to_dev(q, k, v), smooth_k=smooth).double().cpu().numpy()
+        num = den = 0.0
+        for h in range(H):
+            s = (qf[0, :, h] @ kf[0, :, h].T) / math.sqrt(128.0)
+            p = np.exp(s - s.max(axis=1, keepdims=True))
+            ref = (p @ vf[0, :, h]) / p.sum(axis=1, keepdims=True)
+            num += np.sum((o[0, :, h] - ref) ** 2)
+            den += np.sum(ref ** 2)
+        errs.append(math.sqrt(num / den))
+    assert errs[1] < errs[0]
