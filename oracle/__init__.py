@@ -68,6 +68,8 @@ def lib():
             L.ovc_oracle_half_bits_to_float.argtypes = [ctypes.c_uint16]
             L.ovc_oracle_expcast_code.restype = ctypes.c_uint8
             L.ovc_oracle_expcast_code.argtypes = [d, d, d, d]
+            L.ovc_oracle_exp_cast_code.restype = ctypes.c_uint8
+            L.ovc_oracle_exp_cast_code.argtypes = [d, d, d]
             L.ovc_oracle_quantize_blocks.restype = None
             L.ovc_oracle_quantize_blocks.argtypes = [P, ctypes.c_int, i64, i64, i64, i64, i64, i64, P, P, P]
             L.ovc_oracle_k_mean.restype = None
@@ -82,11 +84,11 @@ def lib():
             L.ovc_oracle_repair_quantize.argtypes = [P, ctypes.c_int, i64, i64, i64, i64, i64, i64, P, P, P,
                                                      i64, P, P]
             L.ovc_oracle_block_codes.restype = None
-            L.ovc_oracle_block_codes.argtypes = [P, ctypes.c_float, P, P, i64, i64, d, d, d, d, P]
+            L.ovc_oracle_block_codes.argtypes = [P, ctypes.c_float, P, P, i64, i64, d, d, d, d, ctypes.c_int, P]
             L.ovc_oracle_attention_rows.restype = ctypes.c_int
             L.ovc_oracle_attention_rows.argtypes = (
                 [P, P, P, P, P, P, i64, i64, i64, P, P, P, i64, P, P, i64, d, d, d, d,
-                 ctypes.c_int, ctypes.c_int, P, P, P, P, i64, P, P, ctypes.c_int])
+                 ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P, P, i64, P, P, ctypes.c_int])
             L.ovc_oracle_attention_exact_rows.restype = ctypes.c_int
             L.ovc_oracle_attention_exact_rows.argtypes = (
                 [P, P, P, i64, i64, P, P, i64, d, d, ctypes.c_int, ctypes.c_int, P, P,
@@ -134,6 +136,17 @@ def bf16_from_double(x: np.ndarray) -> np.ndarray:
 def expcast_code(Z: float, m8: float = 0.0, c0: float = C0, beta: float = BETA) -> int:
     """ExpCast byte of a score Z (code units, 8*log2) under reference m8."""
     return int(lib().ovc_oracle_expcast_code(float(Z), float(m8), float(c0), float(beta)))
+
+
+def exp_cast_code(Z: float, m8: float = 0.0, c0: float = C0) -> int:
+    """Exp-then-cast byte: E4M3(fl32(2^((Z - m8 + c0 - 56)/8)))."""
+    return int(lib().ovc_oracle_exp_cast_code(float(Z), float(m8), float(c0)))
+
+
+def exp_cast_codes(Z: np.ndarray, m8: float = 0.0, c0: float = C0) -> np.ndarray:
+    f = lib().ovc_oracle_exp_cast_code
+    return np.array([f(float(z), float(m8), float(c0)) for z in np.ravel(Z)],
+                    dtype=np.uint8).reshape(np.shape(Z))
 
 
 def expcast_codes(Z: np.ndarray, m8: float = 0.0, c0: float = C0, beta: float = BETA) -> np.ndarray:
@@ -258,9 +271,10 @@ class Repair:
 
 
 def attention_rows(prep: Prepared, rows_bh, rows_s, *, sm=None, repair: Repair | None = None,
-                   c0=C0, beta=BETA, tau=TAU, mid_window=True, snap=True,
+                   c0=C0, beta=BETA, tau=TAU, mid_window=True, snap=True, cast=False,
                    dump_block=-1, nthreads=None):
-    """ExpCast attention for query rows (bh = b*H + h, s).
+    """ExpCast attention for query rows (bh = b*H + h, s); cast=True gives the
+    exp-then-cast baseline's bytes, mid_window=False the natural key order.
 
     Returns dict(out [n,128] float64, m8 [n], l [n], nres [n,2], and, when
     dump_block >= 0, codes [n,128] uint8 + dump_m8 [n])."""
@@ -282,7 +296,7 @@ def attention_rows(prep: Prepared, rows_bh, rows_s, *, sm=None, repair: Repair |
     rc = lib().ovc_oracle_attention_rows(
         _ptr(prep.qc), _ptr(prep.sq), _ptr(prep.kc), _ptr(prep.sk), _ptr(prep.vc), _ptr(prep.sv),
         prep.B, prep.S, prep.H, _ptr(ridx), _ptr(rdc), _ptr(rsr), nrep,
-        _ptr(rows_bh), _ptr(rows_s), n, c0, beta, tau, sm, int(mid_window), int(snap),
+        _ptr(rows_bh), _ptr(rows_s), n, c0, beta, tau, sm, int(mid_window), int(snap), int(cast),
         _ptr(out), _ptr(m8), _ptr(l), _ptr(nres), dump_block, _ptr(codes), _ptr(dm8),
         nthreads or default_threads())
     if rc != 0:
@@ -304,8 +318,9 @@ def attention_full(prep: Prepared, **kw):
 
 
 def block_codes(prep: Prepared, bh: int, s: int, j: int, m8: float, *, sm=None,
-                c0=C0, beta=BETA) -> np.ndarray:
-    """Codes of key block j for query row (bh, s) under reference m8."""
+                c0=C0, beta=BETA, cast=False) -> np.ndarray:
+    """Codes of key block j for query row (bh, s) under reference m8
+    (cast=True: exp-then-cast bytes)."""
     sm = 1.0 / np.sqrt(128.0) if sm is None else float(sm)
     B, H = prep.B, prep.H
     qrow = np.ascontiguousarray(prep.qc.reshape(B * H, -1, 128)[bh, s])
@@ -314,7 +329,7 @@ def block_codes(prep: Prepared, bh: int, s: int, j: int, m8: float, *, sm=None,
     sq = float(prep.sq.reshape(B * H, -1)[bh, s // 128])
     codes = np.zeros(128, np.uint8)
     lib().ovc_oracle_block_codes(_ptr(qrow), sq, _ptr(kc), _ptr(sk), prep.S, j, float(m8),
-                                 c0, beta, sm, _ptr(codes))
+                                 c0, beta, sm, int(cast), _ptr(codes))
     return codes
 
 

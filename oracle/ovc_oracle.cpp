@@ -203,6 +203,7 @@ struct Params {
   int exact;        // 1: p = 2^((Z - m8)/8) exactly, no codes (skeleton pin)
   int mid_window;   // 1: cyclic from block floor(nb/2); 0: natural order
   int snap;         // 1: reference on the {k + frac(c0+beta)} grid; 0: = max
+  int cast;         // 1: exp-then-cast bytes (the baseline) instead of ExpCast
 };
 
 // Key-block visiting order.  [OVC-news "Architectural optimisations";
@@ -250,6 +251,24 @@ double expcast_p(double Z, double m8, const Params& P, uint8_t* code_out) {
   const uint8_t c = static_cast<uint8_t>(t);
   if (code_out) *code_out = c;
   return e4m3_value(c);
+}
+
+// Exp-then-cast probability, the path ExpCast replaces: the stored value
+// v = 2^((Z - m8 + c0 - 56) / 8) (= 2^8 p for c0 = 120) is computed, held in
+// FP32 and converted to E4M3 with round to nearest even and saturation;
+// p = dec(code).  [OVC-news "Problem": one exponent per score and a
+// conversion to FP8; VC-summary "ExpCast-FP8": the exp-then-cast path whose
+// bytes ExpCast matches on 79.6% of entries]
+double exp_cast_p(double Z, double m8, const Params& P, uint8_t* code_out) {
+  const double v = std::exp2((Z - m8 + P.c0 - 56.0) / 8.0);
+  const uint8_t c = e4m3_from_float(static_cast<float>(v));
+  if (code_out) *code_out = c;
+  return e4m3_value(c);
+}
+
+// Probability of one score under the configured byte path.
+double prob(double Z, double m8, const Params& P, uint8_t* code_out) {
+  return (P.cast && !P.exact) ? exp_cast_p(Z, m8, P, code_out) : expcast_p(Z, m8, P, code_out);
 }
 
 // Lazy rescale of the running state.  [OVC-mlllm "Context": fewer rescales]
@@ -301,7 +320,7 @@ void attend_row(const double* q, double qscale, const HeadView& hv, const Params
     if (dump && dump_m8) *dump_m8 = m8;
     for (int64_t c = 0; c < nk; ++c) {
       uint8_t code = 0;
-      const double p = expcast_p(Z[c], m8, P, &code);
+      const double p = prob(Z[c], m8, P, &code);
       if (dump) dump_codes[c] = code;
       l += p;
       const double* vr = hv.V + (k0 + c) * 128;
@@ -326,7 +345,7 @@ void attend_row(const double* q, double qscale, const HeadView& hv, const Params
     }
     maybe_rescale(bm, P, &m8, &l, O, Orep, &nres_rep);   // never fires: keys already seen
     for (int64_t c = 0; c < nk; ++c) {
-      const double p = expcast_p(Z[c], m8, P, nullptr);
+      const double p = prob(Z[c], m8, P, nullptr);
       const double* dv = hv.dV + (r0 + c) * 128;
       for (int d = 0; d < 128; ++d) Orep[d] += p * dv[d];
     }
@@ -376,9 +395,17 @@ float ovc_oracle_half_bits_to_float(uint16_t h) { return half_bits_to_float(h); 
 
 // ExpCast code of one score: clamp(rint(Z - m8 + c0 + beta), 0, 126).
 uint8_t ovc_oracle_expcast_code(double Z, double m8, double c0, double beta) {
-  const Params P{c0, beta, 0.75, 1.0, 0, 1, 1};
+  const Params P{c0, beta, 0.75, 1.0, 0, 1, 1, 0};
   uint8_t code = 0;
   expcast_p(Z, m8, P, &code);
+  return code;
+}
+
+// Exp-then-cast code of one score: E4M3(fl32(2^((Z - m8 + c0 - 56) / 8))).
+uint8_t ovc_oracle_exp_cast_code(double Z, double m8, double c0) {
+  const Params P{c0, -0.35, 0.75, 1.0, 0, 1, 1, 1};
+  uint8_t code = 0;
+  exp_cast_p(Z, m8, P, &code);
   return code;
 }
 
@@ -518,13 +545,14 @@ void ovc_oracle_repair_quantize(const uint16_t* v, int fp16, int64_t B, int64_t 
 }
 
 // Codes of one key block for one query row against a given reference m8
-// (used to compare the device's P bytes under the device's own reference).
+// (used to compare the device's P bytes under the device's own reference);
+// cast = 1 gives the exp-then-cast bytes.
 void ovc_oracle_block_codes(const uint8_t* qrow, float sq, const uint8_t* kcodes_head,
                             const float* sk_head, int64_t S, int64_t j, double m8, double c0,
-                            double beta, double sm, uint8_t* codes) {
+                            double beta, double sm, int cast, uint8_t* codes) {
   double q[128];
   for (int d = 0; d < 128; ++d) q[d] = e4m3_value(qrow[d]);
-  Params P{c0, beta, 0.75, sm, 0, 1, 1};
+  Params P{c0, beta, 0.75, sm, 0, 1, 1, cast};
   const double a = 8.0 * kLog2e * sm * static_cast<double>(sq) * static_cast<double>(sk_head[j]);
   for (int c = 0; c < 128; ++c) {
     const int64_t t = j * 128 + c;
@@ -535,12 +563,13 @@ void ovc_oracle_block_codes(const uint8_t* qrow, float sq, const uint8_t* kcodes
     double k[128];
     for (int d = 0; d < 128; ++d) k[d] = e4m3_value(kcodes_head[t * 128 + d]);
     uint8_t code;
-    expcast_p(a * dot128(q, k), m8, P, &code);
+    prob(a * dot128(q, k), m8, P, &code);
     codes[c] = code;
   }
 }
 
-// ExpCast attention for a list of query rows (b*H+h, s).  Inputs are the
+// ExpCast attention (cast = 1: the exp-then-cast baseline; mid_window = 0:
+// natural key order) for a list of query rows (b*H+h, s).  Inputs are the
 // oracle's own quantised tensors: qc/kc [B,H,S_pad,128], sq/sk [B,H,nb],
 // vc token-major [B,H,S_pad,128], sv [B,H].  Optional repair set: rep_idx
 // [B,H,n_rep], rep_dcodes [B,H,n_rep,128], sr [B,H].  Outputs per row: out
@@ -552,11 +581,11 @@ int ovc_oracle_attention_rows(const uint8_t* qc, const float* sq, const uint8_t*
                               const int32_t* rep_idx, const uint8_t* rep_dcodes, const float* sr,
                               int64_t n_rep, const int64_t* row_bh, const int64_t* row_s,
                               int64_t nrows, double c0, double beta, double tau, double sm,
-                              int mid_window, int snap, double* out, double* m8_out, double* l_out,
+                              int mid_window, int snap, int cast, double* out, double* m8_out, double* l_out,
                               int32_t* nres_out, int64_t dump_block, uint8_t* dump_codes,
                               double* dump_m8, int nthreads) {
   const Dims dm = make_dims(B, S, H);
-  const Params P{c0, beta, tau, sm, 0, mid_window, snap};
+  const Params P{c0, beta, tau, sm, 0, mid_window, snap, cast};
   // Process the rows head by head so that one head's keys are decoded once.
   std::vector<int64_t> perm(nrows);
   for (int64_t i = 0; i < nrows; ++i) perm[i] = i;
@@ -626,7 +655,7 @@ int ovc_oracle_attention_exact_rows(const double* q, const double* k, const doub
                                     int64_t nrows, double tau, double sm, int mid_window, int snap,
                                     double* out, int32_t* nres_out, int nthreads) {
   const Dims dm = make_dims(1, S, 1);
-  const Params P{120.0, -0.35, tau, sm, 1, mid_window, snap};
+  const Params P{120.0, -0.35, tau, sm, 1, mid_window, snap, 0};
   std::vector<double> ones(dm.nb, 1.0);
   bool bad = false;
   parallel_for(nrows, nthreads, [&](int64_t r) {
