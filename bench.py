@@ -39,6 +39,8 @@ def _args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--repair-budget", type=float, default=0.005)
+    ap.add_argument("--no-variants", action="store_true",
+                    help="skip timing the exp-then-cast / natural-order kernel variants")
     return ap.parse_args()
 
 
@@ -298,6 +300,26 @@ def run_ours(a):
                   "unit": "TFLOP/s", "n_repaired_per_head": int(rep.desc.n)}
         del rws
 
+    # Kernel variants on the same prepared inputs: the exp-then-cast byte path,
+    # the natural key order, and both (the baseline VC-Attention kernel).
+    variants = None
+    if not a.no_variants:
+        prep = ovc.prepare(qd, kd, vd, workspace=ws)
+        variants = {}
+        for name, fl in (("exp_then_cast", 1), ("natural_order", 2), ("baseline_vc", 3)):
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            ovc.attention_prepared(prep, out=out, flags=fl)
+            ev[0].record(stream)
+            for i in range(3):
+                ovc.attention_prepared(prep, out=out, flags=fl)
+            ev[1].record(stream)
+            torch.cuda.synchronize()
+            ms = ev[0].elapsed_time(ev[1]) / 3
+            variants[name] = {"attention_ms": ms, "value": flop / (ms / 1e3) / 1e12, "unit": "TFLOP/s"}
+        if ovc.device_status() != 0:
+            raise RuntimeError("device-side timeout in a kernel variant")
+        variants["expcast_speedup_over_baseline"] = variants["baseline_vc"]["attention_ms"] / statistics.mean(t_attn)
+
     # End to end through the public API with host buffers.
     e2e = None
     if not a.no_e2e:
@@ -348,6 +370,7 @@ def run_ours(a):
                      "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{which} bf16 sustained x {FP8_PER_BF16:g} (FP8/BF16 nominal)"},
         "repair": repair,
+        "variants": variants,
         "e2e": e2e,
         "gpu_launches": 3 * a.steps,
         "clocks": clocks,

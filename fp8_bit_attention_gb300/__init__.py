@@ -6,9 +6,9 @@ the package does not load the library; the first call does, and fails loudly
 if it has not been built.
 """
 from .api import (OvcError, Prepared, Repair, attention, attention_prepared, attention_probe,
-                  attention_v_repair, device_status, flops, prepare, prepare_v_repair,
-                  prepare_workspace_bytes, repair_workspace_bytes)
+                  attention_v_repair, attn_flags, device_status, flops, prepare, prepare_v_repair,
+                  prepare_workspace_bytes, repair_workspace_bytes, vc_attention_baseline)
 
 __all__ = ["OvcError", "Prepared", "Repair", "attention", "attention_prepared", "attention_probe",
-           "attention_v_repair", "device_status", "flops", "prepare", "prepare_v_repair",
-           "prepare_workspace_bytes", "repair_workspace_bytes"]
+           "attention_v_repair", "attn_flags", "device_status", "flops", "prepare", "prepare_v_repair",
+           "prepare_workspace_bytes", "repair_workspace_bytes", "vc_attention_baseline"]

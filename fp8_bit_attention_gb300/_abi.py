@@ -20,6 +20,9 @@ OVC_ERR_TIMEOUT = 5
 OVC_ERR_SCRATCH_LIMIT = 6
 OVC_NOALLOC_MAX_HEADS = 4096
 OVC_PREPARE_SMOOTH_K = 1
+OVC_ATTN_EXP_THEN_CAST = 1
+OVC_ATTN_NATURAL_ORDER = 2
+OVC_ATTN_BASELINE = 3
 OVC_BF16 = 0
 OVC_FP16 = 1
 
@@ -47,7 +50,8 @@ class OvcRepair(ctypes.Structure):
 class OvcProbe(ctypes.Structure):
     _fields_ = [("dump_bh", c_i64), ("dump_qblock", c_i64), ("dump_kblock", c_i64),
                 ("dump_codes", c_ptr), ("dump_m8", c_ptr), ("wait_timeout_ns", ctypes.c_uint64),
-                ("skip_mma", c_i32), ("force_persistent", c_i32), ("trace", c_ptr)]
+                ("skip_mma", c_i32), ("force_persistent", c_i32), ("trace", c_ptr),
+                ("flags", ctypes.c_uint32)]
 
 
 P = ctypes.POINTER
@@ -56,6 +60,8 @@ SIGNATURES = {
     "ovc_prepare": (c_i32, [P(OvcTensor), P(OvcTensor), P(OvcTensor), c_ptr, ctypes.c_size_t,
                             P(OvcPrepared), c_ptr]),
     "ovc_attention": (c_i32, [P(OvcPrepared), ctypes.c_float, P(OvcOutput), c_ptr]),
+    "ovc_attention_ex": (c_i32, [P(OvcPrepared), P(OvcRepair), ctypes.c_float, P(OvcOutput),
+                                 ctypes.c_uint32, c_ptr]),
     "ovc_repair_workspace_bytes": (ctypes.c_size_t, [c_i64, c_i64, c_i64, ctypes.c_float]),
     "ovc_prepare_v_repair": (c_i32, [P(OvcTensor), P(OvcPrepared), ctypes.c_float, c_ptr,
                                      ctypes.c_size_t, P(OvcRepair), c_ptr]),

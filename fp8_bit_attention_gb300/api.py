@@ -168,15 +168,39 @@ def _out_for(prep: Prepared, out):
     return out
 
 
+def attn_flags(exp_then_cast: bool = False, natural_order: bool = False) -> int:
+    """OVC_ATTN_* bits of a kernel variant (both set: the baseline kernel)."""
+    return (_abi.OVC_ATTN_EXP_THEN_CAST if exp_then_cast else 0) | (
+        _abi.OVC_ATTN_NATURAL_ORDER if natural_order else 0)
+
+
 def attention_prepared(prep: Prepared, *, softmax_scale: float | None = None,
-                       out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """O from prepared inputs (ovc_attention)."""
+                       out: torch.Tensor | None = None, stream=None, flags: int = 0,
+                       rep: "Repair | None" = None) -> torch.Tensor:
+    """O from prepared inputs: ovc_attention, or ovc_attention_ex when a kernel
+    variant (``flags``, see :func:`attn_flags`) or a repair set is given."""
     out = _out_for(prep, out)
     od = _output_desc(out)
-    st = lib().ovc_attention(ctypes.byref(prep.desc), float(softmax_scale or 0.0), ctypes.byref(od),
-                             ctypes.c_void_p(_stream_handle(stream)))
-    check(st, "ovc_attention")
+    h = ctypes.c_void_p(_stream_handle(stream))
+    if flags == 0 and rep is None:
+        st = lib().ovc_attention(ctypes.byref(prep.desc), float(softmax_scale or 0.0), ctypes.byref(od), h)
+        check(st, "ovc_attention")
+    else:
+        st = lib().ovc_attention_ex(ctypes.byref(prep.desc), ctypes.byref(rep.desc) if rep is not None else None,
+                                    float(softmax_scale or 0.0), ctypes.byref(od), int(flags), h)
+        check(st, "ovc_attention_ex")
     return out
+
+
+def vc_attention_baseline(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *,
+                          softmax_scale: float | None = None, out: torch.Tensor | None = None,
+                          stream=None) -> torch.Tensor:
+    """The baseline VC-Attention kernel on CUDA tensors: the same preparation,
+    then exp-then-cast probability bytes and the natural key order
+    ("Open VC Attention": baselines.vc_attention(q, k, v))."""
+    prep = prepare(q, k, v, stream=stream)
+    return attention_prepared(prep, softmax_scale=softmax_scale, out=out, stream=stream,
+                              flags=_abi.OVC_ATTN_BASELINE)
 
 
 def repair_workspace_bytes(B: int, S: int, H: int, budget: float) -> int:
@@ -214,7 +238,8 @@ def attention_v_repair(prep: Prepared, rep: Repair, *, softmax_scale: float | No
 
 def attention_probe(prep: Prepared, rep: Repair | None = None, *, softmax_scale=None, out=None,
                     dump=None, wait_timeout_ns: int = 0, skip_mma: bool = False,
-                    force_persistent: int = 0, trace: torch.Tensor | None = None, stream=None):
+                    force_persistent: int = 0, trace: torch.Tensor | None = None, stream=None,
+                    flags: int = 0):
     """Test hook: attention with P-byte dumps / wait-limit controls.
 
     dump = (bh, qblock, kblock) returns (out, codes [128,128] uint8, m8 [128])."""
@@ -225,6 +250,7 @@ def attention_probe(prep: Prepared, rep: Repair | None = None, *, softmax_scale=
     probe.wait_timeout_ns = int(wait_timeout_ns)
     probe.skip_mma = int(skip_mma)
     probe.force_persistent = int(force_persistent)
+    probe.flags = int(flags)
     if trace is not None:
         assert trace.dtype == torch.int64 and trace.is_cuda and trace.numel() >= 4 * 64 * 8
         probe.trace = trace.data_ptr()

@@ -139,8 +139,16 @@ __device__ __forceinline__ TileCoord tile_coord(const AttnParams& P, int tile) {
   return c;
 }
 
-// Key block visited at step i: cyclic from the middle block.
+// Kernel variants (template argument of attention_kernel): ExpCast with the
+// mid-window order is the method; the exp-then-cast byte path and the natural
+// key order together form the baseline that ExpCast is measured against.
+constexpr int kVarExpThenCast = 1;   // p byte = E4M3(ex2(...)) on the MUFU
+constexpr int kVarNaturalOrder = 2;  // key blocks 0, 1, ..., nb-1
+
+// Key block visited at step i: cyclic from the middle block, or in order.
+template <int kVar>
 __device__ __forceinline__ int key_block(int i, int nb) {
+  if (kVar & kVarNaturalOrder) return i;
   const int j = nb / 2 + i;
   return j >= nb ? j - nb : j;
 }
@@ -222,6 +230,52 @@ __device__ __forceinline__ void expcast_block_cols(const uint32_t* s, const floa
   }
 }
 
+// Exp-then-cast bytes (the baseline path that ExpCast replaces): the stored
+// value v = 2^(s * ac + cc), with ac = a/8 and cc = (c0 - 56 - m8)/8, comes
+// from one FMA and one ex2 on the MUFU, and a pair of values becomes two
+// E4M3 bytes by one FP32->FP8 conversion (round to nearest even, satfinite).
+// A masked score (-inf) gives v = 0, code 0.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+// kGuard: the exponent is first raised to at least -127 (ex2 then flushes to
+// 0), which also turns the NaN of a masked padding column (-inf times a zero
+// key scale) into code 0; the repair blocks need it, the main blocks (key
+// scales > 0) do not.
+template <bool kGuard>
+__device__ __forceinline__ float cast_exponent(uint32_t s, float a, float cc) {
+  const float x = fmaf(__uint_as_float(s), a, cc);
+  return kGuard ? fmaxf(x, -127.0f) : x;
+}
+
+template <bool kGuard>
+__device__ __forceinline__ uint32_t cast_word(uint32_t s0, uint32_t s1, uint32_t s2, uint32_t s3, float a0,
+                                              float a1, float a2, float a3, float cc) {
+  const float v0 = ex2_approx(cast_exponent<kGuard>(s0, a0, cc));
+  const float v1 = ex2_approx(cast_exponent<kGuard>(s1, a1, cc));
+  const float v2 = ex2_approx(cast_exponent<kGuard>(s2, a2, cc));
+  const float v3 = ex2_approx(cast_exponent<kGuard>(s3, a3, cc));
+  return __byte_perm(cvt_e4m3x2(v0, v1), cvt_e4m3x2(v2, v3), 0x5410);
+}
+
+__device__ __forceinline__ void cast_words(const uint32_t* s, float ac, float cc, uint32_t* w) {
+#pragma unroll
+  for (int g = 0; g < 32; ++g) w[g] = cast_word<false>(s[4 * g], s[4 * g + 1], s[4 * g + 2], s[4 * g + 3], ac, ac, ac, ac, cc);
+}
+
+__device__ __forceinline__ void cast_block_cols(const uint32_t* s, const float4* ksel, float c8sq8, float cc,
+                                                uint32_t* w) {
+#pragma unroll
+  for (int g = 0; g < 32; ++g) {
+    const float4 k4 = __ldg(ksel + g);
+    w[g] = cast_word<true>(s[4 * g], s[4 * g + 1], s[4 * g + 2], s[4 * g + 3], c8sq8 * k4.x, c8sq8 * k4.y,
+                     c8sq8 * k4.z, c8sq8 * k4.w, cc);
+  }
+}
+
 // Maximum of 128 FP32 values: eight independent 3-input chains, then a tree.
 __device__ __forceinline__ float rowmax128(const uint32_t* s) {
   float m[8];
@@ -273,6 +327,7 @@ __device__ __forceinline__ void tmem_scale_row128(uint32_t taddr, float f) {
   tmem_wait_st();
 }
 
+template <int kVar>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_ks,
@@ -341,7 +396,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           mbar_arrive_expect_tx(kbar, kTile);
           mbar_arrive_expect_tx(vbar, kTile);
           if (i < P.nb) {
-            const int j = key_block(i, P.nb);
+            const int j = key_block<kVar>(i, P.nb);
             tma_load_2d(smem_addr(sm.k[stage]), &tm_k, kbar, 0, tc.bh * P.S_pad + j * 128);
             tma_load_2d(smem_addr(sm.v[stage]), &tm_v, vbar, j * 128, tc.bh * 128);
           } else {
@@ -472,12 +527,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       float l = 0.0f;
       const bool dump_tile = (P.dump_codes != nullptr) && tc.bh == P.dump_bh && qb == P.dump_qb && store;
       // Key scale of the current block, loaded one block ahead.
-      float sk_next = __ldg(P.sk + tc.bh * P.nb + key_block(0, P.nb));
+      float sk_next = __ldg(P.sk + tc.bh * P.nb + key_block<kVar>(0, P.nb));
       for (int i = 0; i < nblk; ++i) {
         const bool main_blk = i < P.nb;
-        const int j = main_blk ? key_block(i, P.nb) : 0;
+        const int j = main_blk ? key_block<kVar>(i, P.nb) : 0;
         const float skj = sk_next;
-        if (i + 1 < P.nb) sk_next = __ldg(P.sk + tc.bh * P.nb + key_block(i + 1, P.nb));
+        if (i + 1 < P.nb) sk_next = __ldg(P.sk + tc.bh * P.nb + key_block<kVar>(i + 1, P.nb));
         const uint32_t gi = blk_count;
         if (trole >= 0) trace_mark(P, trole, gi, 0);
         ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&sm.s_full[t]), blk_count & 1, tmo, abort_flag));
@@ -510,7 +565,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             rescale = i > 0;
           }
           if (trole >= 0) trace_mark(P, trole, gi, 3);
-          expcast_words<0, 32>(s, as, expcast_scale_c(kCodeBase - kf), w);
+          if (kVar & kVarExpThenCast)
+            cast_words(s, a * 0.125f, (64.0f - kFrac - kf) * 0.125f, w);
+          else
+            expcast_words<0, 32>(s, as, expcast_scale_c(kCodeBase - kf), w);
           if (dump_tile && j == P.dump_kb) {
             uint4* d = reinterpret_cast<uint4*>(P.dump_codes + row * 128);
 #pragma unroll
@@ -526,7 +584,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (c >= valid) s[c] = 0xFF800000u;
           const float4* ks = reinterpret_cast<const float4*>(
               P.sk_sel + static_cast<int64_t>(tc.bh) * P.n_rep_pad + r * 128);
-          expcast_block_cols(s, ks, expcast_scale_a(c8sq), expcast_scale_c(kCodeBase - kf), w);
+          if (kVar & kVarExpThenCast)
+            cast_block_cols(s, ks, c8sq * 0.125f, (64.0f - kFrac - kf) * 0.125f, w);
+          else
+            expcast_block_cols(s, ks, expcast_scale_a(c8sq), expcast_scale_c(kCodeBase - kf), w);
           if (r == 0) {
             f = P.sv[tc.bh] / P.sr[tc.bh];
             rescale = true;

@@ -53,9 +53,10 @@ ovc_status device_state(DeviceState** out) {
     d.supported = (major == 10 && minor == 3);
     d.sms = sms;
     if (d.supported) {
-      if (cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(kAttnSmemBytes)) != cudaSuccess)
-        return OVC_ERR_CUDA;
+      for (auto fn : {attention_kernel<0>, attention_kernel<1>, attention_kernel<2>, attention_kernel<3>})
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kAttnSmemBytes)) != cudaSuccess)
+          return OVC_ERR_CUDA;
       void* p = nullptr;
       if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return OVC_ERR_CUDA;
       d.status = static_cast<unsigned int*>(p);
@@ -189,8 +190,9 @@ bool output_ok(const ovc_output* o) {
 ovc_status launch_status() { return cudaGetLastError() == cudaSuccess ? OVC_OK : OVC_ERR_CUDA; }
 
 ovc_status run_attention(const ovc_prepared* p, const ovc_repair* r, float softmax_scale,
-                         const ovc_output* o, const ovc_probe* probe, void* stream) {
+                         const ovc_output* o, const ovc_probe* probe, uint32_t flags, void* stream) {
   if (!prepared_ok(p) || !output_ok(o)) return OVC_ERR_INVALID_ARG;
+  if (flags & ~(OVC_ATTN_EXP_THEN_CAST | OVC_ATTN_NATURAL_ORDER)) return OVC_ERR_INVALID_ARG;
   if (r) {
     if (!r->idx || !r->k_sel || !r->dvt || !r->sk_sel || !r->sr) return OVC_ERR_INVALID_ARG;
     if (r->B != p->B || r->S != p->S || r->H != p->H) return OVC_ERR_INVALID_ARG;
@@ -259,8 +261,12 @@ ovc_status run_attention(const ovc_prepared* p, const ovc_repair* r, float softm
   // looping over tiles.  Shorter sequences launch one CTA per tile.
   const bool persistent = force > 0 || (force == 0 && p->S >= 32768);
   const int64_t grid = persistent ? (ntiles < dev->sms ? ntiles : dev->sms) : ntiles;
-  attention_kernel<<<static_cast<unsigned>(grid), kAttnThreads, kAttnSmemBytes,
-                     static_cast<cudaStream_t>(stream)>>>(mq, mk, mv, mks, mdv, P);
+  static_assert(OVC_ATTN_EXP_THEN_CAST == kVarExpThenCast && OVC_ATTN_NATURAL_ORDER == kVarNaturalOrder,
+                "flag bits select the kernel variant");
+  decltype(&attention_kernel<0>) kernels[4] = {attention_kernel<0>, attention_kernel<1>, attention_kernel<2>,
+                                               attention_kernel<3>};
+  kernels[flags]<<<static_cast<unsigned>(grid), kAttnThreads, kAttnSmemBytes,
+                   static_cast<cudaStream_t>(stream)>>>(mq, mk, mv, mks, mdv, P);
   return launch_status();
 }
 
@@ -362,7 +368,12 @@ ovc_status ovc_prepare_ex(const ovc_tensor* q, const ovc_tensor* k, const ovc_te
 }
 
 ovc_status ovc_attention(const ovc_prepared* p, float softmax_scale, const ovc_output* o, void* stream) {
-  return run_attention(p, nullptr, softmax_scale, o, nullptr, stream);
+  return run_attention(p, nullptr, softmax_scale, o, nullptr, 0, stream);
+}
+
+ovc_status ovc_attention_ex(const ovc_prepared* p, const ovc_repair* r, float softmax_scale, const ovc_output* o,
+                            uint32_t flags, void* stream) {
+  return run_attention(p, r, softmax_scale, o, nullptr, flags, stream);
 }
 
 size_t ovc_repair_workspace_bytes(int64_t B, int64_t S, int64_t H, float budget) {
@@ -431,12 +442,12 @@ ovc_status ovc_prepare_v_repair(const ovc_tensor* v, const ovc_prepared* p, floa
 ovc_status ovc_attention_v_repair(const ovc_prepared* p, const ovc_repair* r, float softmax_scale,
                                   const ovc_output* o, void* stream) {
   if (!r) return OVC_ERR_INVALID_ARG;
-  return run_attention(p, r, softmax_scale, o, nullptr, stream);
+  return run_attention(p, r, softmax_scale, o, nullptr, 0, stream);
 }
 
 ovc_status ovc_attention_probe(const ovc_prepared* p, const ovc_repair* r, float softmax_scale,
                                const ovc_output* o, const ovc_probe* probe, void* stream) {
-  return run_attention(p, r, softmax_scale, o, probe, stream);
+  return run_attention(p, r, softmax_scale, o, probe, probe ? probe->flags : 0u, stream);
 }
 
 ovc_status ovc_get_device_status(void* stream) {

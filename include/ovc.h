@@ -125,6 +125,26 @@ ovc_status ovc_prepare(const ovc_tensor* q, const ovc_tensor* k, const ovc_tenso
 ovc_status ovc_attention(const ovc_prepared* p, float softmax_scale, const ovc_output* o,
                          void* stream);
 
+/* ovc_attention / ovc_attention_v_repair (r may be NULL) with a kernel
+ * variant.  flags (OR of):
+ *   OVC_ATTN_EXP_THEN_CAST  each probability byte is produced the way
+ *     ExpCast avoids: v = 2^8 p from one FMA and one ex2 on the special
+ *     function unit, then an FP32 -> E4M3 conversion (round to nearest even,
+ *     saturating).  "Open-VC attention", "Problem": one exponent per score
+ *     holds standard FP8 kernels to about half the FP8 peak on B200.
+ *   OVC_ATTN_NATURAL_ORDER  key blocks in order 0..nb-1 instead of cyclically
+ *     from the middle ("Architectural optimisations": mid-window traversal).
+ * Both together (OVC_ATTN_BASELINE) are the baseline VC-Attention kernel the
+ * pages compare against ("Open VC Attention": baselines.vc_attention): the
+ * same quantisation, lazy rescale, row sum (decoded bytes) and pipeline, so
+ * that only the byte path and the order differ.  flags = 0 is ovc_attention.
+ * Unknown flags give OVC_ERR_INVALID_ARG. */
+#define OVC_ATTN_EXP_THEN_CAST 1u
+#define OVC_ATTN_NATURAL_ORDER 2u
+#define OVC_ATTN_BASELINE 3u
+ovc_status ovc_attention_ex(const ovc_prepared* p, const ovc_repair* r, float softmax_scale,
+                            const ovc_output* o, uint32_t flags, void* stream);
+
 /* Bytes of workspace ovc_prepare_v_repair needs (0 if invalid).  budget in (0,1]. */
 size_t ovc_repair_workspace_bytes(int64_t B, int64_t S, int64_t H, float budget);
 
@@ -170,6 +190,7 @@ typedef struct {
   int32_t skip_mma;
   int32_t force_persistent;
   int64_t* trace;   /* device [4][64][8] int64 clock64() stamps of CTA 0, or NULL */
+  uint32_t flags;   /* OVC_ATTN_* variant flags, as for ovc_attention_ex */
 } ovc_probe;
 
 ovc_status ovc_attention_probe(const ovc_prepared* p, const ovc_repair* r, float softmax_scale,

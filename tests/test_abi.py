@@ -6,6 +6,7 @@ import os
 import re
 
 import pytest
+import torch
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -87,6 +88,14 @@ def test_host_validation_rejects_bad_arguments(lib):
     o = _abi.OvcOutput(0x2000, 128 * 128, 128, 128)
     assert lib.ovc_attention(ctypes.byref(_abi.OvcPrepared()), 0.0, ctypes.byref(o), None) == _abi.OVC_ERR_INVALID_ARG
     assert lib.ovc_attention_v_repair(ctypes.byref(_abi.OvcPrepared()), None, 0.0, ctypes.byref(o), None) == _abi.OVC_ERR_INVALID_ARG
+    # kernel-variant flags: unknown bits are rejected before any device call;
+    # known ones pass validation (and then fail only for want of a GPU)
+    p = _abi.OvcPrepared(1, 128, 1, 1, 128, 0x1000, 0x2000, 0x3000, 0x4000, 0x4100, 0x4200, 0x4300, 0x4400)
+    assert lib.ovc_attention_ex(ctypes.byref(p), None, 0.0, ctypes.byref(o), 4, None) == _abi.OVC_ERR_INVALID_ARG
+    assert lib.ovc_attention_ex(ctypes.byref(_abi.OvcPrepared()), None, 0.0, ctypes.byref(o), 3, None) == _abi.OVC_ERR_INVALID_ARG
+    if not torch.cuda.is_available():
+        assert lib.ovc_attention_ex(ctypes.byref(p), None, 0.0, ctypes.byref(o), 3, None) in (
+            _abi.OVC_ERR_CUDA, _abi.OVC_ERR_UNSUPPORTED)
 
 
 def test_status_strings(lib):

@@ -262,3 +262,66 @@ def test_k_smoothing_lowers_error_on_biased_keys():
             den += np.sum(ref ** 2)
         errs.append(math.sqrt(num / den))
     assert errs[1] < errs[0]
+
+
+# ---- kernel variants: exp-then-cast bytes and the natural key order -------
+VARIANTS = [(1, True, False), (2, False, True), (3, True, True)]
+
+
+@pytest.mark.parametrize("flags,cast,natural", VARIANTS)
+@pytest.mark.parametrize("B,H,S", [(1, 2, 1024), (1, 1, 127), (2, 3, 300), (1, 2, 1000)])
+def test_attention_variants_match_oracle(flags, cast, natural, B, H, S):
+    q, k, v = inputs(B, H, S, seed=600 + S)
+    ref, _ = oracle.attention_full(oracle_prep(q, k, v), cast=cast, mid_window=not natural)
+    prep = ovc.prepare(*to_dev(q, k, v))
+    o = ovc.attention_prepared(prep, flags=flags)
+    assert ovc.device_status() == 0
+    got = o.float().cpu().numpy()
+    assert np.isfinite(got).all()
+    assert rel_l2(got, ref) <= TOL_REL_L2
+    if cast or (S + 127) // 128 > 1:              # one key block: both orders coincide
+        base = ovc.attention_prepared(prep).float().cpu().numpy()
+        assert not np.array_equal(got, base)      # the variant really ran
+
+
+@pytest.mark.parametrize("S,qb,kb", [(1024, 3, 0), (1000, 7, 7), (300, 2, 1)])
+def test_baseline_p_codes_within_one_code_under_device_reference(S, qb, kb):
+    H = 2
+    q, k, v = inputs(1, H, S, seed=700 + S)
+    ref = oracle_prep(q, k, v)
+    prep = ovc.prepare(*to_dev(q, k, v))
+    bh = 1
+    _, codes, m8 = ovc.attention_probe(prep, dump=(bh, qb, kb), flags=3)
+    codes = codes.cpu().numpy()
+    m8 = m8.cpu().numpy()
+    diffs = []
+    for r in [r for r in range(128) if qb * 128 + r < S]:
+        assert np.isfinite(m8[r])
+        want = oracle.block_codes(ref, bh, qb * 128 + r, kb, float(m8[r]), cast=True)
+        d = np.abs(codes[r].astype(int) - want.astype(int))
+        assert d.max() <= 1, (r, d.max())
+        diffs.append(d)
+    assert float(np.mean(np.concatenate(diffs) == 0)) > 0.99
+
+
+def test_baseline_with_repair_and_schedules():
+    B, H, S, budget = 1, 2, 1100, 0.02
+    q, k, v = inputs(B, H, S, seed=800)
+    ref = oracle_prep(q, k, v)
+    want, _ = oracle.attention_full(ref, repair=oracle.Repair(ref, budget), cast=True, mid_window=False)
+    qd, kd, vd = to_dev(q, k, v)
+    prep = ovc.prepare(qd, kd, vd)
+    rep = ovc.prepare_v_repair(vd, prep, budget)
+    o = ovc.attention_prepared(prep, rep=rep, flags=3)
+    assert rel_l2(o.float().cpu().numpy(), want) <= TOL_REL_L2
+    a, _, _ = ovc.attention_probe(prep, rep, force_persistent=1, flags=3)
+    b, _, _ = ovc.attention_probe(prep, rep, force_persistent=-1, flags=3)
+    assert ovc.device_status() == 0
+    assert torch.equal(a, b) and torch.equal(a, o)
+
+
+def test_vc_attention_baseline_entry_point():
+    q, k, v = inputs(1, 2, 700, seed=801)
+    want, _ = oracle.attention_full(oracle_prep(q, k, v), cast=True, mid_window=False)
+    o = ovc.vc_attention_baseline(*to_dev(q, k, v))
+    assert rel_l2(o.float().cpu().numpy(), want) <= TOL_REL_L2
