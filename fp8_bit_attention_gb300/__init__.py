@@ -7,8 +7,8 @@ if it has not been built.
 """
 from .api import (OvcError, Prepared, Repair, attention, attention_prepared, attention_probe,
                   attention_v_repair, attn_flags, device_status, flops, prepare, prepare_v_repair,
-                  prepare_workspace_bytes, repair_workspace_bytes, vc_attention_baseline)
+                  prepare_workspace_bytes, repair_workspace_bytes, baseline_attention)
 
 __all__ = ["OvcError", "Prepared", "Repair", "attention", "attention_prepared", "attention_probe",
            "attention_v_repair", "attn_flags", "device_status", "flops", "prepare", "prepare_v_repair",
-           "prepare_workspace_bytes", "repair_workspace_bytes", "vc_attention_baseline"]
+           "prepare_workspace_bytes", "repair_workspace_bytes", "baseline_attention"]

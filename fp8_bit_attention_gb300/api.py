@@ -192,12 +192,13 @@ def attention_prepared(prep: Prepared, *, softmax_scale: float | None = None,
     return out
 
 
-def vc_attention_baseline(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *,
-                          softmax_scale: float | None = None, out: torch.Tensor | None = None,
-                          stream=None) -> torch.Tensor:
-    """The baseline VC-Attention kernel on CUDA tensors: the same preparation,
-    then exp-then-cast probability bytes and the natural key order
-    ("Open VC Attention": baselines.vc_attention(q, k, v))."""
+def baseline_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *,
+                       softmax_scale: float | None = None, out: torch.Tensor | None = None,
+                       stream=None) -> torch.Tensor:
+    """The exp-then-cast baseline on CUDA tensors: the same preparation, then
+    probability bytes from an exponent and an FP8 conversion ("Open-VC
+    attention", "Problem") and the natural key order, in the same kernel
+    pipeline as :func:`attention` so that the two differ only there."""
     prep = prepare(q, k, v, stream=stream)
     return attention_prepared(prep, softmax_scale=softmax_scale, out=out, stream=stream,
                               flags=_abi.OVC_ATTN_BASELINE)

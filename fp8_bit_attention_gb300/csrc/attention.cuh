@@ -141,7 +141,8 @@ __device__ __forceinline__ TileCoord tile_coord(const AttnParams& P, int tile) {
 
 // Kernel variants (template argument of attention_kernel): ExpCast with the
 // mid-window order is the method; the exp-then-cast byte path and the natural
-// key order together form the baseline that ExpCast is measured against.
+// key order together form the standard FP8 kernel that the two techniques
+// improve on, measured in this same pipeline.
 constexpr int kVarExpThenCast = 1;   // p byte = E4M3(ex2(...)) on the MUFU
 constexpr int kVarNaturalOrder = 2;  // key blocks 0, 1, ..., nb-1
 

@@ -134,10 +134,13 @@ ovc_status ovc_attention(const ovc_prepared* p, float softmax_scale, const ovc_o
  *     holds standard FP8 kernels to about half the FP8 peak on B200.
  *   OVC_ATTN_NATURAL_ORDER  key blocks in order 0..nb-1 instead of cyclically
  *     from the middle ("Architectural optimisations": mid-window traversal).
- * Both together (OVC_ATTN_BASELINE) are the baseline VC-Attention kernel the
- * pages compare against ("Open VC Attention": baselines.vc_attention): the
- * same quantisation, lazy rescale, row sum (decoded bytes) and pipeline, so
- * that only the byte path and the order differ.  flags = 0 is ovc_attention.
+ * Both together (OVC_ATTN_BASELINE) make the standard FP8 kernel that ExpCast
+ * and the mid-window order improve on, in this library's own pipeline: the
+ * same quantisation, lazy rescale, row sum (decoded bytes) and warp
+ * specialisation, so that a timing difference isolates the two techniques.
+ * (The pages' baselines.vc_attention is the VC-Attention authors' code, which
+ * already uses ExpCast; that implementation is not reproduced here.)
+ * flags = 0 is ovc_attention.
  * Unknown flags give OVC_ERR_INVALID_ARG. */
 #define OVC_ATTN_EXP_THEN_CAST 1u
 #define OVC_ATTN_NATURAL_ORDER 2u

@@ -320,8 +320,8 @@ def test_baseline_with_repair_and_schedules():
     assert torch.equal(a, b) and torch.equal(a, o)
 
 
-def test_vc_attention_baseline_entry_point():
+def test_baseline_attention_entry_point():
     q, k, v = inputs(1, 2, 700, seed=801)
     want, _ = oracle.attention_full(oracle_prep(q, k, v), cast=True, mid_window=False)
-    o = ovc.vc_attention_baseline(*to_dev(q, k, v))
+    o = ovc.baseline_attention(*to_dev(q, k, v))
     assert rel_l2(o.float().cpu().numpy(), want) <= TOL_REL_L2

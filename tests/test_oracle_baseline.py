@@ -1,7 +1,7 @@
 """Pins of the oracle's baseline path: exp-then-cast probability bytes and the
-natural key order, the kernel that ExpCast is measured against ("Open VC
-Attention" catalogue entry: baselines.vc_attention; "Open-VC attention" news
-item, "Problem": one exponent per score, then a conversion to FP8).
+natural key order, the standard FP8 kernel that ExpCast and the mid-window
+order improve on ("Open-VC attention" news item, "Problem": one exponent per
+score, then a conversion to FP8; "Architectural optimisations").
 
 * The exp-then-cast byte equals torch's own float32 -> float8_e4m3fn cast of
   the stored value 2^((Z - m8 + c0 - 56)/8) (an independent implementation
