@@ -88,10 +88,10 @@ def lib():
             L.ovc_oracle_attention_rows.restype = ctypes.c_int
             L.ovc_oracle_attention_rows.argtypes = (
                 [P, P, P, P, P, P, i64, i64, i64, P, P, P, i64, P, P, i64, d, d, d, d,
-                 ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P, P, i64, P, P, ctypes.c_int])
+                 ctypes.c_int, ctypes.c_int, ctypes.c_int, i64, P, P, P, P, i64, P, P, ctypes.c_int])
             L.ovc_oracle_attention_exact_rows.restype = ctypes.c_int
             L.ovc_oracle_attention_exact_rows.argtypes = (
-                [P, P, P, i64, i64, P, P, i64, d, d, ctypes.c_int, ctypes.c_int, P, P,
+                [P, P, P, i64, i64, P, P, i64, d, d, ctypes.c_int, ctypes.c_int, i64, P, P,
                  ctypes.c_int])
             _lib = L
     return _lib
@@ -271,10 +271,11 @@ class Repair:
 
 
 def attention_rows(prep: Prepared, rows_bh, rows_s, *, sm=None, repair: Repair | None = None,
-                   c0=C0, beta=BETA, tau=TAU, mid_window=True, snap=True, cast=False,
+                   c0=C0, beta=BETA, tau=TAU, mid_window=True, snap=True, cast=False, nsplit=1,
                    dump_block=-1, nthreads=None):
     """ExpCast attention for query rows (bh = b*H + h, s); cast=True gives the
-    exp-then-cast baseline's bytes, mid_window=False the natural key order.
+    exp-then-cast baseline's bytes, mid_window=False the natural key order,
+    nsplit > 1 the split key ranges merged at the end (no repair).
 
     Returns dict(out [n,128] float64, m8 [n], l [n], nres [n,2], and, when
     dump_block >= 0, codes [n,128] uint8 + dump_m8 [n])."""
@@ -297,7 +298,7 @@ def attention_rows(prep: Prepared, rows_bh, rows_s, *, sm=None, repair: Repair |
         _ptr(prep.qc), _ptr(prep.sq), _ptr(prep.kc), _ptr(prep.sk), _ptr(prep.vc), _ptr(prep.sv),
         prep.B, prep.S, prep.H, _ptr(ridx), _ptr(rdc), _ptr(rsr), nrep,
         _ptr(rows_bh), _ptr(rows_s), n, c0, beta, tau, sm, int(mid_window), int(snap), int(cast),
-        _ptr(out), _ptr(m8), _ptr(l), _ptr(nres), dump_block, _ptr(codes), _ptr(dm8),
+        int(nsplit), _ptr(out), _ptr(m8), _ptr(l), _ptr(nres), dump_block, _ptr(codes), _ptr(dm8),
         nthreads or default_threads())
     if rc != 0:
         raise ValueError(f"oracle attention_rows failed ({rc})")
@@ -334,7 +335,7 @@ def block_codes(prep: Prepared, bh: int, s: int, j: int, m8: float, *, sm=None,
 
 
 def attention_exact_rows(q, k, v, rows_bh, rows_s, *, sm=None, tau=TAU, mid_window=True,
-                         snap=True, nthreads=None):
+                         snap=True, nsplit=1, nthreads=None):
     """Online-softmax skeleton with exact exp2 on raw inputs [BH,S,128] (double)."""
     q = np.ascontiguousarray(q, dtype=np.float64)
     k = np.ascontiguousarray(k, dtype=np.float64)
@@ -348,7 +349,7 @@ def attention_exact_rows(q, k, v, rows_bh, rows_s, *, sm=None, tau=TAU, mid_wind
     nres = np.zeros(n, np.int32)
     rc = lib().ovc_oracle_attention_exact_rows(
         _ptr(q), _ptr(k), _ptr(v), BH, S, _ptr(rows_bh), _ptr(rows_s), n, tau, sm,
-        int(mid_window), int(snap), _ptr(out), _ptr(nres), nthreads or default_threads())
+        int(mid_window), int(snap), int(nsplit), _ptr(out), _ptr(nres), nthreads or default_threads())
     if rc != 0:
         raise ValueError(f"oracle attention_exact_rows failed ({rc})")
     return out, nres

@@ -206,13 +206,21 @@ struct Params {
   int cast;         // 1: exp-then-cast bytes (the baseline) instead of ExpCast
 };
 
-// Key-block visiting order.  [OVC-news "Architectural optimisations";
+// Key-block visiting order over the blocks [b0, b1) (the whole sequence, or
+// one key range of a split).  [OVC-news "Architectural optimisations";
 // OVC-lib: keys traversed from the middle of the window]
-std::vector<int64_t> key_block_order(int64_t nb, int mid_window) {
-  std::vector<int64_t> order(nb);
-  const int64_t start = mid_window ? nb / 2 : 0;
-  for (int64_t i = 0; i < nb; ++i) order[i] = (start + i) % nb;
+std::vector<int64_t> key_block_order(int64_t b0, int64_t b1, int mid_window) {
+  const int64_t n = b1 - b0;
+  std::vector<int64_t> order(n);
+  const int64_t start = mid_window ? n / 2 : 0;
+  for (int64_t i = 0; i < n; ++i) order[i] = b0 + (start + i) % n;
   return order;
+}
+
+// Key range of split s of n: blocks [floor(s nb / n), floor((s+1) nb / n)).
+void split_range(int64_t nb, int64_t n, int64_t s, int64_t* b0, int64_t* b1) {
+  *b0 = s * nb / n;
+  *b1 = (s + 1) * nb / n;
 }
 
 // One head, decoded to double.  Keys and values are token-major [S][128].
@@ -296,7 +304,9 @@ double dot128(const double* a, const double* b) {
 // forward MHA, head dim 128; OVC-news "Solution"; VC-summary "V-Smooth":
 // the row sum kept by online softmax]
 void attend_row(const double* q, double qscale, const HeadView& hv, const Params& P,
-                RowResult* res, int64_t dump_block, uint8_t* dump_codes, double* dump_m8) {
+                RowResult* res, int64_t dump_block, uint8_t* dump_codes, double* dump_m8,
+                int64_t b0 = 0, int64_t b1 = -1) {
+  if (b1 < 0) b1 = hv.nb;
   double m8 = -INFINITY;
   double l = 0.0;
   double O[128], Orep[128];
@@ -304,8 +314,8 @@ void attend_row(const double* q, double qscale, const HeadView& hv, const Params
   int32_t nres = 0, nres_rep = 0;
   double Z[128];
 
-  const std::vector<int64_t> order = key_block_order(hv.nb, P.mid_window);
-  for (int64_t i = 0; i < hv.nb; ++i) {
+  const std::vector<int64_t> order = key_block_order(b0, b1, P.mid_window);
+  for (int64_t i = 0; i < b1 - b0; ++i) {
     const int64_t j = order[i];
     const int64_t k0 = j * 128;
     const int64_t nk = std::min<int64_t>(128, hv.S - k0);   // tail block
@@ -356,6 +366,44 @@ void attend_row(const double* q, double qscale, const HeadView& hv, const Params
   res->l = l;
   res->nrescale = nres;
   res->nrescale_repair = nres_rep;
+}
+
+// Split key ranges (short sequences): each of the n ranges runs its own
+// online softmax (own reference m8_s, row sum l_s, output O_s = s_v O_acc/l_s),
+// then the ranges are merged exactly: with M = max m8_s and
+// w_s = l_s 2^((m8_s - M)/8), O = sum w_s O_s / sum w_s.  This is the
+// standard merge of partial softmax results; it changes only where each
+// range's ExpCast reference sits.  No repair set (the caller checks).
+void attend_row_split(const double* q, double qscale, const HeadView& hv, const Params& P, int64_t nsplit,
+                      RowResult* res, int64_t dump_block, uint8_t* dump_codes, double* dump_m8) {
+  if (nsplit <= 1) {
+    attend_row(q, qscale, hv, P, res, dump_block, dump_codes, dump_m8);
+    return;
+  }
+  std::vector<RowResult> part(nsplit);
+  double M = -INFINITY;
+  int32_t nres = 0;
+  for (int64_t s = 0; s < nsplit; ++s) {
+    int64_t b0, b1;
+    split_range(hv.nb, nsplit, s, &b0, &b1);
+    const bool mine = dump_block >= b0 && dump_block < b1;
+    attend_row(q, qscale, hv, P, &part[s], mine ? dump_block : -1, mine ? dump_codes : nullptr,
+               mine ? dump_m8 : nullptr, b0, b1);
+    M = std::max(M, part[s].m8);
+    nres += part[s].nrescale;
+  }
+  double W = 0.0, O[128];
+  for (int d = 0; d < 128; ++d) O[d] = 0.0;
+  for (int64_t s = 0; s < nsplit; ++s) {
+    const double w = part[s].l * std::exp2((part[s].m8 - M) / 8.0);
+    W += w;
+    for (int d = 0; d < 128; ++d) O[d] += w * part[s].O[d];
+  }
+  for (int d = 0; d < 128; ++d) res->O[d] = O[d] / W;
+  res->m8 = M;
+  res->l = W;
+  res->nrescale = nres;
+  res->nrescale_repair = 0;
 }
 
 template <class F>
@@ -581,11 +629,12 @@ int ovc_oracle_attention_rows(const uint8_t* qc, const float* sq, const uint8_t*
                               const int32_t* rep_idx, const uint8_t* rep_dcodes, const float* sr,
                               int64_t n_rep, const int64_t* row_bh, const int64_t* row_s,
                               int64_t nrows, double c0, double beta, double tau, double sm,
-                              int mid_window, int snap, int cast, double* out, double* m8_out, double* l_out,
+                              int mid_window, int snap, int cast, int64_t nsplit, double* out, double* m8_out, double* l_out,
                               int32_t* nres_out, int64_t dump_block, uint8_t* dump_codes,
                               double* dump_m8, int nthreads) {
   const Dims dm = make_dims(B, S, H);
   const Params P{c0, beta, tau, sm, 0, mid_window, snap, cast};
+  if (nsplit < 1 || nsplit > dm.nb || (nsplit > 1 && n_rep > 0)) return 3;
   // Process the rows head by head so that one head's keys are decoded once.
   std::vector<int64_t> perm(nrows);
   for (int64_t i = 0; i < nrows; ++i) perm[i] = i;
@@ -631,8 +680,8 @@ int ovc_oracle_attention_rows(const uint8_t* qc, const float* sq, const uint8_t*
       double q[128];
       for (int d = 0; d < 128; ++d) q[d] = e4m3_value(qc[(bh * dm.S_pad + s) * 128 + d]);
       RowResult rr;
-      attend_row(q, sq[bh * dm.nb + s / 128], hv, P, &rr, dump_block,
-                 dump_codes ? dump_codes + r * 128 : nullptr, dump_m8 ? dump_m8 + r : nullptr);
+      attend_row_split(q, sq[bh * dm.nb + s / 128], hv, P, nsplit, &rr, dump_block,
+                       dump_codes ? dump_codes + r * 128 : nullptr, dump_m8 ? dump_m8 + r : nullptr);
       std::memcpy(out + r * 128, rr.O, sizeof(rr.O));
       if (m8_out) m8_out[r] = rr.m8;
       if (l_out) l_out[r] = rr.l;
@@ -653,9 +702,10 @@ int ovc_oracle_attention_rows(const uint8_t* qc, const float* sq, const uint8_t*
 int ovc_oracle_attention_exact_rows(const double* q, const double* k, const double* v, int64_t BH,
                                     int64_t S, const int64_t* row_bh, const int64_t* row_s,
                                     int64_t nrows, double tau, double sm, int mid_window, int snap,
-                                    double* out, int32_t* nres_out, int nthreads) {
+                                    int64_t nsplit, double* out, int32_t* nres_out, int nthreads) {
   const Dims dm = make_dims(1, S, 1);
   const Params P{120.0, -0.35, tau, sm, 1, mid_window, snap, 0};
+  if (nsplit < 1 || nsplit > dm.nb) return 3;
   std::vector<double> ones(dm.nb, 1.0);
   bool bad = false;
   parallel_for(nrows, nthreads, [&](int64_t r) {
@@ -671,7 +721,7 @@ int ovc_oracle_attention_exact_rows(const double* q, const double* k, const doub
     hv.kscale = ones.data();
     hv.V = v + bh * S * 128;
     RowResult rr;
-    attend_row(q + (bh * S + s) * 128, 1.0, hv, P, &rr, -1, nullptr, nullptr);
+    attend_row_split(q + (bh * S + s) * 128, 1.0, hv, P, nsplit, &rr, -1, nullptr, nullptr);
     std::memcpy(out + r * 128, rr.O, sizeof(rr.O));
     if (nres_out) nres_out[r] = rr.nrescale;
   });
