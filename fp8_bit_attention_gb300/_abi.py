@@ -61,7 +61,9 @@ SIGNATURES = {
                             P(OvcPrepared), c_ptr]),
     "ovc_attention": (c_i32, [P(OvcPrepared), ctypes.c_float, P(OvcOutput), c_ptr]),
     "ovc_attention_ex": (c_i32, [P(OvcPrepared), P(OvcRepair), ctypes.c_float, P(OvcOutput),
-                                 ctypes.c_uint32, c_ptr]),
+                                 ctypes.c_uint32, c_i32, c_ptr, ctypes.c_size_t, c_ptr]),
+    "ovc_attention_workspace_bytes": (ctypes.c_size_t, [P(OvcPrepared), c_i32]),
+    "ovc_attention_auto_split": (c_i32, [c_i64, c_i64, c_i64]),
     "ovc_repair_workspace_bytes": (ctypes.c_size_t, [c_i64, c_i64, c_i64, ctypes.c_float]),
     "ovc_prepare_v_repair": (c_i32, [P(OvcTensor), P(OvcPrepared), ctypes.c_float, c_ptr,
                                      ctypes.c_size_t, P(OvcRepair), c_ptr]),

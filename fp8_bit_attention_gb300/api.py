@@ -174,21 +174,43 @@ def attn_flags(exp_then_cast: bool = False, natural_order: bool = False) -> int:
         _abi.OVC_ATTN_NATURAL_ORDER if natural_order else 0)
 
 
+def auto_split(B: int, S: int, H: int) -> int:
+    """Key ranges the library splits each tile into for these dimensions on
+    the current device when left to choose (1: no split)."""
+    return int(lib().ovc_attention_auto_split(int(B), int(S), int(H)))
+
+
+def attention_workspace_bytes(prep: Prepared, nsplit: int = 0) -> int:
+    """Workspace of split key ranges (0: no split; nsplit = 0: automatic)."""
+    return int(lib().ovc_attention_workspace_bytes(ctypes.byref(prep.desc), int(nsplit)))
+
+
 def attention_prepared(prep: Prepared, *, softmax_scale: float | None = None,
                        out: torch.Tensor | None = None, stream=None, flags: int = 0,
-                       rep: "Repair | None" = None) -> torch.Tensor:
-    """O from prepared inputs: ovc_attention, or ovc_attention_ex when a kernel
-    variant (``flags``, see :func:`attn_flags`) or a repair set is given."""
+                       rep: "Repair | None" = None, nsplit: int | None = None,
+                       workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """O from prepared inputs (ovc_attention_ex): kernel variant ``flags`` (see
+    :func:`attn_flags`), optional repair set, and split key ranges for short
+    sequences -- ``nsplit=None`` lets the library choose and allocates the
+    workspace it needs here; ``nsplit=1`` never splits."""
     out = _out_for(prep, out)
     od = _output_desc(out)
     h = ctypes.c_void_p(_stream_handle(stream))
-    if flags == 0 and rep is None:
-        st = lib().ovc_attention(ctypes.byref(prep.desc), float(softmax_scale or 0.0), ctypes.byref(od), h)
-        check(st, "ovc_attention")
-    else:
-        st = lib().ovc_attention_ex(ctypes.byref(prep.desc), ctypes.byref(rep.desc) if rep is not None else None,
-                                    float(softmax_scale or 0.0), ctypes.byref(od), int(flags), h)
-        check(st, "ovc_attention_ex")
+    ns = 0 if nsplit is None else int(nsplit)
+    if rep is not None and nsplit is None:
+        ns = 1
+    need = attention_workspace_bytes(prep, ns) if ns != 1 else 0
+    if need and (workspace is None or workspace.numel() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=prep.workspace.device)
+    wp = workspace.data_ptr() if (need and workspace is not None) else None
+    if need == 0 and flags == 0 and rep is None:
+        check(lib().ovc_attention(ctypes.byref(prep.desc), float(softmax_scale or 0.0), ctypes.byref(od), h),
+              "ovc_attention")
+        return out
+    st = lib().ovc_attention_ex(ctypes.byref(prep.desc), ctypes.byref(rep.desc) if rep is not None else None,
+                                float(softmax_scale or 0.0), ctypes.byref(od), int(flags), ns,
+                                ctypes.c_void_p(wp), need, h)
+    check(st, "ovc_attention_ex")
     return out
 
 
@@ -344,6 +366,9 @@ def _stream_chunks(q4, k4, v4, o4, chunks, stage_in, stage_out, in_free, out_fre
                    softmax_scale, repair_budget, smooth_k):
     B, S, H, D = q4.shape
     el = q4.element_size()
+    # The key-range split of the whole-tensor call, so that the chunks give its
+    # result bit for bit.
+    nsplit = auto_split(B, S, H)
     for c, (h0, h1) in enumerate(chunks):
         hc, st = h1 - h0, c % 2
         ins = [buf[:B * S * hc * D].view(B, S, hc, D) for buf in stage_in[st]]
@@ -366,7 +391,7 @@ def _stream_chunks(q4, k4, v4, o4, chunks, stage_in, stage_out, in_free, out_fre
         if rep is not None:
             attention_v_repair(prep, rep, softmax_scale=softmax_scale, out=ob)
         else:
-            attention_prepared(prep, softmax_scale=softmax_scale, out=ob)
+            attention_prepared(prep, softmax_scale=softmax_scale, out=ob, nsplit=nsplit)
         done = torch.cuda.Event()
         done.record(comp)
         with torch.cuda.stream(s_out):
@@ -399,6 +424,7 @@ def flops(B: int, S: int, H: int, D: int = 128) -> float:
     return 4.0 * B * H * float(S) ** 2 * D
 
 
-__all__ = ["Prepared", "Repair", "OvcError", "prepare", "attention_prepared", "prepare_v_repair",
+__all__ = ["Prepared", "Repair", "OvcError", "prepare", "attention_prepared", "attention_workspace_bytes",
+           "auto_split", "prepare_v_repair",
            "attention_v_repair", "attention_probe", "device_status", "attention", "memcpy2d",
            "head_chunks", "prepare_workspace_bytes", "repair_workspace_bytes", "flops"]

@@ -36,6 +36,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include <cstdint>
 
@@ -68,6 +69,12 @@ constexpr unsigned kStatusTimeout = 1u;
 
 struct AttnParams {
   int32_t B, S, H, nb, S_pad, npairs, ntiles;
+  // Split key ranges (short sequences): unit u = tile * nsplit + s covers key
+  // blocks [s nb / nsplit, (s+1) nb / nsplit); with nsplit > 1 the epilogue
+  // writes partial results for merge_kernel instead of O.
+  int32_t nsplit, nunits;
+  uint16_t* part_o;       // [nunits][256][128] FP16: O_acc / l of each row
+  float2* part_ml;        // [nunits][256]: (m8, l) of each row
   const float* sq;
   const float* sk;
   const float* sv;
@@ -146,12 +153,28 @@ __device__ __forceinline__ TileCoord tile_coord(const AttnParams& P, int tile) {
 constexpr int kVarExpThenCast = 1;   // p byte = E4M3(ex2(...)) on the MUFU
 constexpr int kVarNaturalOrder = 2;  // key blocks 0, 1, ..., nb-1
 
-// Key block visited at step i: cyclic from the middle block, or in order.
+// Key block visited at step i of a range of n blocks starting at b0 (the
+// whole sequence, or one split range): cyclic from the range's middle block,
+// or in order.
 template <int kVar>
-__device__ __forceinline__ int key_block(int i, int nb) {
-  if (kVar & kVarNaturalOrder) return i;
-  const int j = nb / 2 + i;
-  return j >= nb ? j - nb : j;
+__device__ __forceinline__ int key_block(int i, int b0, int n) {
+  if (kVar & kVarNaturalOrder) return b0 + i;
+  const int j = n / 2 + i;
+  return b0 + (j >= n ? j - n : j);
+}
+
+struct UnitCoord {
+  TileCoord tc;
+  int b0, nbu;            // key blocks [b0, b0 + nbu)
+};
+
+__device__ __forceinline__ UnitCoord unit_coord(const AttnParams& P, int u) {
+  const int tile = u / P.nsplit, sp = u - tile * P.nsplit;
+  UnitCoord c;
+  c.tc = tile_coord(P, tile);
+  c.b0 = sp * P.nb / P.nsplit;
+  c.nbu = (sp + 1) * P.nb / P.nsplit - c.b0;
+  return c;
 }
 
 // ---------------------------------------------------------------------------
@@ -339,7 +362,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const volatile int* abort_flag = &sm.abort;
-  const int nblk = P.nb + P.rep_blocks;
   const uint64_t tmo = P.timeout_ns;
 
   if (warp == kProducerWarp && lane == 0) {
@@ -378,8 +400,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (lane == 0) {
       uint32_t kv_iter = 0, q_iter = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < P.ntiles && ok; tile += gridDim.x) {
-        const TileCoord tc = tile_coord(P, tile);
+      for (int u = blockIdx.x; u < P.nunits && ok; u += gridDim.x) {
+        const UnitCoord uc = unit_coord(P, u);
+        const TileCoord& tc = uc.tc;
+        const int nblk = uc.nbu + P.rep_blocks;
         if (q_iter > 0) ok = mbar_wait(smem_addr(&sm.q_empty), (q_iter - 1) & 1, tmo, abort_flag);
         if (!ok) break;
         const uint32_t qbar = smem_addr(&sm.q_full);
@@ -396,12 +420,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           const uint32_t kbar = smem_addr(&sm.k_full[stage]), vbar = smem_addr(&sm.v_full[stage]);
           mbar_arrive_expect_tx(kbar, kTile);
           mbar_arrive_expect_tx(vbar, kTile);
-          if (i < P.nb) {
-            const int j = key_block<kVar>(i, P.nb);
+          if (i < uc.nbu) {
+            const int j = key_block<kVar>(i, uc.b0, uc.nbu);
             tma_load_2d(smem_addr(sm.k[stage]), &tm_k, kbar, 0, tc.bh * P.S_pad + j * 128);
             tma_load_2d(smem_addr(sm.v[stage]), &tm_v, vbar, j * 128, tc.bh * 128);
           } else {
-            const int r = i - P.nb;
+            const int r = i - uc.nbu;
             tma_load_2d(smem_addr(sm.k[stage]), &tm_ks, kbar, 0, tc.bh * P.n_rep_pad + r * 128);
             tma_load_2d(smem_addr(sm.v[stage]), &tm_dv, vbar, r * 128, tc.bh * 128);
           }
@@ -428,7 +452,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const uint32_t tS0 = tmem + 0, tS1 = tmem + 128;
       const uint32_t tO0 = tmem + 256, tO1 = tmem + 384;
       const uint64_t qd0 = sw128_desc(smem_addr(sm.q[0])), qd1 = sw128_desc(smem_addr(sm.q[1]));
-      for (int tile = blockIdx.x; tile < P.ntiles && ok; tile += gridDim.x) {
+      for (int u = blockIdx.x; u < P.nunits && ok; u += gridDim.x) {
+        const int nblk = unit_coord(P, u).nbu + P.rep_blocks;
         ok = mbar_wait(smem_addr(&sm.q_full), q_iter & 1, tmo, abort_flag);
         if (!ok) break;
         // Scores of the first block for both query tiles.
@@ -518,8 +543,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     uint32_t blk_count = 0, tile_count = 0;
     const int trole = (wq == 0) ? t : -1;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < P.ntiles && ok; tile += gridDim.x) {
-      const TileCoord tc = tile_coord(P, tile);
+    for (int u = blockIdx.x; u < P.nunits && ok; u += gridDim.x) {
+      const UnitCoord uc = unit_coord(P, u);
+      const TileCoord& tc = uc.tc;
+      const int nblk = uc.nbu + P.rep_blocks;
       const int qb = t ? tc.qb1 : tc.qb0;
       const bool store = (t == 0) || tc.has1;
       const float sq = P.sq[tc.bh * P.nb + qb];
@@ -528,12 +555,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       float l = 0.0f;
       const bool dump_tile = (P.dump_codes != nullptr) && tc.bh == P.dump_bh && qb == P.dump_qb && store;
       // Key scale of the current block, loaded one block ahead.
-      float sk_next = __ldg(P.sk + tc.bh * P.nb + key_block<kVar>(0, P.nb));
+      float sk_next = __ldg(P.sk + tc.bh * P.nb + key_block<kVar>(0, uc.b0, uc.nbu));
       for (int i = 0; i < nblk; ++i) {
-        const bool main_blk = i < P.nb;
-        const int j = main_blk ? key_block<kVar>(i, P.nb) : 0;
+        const bool main_blk = i < uc.nbu;
+        const int j = main_blk ? key_block<kVar>(i, uc.b0, uc.nbu) : 0;
         const float skj = sk_next;
-        if (i + 1 < P.nb) sk_next = __ldg(P.sk + tc.bh * P.nb + key_block<kVar>(i + 1, P.nb));
+        if (i + 1 < uc.nbu) sk_next = __ldg(P.sk + tc.bh * P.nb + key_block<kVar>(i + 1, uc.b0, uc.nbu));
         const uint32_t gi = blk_count;
         if (trole >= 0) trace_mark(P, trole, gi, 0);
         ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&sm.s_full[t]), blk_count & 1, tmo, abort_flag));
@@ -578,7 +605,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           }
         } else {
           tmem_load_row128(tS, s);
-          const int r = i - P.nb;
+          const int r = i - uc.nbu;
           const int valid = P.n_rep - r * 128;
 #pragma unroll
           for (int c = 0; c < 128; ++c)
@@ -611,9 +638,35 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       ++tile_count;
       if (!ok) break;
       tc_fence_after();
+      const int q_row = qb * 128 + row;
+      if (P.nsplit > 1) {
+        // Partial result of this key range: O_acc / l as FP16 and (m8, l);
+        // merge_kernel combines the ranges of each row.
+        const float inv_l = 1.0f / l;
+        const int64_t prow = static_cast<int64_t>(u) * 256 + t * 128 + row;
+        uint16_t* po = P.part_o + prow * 128;
+#pragma unroll 1
+        for (int c = 0; c < 128; c += 32) {
+          uint32_t r[32];
+          tmem_ld32(tO + c, r);
+          tmem_wait_ld32(r);
+          if (store && q_row < P.S) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              __half2 h2 = __floats2half2_rn(__uint_as_float(r[2 * e]) * inv_l, __uint_as_float(r[2 * e + 1]) * inv_l);
+              pk[e] = *reinterpret_cast<uint32_t*>(&h2);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(po + c);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+          }
+        }
+        if (store && q_row < P.S) P.part_ml[prow] = make_float2(kf + kFrac, l);
+        continue;
+      }
       // Epilogue: O = scale * O_acc / l, BF16, one 256-byte row per thread.
       const float scale = (P.rep_blocks > 0 ? P.sr[tc.bh] : P.sv[tc.bh]) / l;
-      const int q_row = qb * 128 + row;
       const int b = tc.bh / P.H, h = tc.bh - b * P.H;
       uint16_t* orow = P.o + b * P.os[0] + static_cast<int64_t>(q_row) * P.os[1] + h * P.os[2];
 #pragma unroll 1
@@ -645,6 +698,49 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+}
+
+// ---------------------------------------------------------------------------
+// Merge of split key ranges: for each query row, with M = max_s m8_s and
+// w_s = l_s 2^((m8_s - M)/8),  O = s_v * sum_s w_s Ohat_s / sum_s w_s  (Ohat_s
+// = O_acc / l of range s, FP16), rounded to BF16.  One warp per row, four
+// channels per lane (8-byte loads of each partial, 8-byte stores).
+// ---------------------------------------------------------------------------
+constexpr int kMergeRowsPerBlock = 8;
+
+__global__ void __launch_bounds__(32 * kMergeRowsPerBlock)
+    merge_kernel(const __grid_constant__ AttnParams P) {
+  const int64_t g = static_cast<int64_t>(blockIdx.x) * kMergeRowsPerBlock + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int64_t nrows = static_cast<int64_t>(P.B) * P.H * P.S;
+  if (g >= nrows) return;
+  const int bh = static_cast<int>(g / P.S);
+  const int q = static_cast<int>(g - static_cast<int64_t>(bh) * P.S);
+  const int tile = bh * P.npairs + q / 256;
+  const int64_t prow0 = static_cast<int64_t>(tile) * P.nsplit * 256 + (q & 255);
+  float M = -INFINITY;
+  for (int sp = 0; sp < P.nsplit; ++sp) M = fmaxf(M, P.part_ml[prow0 + sp * 256].x);
+  float W = 0.0f, acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  for (int sp = 0; sp < P.nsplit; ++sp) {
+    const float2 ml = P.part_ml[prow0 + sp * 256];
+    const float w = ml.y * exp2f((ml.x - M) * 0.125f);
+    W += w;
+    const uint2 raw = *reinterpret_cast<const uint2*>(P.part_o + (prow0 + sp * 256) * 128 + 4 * lane);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+    acc[0] += w * a.x;
+    acc[1] += w * a.y;
+    acc[2] += w * b.x;
+    acc[3] += w * b.y;
+  }
+  const float scale = P.sv[bh] / W;
+  const int b = bh / P.H, h = bh - b * P.H;
+  __nv_bfloat162 o01 = __floats2bfloat162_rn(acc[0] * scale, acc[1] * scale);
+  __nv_bfloat162 o23 = __floats2bfloat162_rn(acc[2] * scale, acc[3] * scale);
+  uint2 outv;
+  outv.x = *reinterpret_cast<uint32_t*>(&o01);
+  outv.y = *reinterpret_cast<uint32_t*>(&o23);
+  *reinterpret_cast<uint2*>(P.o + b * P.os[0] + static_cast<int64_t>(q) * P.os[1] + h * P.os[2] + 4 * lane) = outv;
 }
 
 }  // namespace ovc

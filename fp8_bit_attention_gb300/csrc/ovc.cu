@@ -189,10 +189,50 @@ bool output_ok(const ovc_output* o) {
 
 ovc_status launch_status() { return cudaGetLastError() == cudaSuccess ? OVC_OK : OVC_ERR_CUDA; }
 
+// Split key ranges (short sequences).  The per-tile schedule launches one CTA
+// per tile; when the tiles fill the SMs badly (224 tiles on 152 SMs take two
+// full waves) each tile's keys are split into n ranges, giving n times as
+// many shorter units, and merge_kernel combines the ranges.
+constexpr int kMaxSplit = 16;
+constexpr int64_t kMergeCostBlocks = 4;   // merge launch + pass, in key-block times
+
+struct SplitLayout {
+  size_t o, ml, total;
+};
+
+SplitLayout split_layout(int64_t units) {
+  SplitLayout L{};
+  L.o = 0;
+  L.ml = align_up(static_cast<size_t>(units) * 256 * 128 * 2, 256);
+  L.total = L.ml + align_up(static_cast<size_t>(units) * 256 * sizeof(float2), 256);
+  return L;
+}
+
+// Number of ranges that minimises (waves of units) x (key blocks per unit),
+// plus the merge, for the per-tile schedule; ties go to fewer ranges.
+int64_t auto_split(int64_t ntiles, int64_t nb, int sms) {
+  int64_t best = 1, best_cost = (ntiles + sms - 1) / sms * nb;
+  for (int64_t n = 2; n <= kMaxSplit && n <= nb; ++n) {
+    const int64_t cost = (ntiles * n + sms - 1) / sms * ((nb + n - 1) / n) + kMergeCostBlocks;
+    if (cost < best_cost) best = n, best_cost = cost;
+  }
+  return best;
+}
+
+bool persistent_schedule(const ovc_prepared* p, const ovc_probe* probe) {
+  const int force = probe ? probe->force_persistent : 0;
+  return force > 0 || (force == 0 && p->S >= 32768);
+}
+
+int64_t ntiles_of(const ovc_prepared* p) { return p->B * p->H * ((p->nb + 1) / 2); }
+
 ovc_status run_attention(const ovc_prepared* p, const ovc_repair* r, float softmax_scale,
-                         const ovc_output* o, const ovc_probe* probe, uint32_t flags, void* stream) {
+                         const ovc_output* o, const ovc_probe* probe, uint32_t flags, int32_t nsplit,
+                         void* workspace, size_t workspace_bytes, void* stream) {
   if (!prepared_ok(p) || !output_ok(o)) return OVC_ERR_INVALID_ARG;
   if (flags & ~(OVC_ATTN_EXP_THEN_CAST | OVC_ATTN_NATURAL_ORDER)) return OVC_ERR_INVALID_ARG;
+  if (nsplit < 0 || nsplit > kMaxSplit || nsplit > p->nb || (nsplit > 1 && r)) return OVC_ERR_INVALID_ARG;
+  if (nsplit > 1 && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))) return OVC_ERR_INVALID_ARG;
   if (r) {
     if (!r->idx || !r->k_sel || !r->dvt || !r->sk_sel || !r->sr) return OVC_ERR_INVALID_ARG;
     if (r->B != p->B || r->S != p->S || r->H != p->H) return OVC_ERR_INVALID_ARG;
@@ -225,6 +265,22 @@ ovc_status run_attention(const ovc_prepared* p, const ovc_repair* r, float softm
   P.npairs = (P.nb + 1) / 2;
   const int64_t ntiles = BH * P.npairs;   // a tile is a pair of 128-row query blocks
   P.ntiles = static_cast<int32_t>(ntiles);
+  const bool persistent = persistent_schedule(p, probe);
+  int64_t ns = nsplit;
+  if (ns == 0) {   // automatic: only on the per-tile schedule, without repair, given workspace
+    ns = (r || persistent || !workspace) ? 1 : auto_split(ntiles, p->nb, dev->sms);
+    if (ns > 1 && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return OVC_ERR_INVALID_ARG;
+  }
+  const int64_t nunits = ntiles * ns;
+  if (nunits > 0x7FFFFFFF) return OVC_ERR_INVALID_ARG;
+  P.nsplit = static_cast<int32_t>(ns);
+  P.nunits = static_cast<int32_t>(nunits);
+  if (ns > 1) {
+    const SplitLayout SL = split_layout(nunits);
+    if (workspace_bytes < SL.total) return OVC_ERR_WORKSPACE_TOO_SMALL;
+    P.part_o = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + SL.o);
+    P.part_ml = reinterpret_cast<float2*>(static_cast<uint8_t*>(workspace) + SL.ml);
+  }
   P.sq = p->sq;
   P.sk = p->sk;
   P.sv = p->sv;
@@ -243,7 +299,6 @@ ovc_status run_attention(const ovc_prepared* p, const ovc_repair* r, float softm
   }
   P.dump_bh = -1;
   P.timeout_ns = kDefaultTimeoutNs;
-  int force = 0;
   if (probe) {
     P.dump_bh = probe->dump_codes ? probe->dump_bh : -1;
     P.dump_qb = probe->dump_qblock;
@@ -252,21 +307,25 @@ ovc_status run_attention(const ovc_prepared* p, const ovc_repair* r, float softm
     P.dump_m8 = probe->dump_m8;
     if (probe->wait_timeout_ns > 0) P.timeout_ns = probe->wait_timeout_ns;
     P.skip_mma = probe->skip_mma;
-    force = probe->force_persistent;
     P.trace = reinterpret_cast<long long*>(probe->trace);
   }
   P.status = dev->status;
 
   // The packed long-sequence path (S >= 32768) is persistent: one CTA per SM
-  // looping over tiles.  Shorter sequences launch one CTA per tile.
-  const bool persistent = force > 0 || (force == 0 && p->S >= 32768);
-  const int64_t grid = persistent ? (ntiles < dev->sms ? ntiles : dev->sms) : ntiles;
+  // looping over tiles.  Shorter sequences launch one CTA per unit (a tile,
+  // or one key range of a tile).
+  const int64_t grid = persistent ? (nunits < dev->sms ? nunits : dev->sms) : nunits;
   static_assert(OVC_ATTN_EXP_THEN_CAST == kVarExpThenCast && OVC_ATTN_NATURAL_ORDER == kVarNaturalOrder,
                 "flag bits select the kernel variant");
   decltype(&attention_kernel<0>) kernels[4] = {attention_kernel<0>, attention_kernel<1>, attention_kernel<2>,
                                                attention_kernel<3>};
   kernels[flags]<<<static_cast<unsigned>(grid), kAttnThreads, kAttnSmemBytes,
                    static_cast<cudaStream_t>(stream)>>>(mq, mk, mv, mks, mdv, P);
+  if (ns > 1) {
+    const int64_t rows = BH * p->S;
+    merge_kernel<<<static_cast<unsigned>((rows + kMergeRowsPerBlock - 1) / kMergeRowsPerBlock),
+                   32 * kMergeRowsPerBlock, 0, static_cast<cudaStream_t>(stream)>>>(P);
+  }
   return launch_status();
 }
 
@@ -368,12 +427,32 @@ ovc_status ovc_prepare_ex(const ovc_tensor* q, const ovc_tensor* k, const ovc_te
 }
 
 ovc_status ovc_attention(const ovc_prepared* p, float softmax_scale, const ovc_output* o, void* stream) {
-  return run_attention(p, nullptr, softmax_scale, o, nullptr, 0, stream);
+  return run_attention(p, nullptr, softmax_scale, o, nullptr, 0, 1, nullptr, 0, stream);
 }
 
 ovc_status ovc_attention_ex(const ovc_prepared* p, const ovc_repair* r, float softmax_scale, const ovc_output* o,
-                            uint32_t flags, void* stream) {
-  return run_attention(p, r, softmax_scale, o, nullptr, flags, stream);
+                            uint32_t flags, int32_t nsplit, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  return run_attention(p, r, softmax_scale, o, nullptr, flags, nsplit, workspace, workspace_bytes, stream);
+}
+
+int32_t ovc_attention_auto_split(int64_t B, int64_t S, int64_t H) {
+  if (!dims_ok(B, S, H) || S >= 32768) return 1;
+  DeviceState* dev = nullptr;
+  if (device_state(&dev) != OVC_OK) return 1;
+  const int64_t nb = (S + 127) / 128;
+  return static_cast<int32_t>(auto_split(B * H * ((nb + 1) / 2), nb, dev->sms));
+}
+
+size_t ovc_attention_workspace_bytes(const ovc_prepared* p, int32_t nsplit) {
+  if (!prepared_ok(p) || nsplit < 0 || nsplit > kMaxSplit || nsplit > p->nb) return 0;
+  int64_t ns = nsplit;
+  if (ns == 0) {
+    DeviceState* dev = nullptr;
+    if (persistent_schedule(p, nullptr) || device_state(&dev) != OVC_OK) return 0;
+    ns = auto_split(ntiles_of(p), p->nb, dev->sms);
+  }
+  return ns > 1 ? split_layout(ntiles_of(p) * ns).total : 0;
 }
 
 size_t ovc_repair_workspace_bytes(int64_t B, int64_t S, int64_t H, float budget) {
@@ -442,12 +521,12 @@ ovc_status ovc_prepare_v_repair(const ovc_tensor* v, const ovc_prepared* p, floa
 ovc_status ovc_attention_v_repair(const ovc_prepared* p, const ovc_repair* r, float softmax_scale,
                                   const ovc_output* o, void* stream) {
   if (!r) return OVC_ERR_INVALID_ARG;
-  return run_attention(p, r, softmax_scale, o, nullptr, 0, stream);
+  return run_attention(p, r, softmax_scale, o, nullptr, 0, 1, nullptr, 0, stream);
 }
 
 ovc_status ovc_attention_probe(const ovc_prepared* p, const ovc_repair* r, float softmax_scale,
                                const ovc_output* o, const ovc_probe* probe, void* stream) {
-  return run_attention(p, r, softmax_scale, o, probe, probe ? probe->flags : 0u, stream);
+  return run_attention(p, r, softmax_scale, o, probe, probe ? probe->flags : 0u, 1, nullptr, 0, stream);
 }
 
 ovc_status ovc_get_device_status(void* stream) {

@@ -126,7 +126,26 @@ ovc_status ovc_attention(const ovc_prepared* p, float softmax_scale, const ovc_o
                          void* stream);
 
 /* ovc_attention / ovc_attention_v_repair (r may be NULL) with a kernel
- * variant.  flags (OR of):
+ * variant and, for short sequences, split key ranges.
+ *
+ * Split key ranges (nsplit): the per-tile schedule (S < 32768) launches one
+ * CTA per pair of 128-row query blocks; when those fill the SMs badly (224
+ * tiles on 152 SMs run as two full waves), each tile's key blocks are cut
+ * into nsplit contiguous ranges [s nb/nsplit, (s+1) nb/nsplit), each run as
+ * its own online softmax (own reference, own row sum, mid-window order within
+ * the range), and a merge pass combines them: with M = max m8_s and
+ * w_s = l_s 2^((m8_s - M)/8), O = sum w_s O_s / sum w_s.  The partial results
+ * live in caller workspace (ovc_attention_workspace_bytes).
+ *   nsplit     0: automatic (1 without workspace, with a repair set or on the
+ *              persistent schedule); 1..16: forced (<= nb; > 1 needs
+ *              workspace and no repair set).
+ *   workspace  device memory, 256-byte aligned, at least
+ *              ovc_attention_workspace_bytes(p, nsplit) bytes; may be NULL
+ *              when no split is made.  Calls that share it must not overlap.
+ * Errors: OVC_ERR_INVALID_ARG (bad nsplit, repair with nsplit > 1, unaligned
+ * workspace), OVC_ERR_WORKSPACE_TOO_SMALL.
+ *
+ * flags (OR of):
  *   OVC_ATTN_EXP_THEN_CAST  each probability byte is produced the way
  *     ExpCast avoids: v = 2^8 p from one FMA and one ex2 on the special
  *     function unit, then an FP32 -> E4M3 conversion (round to nearest even,
@@ -146,7 +165,18 @@ ovc_status ovc_attention(const ovc_prepared* p, float softmax_scale, const ovc_o
 #define OVC_ATTN_NATURAL_ORDER 2u
 #define OVC_ATTN_BASELINE 3u
 ovc_status ovc_attention_ex(const ovc_prepared* p, const ovc_repair* r, float softmax_scale,
-                            const ovc_output* o, uint32_t flags, void* stream);
+                            const ovc_output* o, uint32_t flags, int32_t nsplit, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+/* Workspace bytes ovc_attention_ex needs for nsplit ranges (nsplit = 0: the
+ * automatic choice on the current device).  0 when no split is made, or for
+ * invalid arguments. */
+size_t ovc_attention_workspace_bytes(const ovc_prepared* p, int32_t nsplit);
+
+/* The number of key ranges the automatic choice (nsplit = 0) makes for these
+ * dimensions on the current device: 1 for S >= 32768 (persistent schedule),
+ * for invalid dimensions or without a usable device. */
+int32_t ovc_attention_auto_split(int64_t B, int64_t S, int64_t H);
 
 /* Bytes of workspace ovc_prepare_v_repair needs (0 if invalid).  budget in (0,1]. */
 size_t ovc_repair_workspace_bytes(int64_t B, int64_t S, int64_t H, float budget);

@@ -23,7 +23,7 @@ def _declared_functions():
     for fn in os.listdir(os.path.join(ROOT, "include")):
         if fn.endswith(".h"):
             text = open(os.path.join(ROOT, "include", fn)).read()
-            names += re.findall(r"^\s*(?:size_t|ovc_status|const char\*)\s+(ovc_\w+)\s*\(", text, re.M)
+            names += re.findall(r"^\s*(?:size_t|ovc_status|int32_t|const char\*)\s+(ovc_\w+)\s*\(", text, re.M)
     return sorted(set(names))
 
 
@@ -91,11 +91,32 @@ def test_host_validation_rejects_bad_arguments(lib):
     # kernel-variant flags: unknown bits are rejected before any device call;
     # known ones pass validation (and then fail only for want of a GPU)
     p = _abi.OvcPrepared(1, 128, 1, 1, 128, 0x1000, 0x2000, 0x3000, 0x4000, 0x4100, 0x4200, 0x4300, 0x4400)
-    assert lib.ovc_attention_ex(ctypes.byref(p), None, 0.0, ctypes.byref(o), 4, None) == _abi.OVC_ERR_INVALID_ARG
-    assert lib.ovc_attention_ex(ctypes.byref(_abi.OvcPrepared()), None, 0.0, ctypes.byref(o), 3, None) == _abi.OVC_ERR_INVALID_ARG
+    def ex(prep, flags, nsplit=0, ws=None, nbytes=0, rep=None):
+        return lib.ovc_attention_ex(ctypes.byref(prep), rep, 0.0, ctypes.byref(o), flags, nsplit,
+                                    ctypes.c_void_p(ws), nbytes, None)
+    assert ex(p, 4) == _abi.OVC_ERR_INVALID_ARG
+    assert ex(_abi.OvcPrepared(), 3) == _abi.OVC_ERR_INVALID_ARG
     if not torch.cuda.is_available():
-        assert lib.ovc_attention_ex(ctypes.byref(p), None, 0.0, ctypes.byref(o), 3, None) in (
-            _abi.OVC_ERR_CUDA, _abi.OVC_ERR_UNSUPPORTED)
+        assert ex(p, 3) in (_abi.OVC_ERR_CUDA, _abi.OVC_ERR_UNSUPPORTED)
+    # split key ranges: nsplit beyond the key blocks, above 16, negative, without workspace,
+    # with an unaligned workspace or with a repair set are rejected before any device call
+    p8 = _abi.OvcPrepared(1, 1000, 1, 8, 1024, 0x1000, 0x2000, 0x3000, 0x4000, 0x4100, 0x4200, 0x4300, 0x4400)
+    assert ex(p8, 0, nsplit=9, ws=0x100000, nbytes=1 << 30) == _abi.OVC_ERR_INVALID_ARG
+    assert ex(p8, 0, nsplit=-1) == _abi.OVC_ERR_INVALID_ARG
+    assert ex(p8, 0, nsplit=2) == _abi.OVC_ERR_INVALID_ARG
+    assert ex(p8, 0, nsplit=2, ws=0x100010, nbytes=1 << 30) == _abi.OVC_ERR_INVALID_ARG
+    r = _abi.OvcRepair(1, 1000, 1, 5, 128, 0x5000, 0x5100, 0x5200, 0x5300, 0x5400)
+    assert ex(p8, 0, nsplit=2, ws=0x100000, nbytes=1 << 30, rep=ctypes.byref(r)) == _abi.OVC_ERR_INVALID_ARG
+    # workspace of a forced split: 4 tiles x n ranges x 256 rows x (128 FP16 + m8, l)
+    for n in (2, 3, 8):
+        units = 4 * n
+        want = -(-units * 256 * 256 // 256) * 256 + -(-units * 256 * 8 // 256) * 256
+        assert lib.ovc_attention_workspace_bytes(ctypes.byref(p8), n) == want
+    assert lib.ovc_attention_workspace_bytes(ctypes.byref(p8), 1) == 0
+    assert lib.ovc_attention_workspace_bytes(ctypes.byref(p8), 9) == 0
+    if not torch.cuda.is_available():
+        assert lib.ovc_attention_workspace_bytes(ctypes.byref(p8), 0) == 0   # automatic needs a device
+        assert lib.ovc_attention_auto_split(1, 1000, 1) == 1
 
 
 def test_status_strings(lib):

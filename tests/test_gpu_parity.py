@@ -14,7 +14,7 @@ import oracle
 import fp8_bit_attention_gb300 as ovc
 from fp8_bit_attention_gb300 import workloads as W
 
-from gpu_util import TOL_REL_L2, inputs, oracle_prep, rel_l2, to_dev
+from gpu_util import TOL_REL_L2, inputs, n_auto, oracle_prep, rel_l2, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -50,7 +50,7 @@ def test_prepare_bit_exact(B, H, S):
 @pytest.mark.parametrize("B,H,S", SHAPES)
 def test_attention_matches_oracle(B, H, S):
     q, k, v = inputs(B, H, S, seed=200 + S)
-    ref, _ = oracle.attention_full(oracle_prep(q, k, v))
+    ref, _ = oracle.attention_full(oracle_prep(q, k, v), nsplit=n_auto(B, S, H))
     o = ovc.attention(*to_dev(q, k, v))
     assert ovc.device_status() == 0
     got = o.float().cpu().numpy()
@@ -60,7 +60,7 @@ def test_attention_matches_oracle(B, H, S):
 
 def test_attention_3d_layout_and_strided_inputs():
     q, k, v = inputs(1, 2, 700, seed=301)
-    ref, _ = oracle.attention_full(oracle_prep(q, k, v))
+    ref, _ = oracle.attention_full(oracle_prep(q, k, v), nsplit=n_auto(1, 700, 2))
     qd, kd, vd = to_dev(q, k, v)
     o3 = ovc.attention(qd[0], kd[0], vd[0])                       # [S,H,128]
     assert rel_l2(o3.float().cpu().numpy(), ref[0]) <= TOL_REL_L2
@@ -85,7 +85,7 @@ def test_persistent_and_plain_schedules_agree_bitwise():
 
 def test_softmax_scale_argument():
     q, k, v = inputs(1, 1, 512, seed=303)
-    ref, _ = oracle.attention_full(oracle_prep(q, k, v), sm=0.05)
+    ref, _ = oracle.attention_full(oracle_prep(q, k, v), sm=0.05, nsplit=n_auto(1, 512, 1))
     o = ovc.attention(*to_dev(q, k, v), softmax_scale=0.05)
     assert rel_l2(o.float().cpu().numpy(), ref) <= TOL_REL_L2
 
@@ -144,7 +144,7 @@ def test_timeout_path_reports_and_recovers():
     prep = ovc.prepare(*to_dev(q, k, v))
     ovc.attention_probe(prep, skip_mma=True, wait_timeout_ns=20_000_000)
     assert ovc.device_status() == 5          # OVC_ERR_TIMEOUT, context still usable
-    ref, _ = oracle.attention_full(oracle_prep(q, k, v))
+    ref, _ = oracle.attention_full(oracle_prep(q, k, v), nsplit=n_auto(1, 512, 1))
     o = ovc.attention_prepared(prep)
     assert ovc.device_status() == 0
     assert rel_l2(o.float().cpu().numpy(), ref) <= TOL_REL_L2
@@ -206,7 +206,7 @@ def test_fp16_inputs_match_oracle(B, H, S):
     o = ovc.attention_prepared(prep).float().cpu().numpy()
     bh = np.repeat(np.arange(B * H), S)
     ss = np.tile(np.arange(S), B * H)
-    r = oracle.attention_rows(ref, bh, ss)["out"].reshape(B, H, S, 128).transpose(0, 2, 1, 3)
+    r = oracle.attention_rows(ref, bh, ss, nsplit=n_auto(B, S, H))["out"].reshape(B, H, S, 128).transpose(0, 2, 1, 3)
     assert rel_l2(o, r) <= TOL_REL_L2
     rep = ovc.prepare_v_repair(vd, prep, 0.02)
     rr = oracle.Repair(ref, 0.02)
@@ -236,7 +236,7 @@ def test_k_smoothing_matches_oracle(B, H, S, fp16):
     o = ovc.attention_prepared(prep).float().cpu().numpy()
     bh = np.repeat(np.arange(B * H), S)
     ss = np.tile(np.arange(S), B * H)
-    r = oracle.attention_rows(ref, bh, ss)["out"].reshape(B, H, S, 128).transpose(0, 2, 1, 3)
+    r = oracle.attention_rows(ref, bh, ss, nsplit=n_auto(B, S, H))["out"].reshape(B, H, S, 128).transpose(0, 2, 1, 3)
     assert rel_l2(o, r) <= TOL_REL_L2
     dev = ovc.attention(qd, kd, vd, smooth_k=True).cpu()
     host = ovc.attention(q.pin_memory(), k.pin_memory(), v.pin_memory(), smooth_k=True)
@@ -274,13 +274,13 @@ def test_attention_variants_match_oracle(flags, cast, natural, B, H, S):
     q, k, v = inputs(B, H, S, seed=600 + S)
     ref, _ = oracle.attention_full(oracle_prep(q, k, v), cast=cast, mid_window=not natural)
     prep = ovc.prepare(*to_dev(q, k, v))
-    o = ovc.attention_prepared(prep, flags=flags)
+    o = ovc.attention_prepared(prep, flags=flags, nsplit=1)
     assert ovc.device_status() == 0
     got = o.float().cpu().numpy()
     assert np.isfinite(got).all()
     assert rel_l2(got, ref) <= TOL_REL_L2
     if cast or (S + 127) // 128 > 1:              # one key block: both orders coincide
-        base = ovc.attention_prepared(prep).float().cpu().numpy()
+        base = ovc.attention_prepared(prep, nsplit=1).float().cpu().numpy()
         assert not np.array_equal(got, base)      # the variant really ran
 
 
@@ -322,6 +322,80 @@ def test_baseline_with_repair_and_schedules():
 
 def test_baseline_attention_entry_point():
     q, k, v = inputs(1, 2, 700, seed=801)
-    want, _ = oracle.attention_full(oracle_prep(q, k, v), cast=True, mid_window=False)
+    want, _ = oracle.attention_full(oracle_prep(q, k, v), cast=True, mid_window=False, nsplit=n_auto(1, 700, 2))
     o = ovc.baseline_attention(*to_dev(q, k, v))
     assert rel_l2(o.float().cpu().numpy(), want) <= TOL_REL_L2
+
+
+# ---- split key ranges (short sequences) ------------------------------------
+@pytest.mark.parametrize("B,H,S,n", [(1, 2, 1024, 2), (1, 2, 1000, 3), (2, 3, 300, 3), (1, 1, 640, 5),
+                                     (1, 2, 1024, 8), (1, 3, 129, 2)])
+def test_split_key_ranges_match_oracle(B, H, S, n):
+    q, k, v = inputs(B, H, S, seed=900 + S + n)
+    ref = oracle_prep(q, k, v)
+    want, _ = oracle.attention_full(ref, nsplit=n)
+    prep = ovc.prepare(*to_dev(q, k, v))
+    assert ovc.attention_workspace_bytes(prep, n) > 0
+    o = ovc.attention_prepared(prep, nsplit=n)
+    assert ovc.device_status() == 0
+    got = o.float().cpu().numpy()
+    assert np.isfinite(got).all()
+    assert rel_l2(got, want) <= TOL_REL_L2
+    # the split is a different computation from the unsplit one (each range
+    # has its own reference); where the two differ clearly, the output follows
+    # the split one
+    unsplit, _ = oracle.attention_full(ref)
+    if rel_l2(want, unsplit) > 4 * TOL_REL_L2:
+        assert rel_l2(got, unsplit) > TOL_REL_L2
+
+
+@pytest.mark.parametrize("flags,cast,natural", VARIANTS)
+def test_split_key_ranges_with_variants(flags, cast, natural):
+    q, k, v = inputs(1, 2, 1000, seed=950 + flags)
+    want, _ = oracle.attention_full(oracle_prep(q, k, v), nsplit=4, cast=cast, mid_window=not natural)
+    prep = ovc.prepare(*to_dev(q, k, v))
+    o = ovc.attention_prepared(prep, nsplit=4, flags=flags)
+    assert rel_l2(o.float().cpu().numpy(), want) <= TOL_REL_L2
+
+
+def test_auto_split_on_short_sequences_and_strided_output():
+    """Seven heads of 8192 tokens (224 tiles): the library splits on its own;
+    sampled rows match the oracle run with the same split; output strides
+    are honoured by the merge pass."""
+    B, H, S = 1, 7, 8192
+    n = ovc.auto_split(B, S, H)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if sms == 152:
+        assert n == 2
+    assert ovc.auto_split(1, 73397, 56) == 1          # persistent schedule: never split
+    q, k, v = inputs(B, H, S, seed=960)
+    ref = oracle_prep(q, k, v)
+    prep = ovc.prepare(*to_dev(q, k, v))
+    big = torch.zeros((B, S, H, 256), dtype=torch.bfloat16, device="cuda")
+    ovc.attention_prepared(prep, out=big[..., 64:192])
+    assert ovc.device_status() == 0
+    rng = np.random.default_rng(961)
+    rows = np.unique(np.concatenate([rng.integers(0, S, 40), [0, S - 1, 4096]]))
+    got = big.float().cpu().numpy()
+    for h in (0, H - 1):
+        r = oracle.attention_rows(ref, np.full_like(rows, h), rows, nsplit=n)["out"]
+        assert rel_l2(got[0, rows, h, 64:192], r) <= TOL_REL_L2
+    assert not big[..., :64].any() and not big[..., 192:].any()
+
+
+def test_split_rejected_with_repair_and_without_workspace():
+    q, k, v = inputs(1, 1, 1000, seed=970)
+    qd, kd, vd = to_dev(q, k, v)
+    prep = ovc.prepare(qd, kd, vd)
+    rep = ovc.prepare_v_repair(vd, prep, 0.02)
+    with pytest.raises(ovc.OvcError):
+        ovc.attention_prepared(prep, rep=rep, nsplit=2)
+    small = torch.empty(16, dtype=torch.uint8, device="cuda")
+    from fp8_bit_attention_gb300 import _abi
+    out = torch.empty_like(qd)
+    od = _abi.OvcOutput(out.data_ptr(), out.stride(0), out.stride(1), out.stride(2))
+    import ctypes
+    st = _abi.lib().ovc_attention_ex(ctypes.byref(prep.desc), None, 0.0, ctypes.byref(od), 0, 2,
+                                     ctypes.c_void_p(small.data_ptr()), 16, None)
+    assert st == _abi.OVC_ERR_WORKSPACE_TOO_SMALL
+    assert ovc.device_status() == 0

@@ -89,7 +89,7 @@ def test_noalloc_prepare_matches_prepare_on_two_calls_in_a_row():
         prep = ovc.prepare(q, k, v)
         _assert_same_prepare(prep, bufs)
         # attention from the no-allocation preparation equals the usual one
-        o_ref = ovc.attention_prepared(prep)
+        o_ref = ovc.attention_prepared(prep, nsplit=1)
         o = torch.empty_like(o_ref)
         od = _abi.OvcOutput(o.data_ptr(), o.stride(0), o.stride(1), o.stride(2))
         st = _abi.lib().ovc_attention(ctypes.byref(desc), 0.0, ctypes.byref(od),
