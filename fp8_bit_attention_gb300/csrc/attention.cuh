@@ -152,6 +152,8 @@ __device__ __forceinline__ TileCoord tile_coord(const AttnParams& P, int tile) {
 // improve on, measured in this same pipeline.
 constexpr int kVarExpThenCast = 1;   // p byte = E4M3(ex2(...)) on the MUFU
 constexpr int kVarNaturalOrder = 2;  // key blocks 0, 1, ..., nb-1
+constexpr int kVarSplit = 4;         // split key ranges (nsplit > 1): partial results for merge_kernel
+constexpr int kNumVariants = 8;
 
 // Key block visited at step i of a range of n blocks starting at b0 (the
 // whole sequence, or one split range): cyclic from the range's middle block,
@@ -168,12 +170,19 @@ struct UnitCoord {
   int b0, nbu;            // key blocks [b0, b0 + nbu)
 };
 
+template <int kVar>
 __device__ __forceinline__ UnitCoord unit_coord(const AttnParams& P, int u) {
-  const int tile = u / P.nsplit, sp = u - tile * P.nsplit;
   UnitCoord c;
-  c.tc = tile_coord(P, tile);
-  c.b0 = sp * P.nb / P.nsplit;
-  c.nbu = (sp + 1) * P.nb / P.nsplit - c.b0;
+  if (kVar & kVarSplit) {
+    const int tile = u / P.nsplit, sp = u - tile * P.nsplit;
+    c.tc = tile_coord(P, tile);
+    c.b0 = sp * P.nb / P.nsplit;
+    c.nbu = (sp + 1) * P.nb / P.nsplit - c.b0;
+  } else {
+    c.tc = tile_coord(P, u);
+    c.b0 = 0;
+    c.nbu = P.nb;
+  }
   return c;
 }
 
@@ -401,7 +410,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       uint32_t kv_iter = 0, q_iter = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < P.nunits && ok; u += gridDim.x) {
-        const UnitCoord uc = unit_coord(P, u);
+        const UnitCoord uc = unit_coord<kVar>(P, u);
         const TileCoord& tc = uc.tc;
         const int nblk = uc.nbu + P.rep_blocks;
         if (q_iter > 0) ok = mbar_wait(smem_addr(&sm.q_empty), (q_iter - 1) & 1, tmo, abort_flag);
@@ -453,7 +462,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const uint32_t tO0 = tmem + 256, tO1 = tmem + 384;
       const uint64_t qd0 = sw128_desc(smem_addr(sm.q[0])), qd1 = sw128_desc(smem_addr(sm.q[1]));
       for (int u = blockIdx.x; u < P.nunits && ok; u += gridDim.x) {
-        const int nblk = unit_coord(P, u).nbu + P.rep_blocks;
+        const int nblk = unit_coord<kVar>(P, u).nbu + P.rep_blocks;
         ok = mbar_wait(smem_addr(&sm.q_full), q_iter & 1, tmo, abort_flag);
         if (!ok) break;
         // Scores of the first block for both query tiles.
@@ -544,7 +553,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int trole = (wq == 0) ? t : -1;
     bool ok = true;
     for (int u = blockIdx.x; u < P.nunits && ok; u += gridDim.x) {
-      const UnitCoord uc = unit_coord(P, u);
+      const UnitCoord uc = unit_coord<kVar>(P, u);
       const TileCoord& tc = uc.tc;
       const int nblk = uc.nbu + P.rep_blocks;
       const int qb = t ? tc.qb1 : tc.qb0;
@@ -639,7 +648,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const int q_row = qb * 128 + row;
-      if (P.nsplit > 1) {
+      if (kVar & kVarSplit) {
         // Partial result of this key range: O_acc / l as FP16 and (m8, l);
         // merge_kernel combines the ranges of each row.
         const float inv_l = 1.0f / l;

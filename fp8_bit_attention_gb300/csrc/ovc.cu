@@ -26,6 +26,11 @@ __device__ unsigned int g_status;
 
 namespace {
 
+// Every instantiation of the attention kernel, indexed by its variant bits.
+const decltype(&attention_kernel<0>) kAttentionKernels[kNumVariants] = {
+    attention_kernel<0>, attention_kernel<1>, attention_kernel<2>, attention_kernel<3>,
+    attention_kernel<4>, attention_kernel<5>, attention_kernel<6>, attention_kernel<7>};
+
 constexpr int kMaxDevices = 64;
 constexpr uint64_t kDefaultTimeoutNs = 4000000000ull;   // 4 s per wait
 
@@ -53,7 +58,7 @@ ovc_status device_state(DeviceState** out) {
     d.supported = (major == 10 && minor == 3);
     d.sms = sms;
     if (d.supported) {
-      for (auto fn : {attention_kernel<0>, attention_kernel<1>, attention_kernel<2>, attention_kernel<3>})
+      for (auto fn : kAttentionKernels)
         if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kAttnSmemBytes)) != cudaSuccess)
           return OVC_ERR_CUDA;
@@ -317,9 +322,7 @@ ovc_status run_attention(const ovc_prepared* p, const ovc_repair* r, float softm
   const int64_t grid = persistent ? (nunits < dev->sms ? nunits : dev->sms) : nunits;
   static_assert(OVC_ATTN_EXP_THEN_CAST == kVarExpThenCast && OVC_ATTN_NATURAL_ORDER == kVarNaturalOrder,
                 "flag bits select the kernel variant");
-  decltype(&attention_kernel<0>) kernels[4] = {attention_kernel<0>, attention_kernel<1>, attention_kernel<2>,
-                                               attention_kernel<3>};
-  kernels[flags]<<<static_cast<unsigned>(grid), kAttnThreads, kAttnSmemBytes,
+  kAttentionKernels[flags | (ns > 1 ? kVarSplit : 0)]<<<static_cast<unsigned>(grid), kAttnThreads, kAttnSmemBytes,
                    static_cast<cudaStream_t>(stream)>>>(mq, mk, mv, mks, mdv, P);
   if (ns > 1) {
     const int64_t rows = BH * p->S;
