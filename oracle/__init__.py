@@ -74,6 +74,8 @@ def lib():
             L.ovc_oracle_quantize_blocks.argtypes = [P, ctypes.c_int, i64, i64, i64, i64, i64, i64, P, P, P]
             L.ovc_oracle_k_mean.restype = None
             L.ovc_oracle_k_mean.argtypes = [P, ctypes.c_int, i64, i64, i64, i64, i64, i64, P]
+            L.ovc_oracle_vsmooth_v.restype = None
+            L.ovc_oracle_vsmooth_v.argtypes = [P, ctypes.c_int, i64, i64, i64, i64, i64, i64, P, P, P, P]
             L.ovc_oracle_quantize_v.restype = None
             L.ovc_oracle_quantize_v.argtypes = [P, ctypes.c_int, i64, i64, i64, i64, i64, i64, P, P, P]
             L.ovc_oracle_repair_count.restype = i64
@@ -87,7 +89,7 @@ def lib():
             L.ovc_oracle_block_codes.argtypes = [P, ctypes.c_float, P, P, i64, i64, d, d, d, d, ctypes.c_int, P]
             L.ovc_oracle_attention_rows.restype = ctypes.c_int
             L.ovc_oracle_attention_rows.argtypes = (
-                [P, P, P, P, P, P, i64, i64, i64, P, P, P, i64, P, P, i64, d, d, d, d,
+                [P, P, P, P, P, P, i64, i64, i64, P, P, P, i64, P, P, P, i64, d, d, d, d,
                  ctypes.c_int, ctypes.c_int, ctypes.c_int, i64, P, P, P, P, i64, P, P, ctypes.c_int])
             L.ovc_oracle_attention_exact_rows.restype = ctypes.c_int
             L.ovc_oracle_attention_exact_rows.argtypes = (
@@ -216,6 +218,20 @@ def quantize_v(v: np.ndarray, fp16: bool = False):
     return codes, sv, energy
 
 
+def vsmooth_v(v: np.ndarray, fp16: bool = False):
+    """V-Smooth of V -> (codes token-major [B,H,S_pad,128], sv [B,H],
+    mu [B,H,nb,128] block means (BF16 values), mprime [B,H,nb,128] = bf16(mu r))."""
+    v, sb, ss, sh = _bf16_view(v)
+    B, S, H, _ = v.shape
+    nb = (S + 127) // 128
+    codes = np.zeros((B, H, nb * 128, 128), np.uint8)
+    sv = np.zeros((B, H), np.float32)
+    mu = np.zeros((B, H, nb, 128), np.float32)
+    mprime = np.zeros((B, H, nb, 128), np.float32)
+    lib().ovc_oracle_vsmooth_v(_ptr(v), int(fp16), B, S, H, sb, ss, sh, _ptr(codes), _ptr(sv), _ptr(mu), _ptr(mprime))
+    return codes, sv, mu, mprime
+
+
 def repair_count(S: int, budget: float) -> int:
     return int(lib().ovc_oracle_repair_count(S, float(np.float32(budget))))
 
@@ -250,16 +266,23 @@ def repair_quantize(v: np.ndarray, vcodes: np.ndarray, sv: np.ndarray, idx: np.n
 class Prepared:
     """The oracle's own quantised tensors for one (Q, K, V) triple."""
 
-    def __init__(self, q, k, v, fp16: bool = False, smooth_k: bool = False):
+    def __init__(self, q, k, v, fp16: bool = False, smooth_k: bool = False, v_smooth: bool = False):
         """q, k, v: uint16 bits [B,S,H,128] of BF16 inputs, or of FP16 ones if
-        fp16.  smooth_k: subtract K's channel means before quantising K."""
+        fp16.  smooth_k: subtract K's channel means before quantising K.
+        v_smooth: V-Smooth (block means subtracted, residual quantised, means
+        restored through the row sums); no residual energies then."""
         self.B, self.S, self.H, _ = q.shape
         self.nb = (self.S + 127) // 128
         self.fp16 = bool(fp16)
         self.kmean = k_mean(k, fp16) if smooth_k else None
         self.qc, self.sq = quantize_blocks(q, fp16)
         self.kc, self.sk = quantize_blocks(k, fp16, self.kmean)
-        self.vc, self.sv, self.energy = quantize_v(v, fp16)
+        self.vmu = self.vmean = None
+        if v_smooth:
+            self.vc, self.sv, self.vmu, self.vmean = vsmooth_v(v, fp16)
+            self.energy = None
+        else:
+            self.vc, self.sv, self.energy = quantize_v(v, fp16)
         self.v = v
 
 
@@ -296,7 +319,7 @@ def attention_rows(prep: Prepared, rows_bh, rows_s, *, sm=None, repair: Repair |
         nrep = 0
     rc = lib().ovc_oracle_attention_rows(
         _ptr(prep.qc), _ptr(prep.sq), _ptr(prep.kc), _ptr(prep.sk), _ptr(prep.vc), _ptr(prep.sv),
-        prep.B, prep.S, prep.H, _ptr(ridx), _ptr(rdc), _ptr(rsr), nrep,
+        prep.B, prep.S, prep.H, _ptr(ridx), _ptr(rdc), _ptr(rsr), nrep, _ptr(prep.vmean),
         _ptr(rows_bh), _ptr(rows_s), n, c0, beta, tau, sm, int(mid_window), int(snap), int(cast),
         int(nsplit), _ptr(out), _ptr(m8), _ptr(l), _ptr(nres), dump_block, _ptr(codes), _ptr(dm8),
         nthreads or default_threads())

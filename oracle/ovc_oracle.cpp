@@ -544,6 +544,54 @@ void ovc_oracle_quantize_v(const uint16_t* v, int fp16, int64_t B, int64_t S, in
     }
 }
 
+// V-Smooth, the VC-Attention paper's treatment of V ([VC-summary "V-Smooth"]:
+// each 128-token hardware block subtracts its mean, only the residual is
+// quantised, and the mean is added back through the row sums that online
+// softmax keeps).  Per head and block b (the tail block: its valid tokens):
+//   mu_b  = bf16( fl( (sum of v_t over the block, FP32 in token order) / n_b ) )
+//   R_t   = fl(v_t - mu_b)
+//   one scale per head from amax |R| (as for V),  code_t = E4M3(fl(R_t r))
+//   M'_b  = bf16( fl(mu_b r) )   (the mean in the scale's units)
+// so that the value restored for token t is s (dec(code_t) + M'_b).  The
+// means cost 16 bits per 128 elements of a channel (0.125 bit per element,
+// as the summary states).
+//   codes [B,H,S_pad,128] token-major; sv [B,H]; mu, mprime [B,H,nb,128].
+void ovc_oracle_vsmooth_v(const uint16_t* v, int fp16, int64_t B, int64_t S, int64_t H, int64_t sb, int64_t ss,
+                          int64_t sh, uint8_t* codes, float* sv, float* mu, float* mprime) {
+  const Dims dm = make_dims(B, S, H);
+  std::vector<float> R(static_cast<size_t>(S) * 128);
+  for (int64_t b = 0; b < B; ++b)
+    for (int64_t h = 0; h < H; ++h) {
+      const int64_t bh = b * H + h;
+      float amax = 0.0f;
+      for (int64_t j = 0; j < dm.nb; ++j) {
+        const int64_t t0 = j * 128, t1 = std::min(S, t0 + 128);
+        for (int d = 0; d < 128; ++d) {
+          volatile float sum = 0.0f;
+          for (int64_t t = t0; t < t1; ++t) sum = sum + input_bits_to_float(v[b * sb + t * ss + h * sh + d], fp16);
+          volatile float mean = sum / static_cast<float>(t1 - t0);
+          const float m = bf16_bits_to_float(bf16_from_double(static_cast<double>(mean)));
+          mu[(bh * dm.nb + j) * 128 + d] = m;
+          for (int64_t t = t0; t < t1; ++t) {
+            volatile float r = input_bits_to_float(v[b * sb + t * ss + h * sh + d], fp16) - m;
+            R[t * 128 + d] = r;
+            amax = std::max(amax, std::fabs(static_cast<float>(r)));
+          }
+        }
+      }
+      const Scale sc = scale_from_amax(amax);
+      sv[bh] = sc.s;
+      for (int64_t j = 0; j < dm.nb; ++j)
+        for (int d = 0; d < 128; ++d) {
+          volatile float mr = mu[(bh * dm.nb + j) * 128 + d] * sc.r;
+          mprime[(bh * dm.nb + j) * 128 + d] = bf16_bits_to_float(bf16_from_double(static_cast<double>(mr)));
+        }
+      uint8_t* out = codes + bh * dm.S_pad * 128;
+      for (int64_t t = 0; t < dm.S_pad; ++t)
+        for (int d = 0; d < 128; ++d) out[t * 128 + d] = t < S ? quantize_value(R[t * 128 + d], sc.r) : 0;
+    }
+}
+
 // Number of repaired tokens per head: n = ceil(budget * S), at least 1.
 int64_t ovc_oracle_repair_count(int64_t S, float budget) {
   const double n = std::ceil(static_cast<double>(budget) * static_cast<double>(S));
@@ -620,21 +668,24 @@ void ovc_oracle_block_codes(const uint8_t* qrow, float sq, const uint8_t* kcodes
 // natural key order) for a list of query rows (b*H+h, s).  Inputs are the
 // oracle's own quantised tensors: qc/kc [B,H,S_pad,128], sq/sk [B,H,nb],
 // vc token-major [B,H,S_pad,128], sv [B,H].  Optional repair set: rep_idx
-// [B,H,n_rep], rep_dcodes [B,H,n_rep,128], sr [B,H].  Outputs per row: out
+// [B,H,n_rep], rep_dcodes [B,H,n_rep,128], sr [B,H].  vmean (V-Smooth, not
+// with repair): [B,H,nb,128] restored block means M'_b, added to every decoded
+// value of the block (the row-sum restore: sum_t p_t M'_b(t) = sum_b l_b M'_b).
+// Outputs per row: out
 // [nrows,128] (double), m8, l, nres [nrows,2] (main, repair).  If dump_codes
 // is given, the codes of key block dump_block are written per row
 // ([nrows,128]) with the reference used for them in dump_m8 ([nrows]).
 int ovc_oracle_attention_rows(const uint8_t* qc, const float* sq, const uint8_t* kc, const float* sk,
                               const uint8_t* vc, const float* sv, int64_t B, int64_t S, int64_t H,
                               const int32_t* rep_idx, const uint8_t* rep_dcodes, const float* sr,
-                              int64_t n_rep, const int64_t* row_bh, const int64_t* row_s,
+                              int64_t n_rep, const float* vmean, const int64_t* row_bh, const int64_t* row_s,
                               int64_t nrows, double c0, double beta, double tau, double sm,
                               int mid_window, int snap, int cast, int64_t nsplit, double* out, double* m8_out, double* l_out,
                               int32_t* nres_out, int64_t dump_block, uint8_t* dump_codes,
                               double* dump_m8, int nthreads) {
   const Dims dm = make_dims(B, S, H);
   const Params P{c0, beta, tau, sm, 0, mid_window, snap, cast};
-  if (nsplit < 1 || nsplit > dm.nb || (nsplit > 1 && n_rep > 0)) return 3;
+  if (nsplit < 1 || nsplit > dm.nb || (nsplit > 1 && n_rep > 0) || (vmean && n_rep > 0)) return 3;
   // Process the rows head by head so that one head's keys are decoded once.
   std::vector<int64_t> perm(nrows);
   for (int64_t i = 0; i < nrows; ++i) perm[i] = i;
@@ -651,7 +702,8 @@ int ovc_oracle_attention_rows(const uint8_t* qc, const float* sq, const uint8_t*
     for (int64_t t = 0; t < S; ++t)
       for (int d = 0; d < 128; ++d) {
         K[t * 128 + d] = e4m3_value(kc[(bh * dm.S_pad + t) * 128 + d]);
-        V[t * 128 + d] = e4m3_value(vc[(bh * dm.S_pad + t) * 128 + d]);
+        V[t * 128 + d] = e4m3_value(vc[(bh * dm.S_pad + t) * 128 + d]) +
+                         (vmean ? static_cast<double>(vmean[(bh * dm.nb + t / 128) * 128 + d]) : 0.0);
       }
     ks.assign(sk + bh * dm.nb, sk + (bh + 1) * dm.nb);
     HeadView hv;
