@@ -20,6 +20,7 @@ OVC_ERR_TIMEOUT = 5
 OVC_ERR_SCRATCH_LIMIT = 6
 OVC_NOALLOC_MAX_HEADS = 4096
 OVC_PREPARE_SMOOTH_K = 1
+OVC_PREPARE_V_SMOOTH = 2
 OVC_ATTN_EXP_THEN_CAST = 1
 OVC_ATTN_NATURAL_ORDER = 2
 OVC_ATTN_BASELINE = 3
@@ -39,7 +40,7 @@ class OvcOutput(ctypes.Structure):
 class OvcPrepared(ctypes.Structure):
     _fields_ = [("B", c_i64), ("S", c_i64), ("H", c_i64), ("nb", c_i64), ("S_pad", c_i64),
                 ("q", c_ptr), ("k", c_ptr), ("vt", c_ptr), ("sq", c_ptr), ("sk", c_ptr),
-                ("sv", c_ptr), ("vamax", c_ptr), ("energy", c_ptr)]
+                ("sv", c_ptr), ("vamax", c_ptr), ("energy", c_ptr), ("vmean", c_ptr)]
 
 
 class OvcRepair(ctypes.Structure):

@@ -107,6 +107,14 @@ class Prepared:
         d = self.desc
         return _view(self.workspace, d.energy, 4 * d.B * d.H * d.S).view(torch.float32).view(d.B, d.H, d.S)
 
+    def v_means(self):
+        """V-Smooth's restored block means M'_b, BF16 [B,H,128,nbk] (None without V-Smooth)."""
+        d = self.desc
+        if not d.vmean:
+            return None
+        nbk = -(-d.nb // 16) * 16
+        return _view(self.workspace, d.vmean, 2 * d.B * d.H * 128 * nbk).view(torch.bfloat16).view(d.B, d.H, 128, nbk)
+
 
 @dataclasses.dataclass
 class Repair:
@@ -134,22 +142,24 @@ class Repair:
         return _view(self.workspace, d.sr, 4 * d.B * d.H).view(torch.float32).view(d.B, d.H)
 
 
-def prepare_workspace_bytes(B: int, S: int, H: int, *, smooth_k: bool = False) -> int:
-    return int(lib().ovc_prepare_workspace_bytes_ex(B, S, H, 128, _prep_flags(smooth_k)))
+def prepare_workspace_bytes(B: int, S: int, H: int, *, smooth_k: bool = False, v_smooth: bool = False) -> int:
+    return int(lib().ovc_prepare_workspace_bytes_ex(B, S, H, 128, _prep_flags(smooth_k, v_smooth)))
 
 
-def _prep_flags(smooth_k: bool) -> int:
-    return _abi.OVC_PREPARE_SMOOTH_K if smooth_k else 0
+def _prep_flags(smooth_k: bool, v_smooth: bool = False) -> int:
+    return (_abi.OVC_PREPARE_SMOOTH_K if smooth_k else 0) | (_abi.OVC_PREPARE_V_SMOOTH if v_smooth else 0)
 
 
 def prepare(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, smooth_k: bool = False,
-            workspace: torch.Tensor | None = None, stream=None) -> Prepared:
+            v_smooth: bool = False, workspace: torch.Tensor | None = None, stream=None) -> Prepared:
     """Quantise Q/K (per 128-token block) and V (per head) to E4M3
     (ovc_prepare_ex).  smooth_k subtracts K's channel means first (optional
-    K smoothing; exact non-causal attention is unchanged by it)."""
+    K smoothing; exact non-causal attention is unchanged by it).  v_smooth
+    quantises V's residuals after each 128-token block's mean and keeps the
+    means for attention to restore (V-Smooth; no repair with it)."""
     tq, tk, tv = _tensor_desc(q), _tensor_desc(k), _tensor_desc(v)
-    flags = _prep_flags(smooth_k)
-    nbytes = prepare_workspace_bytes(tq.B, tq.S, tq.H, smooth_k=smooth_k)
+    flags = _prep_flags(smooth_k, v_smooth)
+    nbytes = prepare_workspace_bytes(tq.B, tq.S, tq.H, smooth_k=smooth_k, v_smooth=v_smooth)
     if nbytes == 0:
         raise ValueError(f"unsupported shape {tuple(q.shape)}")
     if workspace is None:

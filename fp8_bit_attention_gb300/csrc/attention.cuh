@@ -38,6 +38,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <cstddef>
 #include <cstdint>
 
 #include "ptx.cuh"
@@ -57,6 +58,8 @@ constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr uint32_t kTile = 128 * 128;                       // bytes of one E4M3 tile
 constexpr uint32_t kIdesc = idesc_e4m3_f32(128, 128);
+constexpr uint32_t kIdescBf16 = idesc_bf16_f32(128, 128);
+constexpr uint32_t kMeanTile = 128 * 16 * 2;               // bytes of one M' tile: 128 channels x 16 blocks BF16
 constexpr float kMagic = 12582912.0f;                       // 1.5 * 2^23
 // ExpCast constants: c0 = 120 (stored value 2^8 p), beta = -0.35, tau = 0.75.
 constexpr float kCodeBase = 119.0f;                         // floor(c0 + beta)
@@ -123,9 +126,15 @@ struct AttnSmem {
   uint32_t tmem_base;
   int abort;
   int zero;               // always 0: the "never abort" flag of drain waits
+  // V-Smooth only (the other variants are launched without this tail):
+  uint64_t m_full[2], m_empty[2];
+  alignas(1024) uint8_t mv[2][kMeanTile];   // M' tiles of two runs, 32-byte swizzle
+  float lbuf[2][16][128];                   // pending block row sums [tile][block mod 16][row]
 };
 
-constexpr size_t kAttnSmemBytes = sizeof(AttnSmem) + 1024;  // + alignment slack
+// Dynamic shared memory of a launch, + 1024 bytes of alignment slack.
+constexpr size_t kAttnSmemBytes = offsetof(AttnSmem, m_full) + 1024;
+constexpr size_t kAttnSmemBytesVSmooth = sizeof(AttnSmem) + 1024;
 
 __device__ __forceinline__ void record_abort(AttnSmem& sm, const AttnParams& P) {
   if (!*reinterpret_cast<volatile int*>(&sm.abort)) atomicOr(P.status, kStatusTimeout);
@@ -153,7 +162,8 @@ __device__ __forceinline__ TileCoord tile_coord(const AttnParams& P, int tile) {
 constexpr int kVarExpThenCast = 1;   // p byte = E4M3(ex2(...)) on the MUFU
 constexpr int kVarNaturalOrder = 2;  // key blocks 0, 1, ..., nb-1
 constexpr int kVarSplit = 4;         // split key ranges (nsplit > 1): partial results for merge_kernel
-constexpr int kNumVariants = 8;
+constexpr int kVarVSmooth = 8;       // V-Smooth: block means restored through the block row sums
+constexpr int kNumVariants = 9;      // 0-7, and 8 (V-Smooth with ExpCast, mid-window, no split)
 
 // Key block visited at step i of a range of n blocks starting at b0 (the
 // whole sequence, or one split range): cyclic from the range's middle block,
@@ -346,6 +356,35 @@ __device__ __forceinline__ void tmem_load_row128(uint32_t taddr, uint32_t* s) {
   tmem_wait_ld32(s + 96);
 }
 
+// V-Smooth: key blocks are grouped in runs of consecutive visited blocks of
+// one 16-block chunk (block index / 16); each run's row sums meet the run's
+// M' tile in one BF16 MMA.  Visiting step i starts a run when it is the first
+// or its chunk differs from the previous step's.
+template <int kVar>
+__device__ __forceinline__ bool starts_run(int i, int b0, int n) {
+  return i == 0 || (key_block<kVar>(i, b0, n) >> 4) != (key_block<kVar>(i - 1, b0, n) >> 4);
+}
+
+// Writes a run's 16 pending row sums of this thread's row as the A operand of
+// the mean MMA (BF16, two per column, the lower block first): columns
+// [taddr, +8) the rounded values, [taddr + 8, +16) the rounding remainders
+// (together about 16 significant bits), and clears them.
+__device__ __forceinline__ void flush_row_sums(float* lb, uint32_t taddr) {
+  uint32_t r[16];
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    const float a = lb[(2 * m) * 128], b = lb[(2 * m + 1) * 128];
+    const __nv_bfloat16 ah = __float2bfloat16_rn(a), bh = __float2bfloat16_rn(b);
+    const __nv_bfloat16 al = __float2bfloat16_rn(__fsub_rn(a, __bfloat162float(ah)));
+    const __nv_bfloat16 bl = __float2bfloat16_rn(__fsub_rn(b, __bfloat162float(bh)));
+    r[m] = static_cast<uint32_t>(__bfloat16_as_ushort(ah)) | (static_cast<uint32_t>(__bfloat16_as_ushort(bh)) << 16);
+    r[8 + m] = static_cast<uint32_t>(__bfloat16_as_ushort(al)) | (static_cast<uint32_t>(__bfloat16_as_ushort(bl)) << 16);
+    lb[(2 * m) * 128] = 0.0f;
+    lb[(2 * m + 1) * 128] = 0.0f;
+  }
+  tmem_st16(taddr, r);
+}
+
 // O row *= f in tensor memory (one 128-column row per thread).
 __device__ __forceinline__ void tmem_scale_row128(uint32_t taddr, float f) {
 #pragma unroll 1
@@ -364,7 +403,8 @@ template <int kVar>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_ks,
-                     const __grid_constant__ CUtensorMap tm_dv, const __grid_constant__ AttnParams P) {
+                     const __grid_constant__ CUtensorMap tm_dv, const __grid_constant__ CUtensorMap tm_vm,
+                     const __grid_constant__ AttnParams P) {
   extern __shared__ uint8_t smem_raw[];
   AttnSmem& sm = *reinterpret_cast<AttnSmem*>(
       smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023));
@@ -387,6 +427,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(smem_addr(&sm.o_full[t]), 1);
     }
     mbar_init(smem_addr(&sm.drain), 1);
+    if (kVar & kVarVSmooth)
+      for (int r = 0; r < 2; ++r) {
+        mbar_init(smem_addr(&sm.m_full[r]), 1);
+        mbar_init(smem_addr(&sm.m_empty[r]), 1);
+      }
     sm.abort = 0;
     sm.zero = 0;
     fence_mbar_init();
@@ -407,7 +452,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------------ TMA
     if (lane == 0) {
-      uint32_t kv_iter = 0, q_iter = 0;
+      uint32_t kv_iter = 0, q_iter = 0, run = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < P.nunits && ok; u += gridDim.x) {
         const UnitCoord uc = unit_coord<kVar>(P, u);
@@ -433,6 +478,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const int j = key_block<kVar>(i, uc.b0, uc.nbu);
             tma_load_2d(smem_addr(sm.k[stage]), &tm_k, kbar, 0, tc.bh * P.S_pad + j * 128);
             tma_load_2d(smem_addr(sm.v[stage]), &tm_v, vbar, j * 128, tc.bh * 128);
+            if ((kVar & kVarVSmooth) && starts_run<kVar>(i, uc.b0, uc.nbu)) {
+              // The M' tile of the run this block starts: channels of this head, blocks of its chunk.
+              const uint32_t slot = run & 1;
+              if (run >= 2) {
+                ok = mbar_wait(smem_addr(&sm.m_empty[slot]), ((run >> 1) - 1) & 1, tmo, abort_flag);
+                if (!ok) break;
+              }
+              const uint32_t mbar = smem_addr(&sm.m_full[slot]);
+              mbar_arrive_expect_tx(mbar, kMeanTile);
+              tma_load_2d(smem_addr(sm.mv[slot]), &tm_vm, mbar, (j >> 4) * 16, tc.bh * 128);
+              ++run;
+            }
           } else {
             const int r = i - uc.nbu;
             tma_load_2d(smem_addr(sm.k[stage]), &tm_ks, kbar, 0, tc.bh * P.n_rep_pad + r * 128);
@@ -451,18 +508,30 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           mbar_wait(smem_addr(&sm.v_full[stage]), par, kDrainNs, never);
         }
         if (q_iter > 0) mbar_wait(smem_addr(&sm.q_full), (q_iter - 1) & 1, kDrainNs, never);
+        for (uint32_t n = (run > 2 ? run - 2 : 0); n < run; ++n)
+          mbar_wait(smem_addr(&sm.m_full[n & 1]), (n >> 1) & 1, kDrainNs, never);
       }
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA
     if (lane == 0 && !P.skip_mma) {
-      uint32_t kv_iter = 0, q_iter = 0, sp0 = 0, sp1 = 0;
+      uint32_t kv_iter = 0, q_iter = 0, sp0 = 0, sp1 = 0, mrun = 0;
       bool ok = true, issued = false;
+      // V-Smooth: O_t += L_t M'^T for a run's 16 blocks, L_t the BF16 row
+      // sums (rounded values, then remainders) the ExpCast warps left in
+      // S_t's columns [a, a + 16).
+      auto mean_mma = [&](uint32_t tO, uint32_t a, uint32_t slot) {
+        const uint64_t md = sw32_desc(smem_addr(sm.mv[slot]));
+        mma_bf16_ts(tO, a, md, kIdescBf16, 1u);
+        mma_bf16_ts(tO, a + 8, md, kIdescBf16, 1u);
+      };
       const uint32_t tS0 = tmem + 0, tS1 = tmem + 128;
       const uint32_t tO0 = tmem + 256, tO1 = tmem + 384;
       const uint64_t qd0 = sw128_desc(smem_addr(sm.q[0])), qd1 = sw128_desc(smem_addr(sm.q[1]));
       for (int u = blockIdx.x; u < P.nunits && ok; u += gridDim.x) {
-        const int nblk = unit_coord<kVar>(P, u).nbu + P.rep_blocks;
+        const UnitCoord ucm = unit_coord<kVar>(P, u);
+        const int nbu = ucm.nbu, b0 = ucm.b0;
+        const int nblk = nbu + P.rep_blocks;
         ok = mbar_wait(smem_addr(&sm.q_full), q_iter & 1, tmo, abort_flag);
         if (!ok) break;
         // Scores of the first block for both query tiles.
@@ -488,6 +557,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           const uint64_t vd = sw128_desc(smem_addr(sm.v[stage]));
           const bool last = (i + 1 == nblk);
           const uint32_t nstage = (kv_iter + 1) % kStages;
+          // V-Smooth: this block flushes the previous run (it starts a new
+          // one) and, as the unit's last block, its own run.
+          bool fl_prev = false, fl_last = false;
+          uint32_t r_prev = 0, r_last = 0;
+          if ((kVar & kVarVSmooth) && i < nbu) {
+            if (starts_run<kVar>(i, b0, nbu)) {
+              if (i > 0) fl_prev = true, r_prev = mrun - 1;
+              ++mrun;
+            }
+            if (i + 1 == nbu) fl_last = true, r_last = mrun - 1;
+          }
           // ---- query tile 0: O0 += P0 V, then the next block's S0
           ok = mbar_wait(smem_addr(&sm.p_full[0]), sp0, tmo, abort_flag);
           if (!ok) break;
@@ -497,6 +577,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_f8_ts(tO0, tS0 + 8 * kk, vd + 2 * kk, kIdesc, (i > 0 || kk > 0) ? 1u : 0u);
+          if (fl_prev) {
+            ok = mbar_wait(smem_addr(&sm.m_full[r_prev & 1]), (r_prev >> 1) & 1, tmo, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            mean_mma(tO0, tS0 + 32, r_prev & 1);
+          }
+          if (fl_last) {
+            ok = mbar_wait(smem_addr(&sm.m_full[r_last & 1]), (r_last >> 1) & 1, tmo, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            mean_mma(tO0, tS0 + 48, r_last & 1);
+          }
           uint64_t kd_next = 0;
           if (!last) {
             ok = mbar_wait(smem_addr(&sm.k_full[nstage]), ((kv_iter + 1) / kStages) & 1, tmo, abort_flag);
@@ -519,6 +611,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_f8_ts(tO1, tS1 + 8 * kk, vd + 2 * kk, kIdesc, (i > 0 || kk > 0) ? 1u : 0u);
+          if (fl_prev) {
+            mean_mma(tO1, tS1 + 32, r_prev & 1);
+            tc_commit(smem_addr(&sm.m_empty[r_prev & 1]));
+          }
+          if (fl_last) {
+            mean_mma(tO1, tS1 + 48, r_last & 1);
+            tc_commit(smem_addr(&sm.m_empty[r_last & 1]));
+          }
           tc_commit(smem_addr(&sm.kv_empty[stage]));
           if (!last) {
 #pragma unroll
@@ -552,6 +652,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     uint32_t blk_count = 0, tile_count = 0;
     const int trole = (wq == 0) ? t : -1;
     bool ok = true;
+    if (kVar & kVarVSmooth) {
+#pragma unroll
+      for (int c = 0; c < 16; ++c) sm.lbuf[t][c][row] = 0.0f;
+    }
     for (int u = blockIdx.x; u < P.nunits && ok; u += gridDim.x) {
       const UnitCoord uc = unit_coord<kVar>(P, u);
       const TileCoord& tc = uc.tc;
@@ -600,6 +704,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             l *= f;
             kf = kn;
             rescale = i > 0;
+            if ((kVar & kVarVSmooth) && rescale) {
+              // Row sums not yet added to O change units with it.
+#pragma unroll
+              for (int c = 0; c < 16; ++c) sm.lbuf[t][c][row] *= f;
+            }
           }
           if (trole >= 0) trace_mark(P, trole, gi, 3);
           if (kVar & kVarExpThenCast)
@@ -632,6 +741,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         if (trole >= 0) trace_mark(P, trole, gi, 4);
         tmem_st32(tS, w);
+        bool lsum_done = false;
+        if ((kVar & kVarVSmooth) && main_blk) {
+          // V-Smooth: a block that starts a run hands the previous run's row
+          // sums to the mean MMA (columns 32-47 of S_t); the unit's last block
+          // adds its own row sum first and hands its run over too (48-63).
+          float* lb = &sm.lbuf[t][0][row];
+          if (i > 0 && starts_run<kVar>(i, uc.b0, uc.nbu)) flush_row_sums(lb, tS + 32);
+          if (i + 1 == uc.nbu) {
+            const float lbi = codes_sum(w);
+            l += lbi;
+            lb[(j & 15) * 128] = lbi;
+            flush_row_sums(lb, tS + 48);
+            lsum_done = true;
+          }
+        }
         // O is stable here (every earlier MMA of this tile has completed) and
         // the next P.V waits for this thread's arrival below.
         if (rescale) tmem_scale_row128(tO, f);
@@ -639,7 +763,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tc_fence_before();
         mbar_arrive(smem_addr(&sm.p_full[t]));
         // The row sum waits until the codes are on their way to the tensor core.
-        if (main_blk) l += codes_sum(w);
+        if (main_blk && !lsum_done) {
+          const float lbi = codes_sum(w);
+          l += lbi;
+          if (kVar & kVarVSmooth) sm.lbuf[t][j & 15][row] = lbi;
+        }
         if (trole >= 0) trace_mark(P, trole, gi, 6);
       }
       if (!ok) break;

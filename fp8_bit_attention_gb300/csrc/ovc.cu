@@ -28,8 +28,8 @@ namespace {
 
 // Every instantiation of the attention kernel, indexed by its variant bits.
 const decltype(&attention_kernel<0>) kAttentionKernels[kNumVariants] = {
-    attention_kernel<0>, attention_kernel<1>, attention_kernel<2>, attention_kernel<3>,
-    attention_kernel<4>, attention_kernel<5>, attention_kernel<6>, attention_kernel<7>};
+    attention_kernel<0>, attention_kernel<1>, attention_kernel<2>, attention_kernel<3>, attention_kernel<4>,
+    attention_kernel<5>, attention_kernel<6>, attention_kernel<7>, attention_kernel<kVarVSmooth>};
 
 constexpr int kMaxDevices = 64;
 constexpr uint64_t kDefaultTimeoutNs = 4000000000ull;   // 4 s per wait
@@ -58,9 +58,10 @@ ovc_status device_state(DeviceState** out) {
     d.supported = (major == 10 && minor == 3);
     d.sms = sms;
     if (d.supported) {
-      for (auto fn : kAttentionKernels)
-        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kAttnSmemBytes)) != cudaSuccess)
+      for (int v = 0; v < kNumVariants; ++v)
+        if (cudaFuncSetAttribute(kAttentionKernels[v], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(v == kVarVSmooth ? kAttnSmemBytesVSmooth : kAttnSmemBytes)) !=
+            cudaSuccess)
           return OVC_ERR_CUDA;
       void* p = nullptr;
       if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return OVC_ERR_CUDA;
@@ -100,6 +101,21 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, u
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// V-Smooth means [rows][pitch] BF16 (rows = B*H*128 channels, pitch = nbk
+// blocks): 16 x 128 boxes with the 32-byte swizzle; the extent stops at nb
+// blocks so that the boxes of the last chunk read zeros past it.
+bool make_mean_map(CUtensorMap* m, const void* base, uint64_t nb, uint64_t rows, uint64_t pitch_elems) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {nb, rows};
+  cuuint64_t strides[1] = {pitch_elems * 2};
+  cuuint32_t box[2] = {16, 128};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -113,7 +129,7 @@ bool dims_ok(int64_t B, int64_t S, int64_t H) {
 }
 
 struct PrepLayout {
-  size_t q, k, vt, sq, sk, sv, vamax, energy, kpart, kmean, total;
+  size_t q, k, vt, sq, sk, sv, vamax, energy, kpart, kmean, vmu, vmean, total;
 };
 
 PrepLayout prep_layout(int64_t B, int64_t S, int64_t H, uint32_t flags = 0) {
@@ -136,6 +152,10 @@ PrepLayout prep_layout(int64_t B, int64_t S, int64_t H, uint32_t flags = 0) {
   if (flags & OVC_PREPARE_SMOOTH_K) {
     L.kpart = take(static_cast<size_t>(BH) * nb * 128 * 4);
     L.kmean = take(static_cast<size_t>(BH) * 128 * 4);
+  }
+  if (flags & OVC_PREPARE_V_SMOOTH) {
+    L.vmu = take(static_cast<size_t>(BH) * nb * 128 * 4);
+    L.vmean = take(static_cast<size_t>(BH) * 128 * ((nb + 15) / 16 * 16) * 2);
   }
   L.total = off;
   return L;
@@ -238,6 +258,9 @@ ovc_status run_attention(const ovc_prepared* p, const ovc_repair* r, float softm
   if (flags & ~(OVC_ATTN_EXP_THEN_CAST | OVC_ATTN_NATURAL_ORDER)) return OVC_ERR_INVALID_ARG;
   if (nsplit < 0 || nsplit > kMaxSplit || nsplit > p->nb || (nsplit > 1 && r)) return OVC_ERR_INVALID_ARG;
   if (nsplit > 1 && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))) return OVC_ERR_INVALID_ARG;
+  // V-Smooth runs with the method's own kernel only: no repair, no split, no variant.
+  const bool vsmooth = p->vmean != nullptr;
+  if (vsmooth && (r || nsplit > 1 || flags != 0)) return OVC_ERR_INVALID_ARG;
   if (r) {
     if (!r->idx || !r->k_sel || !r->dvt || !r->sk_sel || !r->sr) return OVC_ERR_INVALID_ARG;
     if (r->B != p->B || r->S != p->S || r->H != p->H) return OVC_ERR_INVALID_ARG;
@@ -260,6 +283,8 @@ ovc_status run_attention(const ovc_prepared* p, const ovc_repair* r, float softm
     mks = mk;
     mdv = mv;
   }
+  CUtensorMap mvm = mk;
+  if (vsmooth && !make_mean_map(&mvm, p->vmean, p->nb, BH * 128, (p->nb + 15) / 16 * 16)) return OVC_ERR_CUDA;
 
   AttnParams P{};
   P.B = static_cast<int32_t>(p->B);
@@ -273,7 +298,7 @@ ovc_status run_attention(const ovc_prepared* p, const ovc_repair* r, float softm
   const bool persistent = persistent_schedule(p, probe);
   int64_t ns = nsplit;
   if (ns == 0) {   // automatic: only on the per-tile schedule, without repair, given workspace
-    ns = (r || persistent || !workspace) ? 1 : auto_split(ntiles, p->nb, dev->sms);
+    ns = (r || vsmooth || persistent || !workspace) ? 1 : auto_split(ntiles, p->nb, dev->sms);
     if (ns > 1 && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return OVC_ERR_INVALID_ARG;
   }
   const int64_t nunits = ntiles * ns;
@@ -322,8 +347,10 @@ ovc_status run_attention(const ovc_prepared* p, const ovc_repair* r, float softm
   const int64_t grid = persistent ? (nunits < dev->sms ? nunits : dev->sms) : nunits;
   static_assert(OVC_ATTN_EXP_THEN_CAST == kVarExpThenCast && OVC_ATTN_NATURAL_ORDER == kVarNaturalOrder,
                 "flag bits select the kernel variant");
-  kAttentionKernels[flags | (ns > 1 ? kVarSplit : 0)]<<<static_cast<unsigned>(grid), kAttnThreads, kAttnSmemBytes,
-                   static_cast<cudaStream_t>(stream)>>>(mq, mk, mv, mks, mdv, P);
+  const int variant = vsmooth ? kVarVSmooth : static_cast<int>(flags | (ns > 1 ? kVarSplit : 0));
+  kAttentionKernels[variant]<<<static_cast<unsigned>(grid), kAttnThreads,
+                               vsmooth ? kAttnSmemBytesVSmooth : kAttnSmemBytes,
+                               static_cast<cudaStream_t>(stream)>>>(mq, mk, mv, mks, mdv, mvm, P);
   if (ns > 1) {
     const int64_t rows = BH * p->S;
     merge_kernel<<<static_cast<unsigned>((rows + kMergeRowsPerBlock - 1) / kMergeRowsPerBlock),
@@ -344,7 +371,7 @@ size_t ovc_prepare_workspace_bytes(int64_t B, int64_t S, int64_t H, int64_t D) {
 }
 
 size_t ovc_prepare_workspace_bytes_ex(int64_t B, int64_t S, int64_t H, int64_t D, uint32_t flags) {
-  if (D != 128 || !dims_ok(B, S, H) || (flags & ~OVC_PREPARE_SMOOTH_K)) return 0;
+  if (D != 128 || !dims_ok(B, S, H) || (flags & ~(OVC_PREPARE_SMOOTH_K | OVC_PREPARE_V_SMOOTH))) return 0;
   return prep_layout(B, S, H, flags).total;
 }
 
@@ -355,7 +382,7 @@ ovc_status ovc_prepare(const ovc_tensor* q, const ovc_tensor* k, const ovc_tenso
 
 ovc_status ovc_prepare_ex(const ovc_tensor* q, const ovc_tensor* k, const ovc_tensor* v, uint32_t flags,
                           void* workspace, size_t workspace_bytes, ovc_prepared* out, void* stream) {
-  if (flags & ~OVC_PREPARE_SMOOTH_K) return OVC_ERR_INVALID_ARG;
+  if (flags & ~(OVC_PREPARE_SMOOTH_K | OVC_PREPARE_V_SMOOTH)) return OVC_ERR_INVALID_ARG;
   if (!q || !k || !v || !out) return OVC_ERR_INVALID_ARG;
   if (q->D != 128 || k->D != 128 || v->D != 128) return OVC_ERR_UNSUPPORTED;
   if ((q->dtype != OVC_BF16 && q->dtype != OVC_FP16) || k->dtype != q->dtype || v->dtype != q->dtype)
@@ -385,6 +412,7 @@ ovc_status ovc_prepare_ex(const ovc_tensor* q, const ovc_tensor* k, const ovc_te
   p.sv = reinterpret_cast<float*>(ws + L.sv);
   p.vamax = reinterpret_cast<uint32_t*>(ws + L.vamax);
   p.energy = reinterpret_cast<float*>(ws + L.energy);
+  p.vmean = (flags & OVC_PREPARE_V_SMOOTH) ? reinterpret_cast<uint16_t*>(ws + L.vmean) : nullptr;
 
   PrepParams P{};
   P.q = static_cast<const uint16_t*>(q->ptr);
@@ -420,10 +448,20 @@ ovc_status ovc_prepare_ex(const ovc_tensor* q, const ovc_tensor* k, const ovc_te
     k_mean_partial_kernel<<<dim3(static_cast<unsigned>(p.nb), static_cast<unsigned>(p.B * p.H)), 128, 0, s>>>(P);
     k_mean_final_kernel<<<static_cast<unsigned>(p.B * p.H), 128, 0, s>>>(P);
   }
-  const dim3 g1(static_cast<unsigned>(p.nb), static_cast<unsigned>(p.B * p.H), 3);
+  if (flags & OVC_PREPARE_V_SMOOTH) {
+    P.vmu = reinterpret_cast<float*>(ws + L.vmu);
+    P.vmean = p.vmean;
+    P.nbk = static_cast<int32_t>((p.nb + 15) / 16 * 16);
+    vsmooth_mean_kernel<<<dim3(static_cast<unsigned>(p.nb), static_cast<unsigned>(p.B * p.H)), 128, 0, s>>>(P);
+  }
+  // z = 2 (the amax of V) only without V-Smooth, whose mean pass folds it in
+  const dim3 g1(static_cast<unsigned>(p.nb), static_cast<unsigned>(p.B * p.H), (flags & OVC_PREPARE_V_SMOOTH) ? 2 : 3);
   prepare_qk_kernel<<<g1, 256, 0, s>>>(P);
   const dim3 g2(static_cast<unsigned>(p.nb), static_cast<unsigned>(p.B * p.H), 1);
-  prepare_v_kernel<<<g2, 512, 0, s>>>(P);
+  if (flags & OVC_PREPARE_V_SMOOTH)
+    prepare_v_kernel<true><<<g2, 512, 0, s>>>(P);
+  else
+    prepare_v_kernel<false><<<g2, 512, 0, s>>>(P);
   st = launch_status();
   if (st == OVC_OK) *out = p;
   return st;
@@ -452,7 +490,7 @@ size_t ovc_attention_workspace_bytes(const ovc_prepared* p, int32_t nsplit) {
   int64_t ns = nsplit;
   if (ns == 0) {
     DeviceState* dev = nullptr;
-    if (persistent_schedule(p, nullptr) || device_state(&dev) != OVC_OK) return 0;
+    if (p->vmean || persistent_schedule(p, nullptr) || device_state(&dev) != OVC_OK) return 0;
     ns = auto_split(ntiles_of(p), p->nb, dev->sms);
   }
   return ns > 1 ? split_layout(ntiles_of(p) * ns).total : 0;
@@ -469,6 +507,7 @@ ovc_status ovc_prepare_v_repair(const ovc_tensor* v, const ovc_prepared* p, floa
   if (v->D != 128) return OVC_ERR_UNSUPPORTED;
   if (v->dtype != OVC_BF16 && v->dtype != OVC_FP16) return OVC_ERR_UNSUPPORTED;
   if (!tensor_ok(v) || !prepared_ok(p)) return OVC_ERR_INVALID_ARG;
+  if (p->vmean) return OVC_ERR_INVALID_ARG;   // V-Smooth keeps no residual energies
   if (v->B != p->B || v->S != p->S || v->H != p->H) return OVC_ERR_INVALID_ARG;
   if (!(budget > 0.0f) || budget > 1.0f) return OVC_ERR_INVALID_ARG;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return OVC_ERR_INVALID_ARG;
@@ -670,7 +709,7 @@ extern "C" ovc_status ovc_prepare_noalloc(const ovc_tensor* q, const ovc_tensor*
   const dim3 g1(static_cast<unsigned>(nb), static_cast<unsigned>(BH), 3);
   prepare_qk_kernel<<<g1, 256, 0, s>>>(P);
   const dim3 g2(static_cast<unsigned>(nb), static_cast<unsigned>(BH), 1);
-  prepare_v_kernel<<<g2, 512, 0, s>>>(P);
+  prepare_v_kernel<false><<<g2, 512, 0, s>>>(P);
   if (out->vamax) noalloc_copy_kernel<<<(n + 255) / 256, 256, 0, s>>>(scratch, out->vamax, n);
   return launch_status();
 }

@@ -24,8 +24,12 @@
 //   prepare_v_kernel   grid (nb, B*H): quantises a 128-token block of V with
 //                      the head scale, writes it transposed (keys contiguous)
 //                      and the per-token residual energy.
+// V-Smooth (optional): vsmooth_mean_kernel replaces the z = 2 amax pass (it
+// writes the block means and folds amax|v - mu| into the head maximum), and
+// prepare_v_kernel quantises v - mu and writes the restored means.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include <cstdint>
@@ -53,6 +57,13 @@ struct PrepParams {
   // kmean [B*H][128] channel means subtracted from K before quantising.
   float* kpart;
   float* kmean;
+  // V-Smooth (both NULL when off): vmu [B*H][nb][128] block means of V (BF16
+  // values held as FP32); vmean [B*H][128][nbk] BF16 bits of the restored
+  // means M'_b = bf16(mu_b r), channel-major with blocks contiguous (the B
+  // operand of the mean-restore MMA), nbk = nb rounded up to 16.
+  float* vmu;
+  uint16_t* vmean;
+  int32_t nbk;
 };
 
 // |x| of two packed 16-bit floats, as ordered integers (sign bit cleared).
@@ -133,6 +144,30 @@ __global__ void __launch_bounds__(128) k_mean_final_kernel(const __grid_constant
   float total = 0.0f;
   for (int j = 0; j < P.nb; ++j) total = __fadd_rn(total, part[j * 128]);
   P.kmean[bh * 128 + d] = __fdiv_rn(total, static_cast<float>(P.S));
+}
+
+// V-Smooth ("VC-Attention" summary, "V-Smooth"), first pass: per 128-token
+// block of V and channel, the mean mu = bf16(fl(sum in token order) / n)
+// (n = the block's valid tokens), then the block's amax of fl(v - mu) folded
+// into the head's running maximum.  One thread per channel; every token row
+// is a coalesced 256-byte read, and the second read of the block hits cache.
+__global__ void __launch_bounds__(128) vsmooth_mean_kernel(const __grid_constant__ PrepParams P) {
+  __shared__ uint32_t red[32];
+  const int j = blockIdx.x, bh = blockIdx.y, d = threadIdx.x;
+  const int b = bh / P.H, h = bh % P.H;
+  const int t0 = j * 128, t1 = min(P.S, t0 + 128);
+  const uint16_t* src = P.v + b * P.vs[0] + h * P.vs[2] + d;
+  float sum = 0.0f;
+#pragma unroll 16
+  for (int t = t0; t < t1; ++t) sum = __fadd_rn(sum, half_bits_to_float(__ldg(src + t * P.vs[1]), P.fp16));
+  const float mu = __bfloat162float(__float2bfloat16_rn(__fdiv_rn(sum, static_cast<float>(t1 - t0))));
+  P.vmu[(static_cast<int64_t>(bh) * P.nb + j) * 128 + d] = mu;
+  float m = 0.0f;
+#pragma unroll 16
+  for (int t = t0; t < t1; ++t)
+    m = fmaxf(m, fabsf(__fsub_rn(half_bits_to_float(__ldg(src + t * P.vs[1]), P.fp16), mu)));
+  const uint32_t mb = block_max_u32(__float_as_uint(m), red);
+  if (d == 0) atomicMax(P.vamax + bh, mb);
 }
 
 // One 128-token block of Q or K (z = 0, 1), or the amax of one block of V
@@ -228,6 +263,7 @@ __global__ void __launch_bounds__(256) prepare_qk_kernel(const __grid_constant__
 // with coalesced 128-byte rows, and the residual energy of each token:
 // R = fl(v - fl(s_v * dec(code))), sixteen sequential partial sums over 8
 // channels, then the pairwise tree p_g += p_(g+w), w = 8, 4, 2, 1.
+template <bool kVSmooth>
 __global__ void __launch_bounds__(512) prepare_v_kernel(const __grid_constant__ PrepParams P) {
   __shared__ float part[16][128];
   const int j = blockIdx.x;
@@ -238,6 +274,17 @@ __global__ void __launch_bounds__(512) prepare_v_kernel(const __grid_constant__ 
   const float amax = __uint_as_float(P.vamax[bh]);
   const QScale sc = scale_from_amax(amax);
   if (j == 0 && threadIdx.x == 0) P.sv[bh] = sc.s;
+  constexpr bool vs = kVSmooth;
+  float mu[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) mu[i] = vs ? P.vmu[(static_cast<int64_t>(bh) * P.nb + j) * 128 + 8 * warp + i] : 0.0f;
+  if (vs && lane == 0) {
+    // Restored means in the scale's units, M'_b = bf16(mu_b r).
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      P.vmean[(static_cast<int64_t>(bh) * 128 + 8 * warp + i) * P.nbk + j] =
+          __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(mu[i], sc.r)));
+  }
 
   uint32_t lo[4], hi[4];
 #pragma unroll
@@ -248,7 +295,11 @@ __global__ void __launch_bounds__(512) prepare_v_kernel(const __grid_constant__ 
       x = __ldg(reinterpret_cast<const uint4*>(P.v + b * P.vs[0] + t * P.vs[1] + h * P.vs[2] + 8 * warp));
     const float2 a = unpack2(x.x, P.fp16), c = unpack2(x.y, P.fp16);
     const float2 d = unpack2(x.z, P.fp16), e = unpack2(x.w, P.fp16);
-    const float xv[8] = {a.x, a.y, c.x, c.y, d.x, d.y, e.x, e.y};
+    float xv[8] = {a.x, a.y, c.x, c.y, d.x, d.y, e.x, e.y};
+    if (vs) {   // V-Smooth: the residual fl(v - mu_b) is quantised; padding rows stay 0
+#pragma unroll
+      for (int i = 0; i < 8; ++i) xv[i] = t < P.S ? __fsub_rn(xv[i], mu[i]) : 0.0f;
+    }
     lo[k] = quant4(xv[0], xv[1], xv[2], xv[3], sc.r);
     hi[k] = quant4(xv[4], xv[5], xv[6], xv[7], sc.r);
     float dq[8];
@@ -285,7 +336,7 @@ __global__ void __launch_bounds__(512) prepare_v_kernel(const __grid_constant__ 
   for (int d = 0; d < 8; ++d) *reinterpret_cast<uint32_t*>(vt + static_cast<int64_t>(d) * P.S_pad) = out[d];
 
   __syncthreads();
-  if (threadIdx.x < 128) {
+  if (threadIdx.x < 128 && !vs) {   // V-Smooth computes no repair energies
     const int tok = threadIdx.x;
     const int t = j * 128 + tok;
     if (t < P.S) {

@@ -136,6 +136,33 @@ __device__ __forceinline__ void mma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint
       : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]^T with BF16 A and B, FP32 accumulate.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor for a K-major tile whose rows are 32 bytes
+// (16 BF16) and which TMA wrote with the 32-byte swizzle: 8-row groups 256
+// bytes apart, fixed version bits 46..48 = 0b001, swizzle mode 6 (32 B).
+__device__ __forceinline__ uint64_t sw32_desc(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(1) << 16) |
+         (static_cast<uint64_t>(256 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(6) << 61);
+}
+
+// Instruction descriptor, kind::f16: D = F32 (bits 4-5 = 1), A = B = BF16
+// (format 1 at bits 7-9 and 10-12), both K-major, N >> 3 at bit 17, M >> 4
+// at bit 24.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
 // Shared-memory matrix descriptor for a K-major tile whose rows are 128 bytes
 // and which TMA wrote with the 128-byte swizzle: 8-row groups 1024 bytes
 // apart, fixed version bits 46..48 = 0b001, swizzle mode 2 (128 B).

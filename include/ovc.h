@@ -77,7 +77,12 @@ typedef struct {
  *   sq,sk [B,H,nb]         FP32 scale of each 128-token block, amax/448
  *   sv    [B,H]            FP32 scale of each head of V, amax/448
  *   vamax [B,H]            FP32 bits of each head's amax|V|
- *   energy[B,H,S]          FP32 residual energy ||v_t - sv*dec(code_t)||^2 */
+ *   energy[B,H,S]          FP32 residual energy ||v_t - sv*dec(code_t)||^2
+ *   vmean [B,H,128,nbk]    V-Smooth only (else NULL): BF16 bits of the restored
+ *                          block means M'_b = bf16(mu_b / sv), channel-major,
+ *                          nbk = nb rounded up to 16 (entries >= nb unused);
+ *                          vt then holds the residuals v - mu_b and energy is
+ *                          not computed */
 typedef struct {
   int64_t B, S, H, nb, S_pad;
   uint8_t* q;
@@ -88,6 +93,7 @@ typedef struct {
   float* sv;
   uint32_t* vamax;
   float* energy;
+  uint16_t* vmean;
 } ovc_prepared;
 
 /* V residual repair set written by ovc_prepare_v_repair (n_pad = 128*ceil(n/128)):
@@ -266,10 +272,19 @@ ovc_status ovc_prepare_noalloc(const ovc_tensor* q, const ovc_tensor* k, const o
  *     block in token order, the block sums in block order, then one FP32
  *     division by S) so that it reproduces bit for bit.  The means themselves
  *     are not part of ovc_prepared (attention does not need them).
+ *   OVC_PREPARE_V_SMOOTH  V-Smooth ("VC-Attention" summary, "V-Smooth"), the
+ *     paper's treatment of V that Open-VC replaced with repair.  Per head and
+ *     128-token block b: mu_b = bf16(FP32 mean of the block's valid tokens,
+ *     summed in token order); the residuals v - mu_b are quantised with one
+ *     scale per head (amax of the residuals / 448) and written to vt; the
+ *     restored means M'_b = bf16(mu_b r) go to vmean.  Attention adds M'_b,
+ *     weighted by each row's block row sum, back into O.  Not combinable with
+ *     repair (no energies) or with split key ranges.
  * ovc_prepare_workspace_bytes_ex gives the workspace for the same flags
  * (0 for unknown flags or unsupported shapes); unknown flags make
  * ovc_prepare_ex return OVC_ERR_INVALID_ARG.  Otherwise as ovc_prepare. */
 #define OVC_PREPARE_SMOOTH_K 1u
+#define OVC_PREPARE_V_SMOOTH 2u
 size_t ovc_prepare_workspace_bytes_ex(int64_t B, int64_t S, int64_t H, int64_t D, uint32_t flags);
 ovc_status ovc_prepare_ex(const ovc_tensor* q, const ovc_tensor* k, const ovc_tensor* v, uint32_t flags,
                           void* workspace, size_t workspace_bytes, ovc_prepared* out, void* stream);

@@ -159,9 +159,11 @@ def test_prepare_options_on_the_host(lib):
     assert lib.ovc_prepare_workspace_bytes_ex(1, 73397, 56, 128, 0) == base
     smooth = lib.ovc_prepare_workspace_bytes_ex(1, 73397, 56, 128, _abi.OVC_PREPARE_SMOOTH_K)
     assert smooth >= base + 56 * 574 * 128 * 4 + 56 * 128 * 4
-    assert lib.ovc_prepare_workspace_bytes_ex(1, 73397, 56, 128, 2) == 0        # unknown flag
+    vsm = lib.ovc_prepare_workspace_bytes_ex(1, 73397, 56, 128, _abi.OVC_PREPARE_V_SMOOTH)
+    assert vsm >= base + 56 * 574 * 128 * 4 + 56 * 128 * 576 * 2     # block means + M' tiles
+    assert lib.ovc_prepare_workspace_bytes_ex(1, 73397, 56, 128, 4) == 0        # unknown flag
     t = _abi.OvcTensor(0x1000, _abi.OVC_BF16, 1, 128, 1, 128, 128 * 128, 128, 128)
     out = _abi.OvcPrepared()
-    st = lib.ovc_prepare_ex(ctypes.byref(t), ctypes.byref(t), ctypes.byref(t), 6, ctypes.c_void_p(0x100000),
+    st = lib.ovc_prepare_ex(ctypes.byref(t), ctypes.byref(t), ctypes.byref(t), 12, ctypes.c_void_p(0x100000),
                             1 << 30, ctypes.byref(out), None)
     assert st == _abi.OVC_ERR_INVALID_ARG

@@ -399,3 +399,59 @@ def test_split_rejected_with_repair_and_without_workspace():
                                      ctypes.c_void_p(small.data_ptr()), 16, None)
     assert st == _abi.OVC_ERR_WORKSPACE_TOO_SMALL
     assert ovc.device_status() == 0
+
+
+# ---- V-Smooth ---------------------------------------------------------------
+def _vsmooth_inputs(B, H, S, seed, offset=20.0):
+    """Values with large per-block, per-channel offsets (the case V-Smooth is for)."""
+    q, k, v = inputs(B, H, S, seed=seed)
+    rng = np.random.default_rng(seed)
+    nb = (S + 127) // 128
+    offs = offset * rng.standard_normal((B, nb, H, 128)).astype(np.float32)
+    v = (v.float() + torch.from_numpy(np.repeat(offs, 128, axis=1)[:, :S])).to(torch.bfloat16)
+    return q, k, v
+
+
+@pytest.mark.parametrize("B,H,S", [(1, 2, 1024), (1, 1, 1), (1, 2, 129), (2, 3, 300), (1, 2, 1000), (1, 1, 2300)])
+def test_v_smooth_prepare_bit_exact_and_attention(B, H, S):
+    q, k, v = _vsmooth_inputs(B, H, S, seed=1100 + S)
+    ref = oracle.Prepared(W.bf16_bits(q), W.bf16_bits(k), W.bf16_bits(v), v_smooth=True)
+    prep = ovc.prepare(*to_dev(q, k, v), v_smooth=True)
+    torch.cuda.synchronize()
+    assert np.array_equal(prep.vt_codes().cpu().numpy().transpose(0, 1, 3, 2), ref.vc)
+    assert np.array_equal(prep.v_scales().cpu().numpy(), ref.sv)
+    assert np.array_equal(prep.q_codes().cpu().numpy(), ref.qc) and np.array_equal(prep.k_codes().cpu().numpy(), ref.kc)
+    nb = (S + 127) // 128
+    mp = prep.v_means().float().cpu().numpy()[..., :nb].transpose(0, 1, 3, 2)
+    assert np.array_equal(mp, ref.vmean)
+    want, _ = oracle.attention_full(ref)
+    o = ovc.attention_prepared(prep)
+    assert ovc.device_status() == 0
+    got = o.float().cpu().numpy()
+    assert np.isfinite(got).all()
+    assert rel_l2(got, want) <= TOL_REL_L2
+    # the restore matters here: without it the output is far off
+    plain_ref = oracle.Prepared(W.bf16_bits(q), W.bf16_bits(k), W.bf16_bits(v))
+    if S > 1:
+        base, _ = oracle.attention_full(plain_ref)
+        assert rel_l2(got, base) < 0.05
+
+
+def test_v_smooth_persistent_schedule_and_rejections():
+    q, k, v = _vsmooth_inputs(1, 2, 3000, seed=1200)
+    ref = oracle.Prepared(W.bf16_bits(q), W.bf16_bits(k), W.bf16_bits(v), v_smooth=True)
+    qd, kd, vd = to_dev(q, k, v)
+    prep = ovc.prepare(qd, kd, vd, v_smooth=True)
+    a, _, _ = ovc.attention_probe(prep, force_persistent=1)
+    b, _, _ = ovc.attention_probe(prep, force_persistent=-1)
+    assert ovc.device_status() == 0
+    assert torch.equal(a, b)
+    want, _ = oracle.attention_full(ref)
+    assert rel_l2(a.float().cpu().numpy(), want) <= TOL_REL_L2
+    with pytest.raises(ovc.OvcError):
+        ovc.prepare_v_repair(vd, prep, 0.01)
+    with pytest.raises(ovc.OvcError):
+        ovc.attention_prepared(prep, nsplit=2)
+    with pytest.raises(ovc.OvcError):
+        ovc.attention_prepared(prep, flags=1)
+    assert ovc.device_status() == 0
