@@ -54,6 +54,11 @@ constexpr int kAttnThreads = 384;                          // 3 warpgroups
 constexpr int kSoftmaxRegs = 200;
 constexpr int kControlRegs = 104;
 static_assert(256 * kSoftmaxRegs + 128 * kControlRegs <= kAttnThreads * 168, "register split");
+// V-Smooth's MMA warp keeps the run bookkeeping as well: 192 / 120 (its
+// ExpCast warps fit in 192 with no spill).
+constexpr int kSoftmaxRegsVSmooth = 192;
+constexpr int kControlRegsVSmooth = 120;
+static_assert(256 * kSoftmaxRegsVSmooth + 128 * kControlRegsVSmooth <= kAttnThreads * 168, "register split");
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr uint32_t kTile = 128 * 128;                       // bytes of one E4M3 tile
@@ -448,7 +453,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   if (warp >= 8) {
-    regs_dec<kControlRegs>();
+    regs_dec<(kVar & kVarVSmooth) ? kControlRegsVSmooth : kControlRegs>();
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------------ TMA
     if (lane == 0) {
@@ -520,7 +525,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       // V-Smooth: O_t += L_t M'^T for a run's 16 blocks, L_t the BF16 row
       // sums (rounded values, then remainders) the ExpCast warps left in
       // S_t's columns [a, a + 16).
-      auto mean_mma = [&](uint32_t tO, uint32_t a, uint32_t slot) {
+      auto mean_mma = [&sm](uint32_t tO, uint32_t a, uint32_t slot) {
         const uint64_t md = sw32_desc(smem_addr(sm.mv[slot]));
         mma_bf16_ts(tO, a, md, kIdescBf16, 1u);
         mma_bf16_ts(tO, a + 8, md, kIdescBf16, 1u);
@@ -557,16 +562,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           const uint64_t vd = sw128_desc(smem_addr(sm.v[stage]));
           const bool last = (i + 1 == nblk);
           const uint32_t nstage = (kv_iter + 1) % kStages;
-          // V-Smooth: this block flushes the previous run (it starts a new
-          // one) and, as the unit's last block, its own run.
-          bool fl_prev = false, fl_last = false;
-          uint32_t r_prev = 0, r_last = 0;
+          // V-Smooth: this block flushes the previous run (bit 0: it starts a
+          // new one, run mrun - 2 after the count) and, as the unit's last
+          // block, its own run (bit 1: run mrun - 1).
+          uint32_t fl = 0;
           if ((kVar & kVarVSmooth) && i < nbu) {
             if (starts_run<kVar>(i, b0, nbu)) {
-              if (i > 0) fl_prev = true, r_prev = mrun - 1;
+              fl = i > 0 ? 1u : 0u;
               ++mrun;
             }
-            if (i + 1 == nbu) fl_last = true, r_last = mrun - 1;
+            if (i + 1 == nbu) fl |= 2u;
           }
           // ---- query tile 0: O0 += P0 V, then the next block's S0
           ok = mbar_wait(smem_addr(&sm.p_full[0]), sp0, tmo, abort_flag);
@@ -577,17 +582,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_f8_ts(tO0, tS0 + 8 * kk, vd + 2 * kk, kIdesc, (i > 0 || kk > 0) ? 1u : 0u);
-          if (fl_prev) {
-            ok = mbar_wait(smem_addr(&sm.m_full[r_prev & 1]), (r_prev >> 1) & 1, tmo, abort_flag);
+          if (kVar & kVarVSmooth) {
+#pragma unroll
+            for (uint32_t b = 0; b < 2; ++b)
+              if (fl & (1u << b)) {
+                const uint32_t r = mrun - 2 + b;
+                ok = mbar_wait(smem_addr(&sm.m_full[r & 1]), (r >> 1) & 1, tmo, abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+                mean_mma(tO0, tS0 + 32 + 16 * b, r & 1);
+              }
             if (!ok) break;
-            tc_fence_after();
-            mean_mma(tO0, tS0 + 32, r_prev & 1);
-          }
-          if (fl_last) {
-            ok = mbar_wait(smem_addr(&sm.m_full[r_last & 1]), (r_last >> 1) & 1, tmo, abort_flag);
-            if (!ok) break;
-            tc_fence_after();
-            mean_mma(tO0, tS0 + 48, r_last & 1);
           }
           uint64_t kd_next = 0;
           if (!last) {
@@ -611,13 +616,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_f8_ts(tO1, tS1 + 8 * kk, vd + 2 * kk, kIdesc, (i > 0 || kk > 0) ? 1u : 0u);
-          if (fl_prev) {
-            mean_mma(tO1, tS1 + 32, r_prev & 1);
-            tc_commit(smem_addr(&sm.m_empty[r_prev & 1]));
-          }
-          if (fl_last) {
-            mean_mma(tO1, tS1 + 48, r_last & 1);
-            tc_commit(smem_addr(&sm.m_empty[r_last & 1]));
+          if (kVar & kVarVSmooth) {
+#pragma unroll
+            for (uint32_t b = 0; b < 2; ++b)
+              if (fl & (1u << b)) {
+                const uint32_t r = mrun - 2 + b;
+                mean_mma(tO1, tS1 + 32 + 16 * b, r & 1);
+                tc_commit(smem_addr(&sm.m_empty[r & 1]));
+              }
           }
           tc_commit(smem_addr(&sm.kv_empty[stage]));
           if (!last) {
@@ -641,7 +647,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
   }
   } else {
-    regs_inc<kSoftmaxRegs>();
+    regs_inc<(kVar & kVarVSmooth) ? kSoftmaxRegsVSmooth : kSoftmaxRegs>();
     // ------------------------------------------------------- softmax/ExpCast
     const int t = warp >> 2;                    // query tile 0 or 1
     const int wq = warp & 3;
