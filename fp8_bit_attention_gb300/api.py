@@ -315,10 +315,41 @@ def memcpy2d(dst_ptr: int, dpitch: int, src_ptr: int, spitch: int, width: int, h
           "ovc_memcpy2d")
 
 
-def head_chunks(H: int, chunk_heads: int | None = None) -> list[tuple[int, int]]:
-    """Head ranges of the host-buffer path: about four equal chunks by default."""
-    n = chunk_heads if chunk_heads else max(1, -(-H // 4))
-    return [(h0, min(H, h0 + n)) for h0 in range(0, H, n)]
+def head_chunks(H: int, chunk_heads=None, tiles_per_head: int | None = None,
+                sms: int | None = None) -> list[tuple[int, int]]:
+    """Head ranges of the host-buffer path.
+
+    chunk_heads: an int (equal chunks of that many heads), a sequence of chunk
+    sizes summing to H, or None for the default plan.  The default keeps the
+    first and the last chunk small (about H/18 heads): the first chunk's copy
+    in and the last chunk's copy out are the only copies that no computation
+    hides.  The chunks between take h heads each, h in [H/8, H/4] chosen so
+    that h * tiles_per_head fills whole waves of `sms` CTAs best, the smaller
+    h on a tie (with 287 tile pairs per head on 152 SMs, 9 heads make exactly
+    17 waves); without those figures, about a quarter of H."""
+    if chunk_heads is None:
+        edge = int(round(H / 18))
+        if edge == 0 or H < 8:
+            return head_chunks(H, max(1, -(-H // 4)))
+        mid = H - 2 * edge
+        h = max(1, -(-H // 4))
+        if tiles_per_head and sms:
+            def waste(n):
+                t = n * tiles_per_head
+                return (-(-t // sms) * sms) / t
+            h = min(range(max(1, H // 8), max(2, H // 4) + 1), key=lambda n: (round(waste(n), 4), n))
+        sizes = [edge] + [h] * (mid // h) + ([mid % h] if mid % h else []) + [edge]
+        return head_chunks(H, sizes)
+    if isinstance(chunk_heads, int):
+        n = max(1, chunk_heads)
+        return [(h0, min(H, h0 + n)) for h0 in range(0, H, n)]
+    sizes = [int(x) for x in chunk_heads]
+    if sum(sizes) != H or min(sizes) < 1:
+        raise ValueError(f"chunk sizes {sizes} do not cover {H} heads")
+    bounds = [0]
+    for n in sizes:
+        bounds.append(bounds[-1] + n)
+    return list(zip(bounds[:-1], bounds[1:]))
 
 
 def _attention_device(q, k, v, softmax_scale, repair_budget, out, smooth_k=False):
@@ -351,7 +382,9 @@ def _attention_host(q, k, v, softmax_scale, repair_budget, out, dev, chunk_heads
     o4 = _as4d(out)
     if o4.shape != q4.shape or o4.dtype != torch.bfloat16 or o4.is_cuda or not o4.is_contiguous():
         raise ValueError("out must be a contiguous CPU bfloat16 tensor shaped like q")
-    chunks = head_chunks(H, chunk_heads)
+    nb = -(-S // 128)
+    chunks = head_chunks(H, chunk_heads, tiles_per_head=B * (-(-nb // 2)),
+                         sms=torch.cuda.get_device_properties(dev).multi_processor_count)
     hmax = max(h1 - h0 for h0, h1 in chunks)
     comp = torch.cuda.current_stream(dev)
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
@@ -419,8 +452,9 @@ def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, softmax_scal
 
     CUDA inputs give a CUDA output (asynchronous on the current stream).  CPU
     inputs (pinned for speed) are streamed through `device` (default: the
-    current CUDA device) in head chunks of `chunk_heads` heads (default: about
-    a quarter of H), so that host<->device copies overlap the computation; O
+    current CUDA device) in head chunks (`chunk_heads`: a size, a list of
+    sizes, or None for the default plan of :func:`head_chunks`), so that
+    host<->device copies overlap the computation; O
     lands in `out` (or a new pinned tensor), complete when the call returns.
     smooth_k: optional K smoothing in prepare (see `prepare`)."""
     if q.is_cuda:

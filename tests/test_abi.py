@@ -144,13 +144,19 @@ def test_memcpy2d_validates_on_the_host(lib):
 
 def test_head_chunks_cover_every_head_once():
     from fp8_bit_attention_gb300.api import head_chunks
-    for H in (1, 2, 3, 7, 14, 56, 57):
+    for H in (1, 2, 3, 7, 14, 56, 57, 112):
         for n in (None, 1, 3, 64):
-            ch = head_chunks(H, n)
-            assert ch[0][0] == 0 and ch[-1][1] == H
-            assert all(a1 == b0 for (_, a1), (b0, _) in zip(ch, ch[1:]))
-            assert all(h1 > h0 for h0, h1 in ch)
-    assert len(head_chunks(56)) == 4
+            for tph, sms in ((None, None), (287, 152), (1, 152), (144, 148)):
+                ch = head_chunks(H, n, tiles_per_head=tph, sms=sms)
+                assert ch[0][0] == 0 and ch[-1][1] == H
+                assert all(a1 == b0 for (_, a1), (b0, _) in zip(ch, ch[1:]))
+                assert all(h1 > h0 for h0, h1 in ch)
+    # the default for 56 heads of 73397 tokens on 152 SMs: small edge chunks,
+    # 9-head chunks between (9 x 287 tile pairs = exactly 17 waves)
+    assert [b - a for a, b in head_chunks(56, None, 287, 152)] == [3, 9, 9, 9, 9, 9, 5, 3]
+    assert [b - a for a, b in head_chunks(10, [3, 7])] == [3, 7]
+    with pytest.raises(ValueError):
+        head_chunks(10, [3, 6])
 
 
 def test_prepare_options_on_the_host(lib):
