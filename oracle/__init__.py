@@ -76,6 +76,8 @@ def lib():
             L.ovc_oracle_k_mean.argtypes = [P, ctypes.c_int, i64, i64, i64, i64, i64, i64, P]
             L.ovc_oracle_vsmooth_v.restype = None
             L.ovc_oracle_vsmooth_v.argtypes = [P, ctypes.c_int, i64, i64, i64, i64, i64, i64, P, P, P, P]
+            L.ovc_oracle_kmeans_group.restype = ctypes.c_int
+            L.ovc_oracle_kmeans_group.argtypes = [P, ctypes.c_int, i64, i64, i64, i64, i64, i64, i64, i64, P, P, P]
             L.ovc_oracle_quantize_v.restype = None
             L.ovc_oracle_quantize_v.argtypes = [P, ctypes.c_int, i64, i64, i64, i64, i64, i64, P, P, P]
             L.ovc_oracle_repair_count.restype = i64
@@ -232,6 +234,32 @@ def vsmooth_v(v: np.ndarray, fp16: bool = False):
     return codes, sv, mu, mprime
 
 
+def kmeans_group(v: np.ndarray, clusters: int, iters: int, fp16: bool = False):
+    """V-Smooth grouping of V [B,S,H,128] bits -> (labels [B,H,S] int32,
+    centroids used by the last assignment [B,H,C,128], perm [B,H,S] int32:
+    the token at position t' of the grouped order is perm[t'])."""
+    v, sb, ss, sh = _bf16_view(v)
+    B, S, H, _ = v.shape
+    labels = np.zeros((B, H, S), np.int32)
+    cent = np.zeros((B, H, clusters, 128), np.float32)
+    perm = np.zeros((B, H, S), np.int32)
+    rc = lib().ovc_oracle_kmeans_group(_ptr(v), int(fp16), B, S, H, sb, ss, sh, int(clusters), int(iters),
+                                       _ptr(labels), _ptr(cent), _ptr(perm))
+    if rc != 0:
+        raise ValueError("invalid k-means arguments")
+    return labels, cent, perm
+
+
+def permute_tokens(x: np.ndarray, perm: np.ndarray) -> np.ndarray:
+    """x [B,S,H,D] gathered per (b, h) along S by perm [B,H,S]."""
+    B, S, H, D = x.shape
+    out = np.empty_like(x)
+    for b in range(B):
+        for h in range(H):
+            out[b, :, h] = x[b, perm[b, h], h]
+    return out
+
+
 def repair_count(S: int, budget: float) -> int:
     return int(lib().ovc_oracle_repair_count(S, float(np.float32(budget))))
 
@@ -266,11 +294,17 @@ def repair_quantize(v: np.ndarray, vcodes: np.ndarray, sv: np.ndarray, idx: np.n
 class Prepared:
     """The oracle's own quantised tensors for one (Q, K, V) triple."""
 
-    def __init__(self, q, k, v, fp16: bool = False, smooth_k: bool = False, v_smooth: bool = False):
+    def __init__(self, q, k, v, fp16: bool = False, smooth_k: bool = False, v_smooth: bool = False,
+                 perm: np.ndarray | None = None):
         """q, k, v: uint16 bits [B,S,H,128] of BF16 inputs, or of FP16 ones if
         fp16.  smooth_k: subtract K's channel means before quantising K.
         v_smooth: V-Smooth (block means subtracted, residual quantised, means
-        restored through the row sums); no residual energies then."""
+        restored through the row sums); no residual energies then.  perm
+        [B,H,S]: V-Smooth's grouping -- keys and values are taken in this
+        token order (queries are not)."""
+        if perm is not None:
+            k = permute_tokens(k, perm)
+            v = permute_tokens(v, perm)
         self.B, self.S, self.H, _ = q.shape
         self.nb = (self.S + 127) // 128
         self.fp16 = bool(fp16)

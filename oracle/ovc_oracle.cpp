@@ -592,6 +592,109 @@ void ovc_oracle_vsmooth_v(const uint16_t* v, int fp16, int64_t B, int64_t S, int
     }
 }
 
+// V-Smooth's grouping step ([VC-summary "V-Smooth": online k-means clusters
+// each head's value tokens; keys and values are permuted together, which
+// leaves non-causal attention unchanged): Lloyd's k-means with C clusters and
+// `iters` iterations, then the tokens ordered by (cluster, index).
+// Arithmetic, all FP32 with every step rounded (no fused operations):
+//   start:   mu_c = x_(floor(c S / C)), c = 0..C-1
+//   assign:  n_c = sum_d mu_cd^2 (channel order);
+//            dot(t, c) = 32 partial sums over channels 4k..4k+3 (left to
+//            right), then the pairwise tree p_k <- p_k + p_(k+w), w = 16..1;
+//            d(t, c) = n_c - 2 dot(t, c); the cluster with the smallest d,
+//            ties to the lower c
+//   update:  mu_c = (sum of its tokens) / count, the sum taken per 128-token
+//            block in token order and then over the blocks in block order; a
+//            cluster with no token keeps its centroid
+// One iteration is assign then update; the labels returned are those of the
+// last assignment, and centroids [B,H,C,128] the centroids it used.
+float kmeans_dot(const float* x, const float* mu) {
+  float p[32];
+  for (int k = 0; k < 32; ++k) {
+    volatile float a = x[4 * k] * mu[4 * k];
+    for (int i = 1; i < 4; ++i) {
+      volatile float m = x[4 * k + i] * mu[4 * k + i];
+      a = a + m;
+    }
+    p[k] = a;
+  }
+  for (int w = 16; w >= 1; w >>= 1)
+    for (int k = 0; k < w; ++k) {
+      volatile float q = p[k] + p[k + w];
+      p[k] = q;
+    }
+  return p[0];
+}
+
+int ovc_oracle_kmeans_group(const uint16_t* v, int fp16, int64_t B, int64_t S, int64_t H, int64_t sb, int64_t ss,
+                            int64_t sh, int64_t C, int64_t iters, int32_t* labels, float* centroids, int32_t* perm) {
+  if (C < 1 || C > S || iters < 1) return 1;
+  const Dims dm = make_dims(B, S, H);
+  std::vector<float> x(static_cast<size_t>(S) * 128), mu(static_cast<size_t>(C) * 128), nrm(C);
+  std::vector<float> sum(static_cast<size_t>(C) * 128), part(static_cast<size_t>(C) * 128);
+  std::vector<int64_t> cnt(C);
+  for (int64_t b = 0; b < B; ++b)
+    for (int64_t h = 0; h < H; ++h) {
+      const int64_t bh = b * H + h;
+      for (int64_t t = 0; t < S; ++t)
+        for (int d = 0; d < 128; ++d) x[t * 128 + d] = input_bits_to_float(v[b * sb + t * ss + h * sh + d], fp16);
+      for (int64_t c = 0; c < C; ++c)
+        std::memcpy(&mu[c * 128], &x[(c * S / C) * 128], 128 * sizeof(float));
+      int32_t* lab = labels + bh * S;
+      for (int64_t it = 0; it < iters; ++it) {
+        for (int64_t c = 0; c < C; ++c) {
+          volatile float n = 0.0f;
+          for (int d = 0; d < 128; ++d) {
+            volatile float sq = mu[c * 128 + d] * mu[c * 128 + d];
+            n = n + sq;
+          }
+          nrm[c] = n;
+        }
+        if (it + 1 == iters) std::memcpy(centroids + bh * C * 128, mu.data(), C * 128 * sizeof(float));
+        for (int64_t t = 0; t < S; ++t) {
+          float best = INFINITY;
+          int32_t arg = 0;
+          for (int64_t c = 0; c < C; ++c) {
+            const float dot = kmeans_dot(&x[t * 128], &mu[c * 128]);
+            volatile float dist = nrm[c] - 2.0f * dot;
+            if (dist < best) best = dist, arg = static_cast<int32_t>(c);
+          }
+          lab[t] = arg;
+        }
+        if (it + 1 == iters) break;
+        std::fill(sum.begin(), sum.end(), 0.0f);
+        std::fill(cnt.begin(), cnt.end(), 0);
+        for (int64_t j = 0; j < dm.nb; ++j) {
+          std::fill(part.begin(), part.end(), 0.0f);
+          for (int64_t t = j * 128; t < std::min(S, j * 128 + 128); ++t) {
+            const int64_t c = lab[t];
+            ++cnt[c];
+            for (int d = 0; d < 128; ++d) {
+              volatile float a = part[c * 128 + d] + x[t * 128 + d];
+              part[c * 128 + d] = a;
+            }
+          }
+          for (int64_t i = 0; i < C * 128; ++i) {
+            volatile float a = sum[i] + part[i];
+            sum[i] = a;
+          }
+        }
+        for (int64_t c = 0; c < C; ++c)
+          if (cnt[c] > 0)
+            for (int d = 0; d < 128; ++d) {
+              volatile float m = sum[c * 128 + d] / static_cast<float>(cnt[c]);
+              mu[c * 128 + d] = m;
+            }
+      }
+      // tokens ordered by (cluster, index)
+      std::vector<int32_t> order(S);
+      for (int64_t t = 0; t < S; ++t) order[t] = static_cast<int32_t>(t);
+      std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t c) { return lab[a] < lab[c]; });
+      std::memcpy(perm + bh * S, order.data(), S * sizeof(int32_t));
+    }
+  return 0;
+}
+
 // Number of repaired tokens per head: n = ceil(budget * S), at least 1.
 int64_t ovc_oracle_repair_count(int64_t S, float budget) {
   const double n = std::ceil(static_cast<double>(budget) * static_cast<double>(S));
