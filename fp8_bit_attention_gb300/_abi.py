@@ -40,7 +40,7 @@ class OvcOutput(ctypes.Structure):
 class OvcPrepared(ctypes.Structure):
     _fields_ = [("B", c_i64), ("S", c_i64), ("H", c_i64), ("nb", c_i64), ("S_pad", c_i64),
                 ("q", c_ptr), ("k", c_ptr), ("vt", c_ptr), ("sq", c_ptr), ("sk", c_ptr),
-                ("sv", c_ptr), ("vamax", c_ptr), ("energy", c_ptr), ("vmean", c_ptr)]
+                ("sv", c_ptr), ("vamax", c_ptr), ("energy", c_ptr), ("vmean", c_ptr), ("perm", c_ptr)]
 
 
 class OvcRepair(ctypes.Structure):
@@ -78,6 +78,10 @@ SIGNATURES = {
     "ovc_prepare_workspace_bytes_ex": (ctypes.c_size_t, [c_i64, c_i64, c_i64, c_i64, ctypes.c_uint32]),
     "ovc_prepare_ex": (c_i32, [P(OvcTensor), P(OvcTensor), P(OvcTensor), ctypes.c_uint32, c_ptr,
                                ctypes.c_size_t, P(OvcPrepared), c_ptr]),
+    "ovc_vsmooth_group_workspace_bytes": (ctypes.c_size_t, [c_i64, c_i64, c_i64, c_i32]),
+    "ovc_vsmooth_group": (c_i32, [P(OvcTensor), c_i32, c_i32, c_ptr, ctypes.c_size_t, c_ptr, c_ptr]),
+    "ovc_prepare_grouped": (c_i32, [P(OvcTensor), P(OvcTensor), P(OvcTensor), c_ptr, ctypes.c_uint32, c_ptr,
+                                    ctypes.c_size_t, P(OvcPrepared), c_ptr]),
     "ovc_memcpy2d": (c_i32, [c_ptr, ctypes.c_size_t, c_ptr, ctypes.c_size_t, ctypes.c_size_t,
                              ctypes.c_size_t, c_ptr]),
 }

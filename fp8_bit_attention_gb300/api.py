@@ -66,6 +66,7 @@ class Prepared:
     workspace: torch.Tensor
     shape: tuple
     dtype: torch.dtype
+    perm: torch.Tensor | None = None      # grouping order of K and V, kept alive here
 
     @property
     def B(self):
@@ -150,13 +151,32 @@ def _prep_flags(smooth_k: bool, v_smooth: bool = False) -> int:
     return (_abi.OVC_PREPARE_SMOOTH_K if smooth_k else 0) | (_abi.OVC_PREPARE_V_SMOOTH if v_smooth else 0)
 
 
+def group_v(v: torch.Tensor, clusters: int = 16, iters: int = 4, *, stream=None) -> torch.Tensor:
+    """V-Smooth's grouping (ovc_vsmooth_group): k-means over each head's value
+    tokens, returned as the token order perm [B,H,S] (int32, CUDA) for
+    ``prepare(..., perm=perm)``."""
+    tv = _tensor_desc(v)
+    nbytes = int(lib().ovc_vsmooth_group_workspace_bytes(tv.B, tv.S, tv.H, int(clusters)))
+    if nbytes == 0:
+        raise ValueError("invalid cluster count or shape")
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=v.device)
+    perm = torch.empty((tv.B, tv.H, tv.S), dtype=torch.int32, device=v.device)
+    check(lib().ovc_vsmooth_group(ctypes.byref(tv), int(clusters), int(iters), ctypes.c_void_p(ws.data_ptr()),
+                                  ws.numel(), ctypes.c_void_p(perm.data_ptr()),
+                                  ctypes.c_void_p(_stream_handle(stream))), "ovc_vsmooth_group")
+    return perm
+
+
 def prepare(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, smooth_k: bool = False,
-            v_smooth: bool = False, workspace: torch.Tensor | None = None, stream=None) -> Prepared:
+            v_smooth: bool = False, perm: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+            stream=None) -> Prepared:
     """Quantise Q/K (per 128-token block) and V (per head) to E4M3
     (ovc_prepare_ex).  smooth_k subtracts K's channel means first (optional
     K smoothing; exact non-causal attention is unchanged by it).  v_smooth
     quantises V's residuals after each 128-token block's mean and keeps the
-    means for attention to restore (V-Smooth; no repair with it)."""
+    means for attention to restore (V-Smooth; no repair with it).  perm
+    [B,H,S] int32 (e.g. from :func:`group_v`): K and V are taken in that
+    token order (ovc_prepare_grouped); Q and so O keep theirs."""
     tq, tk, tv = _tensor_desc(q), _tensor_desc(k), _tensor_desc(v)
     flags = _prep_flags(smooth_k, v_smooth)
     nbytes = prepare_workspace_bytes(tq.B, tq.S, tq.H, smooth_k=smooth_k, v_smooth=v_smooth)
@@ -165,11 +185,21 @@ def prepare(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, smooth_k: bool
     if workspace is None:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
     desc = _abi.OvcPrepared()
-    st = lib().ovc_prepare_ex(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv), flags,
-                              ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
-                              ctypes.byref(desc), ctypes.c_void_p(_stream_handle(stream)))
-    check(st, "ovc_prepare_ex")
-    return Prepared(desc, workspace, tuple(q.shape), q.dtype)
+    if perm is None:
+        st = lib().ovc_prepare_ex(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv), flags,
+                                  ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
+                                  ctypes.byref(desc), ctypes.c_void_p(_stream_handle(stream)))
+        check(st, "ovc_prepare_ex")
+    else:
+        if perm.dtype != torch.int32 or not perm.is_cuda or tuple(perm.shape) != (tq.B, tq.H, tq.S):
+            raise ValueError("perm must be a CUDA int32 tensor [B,H,S]")
+        perm = perm.contiguous()
+        st = lib().ovc_prepare_grouped(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv),
+                                       ctypes.c_void_p(perm.data_ptr()), flags,
+                                       ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
+                                       ctypes.byref(desc), ctypes.c_void_p(_stream_handle(stream)))
+        check(st, "ovc_prepare_grouped")
+    return Prepared(desc, workspace, tuple(q.shape), q.dtype, perm)
 
 
 def _out_for(prep: Prepared, out):
@@ -469,6 +499,6 @@ def flops(B: int, S: int, H: int, D: int = 128) -> float:
 
 
 __all__ = ["Prepared", "Repair", "OvcError", "prepare", "attention_prepared", "attention_workspace_bytes",
-           "auto_split", "prepare_v_repair",
+           "auto_split", "group_v", "prepare_v_repair",
            "attention_v_repair", "attention_probe", "device_status", "attention", "memcpy2d",
            "head_chunks", "prepare_workspace_bytes", "repair_workspace_bytes", "flops"]

@@ -15,6 +15,7 @@
 
 #include "ovc.h"
 #include "attention.cuh"
+#include "group.cuh"
 #include "prepare.cuh"
 #include "repair.cuh"
 
@@ -167,6 +168,28 @@ int64_t repair_n(int64_t S, float budget) {
   if (k < 1) k = 1;
   if (k > S) k = S;
   return k;
+}
+
+struct GroupLayout {
+  size_t cent, labels, part, cnt, off, total;
+};
+
+GroupLayout group_layout(int64_t B, int64_t S, int64_t H, int64_t C) {
+  const int64_t nb = (S + 127) / 128, BH = B * H;
+  GroupLayout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes, 256);
+    return at;
+  };
+  L.cent = take(static_cast<size_t>(BH) * C * 128 * 4);
+  L.labels = take(static_cast<size_t>(BH) * S * 4);
+  L.part = take(static_cast<size_t>(BH) * nb * C * 128 * 4);
+  L.cnt = take(static_cast<size_t>(BH) * nb * C * 4);
+  L.off = take(static_cast<size_t>(BH) * nb * C * 4);
+  L.total = off;
+  return L;
 }
 
 struct RepLayout {
@@ -382,7 +405,14 @@ ovc_status ovc_prepare(const ovc_tensor* q, const ovc_tensor* k, const ovc_tenso
 
 ovc_status ovc_prepare_ex(const ovc_tensor* q, const ovc_tensor* k, const ovc_tensor* v, uint32_t flags,
                           void* workspace, size_t workspace_bytes, ovc_prepared* out, void* stream) {
+  return ovc_prepare_grouped(q, k, v, nullptr, flags, workspace, workspace_bytes, out, stream);
+}
+
+ovc_status ovc_prepare_grouped(const ovc_tensor* q, const ovc_tensor* k, const ovc_tensor* v, const int32_t* perm,
+                               uint32_t flags, void* workspace, size_t workspace_bytes, ovc_prepared* out,
+                               void* stream) {
   if (flags & ~(OVC_PREPARE_SMOOTH_K | OVC_PREPARE_V_SMOOTH)) return OVC_ERR_INVALID_ARG;
+  if (perm && (reinterpret_cast<uintptr_t>(perm) & 3u)) return OVC_ERR_INVALID_ARG;
   if (!q || !k || !v || !out) return OVC_ERR_INVALID_ARG;
   if (q->D != 128 || k->D != 128 || v->D != 128) return OVC_ERR_UNSUPPORTED;
   if ((q->dtype != OVC_BF16 && q->dtype != OVC_FP16) || k->dtype != q->dtype || v->dtype != q->dtype)
@@ -413,6 +443,7 @@ ovc_status ovc_prepare_ex(const ovc_tensor* q, const ovc_tensor* k, const ovc_te
   p.vamax = reinterpret_cast<uint32_t*>(ws + L.vamax);
   p.energy = reinterpret_cast<float*>(ws + L.energy);
   p.vmean = (flags & OVC_PREPARE_V_SMOOTH) ? reinterpret_cast<uint16_t*>(ws + L.vmean) : nullptr;
+  p.perm = perm;
 
   PrepParams P{};
   P.q = static_cast<const uint16_t*>(q->ptr);
@@ -439,6 +470,7 @@ ovc_status ovc_prepare_ex(const ovc_tensor* q, const ovc_tensor* k, const ovc_te
   P.sv = p.sv;
   P.vamax = p.vamax;
   P.energy = p.energy;
+  P.perm = perm;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(p.vamax, 0, static_cast<size_t>(p.B * p.H) * 4, s) != cudaSuccess) return OVC_ERR_CUDA;
@@ -508,6 +540,7 @@ ovc_status ovc_prepare_v_repair(const ovc_tensor* v, const ovc_prepared* p, floa
   if (v->dtype != OVC_BF16 && v->dtype != OVC_FP16) return OVC_ERR_UNSUPPORTED;
   if (!tensor_ok(v) || !prepared_ok(p)) return OVC_ERR_INVALID_ARG;
   if (p->vmean) return OVC_ERR_INVALID_ARG;   // V-Smooth keeps no residual energies
+  if (p->perm) return OVC_ERR_INVALID_ARG;    // energies are in the grouped token order
   if (v->B != p->B || v->S != p->S || v->H != p->H) return OVC_ERR_INVALID_ARG;
   if (!(budget > 0.0f) || budget > 1.0f) return OVC_ERR_INVALID_ARG;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return OVC_ERR_INVALID_ARG;
@@ -598,6 +631,58 @@ const char* ovc_status_string(ovc_status s) {
     case OVC_ERR_SCRATCH_LIMIT: return "B*H exceeds the fixed scratch of ovc_prepare_noalloc (OVC_NOALLOC_MAX_HEADS)";
   }
   return "unknown status";
+}
+
+size_t ovc_vsmooth_group_workspace_bytes(int64_t B, int64_t S, int64_t H, int32_t clusters) {
+  if (!dims_ok(B, S, H) || clusters < 1 || clusters > kMaxClusters || clusters > S) return 0;
+  return group_layout(B, S, H, clusters).total;
+}
+
+ovc_status ovc_vsmooth_group(const ovc_tensor* v, int32_t clusters, int32_t iters, void* workspace,
+                             size_t workspace_bytes, int32_t* perm, void* stream) {
+  if (!v || !perm || (reinterpret_cast<uintptr_t>(perm) & 3u)) return OVC_ERR_INVALID_ARG;
+  if (v->D != 128) return OVC_ERR_UNSUPPORTED;
+  if (v->dtype != OVC_BF16 && v->dtype != OVC_FP16) return OVC_ERR_UNSUPPORTED;
+  if (!tensor_ok(v)) return OVC_ERR_INVALID_ARG;
+  if (clusters < 1 || clusters > kMaxClusters || clusters > v->S || iters < 1 || iters > 1000)
+    return OVC_ERR_INVALID_ARG;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return OVC_ERR_INVALID_ARG;
+  const GroupLayout L = group_layout(v->B, v->S, v->H, clusters);
+  if (workspace_bytes < L.total) return OVC_ERR_WORKSPACE_TOO_SMALL;
+  DeviceState* dev = nullptr;
+  ovc_status st = device_state(&dev);
+  if (st != OVC_OK) return st;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  GroupParams G{};
+  G.v = static_cast<const uint16_t*>(v->ptr);
+  G.vs[0] = v->stride_b;
+  G.vs[1] = v->stride_s;
+  G.vs[2] = v->stride_h;
+  G.B = static_cast<int32_t>(v->B);
+  G.S = static_cast<int32_t>(v->S);
+  G.H = static_cast<int32_t>(v->H);
+  G.nb = static_cast<int32_t>((v->S + 127) / 128);
+  G.C = clusters;
+  G.fp16 = v->dtype == OVC_FP16;
+  G.cent = reinterpret_cast<float*>(ws + L.cent);
+  G.labels = reinterpret_cast<int32_t*>(ws + L.labels);
+  G.part = reinterpret_cast<float*>(ws + L.part);
+  G.cnt = reinterpret_cast<int32_t*>(ws + L.cnt);
+  G.off = reinterpret_cast<int32_t*>(ws + L.off);
+  G.perm = perm;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const unsigned BH = static_cast<unsigned>(v->B * v->H), nb = static_cast<unsigned>(G.nb);
+  kmeans_init_kernel<<<dim3(static_cast<unsigned>(clusters), BH), 128, 0, s>>>(G);
+  for (int it = 0; it < iters; ++it) {
+    kmeans_assign_kernel<<<dim3(nb, BH), 256, 0, s>>>(G);
+    if (it + 1 == iters) break;
+    kmeans_partial_kernel<<<dim3(nb, BH), 128, 0, s>>>(G);
+    kmeans_update_kernel<<<dim3(static_cast<unsigned>(clusters), BH), 128, 0, s>>>(G);
+  }
+  group_count_kernel<<<dim3(nb, BH), 128, 0, s>>>(G);
+  group_offset_kernel<<<BH, kMaxClusters, 0, s>>>(G);
+  group_scatter_kernel<<<dim3(nb, BH), 128, 0, s>>>(G);
+  return launch_status();
 }
 
 ovc_status ovc_memcpy2d(void* dst, size_t dpitch, const void* src, size_t spitch, size_t width,

@@ -64,7 +64,15 @@ struct PrepParams {
   float* vmu;
   uint16_t* vmean;
   int32_t nbk;
+  // Grouping (NULL when off): [B*H][S] token order of K and V -- row t of the
+  // prepared K and V is input token perm[t] (Q keeps its order).
+  const int32_t* perm;
 };
+
+// Input row of prepared K/V row t (the identity without grouping).
+__device__ __forceinline__ int kv_row(const PrepParams& P, int bh, int t) {
+  return P.perm != nullptr ? __ldg(P.perm + static_cast<int64_t>(bh) * P.S + t) : t;
+}
 
 // |x| of two packed 16-bit floats, as ordered integers (sign bit cleared).
 __device__ __forceinline__ uint32_t abs2_bits(uint32_t w) { return w & 0x7FFF7FFFu; }
@@ -133,7 +141,8 @@ __global__ void __launch_bounds__(128) k_mean_partial_kernel(const __grid_consta
   // The loads are independent and can be in flight together; the additions
   // stay in token order.
 #pragma unroll 16
-  for (int t = j * 128; t < t1; ++t) part = __fadd_rn(part, half_bits_to_float(__ldg(src + t * P.ks[1]), P.fp16));
+  for (int t = j * 128; t < t1; ++t)
+    part = __fadd_rn(part, half_bits_to_float(__ldg(src + static_cast<int64_t>(kv_row(P, bh, t)) * P.ks[1]), P.fp16));
   P.kpart[(static_cast<int64_t>(bh) * P.nb + j) * 128 + d] = part;
 }
 
@@ -159,13 +168,14 @@ __global__ void __launch_bounds__(128) vsmooth_mean_kernel(const __grid_constant
   const uint16_t* src = P.v + b * P.vs[0] + h * P.vs[2] + d;
   float sum = 0.0f;
 #pragma unroll 16
-  for (int t = t0; t < t1; ++t) sum = __fadd_rn(sum, half_bits_to_float(__ldg(src + t * P.vs[1]), P.fp16));
+  for (int t = t0; t < t1; ++t)
+    sum = __fadd_rn(sum, half_bits_to_float(__ldg(src + static_cast<int64_t>(kv_row(P, bh, t)) * P.vs[1]), P.fp16));
   const float mu = __bfloat162float(__float2bfloat16_rn(__fdiv_rn(sum, static_cast<float>(t1 - t0))));
   P.vmu[(static_cast<int64_t>(bh) * P.nb + j) * 128 + d] = mu;
   float m = 0.0f;
 #pragma unroll 16
   for (int t = t0; t < t1; ++t)
-    m = fmaxf(m, fabsf(__fsub_rn(half_bits_to_float(__ldg(src + t * P.vs[1]), P.fp16), mu)));
+    m = fmaxf(m, fabsf(__fsub_rn(half_bits_to_float(__ldg(src + static_cast<int64_t>(kv_row(P, bh, t)) * P.vs[1]), P.fp16), mu)));
   const uint32_t mb = block_max_u32(__float_as_uint(m), red);
   if (d == 0) atomicMax(P.vamax + bh, mb);
 }
@@ -187,7 +197,8 @@ __global__ void __launch_bounds__(256) prepare_qk_kernel(const __grid_constant__
 
   uint4 x[8];
   if (t < P.S) {
-    const uint4* p = reinterpret_cast<const uint4*>(src + b * st[0] + t * st[1] + h * st[2] + half * 64);
+    const int tr = which > 0 ? kv_row(P, bh, t) : t;
+    const uint4* p = reinterpret_cast<const uint4*>(src + b * st[0] + static_cast<int64_t>(tr) * st[1] + h * st[2] + half * 64);
 #pragma unroll
     for (int i = 0; i < 8; ++i) x[i] = __ldg(p + i);
   } else {
@@ -292,7 +303,8 @@ __global__ void __launch_bounds__(512) prepare_v_kernel(const __grid_constant__ 
     const int t = j * 128 + 4 * lane + k;
     uint4 x = make_uint4(0, 0, 0, 0);
     if (t < P.S)
-      x = __ldg(reinterpret_cast<const uint4*>(P.v + b * P.vs[0] + t * P.vs[1] + h * P.vs[2] + 8 * warp));
+      x = __ldg(reinterpret_cast<const uint4*>(P.v + b * P.vs[0] + static_cast<int64_t>(kv_row(P, bh, t)) * P.vs[1] +
+                                               h * P.vs[2] + 8 * warp));
     const float2 a = unpack2(x.x, P.fp16), c = unpack2(x.y, P.fp16);
     const float2 d = unpack2(x.z, P.fp16), e = unpack2(x.w, P.fp16);
     float xv[8] = {a.x, a.y, c.x, c.y, d.x, d.y, e.x, e.y};

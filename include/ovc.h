@@ -82,7 +82,11 @@ typedef struct {
  *                          block means M'_b = bf16(mu_b / sv), channel-major,
  *                          nbk = nb rounded up to 16 (entries >= nb unused);
  *                          vt then holds the residuals v - mu_b and energy is
- *                          not computed */
+ *                          not computed
+ *   perm  [B,H,S]          grouping only (else NULL): the token order of k, vt
+ *                          and vmean (row t is input token perm[t]); the
+ *                          caller's array, which must outlive the struct's use
+ *                          (q keeps its order, so O does too) */
 typedef struct {
   int64_t B, S, H, nb, S_pad;
   uint8_t* q;
@@ -94,6 +98,7 @@ typedef struct {
   uint32_t* vamax;
   float* energy;
   uint16_t* vmean;
+  const int32_t* perm;
 } ovc_prepared;
 
 /* V residual repair set written by ovc_prepare_v_repair (n_pad = 128*ceil(n/128)):
@@ -286,6 +291,29 @@ ovc_status ovc_prepare_noalloc(const ovc_tensor* q, const ovc_tensor* k, const o
 #define OVC_PREPARE_SMOOTH_K 1u
 #define OVC_PREPARE_V_SMOOTH 2u
 size_t ovc_prepare_workspace_bytes_ex(int64_t B, int64_t S, int64_t H, int64_t D, uint32_t flags);
+
+/* V-Smooth's grouping ("VC-Attention" summary, "V-Smooth": online k-means
+ * clusters each head's value tokens; keys and values are permuted together,
+ * which non-causal attention does not notice).  Per (b,h): Lloyd's k-means
+ * with `clusters` (1..64, <= S) centroids started at tokens floor(c S / C)
+ * and `iters` (1..1000) assign steps, FP32 with a fixed operation order (see
+ * the grouping kernels); then perm [B,H,S] (device, int32, 4-byte aligned)
+ * lists the tokens ordered by (cluster, index).  Pass perm to
+ * ovc_prepare_grouped so that V-Smooth's 128-token blocks hold similar
+ * values.  Workspace: ovc_vsmooth_group_workspace_bytes (256-byte aligned).
+ * Asynchronous on `stream`. */
+size_t ovc_vsmooth_group_workspace_bytes(int64_t B, int64_t S, int64_t H, int32_t clusters);
+ovc_status ovc_vsmooth_group(const ovc_tensor* v, int32_t clusters, int32_t iters, void* workspace,
+                             size_t workspace_bytes, int32_t* perm, void* stream);
+
+/* ovc_prepare_ex with K and V taken in the token order perm [B,H,S] (device,
+ * int32; NULL: the input order), e.g. the grouping of ovc_vsmooth_group.
+ * Queries keep their order, so attention's output rows do too.  perm must
+ * stay valid while the prepared struct is used; repair is not available on
+ * grouped inputs. */
+ovc_status ovc_prepare_grouped(const ovc_tensor* q, const ovc_tensor* k, const ovc_tensor* v, const int32_t* perm,
+                               uint32_t flags, void* workspace, size_t workspace_bytes, ovc_prepared* out,
+                               void* stream);
 ovc_status ovc_prepare_ex(const ovc_tensor* q, const ovc_tensor* k, const ovc_tensor* v, uint32_t flags,
                           void* workspace, size_t workspace_bytes, ovc_prepared* out, void* stream);
 

@@ -455,3 +455,60 @@ def test_v_smooth_persistent_schedule_and_rejections():
     with pytest.raises(ovc.OvcError):
         ovc.attention_prepared(prep, flags=1)
     assert ovc.device_status() == 0
+
+
+# ---- V-Smooth grouping --------------------------------------------------------
+def _clustered_inputs(B, H, S, seed, centres=6):
+    q, k, _ = inputs(B, H, S, seed=seed)
+    rng = np.random.default_rng(seed)
+    c = rng.standard_normal((B, H, centres, 128)).astype(np.float32) * 4.0
+    lab = rng.integers(0, centres, (B, S, H))
+    v = c[np.arange(B)[:, None, None], np.arange(H)[None, None, :], lab]
+    v = v + 0.3 * rng.standard_normal(v.shape).astype(np.float32)
+    return q, k, torch.from_numpy(v).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("B,H,S,C,iters", [(1, 1, 1, 1, 1), (1, 2, 200, 7, 3), (2, 3, 300, 16, 4),
+                                           (1, 2, 1000, 16, 4), (1, 1, 2300, 64, 2)])
+def test_grouping_bit_exact_and_grouped_v_smooth(B, H, S, C, iters):
+    q, k, v = _clustered_inputs(B, H, S, seed=1300 + S)
+    labels, _, perm_ref = oracle.kmeans_group(W.bf16_bits(v), C, iters)
+    qd, kd, vd = to_dev(q, k, v)
+    perm = ovc.group_v(vd, clusters=C, iters=iters)
+    torch.cuda.synchronize()
+    assert np.array_equal(perm.cpu().numpy(), perm_ref)
+    ref = oracle.Prepared(W.bf16_bits(q), W.bf16_bits(k), W.bf16_bits(v), v_smooth=True, perm=perm_ref)
+    prep = ovc.prepare(qd, kd, vd, v_smooth=True, perm=perm)
+    torch.cuda.synchronize()
+    assert np.array_equal(prep.k_codes().cpu().numpy(), ref.kc) and np.array_equal(prep.k_scales().cpu().numpy(), ref.sk)
+    assert np.array_equal(prep.vt_codes().cpu().numpy().transpose(0, 1, 3, 2), ref.vc)
+    assert np.array_equal(prep.v_scales().cpu().numpy(), ref.sv)
+    nb = (S + 127) // 128
+    assert np.array_equal(prep.v_means().float().cpu().numpy()[..., :nb].transpose(0, 1, 3, 2), ref.vmean)
+    want, _ = oracle.attention_full(ref)
+    o = ovc.attention_prepared(prep)
+    assert ovc.device_status() == 0
+    assert rel_l2(o.float().cpu().numpy(), want) <= TOL_REL_L2
+    with pytest.raises(ovc.OvcError):
+        ovc.prepare_v_repair(vd, ovc.prepare(qd, kd, vd, perm=perm), 0.01)
+
+
+def test_grouping_keeps_attention_and_lowers_v_smooth_error():
+    """Grouped keys/values give the same exact attention; on clustered values
+    grouped V-Smooth is closer to exact attention than ungrouped V-Smooth."""
+    B, H, S = 1, 2, 2048
+    q, k, v = _clustered_inputs(B, H, S, seed=1400, centres=12)
+    qd, kd, vd = to_dev(q, k, v)
+    rows = np.arange(0, S, 37)
+    perm = ovc.group_v(vd, clusters=16, iters=4)
+    o_g = ovc.attention_prepared(ovc.prepare(qd, kd, vd, v_smooth=True, perm=perm)).float().cpu().numpy()
+    o_u = ovc.attention_prepared(ovc.prepare(qd, kd, vd, v_smooth=True)).float().cpu().numpy()
+    qq, kk, vv = (x.double().numpy() for x in (q, k, v))
+    e_g, e_u = [], []
+    for h in range(H):
+        s = qq[0, rows, h] @ kk[0, :, h].T / math.sqrt(128.0)
+        p = np.exp(s - s.max(1, keepdims=True))
+        ex = (p @ vv[0, :, h]) / p.sum(1, keepdims=True)
+        e_g.append(rel_l2(o_g[0, rows, h], ex))
+        e_u.append(rel_l2(o_u[0, rows, h], ex))
+    assert np.mean(e_g) < np.mean(e_u), (e_g, e_u)
