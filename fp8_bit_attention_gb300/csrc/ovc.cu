@@ -477,23 +477,40 @@ ovc_status ovc_prepare_grouped(const ovc_tensor* q, const ovc_tensor* k, const o
   if (flags & OVC_PREPARE_SMOOTH_K) {
     P.kpart = reinterpret_cast<float*>(ws + L.kpart);
     P.kmean = reinterpret_cast<float*>(ws + L.kmean);
-    k_mean_partial_kernel<<<dim3(static_cast<unsigned>(p.nb), static_cast<unsigned>(p.B * p.H)), 128, 0, s>>>(P);
+    if (perm)
+      k_mean_partial_kernel<true><<<dim3(static_cast<unsigned>(p.nb), static_cast<unsigned>(p.B * p.H)), 128, 0, s>>>(P);
+    else
+      k_mean_partial_kernel<false><<<dim3(static_cast<unsigned>(p.nb), static_cast<unsigned>(p.B * p.H)), 128, 0, s>>>(P);
     k_mean_final_kernel<<<static_cast<unsigned>(p.B * p.H), 128, 0, s>>>(P);
   }
   if (flags & OVC_PREPARE_V_SMOOTH) {
     P.vmu = reinterpret_cast<float*>(ws + L.vmu);
     P.vmean = p.vmean;
     P.nbk = static_cast<int32_t>((p.nb + 15) / 16 * 16);
-    vsmooth_mean_kernel<<<dim3(static_cast<unsigned>(p.nb), static_cast<unsigned>(p.B * p.H)), 128, 0, s>>>(P);
+    if (perm)
+      vsmooth_mean_kernel<true><<<dim3(static_cast<unsigned>(p.nb), static_cast<unsigned>(p.B * p.H)), 128, 0, s>>>(P);
+    else
+      vsmooth_mean_kernel<false><<<dim3(static_cast<unsigned>(p.nb), static_cast<unsigned>(p.B * p.H)), 128, 0, s>>>(P);
   }
   // z = 2 (the amax of V) only without V-Smooth, whose mean pass folds it in
   const dim3 g1(static_cast<unsigned>(p.nb), static_cast<unsigned>(p.B * p.H), (flags & OVC_PREPARE_V_SMOOTH) ? 2 : 3);
-  prepare_qk_kernel<<<g1, 256, 0, s>>>(P);
+  const int qk_opt = ((flags & OVC_PREPARE_SMOOTH_K) ? kPrepSmoothK : 0) | (perm ? kPrepPerm : 0);
+  switch (qk_opt) {
+    case 0: prepare_qk_kernel<0><<<g1, 256, 0, s>>>(P); break;
+    case kPrepSmoothK: prepare_qk_kernel<kPrepSmoothK><<<g1, 256, 0, s>>>(P); break;
+    case kPrepPerm: prepare_qk_kernel<kPrepPerm><<<g1, 256, 0, s>>>(P); break;
+    default: prepare_qk_kernel<kPrepSmoothK | kPrepPerm><<<g1, 256, 0, s>>>(P); break;
+  }
   const dim3 g2(static_cast<unsigned>(p.nb), static_cast<unsigned>(p.B * p.H), 1);
-  if (flags & OVC_PREPARE_V_SMOOTH)
-    prepare_v_kernel<true><<<g2, 512, 0, s>>>(P);
+  const bool vsm = (flags & OVC_PREPARE_V_SMOOTH) != 0;
+  if (vsm && perm)
+    prepare_v_kernel<true, true><<<g2, 512, 0, s>>>(P);
+  else if (vsm)
+    prepare_v_kernel<true, false><<<g2, 512, 0, s>>>(P);
+  else if (perm)
+    prepare_v_kernel<false, true><<<g2, 512, 0, s>>>(P);
   else
-    prepare_v_kernel<false><<<g2, 512, 0, s>>>(P);
+    prepare_v_kernel<false, false><<<g2, 512, 0, s>>>(P);
   st = launch_status();
   if (st == OVC_OK) *out = p;
   return st;
@@ -792,9 +809,9 @@ extern "C" ovc_status ovc_prepare_noalloc(const ovc_tensor* q, const ovc_tensor*
   const int n = static_cast<int>(BH);
   noalloc_clear_kernel<<<(n + 255) / 256, 256, 0, s>>>(scratch, n);
   const dim3 g1(static_cast<unsigned>(nb), static_cast<unsigned>(BH), 3);
-  prepare_qk_kernel<<<g1, 256, 0, s>>>(P);
+  prepare_qk_kernel<0><<<g1, 256, 0, s>>>(P);
   const dim3 g2(static_cast<unsigned>(nb), static_cast<unsigned>(BH), 1);
-  prepare_v_kernel<false><<<g2, 512, 0, s>>>(P);
+  prepare_v_kernel<false, false><<<g2, 512, 0, s>>>(P);
   if (out->vamax) noalloc_copy_kernel<<<(n + 255) / 256, 256, 0, s>>>(scratch, out->vamax, n);
   return launch_status();
 }

@@ -70,9 +70,15 @@ struct PrepParams {
 };
 
 // Input row of prepared K/V row t (the identity without grouping).
+template <bool kPerm>
 __device__ __forceinline__ int kv_row(const PrepParams& P, int bh, int t) {
-  return P.perm != nullptr ? __ldg(P.perm + static_cast<int64_t>(bh) * P.S + t) : t;
+  return kPerm ? __ldg(P.perm + static_cast<int64_t>(bh) * P.S + t) : t;
 }
+
+// Options of the preparation kernels, as template bits, so that the plain
+// preparation carries none of their tests.
+constexpr int kPrepSmoothK = 1;
+constexpr int kPrepPerm = 2;
 
 // |x| of two packed 16-bit floats, as ordered integers (sign bit cleared).
 __device__ __forceinline__ uint32_t abs2_bits(uint32_t w) { return w & 0x7FFF7FFFu; }
@@ -132,6 +138,7 @@ __device__ __forceinline__ uint32_t block_max_u32(uint32_t m, uint32_t* red) {
 }
 
 // Channel sums of one 128-token block of K, in token order.
+template <bool kPerm>
 __global__ void __launch_bounds__(128) k_mean_partial_kernel(const __grid_constant__ PrepParams P) {
   const int j = blockIdx.x, bh = blockIdx.y, d = threadIdx.x;
   const int b = bh / P.H, h = bh % P.H;
@@ -142,7 +149,7 @@ __global__ void __launch_bounds__(128) k_mean_partial_kernel(const __grid_consta
   // stay in token order.
 #pragma unroll 16
   for (int t = j * 128; t < t1; ++t)
-    part = __fadd_rn(part, half_bits_to_float(__ldg(src + static_cast<int64_t>(kv_row(P, bh, t)) * P.ks[1]), P.fp16));
+    part = __fadd_rn(part, half_bits_to_float(__ldg(src + static_cast<int64_t>(kv_row<kPerm>(P, bh, t)) * P.ks[1]), P.fp16));
   P.kpart[(static_cast<int64_t>(bh) * P.nb + j) * 128 + d] = part;
 }
 
@@ -160,6 +167,7 @@ __global__ void __launch_bounds__(128) k_mean_final_kernel(const __grid_constant
 // (n = the block's valid tokens), then the block's amax of fl(v - mu) folded
 // into the head's running maximum.  One thread per channel; every token row
 // is a coalesced 256-byte read, and the second read of the block hits cache.
+template <bool kPerm>
 __global__ void __launch_bounds__(128) vsmooth_mean_kernel(const __grid_constant__ PrepParams P) {
   __shared__ uint32_t red[32];
   const int j = blockIdx.x, bh = blockIdx.y, d = threadIdx.x;
@@ -169,19 +177,20 @@ __global__ void __launch_bounds__(128) vsmooth_mean_kernel(const __grid_constant
   float sum = 0.0f;
 #pragma unroll 16
   for (int t = t0; t < t1; ++t)
-    sum = __fadd_rn(sum, half_bits_to_float(__ldg(src + static_cast<int64_t>(kv_row(P, bh, t)) * P.vs[1]), P.fp16));
+    sum = __fadd_rn(sum, half_bits_to_float(__ldg(src + static_cast<int64_t>(kv_row<kPerm>(P, bh, t)) * P.vs[1]), P.fp16));
   const float mu = __bfloat162float(__float2bfloat16_rn(__fdiv_rn(sum, static_cast<float>(t1 - t0))));
   P.vmu[(static_cast<int64_t>(bh) * P.nb + j) * 128 + d] = mu;
   float m = 0.0f;
 #pragma unroll 16
   for (int t = t0; t < t1; ++t)
-    m = fmaxf(m, fabsf(__fsub_rn(half_bits_to_float(__ldg(src + static_cast<int64_t>(kv_row(P, bh, t)) * P.vs[1]), P.fp16), mu)));
+    m = fmaxf(m, fabsf(__fsub_rn(half_bits_to_float(__ldg(src + static_cast<int64_t>(kv_row<kPerm>(P, bh, t)) * P.vs[1]), P.fp16), mu)));
   const uint32_t mb = block_max_u32(__float_as_uint(m), red);
   if (d == 0) atomicMax(P.vamax + bh, mb);
 }
 
 // One 128-token block of Q or K (z = 0, 1), or the amax of one block of V
 // (z = 2).  256 threads: two per token row, 64 channels each.
+template <int kOpt>
 __global__ void __launch_bounds__(256) prepare_qk_kernel(const __grid_constant__ PrepParams P) {
   __shared__ uint32_t red[32];
   const int j = blockIdx.x;
@@ -197,7 +206,7 @@ __global__ void __launch_bounds__(256) prepare_qk_kernel(const __grid_constant__
 
   uint4 x[8];
   if (t < P.S) {
-    const int tr = which > 0 ? kv_row(P, bh, t) : t;
+    const int tr = which > 0 ? kv_row<(kOpt & kPrepPerm) != 0>(P, bh, t) : t;
     const uint4* p = reinterpret_cast<const uint4*>(src + b * st[0] + static_cast<int64_t>(tr) * st[1] + h * st[2] + half * 64);
 #pragma unroll
     for (int i = 0; i < 8; ++i) x[i] = __ldg(p + i);
@@ -206,7 +215,7 @@ __global__ void __launch_bounds__(256) prepare_qk_kernel(const __grid_constant__
     for (int i = 0; i < 8; ++i) x[i] = make_uint4(0, 0, 0, 0);
   }
 
-  if (which == 1 && P.kmean != nullptr) {
+  if ((kOpt & kPrepSmoothK) && which == 1) {
     // Smoothed K: the centred values fl(x - mean) set the block amax and are
     // quantised; rows past S stay zero (no code, no part of the amax).
     const float* mu = P.kmean + bh * 128 + half * 64;
@@ -274,7 +283,7 @@ __global__ void __launch_bounds__(256) prepare_qk_kernel(const __grid_constant__
 // with coalesced 128-byte rows, and the residual energy of each token:
 // R = fl(v - fl(s_v * dec(code))), sixteen sequential partial sums over 8
 // channels, then the pairwise tree p_g += p_(g+w), w = 8, 4, 2, 1.
-template <bool kVSmooth>
+template <bool kVSmooth, bool kPerm>
 __global__ void __launch_bounds__(512) prepare_v_kernel(const __grid_constant__ PrepParams P) {
   __shared__ float part[16][128];
   const int j = blockIdx.x;
@@ -303,7 +312,7 @@ __global__ void __launch_bounds__(512) prepare_v_kernel(const __grid_constant__ 
     const int t = j * 128 + 4 * lane + k;
     uint4 x = make_uint4(0, 0, 0, 0);
     if (t < P.S)
-      x = __ldg(reinterpret_cast<const uint4*>(P.v + b * P.vs[0] + static_cast<int64_t>(kv_row(P, bh, t)) * P.vs[1] +
+      x = __ldg(reinterpret_cast<const uint4*>(P.v + b * P.vs[0] + static_cast<int64_t>(kv_row<kPerm>(P, bh, t)) * P.vs[1] +
                                                h * P.vs[2] + 8 * warp));
     const float2 a = unpack2(x.x, P.fp16), c = unpack2(x.y, P.fp16);
     const float2 d = unpack2(x.z, P.fp16), e = unpack2(x.w, P.fp16);
