@@ -15,11 +15,12 @@
 //           the lower c
 //   update  mu_c = sum / count: sums per 128-token block in token order, then
 //           over blocks in block order; an empty cluster keeps its centroid
-// Kernels (grid, block):
+// Kernels (grid, block; the head index runs fastest, so CTAs that run
+// together read whole token rows of V):
 //   kmeans_init_kernel     (C, B*H) x 128
-//   kmeans_assign_kernel   (nb, B*H) x 256: a warp per token, a lane per 4
+//   kmeans_assign_kernel   (B*H, nb) x 256: a warp per token, a lane per 4
 //                          channels; the dot tree is the shuffle-down tree
-//   kmeans_partial_kernel  (nb, B*H) x 128: a thread per channel; per-cluster
+//   kmeans_partial_kernel  (B*H, nb) x 128: a thread per channel; per-cluster
 //                          sums in shared memory, counts by thread 0
 //   kmeans_update_kernel   (C, B*H) x 128
 //   group_count_kernel / group_offset_kernel / group_scatter_kernel: a
@@ -60,7 +61,7 @@ __global__ void __launch_bounds__(128) kmeans_init_kernel(const __grid_constant_
 __global__ void __launch_bounds__(256) kmeans_assign_kernel(const __grid_constant__ GroupParams G) {
   __shared__ float mu[kMaxClusters][128];
   __shared__ float nrm[kMaxClusters];
-  const int j = blockIdx.x, bh = blockIdx.y;
+  const int bh = blockIdx.x, j = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float* cent = G.cent + static_cast<int64_t>(bh) * G.C * 128;
   for (int i = threadIdx.x; i < G.C * 128; i += blockDim.x) mu[i >> 7][i & 127] = cent[i];
@@ -95,7 +96,7 @@ __global__ void __launch_bounds__(256) kmeans_assign_kernel(const __grid_constan
 __global__ void __launch_bounds__(128) kmeans_partial_kernel(const __grid_constant__ GroupParams G) {
   __shared__ float part[kMaxClusters][128];
   __shared__ int cnt[kMaxClusters];
-  const int j = blockIdx.x, bh = blockIdx.y, d = threadIdx.x;
+  const int bh = blockIdx.x, j = blockIdx.y, d = threadIdx.x;
   for (int c = 0; c < G.C; ++c) part[c][d] = 0.0f;
   if (d < G.C) cnt[d] = 0;
   __syncthreads();
@@ -127,7 +128,7 @@ __global__ void __launch_bounds__(128) kmeans_update_kernel(const __grid_constan
 // Members of each cluster in each 128-token block.
 __global__ void __launch_bounds__(128) group_count_kernel(const __grid_constant__ GroupParams G) {
   __shared__ int cnt[kMaxClusters];
-  const int j = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x;
+  const int bh = blockIdx.x, j = blockIdx.y, tid = threadIdx.x;
   if (tid < G.C) cnt[tid] = 0;
   __syncthreads();
   const int t = j * 128 + tid;
@@ -163,7 +164,7 @@ __global__ void __launch_bounds__(kMaxClusters) group_offset_kernel(const __grid
 // block by counting).
 __global__ void __launch_bounds__(128) group_scatter_kernel(const __grid_constant__ GroupParams G) {
   __shared__ int lab[128];
-  const int j = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x;
+  const int bh = blockIdx.x, j = blockIdx.y, tid = threadIdx.x;
   const int t = j * 128 + tid;
   lab[tid] = t < G.S ? G.labels[static_cast<int64_t>(bh) * G.S + t] : -1;
   __syncthreads();

@@ -478,9 +478,9 @@ ovc_status ovc_prepare_grouped(const ovc_tensor* q, const ovc_tensor* k, const o
     P.kpart = reinterpret_cast<float*>(ws + L.kpart);
     P.kmean = reinterpret_cast<float*>(ws + L.kmean);
     if (perm)
-      k_mean_partial_kernel<true><<<dim3(static_cast<unsigned>(p.nb), static_cast<unsigned>(p.B * p.H)), 128, 0, s>>>(P);
+      k_mean_partial_kernel<true><<<dim3(static_cast<unsigned>(p.B * p.H), static_cast<unsigned>(p.nb)), 128, 0, s>>>(P);
     else
-      k_mean_partial_kernel<false><<<dim3(static_cast<unsigned>(p.nb), static_cast<unsigned>(p.B * p.H)), 128, 0, s>>>(P);
+      k_mean_partial_kernel<false><<<dim3(static_cast<unsigned>(p.B * p.H), static_cast<unsigned>(p.nb)), 128, 0, s>>>(P);
     k_mean_final_kernel<<<static_cast<unsigned>(p.B * p.H), 128, 0, s>>>(P);
   }
   if (flags & OVC_PREPARE_V_SMOOTH) {
@@ -488,12 +488,12 @@ ovc_status ovc_prepare_grouped(const ovc_tensor* q, const ovc_tensor* k, const o
     P.vmean = p.vmean;
     P.nbk = static_cast<int32_t>((p.nb + 15) / 16 * 16);
     if (perm)
-      vsmooth_mean_kernel<true><<<dim3(static_cast<unsigned>(p.nb), static_cast<unsigned>(p.B * p.H)), 128, 0, s>>>(P);
+      vsmooth_mean_kernel<true><<<dim3(static_cast<unsigned>(p.B * p.H), static_cast<unsigned>(p.nb)), 128, 0, s>>>(P);
     else
-      vsmooth_mean_kernel<false><<<dim3(static_cast<unsigned>(p.nb), static_cast<unsigned>(p.B * p.H)), 128, 0, s>>>(P);
+      vsmooth_mean_kernel<false><<<dim3(static_cast<unsigned>(p.B * p.H), static_cast<unsigned>(p.nb)), 128, 0, s>>>(P);
   }
   // z = 2 (the amax of V) only without V-Smooth, whose mean pass folds it in
-  const dim3 g1(static_cast<unsigned>(p.nb), static_cast<unsigned>(p.B * p.H), (flags & OVC_PREPARE_V_SMOOTH) ? 2 : 3);
+  const dim3 g1(static_cast<unsigned>(p.B * p.H), static_cast<unsigned>(p.nb), (flags & OVC_PREPARE_V_SMOOTH) ? 2 : 3);
   const int qk_opt = ((flags & OVC_PREPARE_SMOOTH_K) ? kPrepSmoothK : 0) | (perm ? kPrepPerm : 0);
   switch (qk_opt) {
     case 0: prepare_qk_kernel<0><<<g1, 256, 0, s>>>(P); break;
@@ -501,7 +501,7 @@ ovc_status ovc_prepare_grouped(const ovc_tensor* q, const ovc_tensor* k, const o
     case kPrepPerm: prepare_qk_kernel<kPrepPerm><<<g1, 256, 0, s>>>(P); break;
     default: prepare_qk_kernel<kPrepSmoothK | kPrepPerm><<<g1, 256, 0, s>>>(P); break;
   }
-  const dim3 g2(static_cast<unsigned>(p.nb), static_cast<unsigned>(p.B * p.H), 1);
+  const dim3 g2(static_cast<unsigned>(p.B * p.H), static_cast<unsigned>(p.nb), 1);
   const bool vsm = (flags & OVC_PREPARE_V_SMOOTH) != 0;
   if (vsm && perm)
     prepare_v_kernel<true, true><<<g2, 512, 0, s>>>(P);
@@ -691,14 +691,14 @@ ovc_status ovc_vsmooth_group(const ovc_tensor* v, int32_t clusters, int32_t iter
   const unsigned BH = static_cast<unsigned>(v->B * v->H), nb = static_cast<unsigned>(G.nb);
   kmeans_init_kernel<<<dim3(static_cast<unsigned>(clusters), BH), 128, 0, s>>>(G);
   for (int it = 0; it < iters; ++it) {
-    kmeans_assign_kernel<<<dim3(nb, BH), 256, 0, s>>>(G);
+    kmeans_assign_kernel<<<dim3(BH, nb), 256, 0, s>>>(G);
     if (it + 1 == iters) break;
-    kmeans_partial_kernel<<<dim3(nb, BH), 128, 0, s>>>(G);
+    kmeans_partial_kernel<<<dim3(BH, nb), 128, 0, s>>>(G);
     kmeans_update_kernel<<<dim3(static_cast<unsigned>(clusters), BH), 128, 0, s>>>(G);
   }
-  group_count_kernel<<<dim3(nb, BH), 128, 0, s>>>(G);
+  group_count_kernel<<<dim3(BH, nb), 128, 0, s>>>(G);
   group_offset_kernel<<<BH, kMaxClusters, 0, s>>>(G);
-  group_scatter_kernel<<<dim3(nb, BH), 128, 0, s>>>(G);
+  group_scatter_kernel<<<dim3(BH, nb), 128, 0, s>>>(G);
   return launch_status();
 }
 
@@ -808,9 +808,9 @@ extern "C" ovc_status ovc_prepare_noalloc(const ovc_tensor* q, const ovc_tensor*
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int n = static_cast<int>(BH);
   noalloc_clear_kernel<<<(n + 255) / 256, 256, 0, s>>>(scratch, n);
-  const dim3 g1(static_cast<unsigned>(nb), static_cast<unsigned>(BH), 3);
+  const dim3 g1(static_cast<unsigned>(BH), static_cast<unsigned>(nb), 3);
   prepare_qk_kernel<0><<<g1, 256, 0, s>>>(P);
-  const dim3 g2(static_cast<unsigned>(nb), static_cast<unsigned>(BH), 1);
+  const dim3 g2(static_cast<unsigned>(BH), static_cast<unsigned>(nb), 1);
   prepare_v_kernel<false, false><<<g2, 512, 0, s>>>(P);
   if (out->vamax) noalloc_copy_kernel<<<(n + 255) / 256, 256, 0, s>>>(scratch, out->vamax, n);
   return launch_status();

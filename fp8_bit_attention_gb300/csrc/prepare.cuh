@@ -14,14 +14,16 @@
 // K's block scales.  The mean is summed in a fixed order -- per 128-token
 // block in token order, then the block sums in block order, then / S -- so
 // that it is reproducible bit for bit:
-//   k_mean_partial_kernel  grid (nb, B*H) x 128: one thread per channel.
+//   k_mean_partial_kernel  grid (B*H, nb) x 128: one thread per channel.
 //   k_mean_final_kernel    grid (B*H) x 128.
 //
-// Two launches, both HBM-bound and coalesced:
-//   prepare_qk_kernel  grid (nb, B*H, 3): z = 0 quantises a 128-token block of
+// Two launches, both HBM-bound and coalesced.  The head index runs fastest
+// in every grid: CTAs that run together read the same tokens of all heads,
+// i.e. whole contiguous token rows of the [B,S,H,128] inputs.
+//   prepare_qk_kernel  grid (B*H, nb, 3): z = 0 quantises a 128-token block of
 //                      Q, z = 1 of K, z = 2 folds the block's amax|V| into the
 //                      head's running maximum.
-//   prepare_v_kernel   grid (nb, B*H): quantises a 128-token block of V with
+//   prepare_v_kernel   grid (B*H, nb): quantises a 128-token block of V with
 //                      the head scale, writes it transposed (keys contiguous)
 //                      and the per-token residual energy.
 // V-Smooth (optional): vsmooth_mean_kernel replaces the z = 2 amax pass (it
@@ -140,7 +142,7 @@ __device__ __forceinline__ uint32_t block_max_u32(uint32_t m, uint32_t* red) {
 // Channel sums of one 128-token block of K, in token order.
 template <bool kPerm>
 __global__ void __launch_bounds__(128) k_mean_partial_kernel(const __grid_constant__ PrepParams P) {
-  const int j = blockIdx.x, bh = blockIdx.y, d = threadIdx.x;
+  const int bh = blockIdx.x, j = blockIdx.y, d = threadIdx.x;
   const int b = bh / P.H, h = bh % P.H;
   const int t1 = min(P.S, j * 128 + 128);
   const uint16_t* src = P.k + b * P.ks[0] + h * P.ks[2] + d;
@@ -170,7 +172,7 @@ __global__ void __launch_bounds__(128) k_mean_final_kernel(const __grid_constant
 template <bool kPerm>
 __global__ void __launch_bounds__(128) vsmooth_mean_kernel(const __grid_constant__ PrepParams P) {
   __shared__ uint32_t red[32];
-  const int j = blockIdx.x, bh = blockIdx.y, d = threadIdx.x;
+  const int bh = blockIdx.x, j = blockIdx.y, d = threadIdx.x;
   const int b = bh / P.H, h = bh % P.H;
   const int t0 = j * 128, t1 = min(P.S, t0 + 128);
   const uint16_t* src = P.v + b * P.vs[0] + h * P.vs[2] + d;
@@ -193,8 +195,8 @@ __global__ void __launch_bounds__(128) vsmooth_mean_kernel(const __grid_constant
 template <int kOpt>
 __global__ void __launch_bounds__(256) prepare_qk_kernel(const __grid_constant__ PrepParams P) {
   __shared__ uint32_t red[32];
-  const int j = blockIdx.x;
-  const int bh = blockIdx.y;
+  const int bh = blockIdx.x;
+  const int j = blockIdx.y;
   const int which = blockIdx.z;
   const int b = bh / P.H, h = bh % P.H;
   const int tid = threadIdx.x;
@@ -286,8 +288,8 @@ __global__ void __launch_bounds__(256) prepare_qk_kernel(const __grid_constant__
 template <bool kVSmooth, bool kPerm>
 __global__ void __launch_bounds__(512) prepare_v_kernel(const __grid_constant__ PrepParams P) {
   __shared__ float part[16][128];
-  const int j = blockIdx.x;
-  const int bh = blockIdx.y;
+  const int bh = blockIdx.x;
+  const int j = blockIdx.y;
   const int b = bh / P.H, h = bh % P.H;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
