@@ -512,3 +512,30 @@ def test_grouping_keeps_attention_and_lowers_v_smooth_error():
         e_g.append(rel_l2(o_g[0, rows, h], ex))
         e_u.append(rel_l2(o_u[0, rows, h], ex))
     assert np.mean(e_g) < np.mean(e_u), (e_g, e_u)
+
+
+def test_fp16_3d_inputs_through_grouping_v_smooth_and_split():
+    """FP16 [S,H,128] inputs: grouping permutation and grouped V-Smooth
+    preparation bit-exact, O within 5e-3; split key ranges on FP16 inputs."""
+    B, H, S = 1, 2, 1100
+    q, k, v = _clustered_inputs(B, H, S, seed=1500)
+    q, k, v = (x.to(torch.float16) for x in (q, k, v))
+    bits = [x.contiguous().view(torch.int16).numpy().view(np.uint16) for x in (q, k, v)]
+    _, _, perm_ref = oracle.kmeans_group(bits[2], 8, 3, fp16=True)
+    ref = oracle.Prepared(*bits, fp16=True, v_smooth=True, perm=perm_ref)
+    qd, kd, vd = (x[0].cuda() for x in (q, k, v))               # [S,H,128]
+    perm = ovc.group_v(vd, clusters=8, iters=3)
+    assert np.array_equal(perm.cpu().numpy(), perm_ref)
+    prep = ovc.prepare(qd, kd, vd, v_smooth=True, perm=perm)
+    torch.cuda.synchronize()
+    assert np.array_equal(prep.vt_codes().cpu().numpy().transpose(0, 1, 3, 2), ref.vc)
+    assert np.array_equal(prep.k_codes().cpu().numpy(), ref.kc)
+    want, _ = oracle.attention_full(ref)
+    o = ovc.attention_prepared(prep)
+    assert o.shape == (S, H, 128)
+    assert rel_l2(o.float().cpu().numpy(), want[0]) <= TOL_REL_L2
+    plain = oracle.Prepared(*bits, fp16=True)
+    want3, _ = oracle.attention_full(plain, nsplit=3)
+    o3 = ovc.attention_prepared(ovc.prepare(qd, kd, vd), nsplit=3)
+    assert rel_l2(o3.float().cpu().numpy(), want3[0]) <= TOL_REL_L2
+    assert ovc.device_status() == 0
