@@ -205,31 +205,22 @@ __device__ __forceinline__ UnitCoord unit_coord(const AttnParams& P, int u) {
 // The ExpCast step for one row and one block of 128 scores.
 //   s[c]  raw FP32 accumulator bits (masked columns already -inf)
 //   a     per-block multiplier (8 log2e sm sq sk)
-//   cterm (c0 + beta - m8) + 1.5*2^23, an exactly representable integer + magic
-// Produces 32 packed words of codes (bytes in key order) and returns the sum
-// of the decoded codes (accumulated as f16x2 pairs per block).
+//   c     c0 + beta - m8, an integer (the reference sits on its grid)
+// It produces 32 packed words of codes (bytes in key order); codes_sum adds
+// up their decoded values for the row sum.
 // ---------------------------------------------------------------------------
-#ifndef OVC_EXPCAST_SAT
-#define OVC_EXPCAST_SAT 1
-#endif
-
-// One ExpCast code in the low byte of the result.  With OVC_EXPCAST_SAT the
-// inputs are scaled by 1/256 (as = a/256, cs = (c0+beta-m8)/256): a saturating
-// FMA clamps at 0 and a second FMA rounds; otherwise (as = a, cs =
-// c0+beta-m8+1.5*2^23) one FMA rounds and a max clamps.
+// One ExpCast code in the low byte of the result.  The inputs are scaled by
+// 1/256 (as = a/256, cs = (c0+beta-m8)/256): a saturating FMA clamps the code
+// at 0, and a second FMA by 256 adding 1.5*2^23 rounds it to the integer in
+// the low mantissa bits (the code's upper end, 126, is kept by the lazy
+// rescale threshold).
 __device__ __forceinline__ uint32_t expcast_code(uint32_t s, float as, float cs) {
-#if OVC_EXPCAST_SAT
   return __float_as_uint(fmaf(fma_sat(__uint_as_float(s), as, cs), 256.0f, kMagic));
-#else
-  return __float_as_uint(fmaxf(fmaf(__uint_as_float(s), as, cs), kMagic));
-#endif
 }
 
-__device__ __forceinline__ float expcast_scale_a(float a) {
-  return OVC_EXPCAST_SAT ? a * (1.0f / 256.0f) : a;
-}
+__device__ __forceinline__ float expcast_scale_a(float a) { return a * (1.0f / 256.0f); }
 __device__ __forceinline__ float expcast_scale_c(float c) {   // c = c0 + beta - m8 (an integer)
-  return OVC_EXPCAST_SAT ? c * (1.0f / 256.0f) : c + kMagic;
+  return c * (1.0f / 256.0f);
 }
 
 // Codes of the scores s[4 G0 .. 4 (G0 + NG)) into the words w[G0 .. G0 + NG).
