@@ -539,3 +539,33 @@ def test_fp16_3d_inputs_through_grouping_v_smooth_and_split():
     o3 = ovc.attention_prepared(ovc.prepare(qd, kd, vd), nsplit=3)
     assert rel_l2(o3.float().cpu().numpy(), want3[0]) <= TOL_REL_L2
     assert ovc.device_status() == 0
+
+
+def test_no_write_outside_the_output_view():
+    """Canaries: O is a view inside a larger buffer filled with a sentinel
+    (extra tokens after S, an extra head, channels on both sides); every
+    attention path writes its rows of the view and nothing else."""
+    B, H, S = 1, 2, 1000                      # ragged: the last key/query block has 104 rows
+    q, k, v = inputs(B, H, S, seed=1600)
+    qd, kd, vd = to_dev(q, k, v)
+    sentinel = torch.tensor(12345, dtype=torch.int16).view(torch.bfloat16).item()
+    paths = {
+        "plain": lambda prep, out: ovc.attention_prepared(prep, out=out, nsplit=1),
+        "split": lambda prep, out: ovc.attention_prepared(prep, out=out, nsplit=4),
+        "baseline": lambda prep, out: ovc.attention_prepared(prep, out=out, flags=3, nsplit=1),
+        "repair": lambda prep, out: ovc.attention_v_repair(prep, ovc.prepare_v_repair(vd, prep, 0.02), out=out),
+        "v_smooth": None,
+    }
+    for name, run in paths.items():
+        big = torch.full((B, S + 37, H + 1, 192), sentinel, dtype=torch.bfloat16, device="cuda")
+        view = big[:, :S, :H, 32:160]
+        if name == "v_smooth":
+            ovc.attention_prepared(ovc.prepare(qd, kd, vd, v_smooth=True), out=view)
+        else:
+            run(ovc.prepare(qd, kd, vd), view)
+        assert ovc.device_status() == 0, name
+        bits = big.view(torch.int16)
+        mask = torch.ones_like(bits, dtype=torch.bool)
+        mask[:, :S, :H, 32:160] = False
+        assert bool((bits[mask] == 12345).all()), name
+        assert bool((bits[:, :S, :H, 32:160] != 12345).all()), name
