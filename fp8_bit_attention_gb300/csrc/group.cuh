@@ -18,8 +18,8 @@
 // Kernels (grid, block; the head index runs fastest, so CTAs that run
 // together read whole token rows of V):
 //   kmeans_init_kernel     (C, B*H) x 128
-//   kmeans_assign_kernel   (B*H, nb) x 256: a warp per token, a lane per 4
-//                          channels; the dot tree is the shuffle-down tree
+//   kmeans_assign_kernel   (B*H, nb) x 128: a thread per token, its values in
+//                          registers, the centroids in shared memory
 //   kmeans_partial_kernel  (B*H, nb) x 128: a thread per channel; per-cluster
 //                          sums in shared memory, counts by thread 0
 //   kmeans_update_kernel   (C, B*H) x 128
@@ -58,39 +58,57 @@ __global__ void __launch_bounds__(128) kmeans_init_kernel(const __grid_constant_
   G.cent[(static_cast<int64_t>(bh) * G.C + c) * 128 + d] = group_x(G, bh, t, d);
 }
 
-__global__ void __launch_bounds__(256) kmeans_assign_kernel(const __grid_constant__ GroupParams G) {
-  __shared__ float mu[kMaxClusters][128];
+__global__ void __launch_bounds__(128) kmeans_assign_kernel(const __grid_constant__ GroupParams G) {
+  __shared__ __align__(16) float mu[kMaxClusters][128];
   __shared__ float nrm[kMaxClusters];
-  const int bh = blockIdx.x, j = blockIdx.y;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = blockIdx.x, j = blockIdx.y, tid = threadIdx.x;
   const float* cent = G.cent + static_cast<int64_t>(bh) * G.C * 128;
-  for (int i = threadIdx.x; i < G.C * 128; i += blockDim.x) mu[i >> 7][i & 127] = cent[i];
+  for (int i = tid; i < G.C * 128; i += blockDim.x) mu[i >> 7][i & 127] = cent[i];
   __syncthreads();
-  if (threadIdx.x < G.C) {
+  if (tid < G.C) {
     float n = 0.0f;
-    for (int d = 0; d < 128; ++d) n = __fadd_rn(n, __fmul_rn(mu[threadIdx.x][d], mu[threadIdx.x][d]));
-    nrm[threadIdx.x] = n;
+    for (int d = 0; d < 128; ++d) n = __fadd_rn(n, __fmul_rn(mu[tid][d], mu[tid][d]));
+    nrm[tid] = n;
   }
   __syncthreads();
-  const int t1 = min(G.S, j * 128 + 128);
-  for (int t = j * 128 + warp; t < t1; t += 8) {
-    float x[4];
+  // One thread per token: its 128 values in registers, the dot product as
+  // 32 partial sums over 4 channels and then the pairwise tree.
+  const int t = j * 128 + tid;
+  if (t >= G.S) return;
+  const int b = bh / G.H, h = bh - b * G.H;
+  const uint4* row = reinterpret_cast<const uint4*>(G.v + b * G.vs[0] + static_cast<int64_t>(t) * G.vs[1] + h * G.vs[2]);
+  float x[128];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) x[i] = group_x(G, bh, t, 4 * lane + i);
-    float best = INFINITY;
-    int arg = 0;
-    for (int c = 0; c < G.C; ++c) {
-      float p = __fmul_rn(x[0], mu[c][4 * lane]);
+  for (int i = 0; i < 16; ++i) {
+    const uint4 w = __ldg(row + i);
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-      for (int i = 1; i < 4; ++i) p = __fadd_rn(p, __fmul_rn(x[i], mu[c][4 * lane + i]));
-#pragma unroll
-      for (int w = 16; w >= 1; w >>= 1) p = __fadd_rn(p, __shfl_down_sync(0xFFFFFFFFu, p, w));
-      // lane 0 holds the tree's result
-      const float dist = __fsub_rn(nrm[c], 2.0f * p);
-      if (dist < best) best = dist, arg = c;
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = unpack2(ws[e], G.fp16);
+      x[8 * i + 2 * e] = f.x;
+      x[8 * i + 2 * e + 1] = f.y;
     }
-    if (lane == 0) G.labels[static_cast<int64_t>(bh) * G.S + t] = arg;
   }
+  float best = INFINITY;
+  int arg = 0;
+  for (int c = 0; c < G.C; ++c) {
+    float p[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      const float4 m = *reinterpret_cast<const float4*>(&mu[c][4 * k]);
+      float a = __fmul_rn(x[4 * k], m.x);
+      a = __fadd_rn(a, __fmul_rn(x[4 * k + 1], m.y));
+      a = __fadd_rn(a, __fmul_rn(x[4 * k + 2], m.z));
+      p[k] = __fadd_rn(a, __fmul_rn(x[4 * k + 3], m.w));
+    }
+#pragma unroll
+    for (int w = 16; w >= 1; w >>= 1)
+#pragma unroll
+      for (int k = 0; k < w; ++k) p[k] = __fadd_rn(p[k], p[k + w]);
+    const float dist = __fsub_rn(nrm[c], 2.0f * p[0]);
+    if (dist < best) best = dist, arg = c;
+  }
+  G.labels[static_cast<int64_t>(bh) * G.S + t] = arg;
 }
 
 __global__ void __launch_bounds__(128) kmeans_partial_kernel(const __grid_constant__ GroupParams G) {

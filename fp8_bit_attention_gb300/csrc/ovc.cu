@@ -691,7 +691,7 @@ ovc_status ovc_vsmooth_group(const ovc_tensor* v, int32_t clusters, int32_t iter
   const unsigned BH = static_cast<unsigned>(v->B * v->H), nb = static_cast<unsigned>(G.nb);
   kmeans_init_kernel<<<dim3(static_cast<unsigned>(clusters), BH), 128, 0, s>>>(G);
   for (int it = 0; it < iters; ++it) {
-    kmeans_assign_kernel<<<dim3(BH, nb), 256, 0, s>>>(G);
+    kmeans_assign_kernel<<<dim3(BH, nb), 128, 0, s>>>(G);
     if (it + 1 == iters) break;
     kmeans_partial_kernel<<<dim3(BH, nb), 128, 0, s>>>(G);
     kmeans_update_kernel<<<dim3(static_cast<unsigned>(clusters), BH), 128, 0, s>>>(G);
