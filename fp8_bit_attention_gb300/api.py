@@ -26,6 +26,21 @@ def _stream_handle(stream=None) -> int:
     return s.cuda_stream
 
 
+def _device_of(*xs, stream=None) -> torch.device:
+    """The one CUDA device that every tensor in xs (None entries skipped) and
+    an explicit stream live on.  libovc launches on the current device, so
+    each call below runs under ``torch.cuda.device`` of this device."""
+    devs = {x.device for x in xs if x is not None}
+    if len(devs) != 1:
+        raise ValueError(f"all tensors must be on one CUDA device, got {sorted(map(str, devs))}")
+    dev = devs.pop()
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    if stream is not None and stream.device != dev:
+        raise ValueError(f"stream is on {stream.device}, tensors on {dev}")
+    return dev
+
+
 def _as4d(x: torch.Tensor) -> torch.Tensor:
     if x.dim() == 3:
         return x.unsqueeze(0)
@@ -47,10 +62,15 @@ def _tensor_desc(x: torch.Tensor) -> _abi.OvcTensor:
                           x.stride(2))
 
 
-def _output_desc(o: torch.Tensor) -> _abi.OvcOutput:
+def _output_desc(o: torch.Tensor, prep: "Prepared") -> _abi.OvcOutput:
+    """O's pointer and strides.  The C ABI takes no extent for O, so its
+    shape is checked here against the prepared inputs."""
     o = _as4d(o)
     if o.dtype != torch.bfloat16 or not o.is_cuda or o.stride(3) != 1:
         raise ValueError("output must be a CUDA bfloat16 tensor with unit channel stride")
+    want = (prep.B, prep.S, prep.H, 128)
+    if tuple(o.shape) != want:
+        raise ValueError(f"output shape {tuple(o.shape)} does not match the inputs' {want}")
     return _abi.OvcOutput(o.data_ptr(), o.stride(0), o.stride(1), o.stride(2))
 
 
@@ -155,16 +175,18 @@ def group_v(v: torch.Tensor, clusters: int = 16, iters: int = 4, *, stream=None)
     """V-Smooth's grouping (ovc_vsmooth_group): k-means over each head's value
     tokens, returned as the token order perm [B,H,S] (int32, CUDA) for
     ``prepare(..., perm=perm)``."""
-    tv = _tensor_desc(v)
-    nbytes = int(lib().ovc_vsmooth_group_workspace_bytes(tv.B, tv.S, tv.H, int(clusters)))
-    if nbytes == 0:
-        raise ValueError("invalid cluster count or shape")
-    ws = torch.empty(nbytes, dtype=torch.uint8, device=v.device)
-    perm = torch.empty((tv.B, tv.H, tv.S), dtype=torch.int32, device=v.device)
-    check(lib().ovc_vsmooth_group(ctypes.byref(tv), int(clusters), int(iters), ctypes.c_void_p(ws.data_ptr()),
-                                  ws.numel(), ctypes.c_void_p(perm.data_ptr()),
-                                  ctypes.c_void_p(_stream_handle(stream))), "ovc_vsmooth_group")
-    return perm
+    dev = _device_of(v, stream=stream)
+    with torch.cuda.device(dev):
+        tv = _tensor_desc(v)
+        nbytes = int(lib().ovc_vsmooth_group_workspace_bytes(tv.B, tv.S, tv.H, int(clusters)))
+        if nbytes == 0:
+            raise ValueError("invalid cluster count or shape")
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=v.device)
+        perm = torch.empty((tv.B, tv.H, tv.S), dtype=torch.int32, device=v.device)
+        check(lib().ovc_vsmooth_group(ctypes.byref(tv), int(clusters), int(iters), ctypes.c_void_p(ws.data_ptr()),
+                                      ws.numel(), ctypes.c_void_p(perm.data_ptr()),
+                                      ctypes.c_void_p(_stream_handle(stream))), "ovc_vsmooth_group")
+        return perm
 
 
 def prepare(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, smooth_k: bool = False,
@@ -177,29 +199,31 @@ def prepare(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, smooth_k: bool
     means for attention to restore (V-Smooth; no repair with it).  perm
     [B,H,S] int32 (e.g. from :func:`group_v`): K and V are taken in that
     token order (ovc_prepare_grouped); Q and so O keep theirs."""
-    tq, tk, tv = _tensor_desc(q), _tensor_desc(k), _tensor_desc(v)
-    flags = _prep_flags(smooth_k, v_smooth)
-    nbytes = prepare_workspace_bytes(tq.B, tq.S, tq.H, smooth_k=smooth_k, v_smooth=v_smooth)
-    if nbytes == 0:
-        raise ValueError(f"unsupported shape {tuple(q.shape)}")
-    if workspace is None:
-        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
-    desc = _abi.OvcPrepared()
-    if perm is None:
-        st = lib().ovc_prepare_ex(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv), flags,
-                                  ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
-                                  ctypes.byref(desc), ctypes.c_void_p(_stream_handle(stream)))
-        check(st, "ovc_prepare_ex")
-    else:
-        if perm.dtype != torch.int32 or not perm.is_cuda or tuple(perm.shape) != (tq.B, tq.H, tq.S):
-            raise ValueError("perm must be a CUDA int32 tensor [B,H,S]")
-        perm = perm.contiguous()
-        st = lib().ovc_prepare_grouped(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv),
-                                       ctypes.c_void_p(perm.data_ptr()), flags,
-                                       ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
-                                       ctypes.byref(desc), ctypes.c_void_p(_stream_handle(stream)))
-        check(st, "ovc_prepare_grouped")
-    return Prepared(desc, workspace, tuple(q.shape), q.dtype, perm)
+    dev = _device_of(q, k, v, perm, workspace, stream=stream)
+    with torch.cuda.device(dev):
+        tq, tk, tv = _tensor_desc(q), _tensor_desc(k), _tensor_desc(v)
+        flags = _prep_flags(smooth_k, v_smooth)
+        nbytes = prepare_workspace_bytes(tq.B, tq.S, tq.H, smooth_k=smooth_k, v_smooth=v_smooth)
+        if nbytes == 0:
+            raise ValueError(f"unsupported shape {tuple(q.shape)}")
+        if workspace is None:
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+        desc = _abi.OvcPrepared()
+        if perm is None:
+            st = lib().ovc_prepare_ex(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv), flags,
+                                      ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
+                                      ctypes.byref(desc), ctypes.c_void_p(_stream_handle(stream)))
+            check(st, "ovc_prepare_ex")
+        else:
+            if perm.dtype != torch.int32 or not perm.is_cuda or tuple(perm.shape) != (tq.B, tq.H, tq.S):
+                raise ValueError("perm must be a CUDA int32 tensor [B,H,S]")
+            perm = perm.contiguous()
+            st = lib().ovc_prepare_grouped(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv),
+                                           ctypes.c_void_p(perm.data_ptr()), flags,
+                                           ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
+                                           ctypes.byref(desc), ctypes.c_void_p(_stream_handle(stream)))
+            check(st, "ovc_prepare_grouped")
+        return Prepared(desc, workspace, tuple(q.shape), q.dtype, perm)
 
 
 def _out_for(prep: Prepared, out):
@@ -233,25 +257,27 @@ def attention_prepared(prep: Prepared, *, softmax_scale: float | None = None,
     :func:`attn_flags`), optional repair set, and split key ranges for short
     sequences -- ``nsplit=None`` lets the library choose and allocates the
     workspace it needs here; ``nsplit=1`` never splits."""
-    out = _out_for(prep, out)
-    od = _output_desc(out)
-    h = ctypes.c_void_p(_stream_handle(stream))
-    ns = 0 if nsplit is None else int(nsplit)
-    if rep is not None and nsplit is None:
-        ns = 1
-    need = attention_workspace_bytes(prep, ns) if ns != 1 else 0
-    if need and (workspace is None or workspace.numel() < need):
-        workspace = torch.empty(need, dtype=torch.uint8, device=prep.workspace.device)
-    wp = workspace.data_ptr() if (need and workspace is not None) else None
-    if need == 0 and flags == 0 and rep is None:
-        check(lib().ovc_attention(ctypes.byref(prep.desc), float(softmax_scale or 0.0), ctypes.byref(od), h),
-              "ovc_attention")
+    dev = _device_of(prep.workspace, out, workspace, None if rep is None else rep.workspace, stream=stream)
+    with torch.cuda.device(dev):
+        out = _out_for(prep, out)
+        od = _output_desc(out, prep)
+        h = ctypes.c_void_p(_stream_handle(stream))
+        ns = 0 if nsplit is None else int(nsplit)
+        if rep is not None and nsplit is None:
+            ns = 1
+        need = attention_workspace_bytes(prep, ns) if ns != 1 else 0
+        if need and (workspace is None or workspace.numel() < need):
+            workspace = torch.empty(need, dtype=torch.uint8, device=prep.workspace.device)
+        wp = workspace.data_ptr() if (need and workspace is not None) else None
+        if need == 0 and flags == 0 and rep is None:
+            check(lib().ovc_attention(ctypes.byref(prep.desc), float(softmax_scale or 0.0), ctypes.byref(od), h),
+                  "ovc_attention")
+            return out
+        st = lib().ovc_attention_ex(ctypes.byref(prep.desc), ctypes.byref(rep.desc) if rep is not None else None,
+                                    float(softmax_scale or 0.0), ctypes.byref(od), int(flags), ns,
+                                    ctypes.c_void_p(wp), need, h)
+        check(st, "ovc_attention_ex")
         return out
-    st = lib().ovc_attention_ex(ctypes.byref(prep.desc), ctypes.byref(rep.desc) if rep is not None else None,
-                                float(softmax_scale or 0.0), ctypes.byref(od), int(flags), ns,
-                                ctypes.c_void_p(wp), need, h)
-    check(st, "ovc_attention_ex")
-    return out
 
 
 def baseline_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *,
@@ -273,30 +299,34 @@ def repair_workspace_bytes(B: int, S: int, H: int, budget: float) -> int:
 def prepare_v_repair(v: torch.Tensor, prep: Prepared, budget: float = 0.005, *,
                      workspace: torch.Tensor | None = None, stream=None) -> Repair:
     """Select and quantise the V residuals of the worst tokens (ovc_prepare_v_repair)."""
-    tv = _tensor_desc(v)
-    nbytes = repair_workspace_bytes(tv.B, tv.S, tv.H, budget)
-    if nbytes == 0:
-        raise ValueError("invalid repair budget or shape")
-    if workspace is None:
-        workspace = torch.empty(nbytes, dtype=torch.uint8, device=v.device)
-    desc = _abi.OvcRepair()
-    st = lib().ovc_prepare_v_repair(ctypes.byref(tv), ctypes.byref(prep.desc), float(budget),
-                                    ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
-                                    ctypes.byref(desc), ctypes.c_void_p(_stream_handle(stream)))
-    check(st, "ovc_prepare_v_repair")
-    return Repair(desc, workspace)
+    dev = _device_of(v, prep.workspace, workspace, stream=stream)
+    with torch.cuda.device(dev):
+        tv = _tensor_desc(v)
+        nbytes = repair_workspace_bytes(tv.B, tv.S, tv.H, budget)
+        if nbytes == 0:
+            raise ValueError("invalid repair budget or shape")
+        if workspace is None:
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device=v.device)
+        desc = _abi.OvcRepair()
+        st = lib().ovc_prepare_v_repair(ctypes.byref(tv), ctypes.byref(prep.desc), float(budget),
+                                        ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
+                                        ctypes.byref(desc), ctypes.c_void_p(_stream_handle(stream)))
+        check(st, "ovc_prepare_v_repair")
+        return Repair(desc, workspace)
 
 
 def attention_v_repair(prep: Prepared, rep: Repair, *, softmax_scale: float | None = None,
                        out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """O with the repair term (ovc_attention_v_repair)."""
-    out = _out_for(prep, out)
-    od = _output_desc(out)
-    st = lib().ovc_attention_v_repair(ctypes.byref(prep.desc), ctypes.byref(rep.desc),
-                                      float(softmax_scale or 0.0), ctypes.byref(od),
-                                      ctypes.c_void_p(_stream_handle(stream)))
-    check(st, "ovc_attention_v_repair")
-    return out
+    dev = _device_of(prep.workspace, rep.workspace, out, stream=stream)
+    with torch.cuda.device(dev):
+        out = _out_for(prep, out)
+        od = _output_desc(out, prep)
+        st = lib().ovc_attention_v_repair(ctypes.byref(prep.desc), ctypes.byref(rep.desc),
+                                          float(softmax_scale or 0.0), ctypes.byref(od),
+                                          ctypes.c_void_p(_stream_handle(stream)))
+        check(st, "ovc_attention_v_repair")
+        return out
 
 
 def attention_probe(prep: Prepared, rep: Repair | None = None, *, softmax_scale=None, out=None,
@@ -306,31 +336,33 @@ def attention_probe(prep: Prepared, rep: Repair | None = None, *, softmax_scale=
     """Test hook: attention with P-byte dumps / wait-limit controls.
 
     dump = (bh, qblock, kblock) returns (out, codes [128,128] uint8, m8 [128])."""
-    out = _out_for(prep, out)
-    od = _output_desc(out)
-    probe = _abi.OvcProbe()
-    probe.dump_bh = -1
-    probe.wait_timeout_ns = int(wait_timeout_ns)
-    probe.skip_mma = int(skip_mma)
-    probe.force_persistent = int(force_persistent)
-    probe.flags = int(flags)
-    if trace is not None:
-        assert trace.dtype == torch.int64 and trace.is_cuda and trace.numel() >= 4 * 64 * 8
-        probe.trace = trace.data_ptr()
-    codes = m8 = None
-    if dump is not None:
-        dev = prep.workspace.device
-        codes = torch.zeros((128, 128), dtype=torch.uint8, device=dev)
-        m8 = torch.full((128,), float("nan"), dtype=torch.float32, device=dev)
-        probe.dump_bh, probe.dump_qblock, probe.dump_kblock = (int(x) for x in dump)
-        probe.dump_codes = codes.data_ptr()
-        probe.dump_m8 = m8.data_ptr()
-    st = lib().ovc_attention_probe(ctypes.byref(prep.desc),
-                                   ctypes.byref(rep.desc) if rep is not None else None,
-                                   float(softmax_scale or 0.0), ctypes.byref(od), ctypes.byref(probe),
-                                   ctypes.c_void_p(_stream_handle(stream)))
-    check(st, "ovc_attention_probe")
-    return out, codes, m8
+    dev = _device_of(prep.workspace, None if rep is None else rep.workspace, out, trace, stream=stream)
+    with torch.cuda.device(dev):
+        out = _out_for(prep, out)
+        od = _output_desc(out, prep)
+        probe = _abi.OvcProbe()
+        probe.dump_bh = -1
+        probe.wait_timeout_ns = int(wait_timeout_ns)
+        probe.skip_mma = int(skip_mma)
+        probe.force_persistent = int(force_persistent)
+        probe.flags = int(flags)
+        if trace is not None:
+            assert trace.dtype == torch.int64 and trace.is_cuda and trace.numel() >= 4 * 64 * 8
+            probe.trace = trace.data_ptr()
+        codes = m8 = None
+        if dump is not None:
+            dev = prep.workspace.device
+            codes = torch.zeros((128, 128), dtype=torch.uint8, device=dev)
+            m8 = torch.full((128,), float("nan"), dtype=torch.float32, device=dev)
+            probe.dump_bh, probe.dump_qblock, probe.dump_kblock = (int(x) for x in dump)
+            probe.dump_codes = codes.data_ptr()
+            probe.dump_m8 = m8.data_ptr()
+        st = lib().ovc_attention_probe(ctypes.byref(prep.desc),
+                                       ctypes.byref(rep.desc) if rep is not None else None,
+                                       float(softmax_scale or 0.0), ctypes.byref(od), ctypes.byref(probe),
+                                       ctypes.c_void_p(_stream_handle(stream)))
+        check(st, "ovc_attention_probe")
+        return out, codes, m8
 
 
 def device_status(stream=None) -> int:
@@ -490,7 +522,8 @@ def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, softmax_scal
     if q.is_cuda:
         return _attention_device(q, k, v, softmax_scale, repair_budget, out, smooth_k)
     dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
-    return _attention_host(q, k, v, softmax_scale, repair_budget, out, dev, chunk_heads, smooth_k)
+    with torch.cuda.device(dev):
+        return _attention_host(q, k, v, softmax_scale, repair_budget, out, dev, chunk_heads, smooth_k)
 
 
 def flops(B: int, S: int, H: int, D: int = 128) -> float:

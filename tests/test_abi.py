@@ -173,3 +173,16 @@ def test_prepare_options_on_the_host(lib):
     st = lib.ovc_prepare_ex(ctypes.byref(t), ctypes.byref(t), ctypes.byref(t), 12, ctypes.c_void_p(0x100000),
                             1 << 30, ctypes.byref(out), None)
     assert st == _abi.OVC_ERR_INVALID_ARG
+
+
+def test_binding_keeps_every_call_on_one_cuda_device():
+    """libovc launches on the current device, so the binding finds the one
+    device of a call's tensors (and rejects host tensors or a mix) before
+    any launch; checked here with host and meta tensors."""
+    from fp8_bit_attention_gb300.api import _device_of
+    with pytest.raises(ValueError, match="CUDA"):
+        _device_of(torch.zeros(4))
+    with pytest.raises(ValueError, match="one CUDA device"):
+        _device_of(torch.zeros(4), torch.zeros(4, device="meta"))
+    with pytest.raises(ValueError, match="one CUDA device"):
+        _device_of()

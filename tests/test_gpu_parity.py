@@ -569,3 +569,27 @@ def test_no_write_outside_the_output_view():
         mask[:, :S, :H, 32:160] = False
         assert bool((bits[mask] == 12345).all()), name
         assert bool((bits[:, :S, :H, 32:160] != 12345).all()), name
+
+
+def test_output_and_device_checks_of_the_binding():
+    """The C ABI takes O as a pointer and strides only, so the binding checks
+    O's shape, dtype and device against the prepared inputs before launching."""
+    B, H, S = 1, 2, 300
+    q, k, v = inputs(B, H, S, seed=1700)
+    qd, kd, vd = to_dev(q, k, v)
+    prep = ovc.prepare(qd, kd, vd)
+    rep = ovc.prepare_v_repair(vd, prep, 0.02)
+    bad = [torch.empty((B, S - 1, H, 128), dtype=torch.bfloat16, device="cuda"),     # too few rows
+           torch.empty((B, S, H + 1, 128), dtype=torch.bfloat16, device="cuda"),     # an extra head
+           torch.empty((B, S, H, 128), dtype=torch.float16, device="cuda"),          # dtype
+           torch.empty((B, S, H, 128), dtype=torch.bfloat16)]                         # host memory
+    for out in bad:
+        with pytest.raises(ValueError):
+            ovc.attention_prepared(prep, out=out)
+        with pytest.raises(ValueError):
+            ovc.attention_v_repair(prep, rep, out=out)
+    with pytest.raises(ValueError):
+        ovc.prepare(qd, kd, vd.cpu())
+    o = ovc.attention_prepared(prep, out=torch.empty((S, H, 128), dtype=torch.bfloat16, device="cuda"))
+    assert o.shape == (S, H, 128)
+    assert ovc.device_status() == 0
