@@ -382,25 +382,28 @@ def head_chunks(H: int, chunk_heads=None, tiles_per_head: int | None = None,
     """Head ranges of the host-buffer path.
 
     chunk_heads: an int (equal chunks of that many heads), a sequence of chunk
-    sizes summing to H, or None for the default plan.  The default keeps the
-    first and the last chunk small (about H/18 heads): the first chunk's copy
+    sizes summing to H, or None for the default plan.  The first chunk's copy
     in and the last chunk's copy out are the only copies that no computation
-    hides.  The chunks between take h heads each, h in [H/8, H/4] chosen so
-    that h * tiles_per_head fills whole waves of `sms` CTAs best, the smaller
-    h on a tie (with 287 tile pairs per head on 152 SMs, 9 heads make exactly
-    17 waves); without those figures, about a quarter of H."""
+    hides, so the default ramps: e and 2e heads first, 2e and e last, with
+    e = H/56 rounded (at least 1).  A chunk's attention takes about five
+    times as long as the copy of as many heads (73397 tokens on a GB300), so
+    each chunk still hides the next one's copy.  The chunks between take h
+    heads each, h in [H/8, H/4] chosen so that h * tiles_per_head fills whole
+    waves of `sms` CTAs best, the smaller h on a tie (with 287 tile pairs per
+    head on 152 SMs, 9 heads make exactly 17 waves); without those figures,
+    about a quarter of H."""
     if chunk_heads is None:
-        edge = int(round(H / 18))
-        if edge == 0 or H < 8:
+        e = max(1, int(round(H / 56)))
+        if H < 12:
             return head_chunks(H, max(1, -(-H // 4)))
-        mid = H - 2 * edge
+        mid = H - 6 * e
         h = max(1, -(-H // 4))
         if tiles_per_head and sms:
             def waste(n):
                 t = n * tiles_per_head
                 return (-(-t // sms) * sms) / t
             h = min(range(max(1, H // 8), max(2, H // 4) + 1), key=lambda n: (round(waste(n), 4), n))
-        sizes = [edge] + [h] * (mid // h) + ([mid % h] if mid % h else []) + [edge]
+        sizes = [e, 2 * e] + [h] * (mid // h) + ([mid % h] if mid % h else []) + [2 * e, e]
         return head_chunks(H, sizes)
     if isinstance(chunk_heads, int):
         n = max(1, chunk_heads)

@@ -151,9 +151,10 @@ def test_head_chunks_cover_every_head_once():
                 assert ch[0][0] == 0 and ch[-1][1] == H
                 assert all(a1 == b0 for (_, a1), (b0, _) in zip(ch, ch[1:]))
                 assert all(h1 > h0 for h0, h1 in ch)
-    # the default for 56 heads of 73397 tokens on 152 SMs: small edge chunks,
-    # 9-head chunks between (9 x 287 tile pairs = exactly 17 waves)
-    assert [b - a for a, b in head_chunks(56, None, 287, 152)] == [3, 9, 9, 9, 9, 9, 5, 3]
+    # the default for 56 heads of 73397 tokens on 152 SMs: a 1, 2 ramp at
+    # both ends, 9-head chunks between (9 x 287 tile pairs = exactly 17 waves)
+    assert [b - a for a, b in head_chunks(56, None, 287, 152)] == [1, 2, 9, 9, 9, 9, 9, 5, 2, 1]
+    assert [b - a for a, b in head_chunks(112, None, 287, 152)][:2] == [2, 4]
     assert [b - a for a, b in head_chunks(10, [3, 7])] == [3, 7]
     with pytest.raises(ValueError):
         head_chunks(10, [3, 6])
