@@ -9,9 +9,10 @@
 // Lloyd's algorithm in FP32 with every step rounded in a fixed order (so the
 // labels and the permutation reproduce bit for bit):
 //   start   mu_c = x_(floor(c S / C))
-//   assign  n_c = sum_d mu_cd^2 (channel order); dot = 32 partial sums over
-//           channels 4k..4k+3 (left to right), then the pairwise tree
-//           p_k += p_(k+w), w = 16..1; d = n_c - 2 dot; smallest d, ties to
+//   assign  n_c = sum_d mu_cd^2 (channel order); dot = 16 partial sums over
+//           channels 8k..8k+7 (the first product rounded, then fused
+//           multiply-adds left to right), then the pairwise tree
+//           p_k += p_(k+w), w = 8..1; d = n_c - 2 dot; smallest d, ties to
 //           the lower c
 //   update  mu_c = sum / count: sums per 128-token block in token order, then
 //           over blocks in block order; an empty cluster keeps its centroid
@@ -20,8 +21,10 @@
 //   kmeans_init_kernel     (C, B*H) x 128
 //   kmeans_assign_kernel   (B*H, nb) x 128: a thread per token, its values in
 //                          registers, the centroids in shared memory
-//   kmeans_partial_kernel  (B*H, nb) x 128: a thread per channel; per-cluster
-//                          sums in shared memory, counts by thread 0
+//   kmeans_partial_kernel  (B*H, nb) x 128: the block's tokens staged in shared
+//                          memory by 16-byte loads and listed per cluster in
+//                          token order; a thread per channel then sums each
+//                          cluster's members in a register
 //   kmeans_update_kernel   (C, B*H) x 128
 //   group_count_kernel / group_offset_kernel / group_scatter_kernel: a
 //                          stable counting sort of the labels
@@ -72,7 +75,9 @@ __global__ void __launch_bounds__(128) kmeans_assign_kernel(const __grid_constan
   }
   __syncthreads();
   // One thread per token: its 128 values in registers, the dot product as
-  // 32 partial sums over 4 channels and then the pairwise tree.
+  // 16 partial sums over 8 channels (fused multiply-adds) and then the
+  // pairwise tree.  The centroids are read from shared memory as warp-wide
+  // broadcasts; their delivery to every lane's registers bounds the kernel.
   const int t = j * 128 + tid;
   if (t >= G.S) return;
   const int b = bh / G.H, h = bh - b * G.H;
@@ -92,17 +97,22 @@ __global__ void __launch_bounds__(128) kmeans_assign_kernel(const __grid_constan
   float best = INFINITY;
   int arg = 0;
   for (int c = 0; c < G.C; ++c) {
-    float p[32];
+    float p[16];
 #pragma unroll
-    for (int k = 0; k < 32; ++k) {
-      const float4 m = *reinterpret_cast<const float4*>(&mu[c][4 * k]);
-      float a = __fmul_rn(x[4 * k], m.x);
-      a = __fadd_rn(a, __fmul_rn(x[4 * k + 1], m.y));
-      a = __fadd_rn(a, __fmul_rn(x[4 * k + 2], m.z));
-      p[k] = __fadd_rn(a, __fmul_rn(x[4 * k + 3], m.w));
+    for (int k = 0; k < 16; ++k) {
+      const float4 m0 = *reinterpret_cast<const float4*>(&mu[c][8 * k]);
+      const float4 m1 = *reinterpret_cast<const float4*>(&mu[c][8 * k + 4]);
+      float a = __fmul_rn(x[8 * k], m0.x);
+      a = __fmaf_rn(x[8 * k + 1], m0.y, a);
+      a = __fmaf_rn(x[8 * k + 2], m0.z, a);
+      a = __fmaf_rn(x[8 * k + 3], m0.w, a);
+      a = __fmaf_rn(x[8 * k + 4], m1.x, a);
+      a = __fmaf_rn(x[8 * k + 5], m1.y, a);
+      a = __fmaf_rn(x[8 * k + 6], m1.z, a);
+      p[k] = __fmaf_rn(x[8 * k + 7], m1.w, a);
     }
 #pragma unroll
-    for (int w = 16; w >= 1; w >>= 1)
+    for (int w = 8; w >= 1; w >>= 1)
 #pragma unroll
       for (int k = 0; k < w; ++k) p[k] = __fadd_rn(p[k], p[k + w]);
     const float dist = __fsub_rn(nrm[c], 2.0f * p[0]);
@@ -111,23 +121,71 @@ __global__ void __launch_bounds__(128) kmeans_assign_kernel(const __grid_constan
   G.labels[static_cast<int64_t>(bh) * G.S + t] = arg;
 }
 
+// Dynamic shared memory of kmeans_partial_kernel: the block's tokens
+// (kXsPitch 16-bit values a row, rows 16-byte aligned), their labels, the
+// members of each cluster in token order, and per-cluster counts and offsets.
+constexpr int kXsPitch = 136;
+
+__host__ __device__ constexpr size_t kmeans_partial_smem() {
+  return 128 * kXsPitch * 2 + 3 * 128 * 4 + 2 * kMaxClusters * 4;
+}
+
 __global__ void __launch_bounds__(128) kmeans_partial_kernel(const __grid_constant__ GroupParams G) {
-  __shared__ float part[kMaxClusters][128];
-  __shared__ int cnt[kMaxClusters];
+  extern __shared__ __align__(16) uint8_t smem[];
+  uint16_t* xs = reinterpret_cast<uint16_t*>(smem);
+  int* lab = reinterpret_cast<int*>(smem + 128 * kXsPitch * 2);
+  int* rank = lab + 128;
+  int* member = rank + 128;
+  int* cnt = member + 128;
+  int* first = cnt + kMaxClusters;
   const int bh = blockIdx.x, j = blockIdx.y, d = threadIdx.x;
-  for (int c = 0; c < G.C; ++c) part[c][d] = 0.0f;
+  const int b = bh / G.H, h = bh - b * G.H;
+  const int t0 = j * 128, nt = min(128, G.S - t0);
+  // The block's tokens in one round of 16-byte loads (all in flight before
+  // the first store), and their labels.
+  const uint16_t* vb = G.v + b * G.vs[0] + static_cast<int64_t>(t0) * G.vs[1] + h * G.vs[2];
+  uint4 w[16];
+#pragma unroll
+  for (int q = 0; q < 16; ++q) {
+    const int t = (d >> 4) + 8 * q, c = d & 15;
+    if (t < nt) w[q] = __ldg(reinterpret_cast<const uint4*>(vb + static_cast<int64_t>(t) * G.vs[1]) + c);
+  }
+#pragma unroll
+  for (int q = 0; q < 16; ++q) {
+    const int t = (d >> 4) + 8 * q, c = d & 15;
+    if (t < nt) *reinterpret_cast<uint4*>(xs + t * kXsPitch + 8 * c) = w[q];
+  }
+  if (d < nt) lab[d] = __ldg(G.labels + static_cast<int64_t>(bh) * G.S + t0 + d);
   if (d < G.C) cnt[d] = 0;
   __syncthreads();
-  const int32_t* lab = G.labels + static_cast<int64_t>(bh) * G.S;
-  const int t1 = min(G.S, j * 128 + 128);
-  for (int t = j * 128; t < t1; ++t) {
-    const int c = __ldg(lab + t);
-    part[c][d] = __fadd_rn(part[c][d], group_x(G, bh, t, d));
-    if (d == 0) ++cnt[c];
+  // Members of each cluster, in token order: a token's place is the number
+  // of earlier tokens with its label.
+  if (d < nt) {
+    const int c = lab[d];
+    int r = 0;
+    for (int t = 0; t < d; ++t) r += (lab[t] == c);
+    rank[d] = r;
+    atomicAdd(&cnt[c], 1);
   }
   __syncthreads();
+  if (d == 0) {
+    int pos = 0;
+    for (int c = 0; c < G.C; ++c) {
+      first[c] = pos;
+      pos += cnt[c];
+    }
+  }
+  __syncthreads();
+  if (d < nt) member[first[lab[d]] + rank[d]] = d;
+  __syncthreads();
+  // A thread per channel: each cluster's sum in token order.
   const int64_t base = (static_cast<int64_t>(bh) * G.nb + j) * G.C;
-  for (int c = 0; c < G.C; ++c) G.part[(base + c) * 128 + d] = part[c][d];
+  for (int c = 0; c < G.C; ++c) {
+    float acc = 0.0f;
+    const int m1 = first[c] + cnt[c];
+    for (int m = first[c]; m < m1; ++m) acc = __fadd_rn(acc, half_bits_to_float(xs[member[m] * kXsPitch + d], G.fp16));
+    G.part[(base + c) * 128 + d] = acc;
+  }
   if (d < G.C) G.cnt[base + d] = cnt[d];
 }
 
@@ -135,8 +193,26 @@ __global__ void __launch_bounds__(128) kmeans_update_kernel(const __grid_constan
   const int c = blockIdx.x, bh = blockIdx.y, d = threadIdx.x;
   float s = 0.0f;
   int n = 0;
-  for (int j = 0; j < G.nb; ++j) {
-    const int64_t base = (static_cast<int64_t>(bh) * G.nb + j) * G.C + c;
+  // Sums in block order; the loads of eight blocks are issued together.
+  const int64_t base0 = static_cast<int64_t>(bh) * G.nb * G.C + c;
+  int j = 0;
+  for (; j + 8 <= G.nb; j += 8) {
+    float v[8];
+    int k[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int64_t base = base0 + static_cast<int64_t>(j + e) * G.C;
+      v[e] = __ldg(G.part + base * 128 + d);
+      k[e] = __ldg(G.cnt + base);
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      s = __fadd_rn(s, v[e]);
+      n += k[e];
+    }
+  }
+  for (; j < G.nb; ++j) {
+    const int64_t base = base0 + static_cast<int64_t>(j) * G.C;
     s = __fadd_rn(s, G.part[base * 128 + d]);
     n += G.cnt[base];
   }

@@ -64,6 +64,9 @@ ovc_status device_state(DeviceState** out) {
                                  static_cast<int>(v == kVarVSmooth ? kAttnSmemBytesVSmooth : kAttnSmemBytes)) !=
             cudaSuccess)
           return OVC_ERR_CUDA;
+      if (cudaFuncSetAttribute(kmeans_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(kmeans_partial_smem())) != cudaSuccess)
+        return OVC_ERR_CUDA;
       void* p = nullptr;
       if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return OVC_ERR_CUDA;
       d.status = static_cast<unsigned int*>(p);
@@ -693,7 +696,7 @@ ovc_status ovc_vsmooth_group(const ovc_tensor* v, int32_t clusters, int32_t iter
   for (int it = 0; it < iters; ++it) {
     kmeans_assign_kernel<<<dim3(BH, nb), 128, 0, s>>>(G);
     if (it + 1 == iters) break;
-    kmeans_partial_kernel<<<dim3(BH, nb), 128, 0, s>>>(G);
+    kmeans_partial_kernel<<<dim3(BH, nb), 128, kmeans_partial_smem(), s>>>(G);
     kmeans_update_kernel<<<dim3(static_cast<unsigned>(clusters), BH), 128, 0, s>>>(G);
   }
   group_count_kernel<<<dim3(BH, nb), 128, 0, s>>>(G);

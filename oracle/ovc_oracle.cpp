@@ -596,11 +596,13 @@ void ovc_oracle_vsmooth_v(const uint16_t* v, int fp16, int64_t B, int64_t S, int
 // each head's value tokens; keys and values are permuted together, which
 // leaves non-causal attention unchanged): Lloyd's k-means with C clusters and
 // `iters` iterations, then the tokens ordered by (cluster, index).
-// Arithmetic, all FP32 with every step rounded (no fused operations):
+// Arithmetic, all FP32 with every step rounded; the only fused operation is
+// the multiply-add of the dot product (one rounding, as fmaf):
 //   start:   mu_c = x_(floor(c S / C)), c = 0..C-1
-//   assign:  n_c = sum_d mu_cd^2 (channel order);
-//            dot(t, c) = 32 partial sums over channels 4k..4k+3 (left to
-//            right), then the pairwise tree p_k <- p_k + p_(k+w), w = 16..1;
+//   assign:  n_c = sum_d mu_cd^2 (channel order, products rounded);
+//            dot(t, c) = 16 partial sums over channels 8k..8k+7: the first
+//            product rounded, then p_k <- fma(x_i, mu_i, p_k) left to right;
+//            then the pairwise tree p_k <- p_k + p_(k+w), w = 8..1;
 //            d(t, c) = n_c - 2 dot(t, c); the cluster with the smallest d,
 //            ties to the lower c
 //   update:  mu_c = (sum of its tokens) / count, the sum taken per 128-token
@@ -609,16 +611,13 @@ void ovc_oracle_vsmooth_v(const uint16_t* v, int fp16, int64_t B, int64_t S, int
 // One iteration is assign then update; the labels returned are those of the
 // last assignment, and centroids [B,H,C,128] the centroids it used.
 float kmeans_dot(const float* x, const float* mu) {
-  float p[32];
-  for (int k = 0; k < 32; ++k) {
-    volatile float a = x[4 * k] * mu[4 * k];
-    for (int i = 1; i < 4; ++i) {
-      volatile float m = x[4 * k + i] * mu[4 * k + i];
-      a = a + m;
-    }
+  float p[16];
+  for (int k = 0; k < 16; ++k) {
+    volatile float a = x[8 * k] * mu[8 * k];
+    for (int i = 1; i < 8; ++i) a = std::fma(x[8 * k + i], mu[8 * k + i], static_cast<float>(a));
     p[k] = a;
   }
-  for (int w = 16; w >= 1; w >>= 1)
+  for (int w = 8; w >= 1; w >>= 1)
     for (int k = 0; k < w; ++k) {
       volatile float q = p[k] + p[k + w];
       p[k] = q;
