@@ -521,7 +521,19 @@ def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, softmax_scal
     sizes, or None for the default plan of :func:`head_chunks`), so that
     host<->device copies overlap the computation; O
     lands in `out` (or a new pinned tensor), complete when the call returns.
-    smooth_k: optional K smoothing in prepare (see `prepare`)."""
+    smooth_k: optional K smoothing in prepare (see `prepare`).
+
+    Empty inputs (B, S or H of 0: no query rows) give an empty output
+    without a launch; the C ABI itself rejects zero sizes."""
+    if q.numel() == 0 or k.numel() == 0 or v.numel() == 0:
+        q4, k4, v4 = (_as4d(x) for x in (q, k, v))
+        if k4.shape != q4.shape or v4.shape != q4.shape or q4.shape[3] != 128:
+            raise ValueError("q, k and v must have the same [B,S,H,128] shape")
+        if out is None:
+            out = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
+        if tuple(out.shape) != tuple(q.shape) or out.dtype != torch.bfloat16:
+            raise ValueError("out must be a bfloat16 tensor shaped like q")
+        return out
     if q.is_cuda:
         return _attention_device(q, k, v, softmax_scale, repair_budget, out, smooth_k)
     dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())

@@ -187,3 +187,16 @@ def test_binding_keeps_every_call_on_one_cuda_device():
         _device_of(torch.zeros(4), torch.zeros(4, device="meta"))
     with pytest.raises(ValueError, match="one CUDA device"):
         _device_of()
+
+
+def test_empty_inputs_give_an_empty_output_without_a_launch():
+    """No query rows (S, H or B of 0) means nothing to compute: the binding
+    returns an empty BF16 output on the inputs' device (checked here on the
+    host, where no GPU exists to launch on)."""
+    import fp8_bit_attention_gb300 as ovc
+    for shape in [(0, 4, 128), (1, 0, 4, 128), (0, 8, 2, 128), (2, 8, 0, 128)]:
+        q = torch.zeros(shape, dtype=torch.bfloat16)
+        o = ovc.attention(q, q.clone(), q.clone())
+        assert o.shape == q.shape and o.dtype == torch.bfloat16 and o.numel() == 0
+    with pytest.raises(ValueError):
+        ovc.attention(torch.zeros((0, 4, 128)), torch.zeros((0, 5, 128)), torch.zeros((0, 4, 128)))
