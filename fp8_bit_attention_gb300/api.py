@@ -541,12 +541,54 @@ def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, softmax_scal
         return _attention_host(q, k, v, softmax_scale, repair_budget, out, dev, chunk_heads, smooth_k)
 
 
+class CapturedAttention:
+    """The full call on CUDA tensors of fixed shape -- prepare, then attention
+    (with V residual repair when ``repair_budget`` is set) -- captured once as
+    a CUDA graph and replayed.
+
+    Every libovc call is asynchronous on the current stream, allocates no
+    memory and never synchronises, so the sequence captures as it stands; a
+    replay then costs one graph launch instead of one host call per kernel,
+    which is what bounds short sequences.  The inputs are copied into the
+    graph's own buffers on each call (``q``, ``k``, ``v`` of the captured
+    shape, dtype and device), or, called without arguments, the replay reads
+    whatever those buffers (``self.q``, ``self.k``, ``self.v``) hold.  The
+    result is written to ``self.out`` and returned; it is the eager call's
+    output bit for bit."""
+
+    def __init__(self, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, softmax_scale: float | None = None,
+                 repair_budget: float | None = None, smooth_k: bool = False):
+        dev = _device_of(q, k, v)
+        with torch.cuda.device(dev):
+            self.q, self.k, self.v = (x.clone() for x in (q, k, v))
+            self._args = dict(softmax_scale=softmax_scale, repair_budget=repair_budget, smooth_k=smooth_k)
+            # One eager call first: it loads the library and sets its
+            # per-device state, which must not happen during the capture.
+            _attention_device(self.q, self.k, self.v, softmax_scale, repair_budget, None, smooth_k)
+            torch.cuda.synchronize(dev)
+            self.graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(self.graph):
+                self.out = _attention_device(self.q, self.k, self.v, softmax_scale, repair_budget, None, smooth_k)
+            self.device = dev
+
+    def __call__(self, q: torch.Tensor | None = None, k: torch.Tensor | None = None,
+                 v: torch.Tensor | None = None) -> torch.Tensor:
+        with torch.cuda.device(self.device):
+            for src, dst in ((q, self.q), (k, self.k), (v, self.v)):
+                if src is not None:
+                    if src.shape != dst.shape or src.dtype != dst.dtype or src.device != dst.device:
+                        raise ValueError("inputs must match the captured shape, dtype and device")
+                    dst.copy_(src)
+            self.graph.replay()
+            return self.out
+
+
 def flops(B: int, S: int, H: int, D: int = 128) -> float:
     """Attention FLOPs counted as 4 * B * H * S^2 * D."""
     return 4.0 * B * H * float(S) ** 2 * D
 
 
-__all__ = ["Prepared", "Repair", "OvcError", "prepare", "attention_prepared", "attention_workspace_bytes",
+__all__ = ["Prepared", "Repair", "OvcError", "CapturedAttention", "prepare", "attention_prepared", "attention_workspace_bytes",
            "auto_split", "group_v", "prepare_v_repair",
            "attention_v_repair", "attention_probe", "device_status", "attention", "memcpy2d",
            "head_chunks", "prepare_workspace_bytes", "repair_workspace_bytes", "flops"]

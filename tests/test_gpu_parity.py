@@ -593,3 +593,19 @@ def test_output_and_device_checks_of_the_binding():
     o = ovc.attention_prepared(prep, out=torch.empty((S, H, 128), dtype=torch.bfloat16, device="cuda"))
     assert o.shape == (S, H, 128)
     assert ovc.device_status() == 0
+
+
+@pytest.mark.parametrize("B,H,S,budget", [(1, 2, 1024, None), (1, 3, 1000, 0.02), (2, 2, 300, None)])
+def test_captured_full_call_replays_the_eager_result(B, H, S, budget):
+    """The CUDA-graph capture of prepare + attention (+ repair) gives the
+    eager call's output bit for bit, also after new inputs are copied in."""
+    q, k, v = to_dev(*inputs(B, H, S, seed=1800 + S))
+    cap = ovc.CapturedAttention(q, k, v, repair_budget=budget)
+    assert torch.equal(cap(), ovc.attention(q, k, v, repair_budget=budget))
+    q2, k2, v2 = to_dev(*inputs(B, H, S, seed=1801 + S))
+    got = cap(q2, k2, v2).clone()
+    assert torch.equal(got, ovc.attention(q2, k2, v2, repair_budget=budget))
+    assert not torch.equal(got, cap(q, k, v))
+    with pytest.raises(ValueError):
+        cap(q2[:, :-1])
+    assert ovc.device_status() == 0
