@@ -150,7 +150,7 @@ def _gpu_uuid(torch):
     try:
         u = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
         return u if u.startswith("GPU-") else "GPU-" + u
-    except Exception:
+    except (RuntimeError, AttributeError):    # no device, or a torch without .uuid
         return None
 
 

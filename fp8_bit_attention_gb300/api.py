@@ -347,7 +347,8 @@ def attention_probe(prep: Prepared, rep: Repair | None = None, *, softmax_scale=
         probe.force_persistent = int(force_persistent)
         probe.flags = int(flags)
         if trace is not None:
-            assert trace.dtype == torch.int64 and trace.is_cuda and trace.numel() >= 4 * 64 * 8
+            if trace.dtype != torch.int64 or not trace.is_cuda or trace.numel() < 4 * 64 * 8:
+                raise ValueError("trace must be a CUDA int64 tensor of at least 4 * 64 * 8 entries")
             probe.trace = trace.data_ptr()
         codes = m8 = None
         if dump is not None:

@@ -120,5 +120,6 @@ def generate(w: Workload, *, pin: bool = False):
 
 def bf16_bits(t: torch.Tensor) -> np.ndarray:
     """View a CPU BF16 tensor as a numpy uint16 array of its bits (no copy)."""
-    assert t.dtype == torch.bfloat16 and t.device.type == "cpu"
+    if t.dtype != torch.bfloat16 or t.device.type != "cpu":
+        raise ValueError("expected a CPU bfloat16 tensor")
     return t.view(torch.int16).numpy().view(np.uint16)
