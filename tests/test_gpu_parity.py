@@ -609,3 +609,25 @@ def test_captured_full_call_replays_the_eager_result(B, H, S, budget):
     with pytest.raises(ValueError):
         cap(q2[:, :-1])
     assert ovc.device_status() == 0
+
+
+@pytest.mark.parametrize("B,H,S,budget", [(1, 2, 300, 1.0), (1, 1, 1, 1.0), (1, 3, 129, 0.5), (2, 1, 640, 1.0)])
+def test_repair_edge_budgets(B, H, S, budget):
+    """Budget 1 repairs every token (n = S, the largest repair set: as many
+    repair blocks as key blocks); S = 1 and a ragged S = 129 cover the
+    degenerate sizes.  Selection bit-exact, output within the tolerance."""
+    q, k, v = inputs(B, H, S, seed=2100 + S)
+    ref = oracle_prep(q, k, v)
+    rep_ref = oracle.Repair(ref, budget)
+    qd, kd, vd = to_dev(q, k, v)
+    prep = ovc.prepare(qd, kd, vd)
+    rep = ovc.prepare_v_repair(vd, prep, budget)
+    torch.cuda.synchronize()
+    assert rep.desc.n == rep_ref.n == (S if budget == 1.0 else rep_ref.n)
+    assert np.array_equal(rep.idx().cpu().numpy(), rep_ref.idx)
+    assert np.array_equal(rep.sr().cpu().numpy(), rep_ref.sr)
+    want, _ = oracle.attention_full(ref, repair=rep_ref)
+    for force in (0, 1):
+        o = ovc.attention_probe(prep, rep, force_persistent=force)[0]
+        assert ovc.device_status() == 0
+        assert rel_l2(o.float().cpu().numpy(), want) <= TOL_REL_L2
