@@ -631,3 +631,26 @@ def test_repair_edge_budgets(B, H, S, budget):
         o = ovc.attention_probe(prep, rep, force_persistent=force)[0]
         assert ovc.device_status() == 0
         assert rel_l2(o.float().cpu().numpy(), want) <= TOL_REL_L2
+
+
+def test_many_heads_ragged_sequence():
+    """2000 heads of 130 tokens (two key blocks, the second with 2 keys):
+    large head grids and the head-fastest preparation.  The quantised tensors
+    are compared in full, O on every row of a sample of heads (first, last
+    and spread between)."""
+    B, H, S = 1, 2000, 130
+    q, k, v = inputs(B, H, S, seed=2200)
+    ref = oracle_prep(q, k, v)
+    qd, kd, vd = to_dev(q, k, v)
+    prep = ovc.prepare(qd, kd, vd)
+    o = ovc.attention_prepared(prep, nsplit=1)
+    assert ovc.device_status() == 0
+    assert np.array_equal(prep.q_codes().cpu().numpy()[..., :S, :], ref.qc[..., :S, :])
+    assert np.array_equal(prep.vt_codes().cpu().numpy()[..., :S], ref.vc.transpose(0, 1, 3, 2)[..., :S])
+    assert np.array_equal(prep.v_scales().cpu().numpy(), ref.sv)
+    heads = np.array([0, 1, 777, 1234, 1998, 1999])
+    rows_bh = np.repeat(heads, S)
+    rows_s = np.tile(np.arange(S), heads.size)
+    want = oracle.attention_rows(ref, rows_bh, rows_s)["out"]
+    got = o.float().cpu().numpy()[0][:, heads, :].transpose(1, 0, 2).reshape(-1, 128)
+    assert rel_l2(got, want) <= TOL_REL_L2
