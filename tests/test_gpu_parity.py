@@ -654,3 +654,28 @@ def test_many_heads_ragged_sequence():
     want = oracle.attention_rows(ref, rows_bh, rows_s)["out"]
     got = o.float().cpu().numpy()[0][:, heads, :].transpose(1, 0, 2).reshape(-1, 128)
     assert rel_l2(got, want) <= TOL_REL_L2
+
+
+@pytest.mark.parametrize("B,H,S,budget", [(1, 2, 1000, 0.02), (2, 1, 300, 0.3)])
+def test_k_smoothing_with_repair(B, H, S, budget):
+    """K smoothing and V residual repair together: the repair set's keys are
+    gathered from the smoothed K codes with their block scales; selection
+    bit-exact and O within 5e-3 of the oracle doing the same."""
+    q, k, v = inputs(B, H, S, seed=2300 + S)
+    bits = [x.contiguous().view(torch.int16).numpy().view(np.uint16) for x in (q, k, v)]
+    ref = oracle.Prepared(*bits, smooth_k=True)
+    rep_ref = oracle.Repair(ref, budget)
+    qd, kd, vd = to_dev(q, k, v)
+    prep = ovc.prepare(qd, kd, vd, smooth_k=True)
+    rep = ovc.prepare_v_repair(vd, prep, budget)
+    torch.cuda.synchronize()
+    assert np.array_equal(rep.idx().cpu().numpy(), rep_ref.idx)
+    n = rep_ref.n
+    ksel = rep.k_sel().cpu().numpy()
+    for b in range(B):
+        for h in range(H):
+            assert np.array_equal(ksel[b, h, :n], ref.kc[b, h, rep_ref.idx[b, h]])
+    want, _ = oracle.attention_full(ref, repair=rep_ref)
+    o = ovc.attention_v_repair(prep, rep)
+    assert ovc.device_status() == 0
+    assert rel_l2(o.float().cpu().numpy(), want) <= TOL_REL_L2
