@@ -452,7 +452,10 @@ def _attention_host(q, k, v, softmax_scale, repair_budget, out, dev, chunk_heads
     chunks = head_chunks(H, chunk_heads, tiles_per_head=B * (-(-nb // 2)),
                          sms=torch.cuda.get_device_properties(dev).multi_processor_count)
     hmax = max(h1 - h0 for h0, h1 in chunks)
-    comp = torch.cuda.current_stream(dev)
+    # Chunks alternate between two compute streams, so that a chunk's
+    # preparation and first CTAs can start on the SMs that the previous
+    # chunk's last, partly filled wave leaves idle.
+    comps = [torch.cuda.current_stream(dev), torch.cuda.Stream(dev)]
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     # Two sets of staging buffers: chunk c uses set c % 2.
     n_el = B * S * hmax * D
@@ -461,17 +464,18 @@ def _attention_host(q, k, v, softmax_scale, repair_budget, out, dev, chunk_heads
     in_free = [None, None]      # compute has consumed the set's inputs
     out_free = [None, None]     # the set's output has been copied out
     try:
-        _stream_chunks(q4, k4, v4, o4, chunks, stage_in, stage_out, in_free, out_free, comp, s_in, s_out,
+        _stream_chunks(q4, k4, v4, o4, chunks, stage_in, stage_out, in_free, out_free, comps, s_in, s_out,
                        softmax_scale, repair_budget, smooth_k)
     finally:
         # The staging buffers die with this frame: let every stream finish with them.
         s_out.synchronize()
         s_in.synchronize()
-        comp.synchronize()
+        for cs in comps:
+            cs.synchronize()
     return out
 
 
-def _stream_chunks(q4, k4, v4, o4, chunks, stage_in, stage_out, in_free, out_free, comp, s_in, s_out,
+def _stream_chunks(q4, k4, v4, o4, chunks, stage_in, stage_out, in_free, out_free, comps, s_in, s_out,
                    softmax_scale, repair_budget, smooth_k):
     B, S, H, D = q4.shape
     el = q4.element_size()
@@ -489,20 +493,22 @@ def _stream_chunks(q4, k4, v4, o4, chunks, stage_in, stage_out, in_free, out_fre
                          hc * D * el, B * S, s_in)
             ready = torch.cuda.Event()
             ready.record(s_in)
-        comp.wait_event(ready)
-        prep = prepare(*ins, smooth_k=smooth_k)
-        rep = prepare_v_repair(ins[2], prep, repair_budget) if repair_budget else None
-        in_free[st] = torch.cuda.Event()
-        in_free[st].record(comp)
-        if out_free[st] is not None:
-            comp.wait_event(out_free[st])
-        ob = stage_out[st][:B * S * hc * D].view(B, S, hc, D)
-        if rep is not None:
-            attention_v_repair(prep, rep, softmax_scale=softmax_scale, out=ob)
-        else:
-            attention_prepared(prep, softmax_scale=softmax_scale, out=ob, nsplit=nsplit)
-        done = torch.cuda.Event()
-        done.record(comp)
+        comp = comps[st]             # staging set st and compute stream st go together
+        with torch.cuda.stream(comp):
+            comp.wait_event(ready)
+            prep = prepare(*ins, smooth_k=smooth_k)
+            rep = prepare_v_repair(ins[2], prep, repair_budget) if repair_budget else None
+            in_free[st] = torch.cuda.Event()
+            in_free[st].record(comp)
+            if out_free[st] is not None:
+                comp.wait_event(out_free[st])
+            ob = stage_out[st][:B * S * hc * D].view(B, S, hc, D)
+            if rep is not None:
+                attention_v_repair(prep, rep, softmax_scale=softmax_scale, out=ob)
+            else:
+                attention_prepared(prep, softmax_scale=softmax_scale, out=ob, nsplit=nsplit)
+            done = torch.cuda.Event()
+            done.record(comp)
         with torch.cuda.stream(s_out):
             s_out.wait_event(done)
             memcpy2d(o4.data_ptr() + h0 * D * 2, H * D * 2, ob.data_ptr(), hc * D * 2, hc * D * 2,
