@@ -388,11 +388,12 @@ def head_chunks(H: int, chunk_heads=None, tiles_per_head: int | None = None,
     hides, so the default ramps: e and 2e heads first, 2e and e last, with
     e = H/56 rounded (at least 1).  A chunk's attention takes about five
     times as long as the copy of as many heads (73397 tokens on a GB300), so
-    each chunk still hides the next one's copy.  The chunks between take h
-    heads each, h in [H/8, H/4] chosen so that h * tiles_per_head fills whole
-    waves of `sms` CTAs best, the smaller h on a tie (with 287 tile pairs per
-    head on 152 SMs, 9 heads make exactly 17 waves); without those figures,
-    about a quarter of H."""
+    each chunk still hides the next one's copy; hence also h <= 10 e below.
+    The chunks between take h heads each, h in [H/8, min(H/4, 10 e)] chosen
+    so that h * tiles_per_head fills whole waves of `sms` CTAs best, the
+    larger h on a tie (fewer chunks; with 287 tile pairs per head on 152 SMs,
+    9 heads make exactly 17 waves); without those figures, about a quarter
+    of H."""
     if chunk_heads is None:
         e = max(1, int(round(H / 56)))
         if H < 12:
@@ -403,7 +404,9 @@ def head_chunks(H: int, chunk_heads=None, tiles_per_head: int | None = None,
             def waste(n):
                 t = n * tiles_per_head
                 return (-(-t // sms) * sms) / t
-            h = min(range(max(1, H // 8), max(2, H // 4) + 1), key=lambda n: (round(waste(n), 4), n))
+            # at most 10 e heads: the 2e-head chunk before must hide its copy
+            hi = max(2, min(H // 4, 10 * e))
+            h = min(range(max(1, min(H // 8, hi)), hi + 1), key=lambda n: (round(waste(n), 4), -n))
         sizes = [e, 2 * e] + [h] * (mid // h) + ([mid % h] if mid % h else []) + [2 * e, e]
         return head_chunks(H, sizes)
     if isinstance(chunk_heads, int):
