@@ -18,6 +18,7 @@ OVC_ERR_WORKSPACE_TOO_SMALL = 3
 OVC_ERR_CUDA = 4
 OVC_ERR_TIMEOUT = 5
 OVC_ERR_SCRATCH_LIMIT = 6
+OVC_NOALLOC_MAX_HEADS = 4096
 OVC_PREPARE_SMOOTH_K = 1
 OVC_PREPARE_V_SMOOTH = 2
 OVC_ATTN_EXP_THEN_CAST = 1

@@ -648,7 +648,7 @@ const char* ovc_status_string(ovc_status s) {
     case OVC_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
     case OVC_ERR_CUDA: return "CUDA runtime error";
     case OVC_ERR_TIMEOUT: return "a device-side wait timed out";
-    case OVC_ERR_SCRATCH_LIMIT: return "scratch limit (reserved; no call returns it)";
+    case OVC_ERR_SCRATCH_LIMIT: return "B*H exceeds the fixed scratch of ovc_prepare_noalloc (OVC_NOALLOC_MAX_HEADS)";
   }
   return "unknown status";
 }
@@ -718,20 +718,39 @@ ovc_status ovc_memcpy2d(void* dst, size_t dpitch, const void* src, size_t spitch
 }  // extern "C"
 
 // ---------------------------------------------------------------------------
-// ovc_prepare_noalloc: ovc_prepare without any caller workspace for scratch.
-// The per-head amax of V accumulates in the caller's V-scale buffer (FP32 bit
-// patterns of non-negative values order like unsigned integers), and a last
-// launch turns it into the scale in place.
+// ovc_prepare_noalloc: ovc_prepare for callers that cannot allocate.  The
+// one piece of scratch the preparation needs beyond its outputs, the per-head
+// running amax of V, lives in a fixed array inside the library instead of in
+// caller workspace.
 // ---------------------------------------------------------------------------
 namespace ovc {
 namespace {
 
-__global__ void noalloc_scale_kernel(uint32_t* sv_bits, uint32_t* vamax_out, int n) {
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
-    const uint32_t bits = sv_bits[i];
-    if (vamax_out != nullptr) vamax_out[i] = bits;
-    sv_bits[i] = __float_as_uint(scale_from_amax(__uint_as_float(bits)).s);
+// The scratch: one FP32 amax (as ordered bits) per (batch, head).  Every GPU
+// that loads the library holds it until the process exits.
+static __device__ __align__(256) uint32_t g_noalloc_amax[OVC_NOALLOC_MAX_HEADS];
+
+// Device address of g_noalloc_amax on each device.  In host code the
+// symbol's name is only a host-side stand-in for the array, so the address a
+// kernel can use is looked up once per device, with that device current.
+uint32_t* g_noalloc_ptr[kMaxDevices] = {};
+std::mutex g_noalloc_mu;
+
+ovc_status noalloc_scratch(uint32_t** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return OVC_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_amax) != cudaSuccess || p == nullptr) return OVC_ERR_CUDA;
+    g_noalloc_ptr[dev] = static_cast<uint32_t*>(p);
   }
+  *out = g_noalloc_ptr[dev];
+  return OVC_OK;
+}
+
+__global__ void noalloc_copy_kernel(const uint32_t* scratch, uint32_t* dst, int n) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) dst[i] = scratch[i];
 }
 
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
@@ -751,18 +770,22 @@ extern "C" ovc_status ovc_prepare_noalloc(const ovc_tensor* q, const ovc_tensor*
   const int64_t nb = (q->S + 127) / 128;
   if (out->B != q->B || out->S != q->S || out->H != q->H || out->nb != nb || out->S_pad != nb * 128)
     return OVC_ERR_INVALID_ARG;
-  if (!out->q || !out->k || !out->vt || !out->sq || !out->sk || !out->sv || !out->energy) return OVC_ERR_INVALID_ARG;
-  if (!aligned16(out->q) || !aligned16(out->k) || !aligned16(out->vt)) return OVC_ERR_INVALID_ARG;
-  if (!aligned4(out->sq) || !aligned4(out->sk) || !aligned4(out->sv) || !aligned4(out->energy) ||
-      (out->vamax && !aligned4(out->vamax)))
+  if (!out->q || !out->k || !out->vt || !out->sq || !out->sk || !out->sv || !out->vamax || !out->energy)
     return OVC_ERR_INVALID_ARG;
-  if (out->vamax && reinterpret_cast<const void*>(out->vamax) == reinterpret_cast<const void*>(out->sv))
+  // A plain preparation: no V-Smooth means, no grouping order.
+  if (out->vmean || out->perm) return OVC_ERR_INVALID_ARG;
+  if (!aligned16(out->q) || !aligned16(out->k) || !aligned16(out->vt)) return OVC_ERR_INVALID_ARG;
+  if (!aligned4(out->sq) || !aligned4(out->sk) || !aligned4(out->sv) || !aligned4(out->vamax) ||
+      !aligned4(out->energy))
     return OVC_ERR_INVALID_ARG;
   const int64_t BH = q->B * q->H;
+  if (BH > OVC_NOALLOC_MAX_HEADS) return OVC_ERR_SCRATCH_LIMIT;
   DeviceState* dev = nullptr;
   ovc_status st = device_state(&dev);
   if (st != OVC_OK) return st;
-  uint32_t* amax = reinterpret_cast<uint32_t*>(out->sv);
+  uint32_t* scratch = nullptr;
+  st = noalloc_scratch(&scratch);
+  if (st != OVC_OK) return st;
 
   PrepParams P{};
   P.q = static_cast<const uint16_t*>(q->ptr);
@@ -786,17 +809,18 @@ extern "C" ovc_status ovc_prepare_noalloc(const ovc_tensor* q, const ovc_tensor*
   P.vt = out->vt;
   P.sq = out->sq;
   P.sk = out->sk;
-  P.sv = nullptr;             // written by noalloc_scale_kernel
-  P.vamax = amax;             // the V-scale buffer holds the amax meanwhile
+  P.sv = out->sv;
+  P.vamax = scratch;          // the fixed array instead of caller workspace
   P.energy = out->energy;
 
+  // The array keeps the previous call's maxima: clear this call's entries.
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int n = static_cast<int>(BH);
-  if (cudaMemsetAsync(amax, 0, static_cast<size_t>(BH) * 4, s) != cudaSuccess) return OVC_ERR_CUDA;
+  if (cudaMemsetAsync(scratch, 0, static_cast<size_t>(BH) * 4, s) != cudaSuccess) return OVC_ERR_CUDA;
   const dim3 g1(static_cast<unsigned>(BH), static_cast<unsigned>(nb), 3);
   prepare_qk_kernel<0><<<g1, 256, 0, s>>>(P);
   const dim3 g2(static_cast<unsigned>(BH), static_cast<unsigned>(nb), 1);
   prepare_v_kernel<false, false><<<g2, 512, 0, s>>>(P);
-  noalloc_scale_kernel<<<(n + 255) / 256, 256, 0, s>>>(amax, out->vamax, n);
+  noalloc_copy_kernel<<<(n + 255) / 256, 256, 0, s>>>(scratch, out->vamax, n);
   return launch_status();
 }

@@ -295,9 +295,7 @@ __global__ void __launch_bounds__(512) prepare_v_kernel(const __grid_constant__ 
 
   const float amax = __uint_as_float(P.vamax[bh]);
   const QScale sc = scale_from_amax(amax);
-  // sv == nullptr: the caller turns the amax into the scale after this launch
-  // (the amax may sit in the scale's own buffer).
-  if (j == 0 && threadIdx.x == 0 && P.sv != nullptr) P.sv[bh] = sc.s;
+  if (j == 0 && threadIdx.x == 0) P.sv[bh] = sc.s;
   constexpr bool vs = kVSmooth;
   float mu[8];
 #pragma unroll

@@ -50,7 +50,7 @@ typedef enum {
   OVC_ERR_WORKSPACE_TOO_SMALL = 3,  /* workspace_bytes below the *_workspace_bytes() figure */
   OVC_ERR_CUDA = 4,                 /* a CUDA runtime call failed */
   OVC_ERR_TIMEOUT = 5,              /* a device-side wait hit its limit */
-  OVC_ERR_SCRATCH_LIMIT = 6         /* reserved: no call returns it */
+  OVC_ERR_SCRATCH_LIMIT = 6         /* ovc_prepare_noalloc: B*H above its fixed scratch */
 } ovc_status;
 
 enum { OVC_BF16 = 0, OVC_FP16 = 1 };
@@ -240,23 +240,32 @@ typedef struct {
 ovc_status ovc_attention_probe(const ovc_prepared* p, const ovc_repair* r, float softmax_scale,
                                const ovc_output* o, const ovc_probe* probe, void* stream);
 
-/* ovc_prepare for callers that cannot allocate device memory -- no
- * counterpart in the paper; it exists for integration only.  Some hosts own
- * every device allocation themselves (plugin interfaces that lend a kernel
- * fixed buffers, or code on a latency-critical path where cudaMalloc is not
- * allowed), so they cannot provide the workspace that ovc_prepare asks for.
- * This entry point computes exactly what ovc_prepare computes, allocates
- * nothing and keeps no state: its only scratch, the per-head running amax of
- * V, accumulates in the caller's sv buffer (as FP32 bit patterns), which the
- * call's last kernel turns into the V scales in place.
+/* ovc_prepare for callers that cannot allocate device memory -- the paper
+ * has no counterpart; it exists for integration only.  Some callers cannot
+ * call cudaMalloc or provide the workspace that ovc_prepare asks for: plugin
+ * interfaces whose host owns every device allocation and lends a kernel only
+ * fixed input and output buffers, or code on a latency-critical or captured
+ * path where allocation is not allowed.  This entry point computes exactly
+ * what ovc_prepare computes and allocates nothing (no cudaMalloc, cudaFree or
+ * allocating library routine): the only scratch it needs beyond its outputs,
+ * the per-head running amax of V, lives in a fixed device array of
+ * OVC_NOALLOC_MAX_HEADS 32-bit entries inside the library, which every GPU
+ * that loads the library holds until the process exits.
  *   out: filled in by the caller: B, S, H, nb = ceil(S/128), S_pad = 128*nb,
- *        and the output buffers q, k, vt (16-byte aligned), sq, sk, sv,
- *        energy (4-byte aligned), in the layouts of ovc_prepared.  vamax may be
- *        NULL; if set (a buffer other than sv), it receives the per-head amax
- *        bits (needed by ovc_prepare_v_repair).  The struct is then usable with
- *        ovc_attention like one filled by ovc_prepare.
- * Calls share nothing, so calls on different streams may overlap.  The launch
- * sequence is a memset and three kernels on `stream`, all capturable. */
+ *        and the output buffers q, k, vt (16-byte aligned), sq, sk, sv, vamax,
+ *        energy (4-byte aligned), in the layouts of ovc_prepared; vmean and
+ *        perm must be NULL.  The struct is then usable with ovc_attention and
+ *        ovc_prepare_v_repair like one filled by ovc_prepare.
+ * Errors: OVC_ERR_SCRATCH_LIMIT if B*H > OVC_NOALLOC_MAX_HEADS (nothing is
+ * launched); OVC_ERR_INVALID_ARG for a NULL or misaligned buffer, a vmean or
+ * perm that is not NULL, or dimensions that do not match the inputs.
+ * The first call on a device looks up the array's device address on that
+ * device (cudaGetSymbolAddress); make that first call before any stream
+ * capture.  Every call shares the one array, which keeps the last call's
+ * contents (each call clears the entries it uses first), so calls whose
+ * kernels could overlap on the GPU race: issue them on one stream or
+ * otherwise serialise them. */
+#define OVC_NOALLOC_MAX_HEADS 4096
 ovc_status ovc_prepare_noalloc(const ovc_tensor* q, const ovc_tensor* k, const ovc_tensor* v,
                                const ovc_prepared* out, void* stream);
 
