@@ -6,9 +6,9 @@ the package does not load the library; the first call does, and fails loudly
 if it has not been built.
 """
 from .api import (CapturedAttention, OvcError, Prepared, Repair, attention, attention_prepared, attention_probe,
-                  attention_v_repair, attention_workspace_bytes, attn_flags, auto_split, group_v, device_status, flops, prepare, prepare_v_repair,
+                  attention_v_repair, attention_workspace_bytes, attn_flags, group_v, device_status, flops, prepare, prepare_v_repair,
                   prepare_workspace_bytes, repair_workspace_bytes, baseline_attention)
 
 __all__ = ["CapturedAttention", "OvcError", "Prepared", "Repair", "attention", "attention_prepared", "attention_probe",
-           "attention_v_repair", "attention_workspace_bytes", "attn_flags", "auto_split", "group_v", "device_status", "flops", "prepare", "prepare_v_repair",
+           "attention_v_repair", "attention_workspace_bytes", "attn_flags", "group_v", "device_status", "flops", "prepare", "prepare_v_repair",
            "prepare_workspace_bytes", "repair_workspace_bytes", "baseline_attention"]

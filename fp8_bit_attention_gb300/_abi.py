@@ -21,6 +21,7 @@ OVC_ERR_SCRATCH_LIMIT = 6
 OVC_NOALLOC_MAX_HEADS = 4096
 OVC_PREPARE_SMOOTH_K = 1
 OVC_PREPARE_V_SMOOTH = 2
+OVC_PREPARE_SMOOTH_Q = 4
 OVC_ATTN_EXP_THEN_CAST = 1
 OVC_ATTN_NATURAL_ORDER = 2
 OVC_ATTN_BASELINE = 3
@@ -40,12 +41,14 @@ class OvcOutput(ctypes.Structure):
 class OvcPrepared(ctypes.Structure):
     _fields_ = [("B", c_i64), ("S", c_i64), ("H", c_i64), ("nb", c_i64), ("S_pad", c_i64),
                 ("q", c_ptr), ("k", c_ptr), ("vt", c_ptr), ("sq", c_ptr), ("sk", c_ptr),
-                ("sv", c_ptr), ("vamax", c_ptr), ("energy", c_ptr), ("vmean", c_ptr), ("perm", c_ptr)]
+                ("sv", c_ptr), ("vamax", c_ptr), ("energy", c_ptr), ("vmean", c_ptr), ("perm", c_ptr),
+                ("kbias", c_ptr)]
 
 
 class OvcRepair(ctypes.Structure):
     _fields_ = [("B", c_i64), ("S", c_i64), ("H", c_i64), ("n", c_i64), ("n_pad", c_i64),
-                ("idx", c_ptr), ("k_sel", c_ptr), ("dvt", c_ptr), ("sk_sel", c_ptr), ("sr", c_ptr)]
+                ("idx", c_ptr), ("k_sel", c_ptr), ("dvt", c_ptr), ("sk_sel", c_ptr), ("sr", c_ptr),
+                ("kb_sel", c_ptr)]
 
 
 class OvcProbe(ctypes.Structure):
@@ -64,7 +67,6 @@ SIGNATURES = {
     "ovc_attention_ex": (c_i32, [P(OvcPrepared), P(OvcRepair), ctypes.c_float, P(OvcOutput),
                                  ctypes.c_uint32, c_i32, c_ptr, ctypes.c_size_t, c_ptr]),
     "ovc_attention_workspace_bytes": (ctypes.c_size_t, [P(OvcPrepared), c_i32]),
-    "ovc_attention_auto_split": (c_i32, [c_i64, c_i64, c_i64]),
     "ovc_repair_workspace_bytes": (ctypes.c_size_t, [c_i64, c_i64, c_i64, ctypes.c_float]),
     "ovc_prepare_v_repair": (c_i32, [P(OvcTensor), P(OvcPrepared), ctypes.c_float, c_ptr,
                                      ctypes.c_size_t, P(OvcRepair), c_ptr]),

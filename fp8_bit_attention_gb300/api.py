@@ -128,6 +128,14 @@ class Prepared:
         d = self.desc
         return _view(self.workspace, d.energy, 4 * d.B * d.H * d.S).view(torch.float32).view(d.B, d.H, d.S)
 
+    def key_bias(self):
+        """Q smoothing's key bias rows, BF16 [B,H,S_pad,16] (None without it)."""
+        d = self.desc
+        if not d.kbias:
+            return None
+        return _view(self.workspace, d.kbias, 32 * d.B * d.H * d.S_pad).view(torch.bfloat16).view(
+            d.B, d.H, d.S_pad, 16)
+
     def v_means(self):
         """V-Smooth's restored block means M'_b, BF16 [B,H,128,nbk] (None without V-Smooth)."""
         d = self.desc
@@ -163,18 +171,22 @@ class Repair:
         return _view(self.workspace, d.sr, 4 * d.B * d.H).view(torch.float32).view(d.B, d.H)
 
 
-def prepare_workspace_bytes(B: int, S: int, H: int, *, smooth_k: bool = False, v_smooth: bool = False) -> int:
-    return int(lib().ovc_prepare_workspace_bytes_ex(B, S, H, 128, _prep_flags(smooth_k, v_smooth)))
+def prepare_workspace_bytes(B: int, S: int, H: int, *, smooth_k: bool = False, v_smooth: bool = False,
+                            smooth_q: bool = False) -> int:
+    return int(lib().ovc_prepare_workspace_bytes_ex(B, S, H, 128, _prep_flags(smooth_k, v_smooth, smooth_q)))
 
 
-def _prep_flags(smooth_k: bool, v_smooth: bool = False) -> int:
-    return (_abi.OVC_PREPARE_SMOOTH_K if smooth_k else 0) | (_abi.OVC_PREPARE_V_SMOOTH if v_smooth else 0)
+def _prep_flags(smooth_k: bool, v_smooth: bool = False, smooth_q: bool = False) -> int:
+    return ((_abi.OVC_PREPARE_SMOOTH_K if smooth_k else 0) | (_abi.OVC_PREPARE_V_SMOOTH if v_smooth else 0) |
+            (_abi.OVC_PREPARE_SMOOTH_Q if smooth_q else 0))
 
 
-def group_v(v: torch.Tensor, clusters: int = 16, iters: int = 4, *, stream=None) -> torch.Tensor:
+def group_v(v: torch.Tensor, clusters: int = 16, iters: int = 4, *, stream=None, return_state: bool = False):
     """V-Smooth's grouping (ovc_vsmooth_group): k-means over each head's value
     tokens, returned as the token order perm [B,H,S] (int32, CUDA) for
-    ``prepare(..., perm=perm)``."""
+    ``prepare(..., perm=perm)``.  return_state=True also returns the last
+    assignment step's labels [B,H,S] (int32) and the centroids it used
+    [B,H,C,128] (float32), views of the call's workspace."""
     dev = _device_of(v, stream=stream)
     with torch.cuda.device(dev):
         tv = _tensor_desc(v)
@@ -186,24 +198,32 @@ def group_v(v: torch.Tensor, clusters: int = 16, iters: int = 4, *, stream=None)
         check(lib().ovc_vsmooth_group(ctypes.byref(tv), int(clusters), int(iters), ctypes.c_void_p(ws.data_ptr()),
                                       ws.numel(), ctypes.c_void_p(perm.data_ptr()),
                                       ctypes.c_void_p(_stream_handle(stream))), "ovc_vsmooth_group")
-        return perm
+        if not return_state:
+            return perm
+        ncent = tv.B * tv.H * int(clusters) * 128 * 4
+        cent = ws[:ncent].view(torch.float32).view(tv.B, tv.H, int(clusters), 128)
+        off = -(-ncent // 256) * 256
+        labels = ws[off:off + 4 * tv.B * tv.H * tv.S].view(torch.int32).view(tv.B, tv.H, tv.S)
+        return perm, labels, cent
 
 
 def prepare(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, smooth_k: bool = False,
             v_smooth: bool = False, perm: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
-            stream=None) -> Prepared:
+            stream=None, smooth_q: bool = False) -> Prepared:
     """Quantise Q/K (per 128-token block) and V (per head) to E4M3
     (ovc_prepare_ex).  smooth_k subtracts K's channel means first (optional
     K smoothing; exact non-causal attention is unchanged by it).  v_smooth
     quantises V's residuals after each 128-token block's mean and keeps the
     means for attention to restore (V-Smooth; no repair with it).  perm
     [B,H,S] int32 (e.g. from :func:`group_v`): K and V are taken in that
-    token order (ovc_prepare_grouped); Q and so O keep theirs."""
+    token order (ovc_prepare_grouped); Q and so O keep theirs.  smooth_q
+    subtracts Q's channel means and adds each key's bias mu_q . k back in
+    attention (Q smoothing; not with v_smooth)."""
     dev = _device_of(q, k, v, perm, workspace, stream=stream)
     with torch.cuda.device(dev):
         tq, tk, tv = _tensor_desc(q), _tensor_desc(k), _tensor_desc(v)
-        flags = _prep_flags(smooth_k, v_smooth)
-        nbytes = prepare_workspace_bytes(tq.B, tq.S, tq.H, smooth_k=smooth_k, v_smooth=v_smooth)
+        flags = _prep_flags(smooth_k, v_smooth, smooth_q)
+        nbytes = prepare_workspace_bytes(tq.B, tq.S, tq.H, smooth_k=smooth_k, v_smooth=v_smooth, smooth_q=smooth_q)
         if nbytes == 0:
             raise ValueError(f"unsupported shape {tuple(q.shape)}")
         if workspace is None:
@@ -238,14 +258,8 @@ def attn_flags(exp_then_cast: bool = False, natural_order: bool = False) -> int:
         _abi.OVC_ATTN_NATURAL_ORDER if natural_order else 0)
 
 
-def auto_split(B: int, S: int, H: int) -> int:
-    """Key ranges the library splits each tile into for these dimensions on
-    the current device when left to choose (1: no split)."""
-    return int(lib().ovc_attention_auto_split(int(B), int(S), int(H)))
-
-
-def attention_workspace_bytes(prep: Prepared, nsplit: int = 0) -> int:
-    """Workspace of split key ranges (0: no split; nsplit = 0: automatic)."""
+def attention_workspace_bytes(prep: Prepared, nsplit: int = 1) -> int:
+    """Workspace of split key ranges (0 when nsplit is 0 or 1: no split)."""
     return int(lib().ovc_attention_workspace_bytes(ctypes.byref(prep.desc), int(nsplit)))
 
 
@@ -254,22 +268,22 @@ def attention_prepared(prep: Prepared, *, softmax_scale: float | None = None,
                        rep: "Repair | None" = None, nsplit: int | None = None,
                        workspace: torch.Tensor | None = None) -> torch.Tensor:
     """O from prepared inputs (ovc_attention_ex): kernel variant ``flags`` (see
-    :func:`attn_flags`), optional repair set, and split key ranges for short
-    sequences -- ``nsplit=None`` lets the library choose and allocates the
-    workspace it needs here; ``nsplit=1`` never splits."""
+    :func:`attn_flags`), optional repair set.  ``nsplit`` > 1 asks for split
+    key ranges, a different computation from the method's single pass (each
+    range takes its bytes against its own reference) that only the caller
+    chooses; ``None``, 0 and 1 never split, and the result is then
+    ovc_attention's bit for bit."""
     dev = _device_of(prep.workspace, out, workspace, None if rep is None else rep.workspace, stream=stream)
     with torch.cuda.device(dev):
         out = _out_for(prep, out)
         od = _output_desc(out, prep)
         h = ctypes.c_void_p(_stream_handle(stream))
-        ns = 0 if nsplit is None else int(nsplit)
-        if rep is not None and nsplit is None:
-            ns = 1
-        need = attention_workspace_bytes(prep, ns) if ns != 1 else 0
+        ns = 1 if nsplit is None else int(nsplit)
+        need = attention_workspace_bytes(prep, ns) if ns > 1 else 0
         if need and (workspace is None or workspace.numel() < need):
             workspace = torch.empty(need, dtype=torch.uint8, device=prep.workspace.device)
         wp = workspace.data_ptr() if (need and workspace is not None) else None
-        if need == 0 and flags == 0 and rep is None:
+        if ns <= 1 and flags == 0 and rep is None:
             check(lib().ovc_attention(ctypes.byref(prep.desc), float(softmax_scale or 0.0), ctypes.byref(od), h),
                   "ovc_attention")
             return out
@@ -421,15 +435,15 @@ def head_chunks(H: int, chunk_heads=None, tiles_per_head: int | None = None,
     return list(zip(bounds[:-1], bounds[1:]))
 
 
-def _attention_device(q, k, v, softmax_scale, repair_budget, out, smooth_k=False):
-    prep = prepare(q, k, v, smooth_k=smooth_k)
+def _attention_device(q, k, v, softmax_scale, repair_budget, out, smooth_k=False, smooth_q=False):
+    prep = prepare(q, k, v, smooth_k=smooth_k, smooth_q=smooth_q)
     if repair_budget:
         rep = prepare_v_repair(v, prep, repair_budget)
         return attention_v_repair(prep, rep, softmax_scale=softmax_scale, out=out)
     return attention_prepared(prep, softmax_scale=softmax_scale, out=out)
 
 
-def _attention_host(q, k, v, softmax_scale, repair_budget, out, dev, chunk_heads, smooth_k=False):
+def _attention_host(q, k, v, softmax_scale, repair_budget, out, dev, chunk_heads, smooth_k=False, smooth_q=False):
     """Host-resident inputs streamed through the GPU in head chunks.
 
     Every head is computed independently (its V scale, residual ranking and
@@ -464,11 +478,16 @@ def _attention_host(q, k, v, softmax_scale, repair_budget, out, dev, chunk_heads
     n_el = B * S * hmax * D
     stage_in = [[torch.empty(n_el, dtype=q4.dtype, device=dev) for _ in range(3)] for _ in range(2)]
     stage_out = [torch.empty(n_el, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    # The staging buffers come from the caching allocator on the current
+    # stream (comps[0]); a block freed by work still pending there may be
+    # handed out, so the other streams start only after that work.
+    for s in (s_in, s_out, comps[1]):
+        s.wait_stream(comps[0])
     in_free = [None, None]      # compute has consumed the set's inputs
     out_free = [None, None]     # the set's output has been copied out
     try:
         _stream_chunks(q4, k4, v4, o4, chunks, stage_in, stage_out, in_free, out_free, comps, s_in, s_out,
-                       softmax_scale, repair_budget, smooth_k)
+                       softmax_scale, repair_budget, smooth_k, smooth_q)
     finally:
         # The staging buffers die with this frame: let every stream finish with them.
         s_out.synchronize()
@@ -479,12 +498,9 @@ def _attention_host(q, k, v, softmax_scale, repair_budget, out, dev, chunk_heads
 
 
 def _stream_chunks(q4, k4, v4, o4, chunks, stage_in, stage_out, in_free, out_free, comps, s_in, s_out,
-                   softmax_scale, repair_budget, smooth_k):
+                   softmax_scale, repair_budget, smooth_k, smooth_q):
     B, S, H, D = q4.shape
     el = q4.element_size()
-    # The key-range split of the whole-tensor call, so that the chunks give its
-    # result bit for bit.
-    nsplit = auto_split(B, S, H)
     for c, (h0, h1) in enumerate(chunks):
         hc, st = h1 - h0, c % 2
         ins = [buf[:B * S * hc * D].view(B, S, hc, D) for buf in stage_in[st]]
@@ -499,7 +515,7 @@ def _stream_chunks(q4, k4, v4, o4, chunks, stage_in, stage_out, in_free, out_fre
         comp = comps[st]             # staging set st and compute stream st go together
         with torch.cuda.stream(comp):
             comp.wait_event(ready)
-            prep = prepare(*ins, smooth_k=smooth_k)
+            prep = prepare(*ins, smooth_k=smooth_k, smooth_q=smooth_q)
             rep = prepare_v_repair(ins[2], prep, repair_budget) if repair_budget else None
             in_free[st] = torch.cuda.Event()
             in_free[st].record(comp)
@@ -509,7 +525,7 @@ def _stream_chunks(q4, k4, v4, o4, chunks, stage_in, stage_out, in_free, out_fre
             if rep is not None:
                 attention_v_repair(prep, rep, softmax_scale=softmax_scale, out=ob)
             else:
-                attention_prepared(prep, softmax_scale=softmax_scale, out=ob, nsplit=nsplit)
+                attention_prepared(prep, softmax_scale=softmax_scale, out=ob)
             done = torch.cuda.Event()
             done.record(comp)
         with torch.cuda.stream(s_out):
@@ -522,7 +538,8 @@ def _stream_chunks(q4, k4, v4, o4, chunks, stage_in, stage_out, in_free, out_fre
 
 def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, softmax_scale: float | None = None,
               repair_budget: float | None = None, out: torch.Tensor | None = None,
-              device=None, chunk_heads: int | None = None, smooth_k: bool = False) -> torch.Tensor:
+              device=None, chunk_heads: int | None = None, smooth_k: bool = False,
+              smooth_q: bool = False) -> torch.Tensor:
     """Full call: prepare + ExpCast attention (+ optional V residual repair).
 
     CUDA inputs give a CUDA output (asynchronous on the current stream).  CPU
@@ -531,7 +548,7 @@ def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, softmax_scal
     sizes, or None for the default plan of :func:`head_chunks`), so that
     host<->device copies overlap the computation; O
     lands in `out` (or a new pinned tensor), complete when the call returns.
-    smooth_k: optional K smoothing in prepare (see `prepare`).
+    smooth_k, smooth_q: optional K and Q smoothing in prepare (see `prepare`).
 
     Empty inputs (B, S or H of 0: no query rows) give an empty output
     without a launch; the C ABI itself rejects zero sizes."""
@@ -545,10 +562,10 @@ def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, softmax_scal
             raise ValueError("out must be a bfloat16 tensor shaped like q")
         return out
     if q.is_cuda:
-        return _attention_device(q, k, v, softmax_scale, repair_budget, out, smooth_k)
+        return _attention_device(q, k, v, softmax_scale, repair_budget, out, smooth_k, smooth_q)
     dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
     with torch.cuda.device(dev):
-        return _attention_host(q, k, v, softmax_scale, repair_budget, out, dev, chunk_heads, smooth_k)
+        return _attention_host(q, k, v, softmax_scale, repair_budget, out, dev, chunk_heads, smooth_k, smooth_q)
 
 
 class CapturedAttention:
@@ -599,6 +616,6 @@ def flops(B: int, S: int, H: int, D: int = 128) -> float:
 
 
 __all__ = ["Prepared", "Repair", "OvcError", "CapturedAttention", "prepare", "attention_prepared", "attention_workspace_bytes",
-           "auto_split", "group_v", "prepare_v_repair",
+           "group_v", "prepare_v_repair",
            "attention_v_repair", "attention_probe", "device_status", "attention", "memcpy2d",
            "head_chunks", "prepare_workspace_bytes", "repair_workspace_bytes", "flops"]

@@ -65,6 +65,7 @@ constexpr uint32_t kTile = 128 * 128;                       // bytes of one E4M3
 constexpr uint32_t kIdesc = idesc_e4m3_f32(128, 128);
 constexpr uint32_t kIdescBf16 = idesc_bf16_f32(128, 128);
 constexpr uint32_t kMeanTile = 128 * 16 * 2;               // bytes of one M' tile: 128 channels x 16 blocks BF16
+constexpr uint32_t kBiasTile = 128 * 16 * 2;               // bytes of one Q-smoothing operand tile: 128 rows x 16 BF16
 constexpr float kMagic = 12582912.0f;                       // 1.5 * 2^23
 // ExpCast constants: c0 = 120 (stored value 2^8 p), beta = -0.35, tau = 0.75.
 constexpr float kCodeBase = 119.0f;                         // floor(c0 + beta)
@@ -93,6 +94,9 @@ struct AttnParams {
   int32_t n_rep, n_rep_pad, rep_blocks;
   const float* sk_sel;
   const float* sr;
+  // Q smoothing: each key's bias tile rides with its key block (TMA) and one
+  // BF16 MMA per block adds beta_j / s_q to the scores (0: off)
+  int32_t qbias;
   // probe
   int64_t dump_bh, dump_qb, dump_kb;
   uint8_t* dump_codes;
@@ -135,11 +139,17 @@ struct AttnSmem {
   uint64_t m_full[2], m_empty[2];
   alignas(1024) uint8_t mv[2][kMeanTile];   // M' tiles of two runs, 32-byte swizzle
   float lbuf[2][16][128];                   // pending block row sums [tile][block mod 16][row]
+  // Q smoothing only (never with V-Smooth; launched with the whole struct):
+  uint64_t a_full[2];                        // the tiles' A operands are written
+  alignas(1024) uint8_t kb[kStages][kBiasTile];   // key bias rows of each stage's keys (32-byte swizzle)
+  alignas(1024) uint8_t ab[2][kBiasTile];         // per query tile: 128 rows of (hi, lo) parts of 1/s_q
 };
 
 // Dynamic shared memory of a launch, + 1024 bytes of alignment slack.
 constexpr size_t kAttnSmemBytes = offsetof(AttnSmem, m_full) + 1024;
-constexpr size_t kAttnSmemBytesVSmooth = sizeof(AttnSmem) + 1024;
+constexpr size_t kAttnSmemBytesVSmooth = offsetof(AttnSmem, a_full) + 1024;
+constexpr size_t kAttnSmemBytesQBias = sizeof(AttnSmem) + 1024;
+static_assert(kAttnSmemBytesQBias <= 232448, "shared memory per CTA");
 
 __device__ __forceinline__ void record_abort(AttnSmem& sm, const AttnParams& P) {
   if (!*reinterpret_cast<volatile int*>(&sm.abort)) atomicOr(P.status, kStatusTimeout);
@@ -400,6 +410,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_ks,
                      const __grid_constant__ CUtensorMap tm_dv, const __grid_constant__ CUtensorMap tm_vm,
+                     const __grid_constant__ CUtensorMap tm_kb, const __grid_constant__ CUtensorMap tm_kbs,
                      const __grid_constant__ AttnParams P) {
   extern __shared__ uint8_t smem_raw[];
   AttnSmem& sm = *reinterpret_cast<AttnSmem*>(
@@ -428,6 +439,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         mbar_init(smem_addr(&sm.m_full[r]), 1);
         mbar_init(smem_addr(&sm.m_empty[r]), 1);
       }
+    if (!(kVar & kVarVSmooth) && P.qbias)
+      for (int t = 0; t < 2; ++t) mbar_init(smem_addr(&sm.a_full[t]), 128);
     sm.abort = 0;
     sm.zero = 0;
     fence_mbar_init();
@@ -468,11 +481,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (!ok) break;
           }
           const uint32_t kbar = smem_addr(&sm.k_full[stage]), vbar = smem_addr(&sm.v_full[stage]);
-          mbar_arrive_expect_tx(kbar, kTile);
+          const bool qbias = !(kVar & kVarVSmooth) && P.qbias;
+          mbar_arrive_expect_tx(kbar, qbias ? kTile + kBiasTile : kTile);
           mbar_arrive_expect_tx(vbar, kTile);
           if (i < uc.nbu) {
             const int j = key_block<kVar>(i, uc.b0, uc.nbu);
             tma_load_2d(smem_addr(sm.k[stage]), &tm_k, kbar, 0, tc.bh * P.S_pad + j * 128);
+            if (qbias) tma_load_2d(smem_addr(sm.kb[stage]), &tm_kb, kbar, 0, tc.bh * P.S_pad + j * 128);
             tma_load_2d(smem_addr(sm.v[stage]), &tm_v, vbar, j * 128, tc.bh * 128);
             if ((kVar & kVarVSmooth) && starts_run<kVar>(i, uc.b0, uc.nbu)) {
               // The M' tile of the run this block starts: channels of this head, blocks of its chunk.
@@ -489,6 +504,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           } else {
             const int r = i - uc.nbu;
             tma_load_2d(smem_addr(sm.k[stage]), &tm_ks, kbar, 0, tc.bh * P.n_rep_pad + r * 128);
+            if (qbias) tma_load_2d(smem_addr(sm.kb[stage]), &tm_kbs, kbar, 0, tc.bh * P.n_rep_pad + r * 128);
             tma_load_2d(smem_addr(sm.v[stage]), &tm_dv, vbar, r * 128, tc.bh * 128);
           }
           ++kv_iter;
@@ -524,12 +540,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const uint32_t tS0 = tmem + 0, tS1 = tmem + 128;
       const uint32_t tO0 = tmem + 256, tO1 = tmem + 384;
       const uint64_t qd0 = sw128_desc(smem_addr(sm.q[0])), qd1 = sw128_desc(smem_addr(sm.q[1]));
+      // Q smoothing: after S_t = Q_t K^T, one BF16 MMA adds (1/s_q)(beta_j)
+      // from the tile's A operand and the stage's key bias rows.
+      const bool qbias = !(kVar & kVarVSmooth) && P.qbias;
+      uint64_t abd0 = 0, abd1 = 0;
+      if (qbias) {
+        abd0 = sw32_desc(smem_addr(sm.ab[0]));
+        abd1 = sw32_desc(smem_addr(sm.ab[1]));
+      }
       for (int u = blockIdx.x; u < P.nunits && ok; u += gridDim.x) {
         const UnitCoord ucm = unit_coord<kVar>(P, u);
         const int nbu = ucm.nbu, b0 = ucm.b0;
         const int nblk = nbu + P.rep_blocks;
         ok = mbar_wait(smem_addr(&sm.q_full), q_iter & 1, tmo, abort_flag);
         if (!ok) break;
+        if (qbias) {
+          ok = mbar_wait(smem_addr(&sm.a_full[0]), q_iter & 1, tmo, abort_flag) &&
+               mbar_wait(smem_addr(&sm.a_full[1]), q_iter & 1, tmo, abort_flag);
+          if (!ok) break;
+        }
         // Scores of the first block for both query tiles.
         {
           const uint32_t stage = kv_iter % kStages;
@@ -537,11 +566,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           if (!ok) break;
           tc_fence_after();
           const uint64_t kd = sw128_desc(smem_addr(sm.k[stage]));
+          const uint64_t kbd = qbias ? sw32_desc(smem_addr(sm.kb[stage])) : 0;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) mma_f8_ss(tS0, qd0 + 2 * kk, kd + 2 * kk, kIdesc, kk > 0);
+          if (qbias) mma_bf16_ss(tS0, abd0, kbd, kIdescBf16, 1u);
           tc_commit(smem_addr(&sm.s_full[0]));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) mma_f8_ss(tS1, qd1 + 2 * kk, kd + 2 * kk, kIdesc, kk > 0);
+          if (qbias) mma_bf16_ss(tS1, abd1, kbd, kIdescBf16, 1u);
           tc_commit(smem_addr(&sm.s_full[1]));
           issued = true;
         }
@@ -593,6 +625,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             kd_next = sw128_desc(smem_addr(sm.k[nstage]));
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) mma_f8_ss(tS0, qd0 + 2 * kk, kd_next + 2 * kk, kIdesc, kk > 0);
+            if (qbias) mma_bf16_ss(tS0, abd0, sw32_desc(smem_addr(sm.kb[nstage])), kIdescBf16, 1u);
             tc_commit(smem_addr(&sm.s_full[0]));
           } else {
             tc_commit(smem_addr(&sm.o_full[0]));
@@ -620,6 +653,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           if (!last) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) mma_f8_ss(tS1, qd1 + 2 * kk, kd_next + 2 * kk, kIdesc, kk > 0);
+            if (qbias) mma_bf16_ss(tS1, abd1, sw32_desc(smem_addr(sm.kb[nstage])), kIdescBf16, 1u);
             tc_commit(smem_addr(&sm.s_full[1]));
           } else {
             tc_commit(smem_addr(&sm.o_full[1]));
@@ -664,6 +698,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       float kf = -INFINITY;                     // reference m8 = kf + frac(c0+beta)
       float l = 0.0f;
       const bool dump_tile = (P.dump_codes != nullptr) && tc.bh == P.dump_bh && qb == P.dump_qb && store;
+      if (!(kVar & kVarVSmooth) && P.qbias) {
+        // Q smoothing: this row of the tile's A operand, the BF16 pair
+        // (hi, lo) of 1/s_q twice, (hi, hi, lo, lo, 0, 0, 0, 0) in every
+        // 16-byte chunk (the same in every row and chunk, so the 32-byte
+        // swizzle of the operand changes nothing).  The previous unit's
+        // MMAs have completed (its epilogue waited for them).
+        const float x = __frcp_rn(sq);
+        const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+        const uint32_t hh = static_cast<uint32_t>(__bfloat16_as_ushort(hi)) * 0x10001u;
+        const uint32_t ll = static_cast<uint32_t>(__bfloat16_as_ushort(lo)) * 0x10001u;
+        uint4* a = reinterpret_cast<uint4*>(sm.ab[t] + row * 32);
+        a[0] = make_uint4(hh, ll, 0u, 0u);
+        a[1] = make_uint4(hh, ll, 0u, 0u);
+        fence_proxy_async_smem();
+        mbar_arrive(smem_addr(&sm.a_full[t]));
+      }
       // Key scale of the current block, loaded one block ahead.
       float sk_next = __ldg(P.sk + tc.bh * P.nb + key_block<kVar>(0, uc.b0, uc.nbu));
       for (int i = 0; i < nblk; ++i) {

@@ -33,6 +33,7 @@ const decltype(&attention_kernel<0>) kAttentionKernels[kNumVariants] = {
     attention_kernel<5>, attention_kernel<6>, attention_kernel<7>, attention_kernel<kVarVSmooth>};
 
 constexpr int kMaxDevices = 64;
+constexpr uint32_t kPrepareFlags = OVC_PREPARE_SMOOTH_K | OVC_PREPARE_V_SMOOTH | OVC_PREPARE_SMOOTH_Q;
 constexpr uint64_t kDefaultTimeoutNs = 4000000000ull;   // 4 s per wait
 
 struct DeviceState {
@@ -61,7 +62,7 @@ ovc_status device_state(DeviceState** out) {
     if (d.supported) {
       for (int v = 0; v < kNumVariants; ++v)
         if (cudaFuncSetAttribute(kAttentionKernels[v], cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(v == kVarVSmooth ? kAttnSmemBytesVSmooth : kAttnSmemBytes)) !=
+                                 static_cast<int>(v == kVarVSmooth ? kAttnSmemBytesVSmooth : kAttnSmemBytesQBias)) !=
             cudaSuccess)
           return OVC_ERR_CUDA;
       if (cudaFuncSetAttribute(kmeans_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -120,6 +121,20 @@ bool make_mean_map(CUtensorMap* m, const void* base, uint64_t nb, uint64_t rows,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Q smoothing's key bias rows [rows][16] BF16 (32 bytes a key): 16 x 128
+// boxes with the 32-byte swizzle, the B operand layout of the bias MMA.
+bool make_bias_map(CUtensorMap* m, const void* base, uint64_t rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {16, rows};
+  cuuint64_t strides[1] = {32};
+  cuuint32_t box[2] = {16, 128};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -133,7 +148,7 @@ bool dims_ok(int64_t B, int64_t S, int64_t H) {
 }
 
 struct PrepLayout {
-  size_t q, k, vt, sq, sk, sv, vamax, energy, kpart, kmean, vmu, vmean, total;
+  size_t q, k, vt, sq, sk, sv, vamax, energy, kpart, kmean, vmu, vmean, qpart, qmean, kbias, total;
 };
 
 PrepLayout prep_layout(int64_t B, int64_t S, int64_t H, uint32_t flags = 0) {
@@ -160,6 +175,11 @@ PrepLayout prep_layout(int64_t B, int64_t S, int64_t H, uint32_t flags = 0) {
   if (flags & OVC_PREPARE_V_SMOOTH) {
     L.vmu = take(static_cast<size_t>(BH) * nb * 128 * 4);
     L.vmean = take(static_cast<size_t>(BH) * 128 * ((nb + 15) / 16 * 16) * 2);
+  }
+  if (flags & OVC_PREPARE_SMOOTH_Q) {
+    L.qpart = take(static_cast<size_t>(BH) * nb * 128 * 4);
+    L.qmean = take(static_cast<size_t>(BH) * 128 * 4);
+    L.kbias = take(static_cast<size_t>(BH) * S_pad * 32);
   }
   L.total = off;
   return L;
@@ -196,7 +216,7 @@ GroupLayout group_layout(int64_t B, int64_t S, int64_t H, int64_t C) {
 }
 
 struct RepLayout {
-  size_t idx, k_sel, dvt, sk_sel, sr, total;
+  size_t idx, k_sel, dvt, sk_sel, sr, kb_sel, total;
 };
 
 RepLayout rep_layout(int64_t B, int64_t H, int64_t n) {
@@ -213,6 +233,7 @@ RepLayout rep_layout(int64_t B, int64_t H, int64_t n) {
   L.dvt = take(static_cast<size_t>(BH) * n_pad * 128);
   L.sk_sel = take(static_cast<size_t>(BH) * n_pad * 4);
   L.sr = take(static_cast<size_t>(BH) * 4);
+  L.kb_sel = take(static_cast<size_t>(BH) * n_pad * 32);   // used with Q smoothing only
   L.total = off;
   return L;
 }
@@ -240,12 +261,11 @@ bool output_ok(const ovc_output* o) {
 
 ovc_status launch_status() { return cudaGetLastError() == cudaSuccess ? OVC_OK : OVC_ERR_CUDA; }
 
-// Split key ranges (short sequences).  The per-tile schedule launches one CTA
-// per tile; when the tiles fill the SMs badly (224 tiles on 152 SMs take two
-// full waves) each tile's keys are split into n ranges, giving n times as
-// many shorter units, and merge_kernel combines the ranges.
+// Split key ranges (short sequences, opt-in): each tile's keys are cut into
+// n ranges, each its own online softmax, and merge_kernel combines them.  A
+// different computation from the unsplit method (each range has its own
+// reference), so it runs only when the caller asks for it.
 constexpr int kMaxSplit = 16;
-constexpr int64_t kMergeCostBlocks = 4;   // merge launch + pass, in key-block times
 
 struct SplitLayout {
   size_t o, ml, total;
@@ -257,17 +277,6 @@ SplitLayout split_layout(int64_t units) {
   L.ml = align_up(static_cast<size_t>(units) * 256 * 128 * 2, 256);
   L.total = L.ml + align_up(static_cast<size_t>(units) * 256 * sizeof(float2), 256);
   return L;
-}
-
-// Number of ranges that minimises (waves of units) x (key blocks per unit),
-// plus the merge, for the per-tile schedule; ties go to fewer ranges.
-int64_t auto_split(int64_t ntiles, int64_t nb, int sms) {
-  int64_t best = 1, best_cost = (ntiles + sms - 1) / sms * nb;
-  for (int64_t n = 2; n <= kMaxSplit && n <= nb; ++n) {
-    const int64_t cost = (ntiles * n + sms - 1) / sms * ((nb + n - 1) / n) + kMergeCostBlocks;
-    if (cost < best_cost) best = n, best_cost = cost;
-  }
-  return best;
 }
 
 bool persistent_schedule(const ovc_prepared* p, const ovc_probe* probe) {
@@ -286,9 +295,11 @@ ovc_status run_attention(const ovc_prepared* p, const ovc_repair* r, float softm
   if (nsplit > 1 && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))) return OVC_ERR_INVALID_ARG;
   // V-Smooth runs with the method's own kernel only: no repair, no split, no variant.
   const bool vsmooth = p->vmean != nullptr;
-  if (vsmooth && (r || nsplit > 1 || flags != 0)) return OVC_ERR_INVALID_ARG;
+  if (vsmooth && (r || nsplit > 1 || flags != 0 || p->kbias)) return OVC_ERR_INVALID_ARG;
+  const bool qbias = p->kbias != nullptr;
   if (r) {
     if (!r->idx || !r->k_sel || !r->dvt || !r->sk_sel || !r->sr) return OVC_ERR_INVALID_ARG;
+    if (qbias != (r->kb_sel != nullptr)) return OVC_ERR_INVALID_ARG;   // made from this preparation
     if (r->B != p->B || r->S != p->S || r->H != p->H) return OVC_ERR_INVALID_ARG;
     if (r->n < 1 || r->n > p->S || r->n_pad != (r->n + 127) / 128 * 128) return OVC_ERR_INVALID_ARG;
   }
@@ -311,6 +322,12 @@ ovc_status run_attention(const ovc_prepared* p, const ovc_repair* r, float softm
   }
   CUtensorMap mvm = mk;
   if (vsmooth && !make_mean_map(&mvm, p->vmean, p->nb, BH * 128, (p->nb + 15) / 16 * 16)) return OVC_ERR_CUDA;
+  CUtensorMap mkb = mk, mkbs = mk;
+  if (qbias) {
+    if (!make_bias_map(&mkb, p->kbias, BH * p->S_pad)) return OVC_ERR_CUDA;
+    mkbs = mkb;
+    if (r && !make_bias_map(&mkbs, r->kb_sel, BH * r->n_pad)) return OVC_ERR_CUDA;
+  }
 
   AttnParams P{};
   P.B = static_cast<int32_t>(p->B);
@@ -322,11 +339,7 @@ ovc_status run_attention(const ovc_prepared* p, const ovc_repair* r, float softm
   const int64_t ntiles = BH * P.npairs;   // a tile is a pair of 128-row query blocks
   P.ntiles = static_cast<int32_t>(ntiles);
   const bool persistent = persistent_schedule(p, probe);
-  int64_t ns = nsplit;
-  if (ns == 0) {   // automatic: only on the per-tile schedule, without repair, given workspace
-    ns = (r || vsmooth || persistent || !workspace) ? 1 : auto_split(ntiles, p->nb, dev->sms);
-    if (ns > 1 && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return OVC_ERR_INVALID_ARG;
-  }
+  const int64_t ns = nsplit > 1 ? nsplit : 1;   // 0 and 1: no split
   const int64_t nunits = ntiles * ns;
   if (nunits > 0x7FFFFFFF) return OVC_ERR_INVALID_ARG;
   P.nsplit = static_cast<int32_t>(ns);
@@ -340,6 +353,7 @@ ovc_status run_attention(const ovc_prepared* p, const ovc_repair* r, float softm
   P.sq = p->sq;
   P.sk = p->sk;
   P.sv = p->sv;
+  P.qbias = qbias ? 1 : 0;
   P.o = static_cast<uint16_t*>(o->ptr);
   P.os[0] = o->stride_b;
   P.os[1] = o->stride_s;
@@ -374,9 +388,9 @@ ovc_status run_attention(const ovc_prepared* p, const ovc_repair* r, float softm
   static_assert(OVC_ATTN_EXP_THEN_CAST == kVarExpThenCast && OVC_ATTN_NATURAL_ORDER == kVarNaturalOrder,
                 "flag bits select the kernel variant");
   const int variant = vsmooth ? kVarVSmooth : static_cast<int>(flags | (ns > 1 ? kVarSplit : 0));
-  kAttentionKernels[variant]<<<static_cast<unsigned>(grid), kAttnThreads,
-                               vsmooth ? kAttnSmemBytesVSmooth : kAttnSmemBytes,
-                               static_cast<cudaStream_t>(stream)>>>(mq, mk, mv, mks, mdv, mvm, P);
+  const size_t smem = vsmooth ? kAttnSmemBytesVSmooth : (qbias ? kAttnSmemBytesQBias : kAttnSmemBytes);
+  kAttentionKernels[variant]<<<static_cast<unsigned>(grid), kAttnThreads, smem, static_cast<cudaStream_t>(stream)>>>(
+      mq, mk, mv, mks, mdv, mvm, mkb, mkbs, P);
   if (ns > 1) {
     const int64_t rows = BH * p->S;
     merge_kernel<<<static_cast<unsigned>((rows + kMergeRowsPerBlock - 1) / kMergeRowsPerBlock),
@@ -397,7 +411,8 @@ size_t ovc_prepare_workspace_bytes(int64_t B, int64_t S, int64_t H, int64_t D) {
 }
 
 size_t ovc_prepare_workspace_bytes_ex(int64_t B, int64_t S, int64_t H, int64_t D, uint32_t flags) {
-  if (D != 128 || !dims_ok(B, S, H) || (flags & ~(OVC_PREPARE_SMOOTH_K | OVC_PREPARE_V_SMOOTH))) return 0;
+  if (D != 128 || !dims_ok(B, S, H) || (flags & ~kPrepareFlags)) return 0;
+  if ((flags & OVC_PREPARE_SMOOTH_Q) && (flags & OVC_PREPARE_V_SMOOTH)) return 0;
   return prep_layout(B, S, H, flags).total;
 }
 
@@ -414,7 +429,8 @@ ovc_status ovc_prepare_ex(const ovc_tensor* q, const ovc_tensor* k, const ovc_te
 ovc_status ovc_prepare_grouped(const ovc_tensor* q, const ovc_tensor* k, const ovc_tensor* v, const int32_t* perm,
                                uint32_t flags, void* workspace, size_t workspace_bytes, ovc_prepared* out,
                                void* stream) {
-  if (flags & ~(OVC_PREPARE_SMOOTH_K | OVC_PREPARE_V_SMOOTH)) return OVC_ERR_INVALID_ARG;
+  if (flags & ~kPrepareFlags) return OVC_ERR_INVALID_ARG;
+  if ((flags & OVC_PREPARE_SMOOTH_Q) && (flags & OVC_PREPARE_V_SMOOTH)) return OVC_ERR_INVALID_ARG;
   if (perm && (reinterpret_cast<uintptr_t>(perm) & 3u)) return OVC_ERR_INVALID_ARG;
   if (!q || !k || !v || !out) return OVC_ERR_INVALID_ARG;
   if (q->D != 128 || k->D != 128 || v->D != 128) return OVC_ERR_UNSUPPORTED;
@@ -447,6 +463,7 @@ ovc_status ovc_prepare_grouped(const ovc_tensor* q, const ovc_tensor* k, const o
   p.energy = reinterpret_cast<float*>(ws + L.energy);
   p.vmean = (flags & OVC_PREPARE_V_SMOOTH) ? reinterpret_cast<uint16_t*>(ws + L.vmean) : nullptr;
   p.perm = perm;
+  p.kbias = (flags & OVC_PREPARE_SMOOTH_Q) ? reinterpret_cast<uint16_t*>(ws + L.kbias) : nullptr;
 
   PrepParams P{};
   P.q = static_cast<const uint16_t*>(q->ptr);
@@ -486,6 +503,13 @@ ovc_status ovc_prepare_grouped(const ovc_tensor* q, const ovc_tensor* k, const o
       k_mean_partial_kernel<false><<<dim3(static_cast<unsigned>(p.B * p.H), static_cast<unsigned>(p.nb)), 128, 0, s>>>(P);
     k_mean_final_kernel<<<static_cast<unsigned>(p.B * p.H), 128, 0, s>>>(P);
   }
+  if (flags & OVC_PREPARE_SMOOTH_Q) {
+    P.qpart = reinterpret_cast<float*>(ws + L.qpart);
+    P.qmean = reinterpret_cast<float*>(ws + L.qmean);
+    P.kbias = p.kbias;
+    k_mean_partial_kernel<false, true><<<dim3(static_cast<unsigned>(p.B * p.H), static_cast<unsigned>(p.nb)), 128, 0, s>>>(P);
+    k_mean_final_kernel<true><<<static_cast<unsigned>(p.B * p.H), 128, 0, s>>>(P);
+  }
   if (flags & OVC_PREPARE_V_SMOOTH) {
     P.vmu = reinterpret_cast<float*>(ws + L.vmu);
     P.vmean = p.vmean;
@@ -497,13 +521,13 @@ ovc_status ovc_prepare_grouped(const ovc_tensor* q, const ovc_tensor* k, const o
   }
   // z = 2 (the amax of V) only without V-Smooth, whose mean pass folds it in
   const dim3 g1(static_cast<unsigned>(p.B * p.H), static_cast<unsigned>(p.nb), (flags & OVC_PREPARE_V_SMOOTH) ? 2 : 3);
-  const int qk_opt = ((flags & OVC_PREPARE_SMOOTH_K) ? kPrepSmoothK : 0) | (perm ? kPrepPerm : 0);
-  switch (qk_opt) {
-    case 0: prepare_qk_kernel<0><<<g1, 256, 0, s>>>(P); break;
-    case kPrepSmoothK: prepare_qk_kernel<kPrepSmoothK><<<g1, 256, 0, s>>>(P); break;
-    case kPrepPerm: prepare_qk_kernel<kPrepPerm><<<g1, 256, 0, s>>>(P); break;
-    default: prepare_qk_kernel<kPrepSmoothK | kPrepPerm><<<g1, 256, 0, s>>>(P); break;
-  }
+  const int qk_opt = ((flags & OVC_PREPARE_SMOOTH_K) ? kPrepSmoothK : 0) | (perm ? kPrepPerm : 0) |
+                     ((flags & OVC_PREPARE_SMOOTH_Q) ? kPrepSmoothQ : 0);
+  static const decltype(&prepare_qk_kernel<0>) kQK[8] = {
+      prepare_qk_kernel<0>, prepare_qk_kernel<1>, prepare_qk_kernel<2>, prepare_qk_kernel<3>,
+      prepare_qk_kernel<4>, prepare_qk_kernel<5>, prepare_qk_kernel<6>, prepare_qk_kernel<7>};
+  static_assert(kPrepSmoothK == 1 && kPrepPerm == 2 && kPrepSmoothQ == 4, "option bits index the table");
+  kQK[qk_opt]<<<g1, 256, 0, s>>>(P);
   const dim3 g2(static_cast<unsigned>(p.B * p.H), static_cast<unsigned>(p.nb), 1);
   const bool vsm = (flags & OVC_PREPARE_V_SMOOTH) != 0;
   if (vsm && perm)
@@ -529,23 +553,9 @@ ovc_status ovc_attention_ex(const ovc_prepared* p, const ovc_repair* r, float so
   return run_attention(p, r, softmax_scale, o, nullptr, flags, nsplit, workspace, workspace_bytes, stream);
 }
 
-int32_t ovc_attention_auto_split(int64_t B, int64_t S, int64_t H) {
-  if (!dims_ok(B, S, H) || S >= 32768) return 1;
-  DeviceState* dev = nullptr;
-  if (device_state(&dev) != OVC_OK) return 1;
-  const int64_t nb = (S + 127) / 128;
-  return static_cast<int32_t>(auto_split(B * H * ((nb + 1) / 2), nb, dev->sms));
-}
-
 size_t ovc_attention_workspace_bytes(const ovc_prepared* p, int32_t nsplit) {
   if (!prepared_ok(p) || nsplit < 0 || nsplit > kMaxSplit || nsplit > p->nb) return 0;
-  int64_t ns = nsplit;
-  if (ns == 0) {
-    DeviceState* dev = nullptr;
-    if (p->vmean || persistent_schedule(p, nullptr) || device_state(&dev) != OVC_OK) return 0;
-    ns = auto_split(ntiles_of(p), p->nb, dev->sms);
-  }
-  return ns > 1 ? split_layout(ntiles_of(p) * ns).total : 0;
+  return nsplit > 1 ? split_layout(ntiles_of(p) * nsplit).total : 0;
 }
 
 size_t ovc_repair_workspace_bytes(int64_t B, int64_t S, int64_t H, float budget) {
@@ -583,6 +593,7 @@ ovc_status ovc_prepare_v_repair(const ovc_tensor* v, const ovc_prepared* p, floa
   r.dvt = ws + L.dvt;
   r.sk_sel = reinterpret_cast<float*>(ws + L.sk_sel);
   r.sr = reinterpret_cast<float*>(ws + L.sr);
+  r.kb_sel = p->kbias ? reinterpret_cast<uint16_t*>(ws + L.kb_sel) : nullptr;
 
   RepairParams P{};
   P.v = static_cast<const uint16_t*>(v->ptr);
@@ -606,6 +617,8 @@ ovc_status ovc_prepare_v_repair(const ovc_tensor* v, const ovc_prepared* p, floa
   P.dvt = r.dvt;
   P.sk_sel = r.sk_sel;
   P.sr = r.sr;
+  P.kbias = p->kbias;
+  P.kb_sel = r.kb_sel;
   repair_prepare_kernel<<<static_cast<unsigned>(p->B * p->H), kRepairThreads, 0,
                           static_cast<cudaStream_t>(stream)>>>(P);
   st = launch_status();
@@ -772,8 +785,8 @@ extern "C" ovc_status ovc_prepare_noalloc(const ovc_tensor* q, const ovc_tensor*
     return OVC_ERR_INVALID_ARG;
   if (!out->q || !out->k || !out->vt || !out->sq || !out->sk || !out->sv || !out->vamax || !out->energy)
     return OVC_ERR_INVALID_ARG;
-  // A plain preparation: no V-Smooth means, no grouping order.
-  if (out->vmean || out->perm) return OVC_ERR_INVALID_ARG;
+  // A plain preparation: no V-Smooth means, no grouping order, no Q smoothing.
+  if (out->vmean || out->perm || out->kbias) return OVC_ERR_INVALID_ARG;
   if (!aligned16(out->q) || !aligned16(out->k) || !aligned16(out->vt)) return OVC_ERR_INVALID_ARG;
   if (!aligned4(out->sq) || !aligned4(out->sk) || !aligned4(out->sv) || !aligned4(out->vamax) ||
       !aligned4(out->energy))

@@ -16,6 +16,12 @@
 // that it is reproducible bit for bit:
 //   k_mean_partial_kernel  grid (B*H, nb) x 128: one thread per channel.
 //   k_mean_final_kernel    grid (B*H) x 128.
+// Q smoothing (optional, same summary): Q's channel means mu_q, summed the
+// same way, are subtracted before Q is quantised.  That moves every score of
+// key t by mu_q . k_t, which differs from key to key, so it is added back:
+// while K is quantised, each key's bias beta_t = mu_q . dec(K^_t) is written
+// as a BF16 pair (hi, lo), hi + lo ~ beta_t to 16 bits, laid out as the B
+// operand of a BF16 MMA that adds beta_t / s_q to the key's scores.
 //
 // Two launches, both HBM-bound and coalesced.  The head index runs fastest
 // in every grid: CTAs that run together read the same tokens of all heads,
@@ -59,6 +65,12 @@ struct PrepParams {
   // kmean [B*H][128] channel means subtracted from K before quantising.
   float* kpart;
   float* kmean;
+  // Q smoothing (all NULL when off): qpart, qmean as kpart, kmean for Q;
+  // kbias [B*H][S_pad][16] BF16 bits, key t's row (hi, lo, hi, lo, 0 x 12)
+  // of beta_t = mu_q . dec(K^_t) (rows >= S zero).
+  float* qpart;
+  float* qmean;
+  uint16_t* kbias;
   // V-Smooth (both NULL when off): vmu [B*H][nb][128] block means of V (BF16
   // values held as FP32); vmean [B*H][128][nbk] BF16 bits of the restored
   // means M'_b = bf16(mu_b r), channel-major with blocks contiguous (the B
@@ -81,6 +93,7 @@ __device__ __forceinline__ int kv_row(const PrepParams& P, int bh, int t) {
 // preparation carries none of their tests.
 constexpr int kPrepSmoothK = 1;
 constexpr int kPrepPerm = 2;
+constexpr int kPrepSmoothQ = 4;
 
 // |x| of two packed 16-bit floats, as ordered integers (sign bit cleared).
 __device__ __forceinline__ uint32_t abs2_bits(uint32_t w) { return w & 0x7FFF7FFFu; }
@@ -139,29 +152,60 @@ __device__ __forceinline__ uint32_t block_max_u32(uint32_t m, uint32_t* red) {
   return r;
 }
 
-// Channel sums of one 128-token block of K, in token order.
-template <bool kPerm>
+// Channel sums of one 128-token block of K (kQ: of Q, which keeps its token
+// order), in token order.
+template <bool kPerm, bool kQ = false>
 __global__ void __launch_bounds__(128) k_mean_partial_kernel(const __grid_constant__ PrepParams P) {
   const int bh = blockIdx.x, j = blockIdx.y, d = threadIdx.x;
   const int b = bh / P.H, h = bh % P.H;
   const int t1 = min(P.S, j * 128 + 128);
-  const uint16_t* src = P.k + b * P.ks[0] + h * P.ks[2] + d;
+  const int64_t* st = kQ ? P.qs : P.ks;
+  const uint16_t* src = (kQ ? P.q : P.k) + b * st[0] + h * st[2] + d;
   float part = 0.0f;
   // The loads are independent and can be in flight together; the additions
   // stay in token order.
 #pragma unroll 16
-  for (int t = j * 128; t < t1; ++t)
-    part = __fadd_rn(part, half_bits_to_float(__ldg(src + static_cast<int64_t>(kv_row<kPerm>(P, bh, t)) * P.ks[1]), P.fp16));
-  P.kpart[(static_cast<int64_t>(bh) * P.nb + j) * 128 + d] = part;
+  for (int t = j * 128; t < t1; ++t) {
+    const int tr = kQ ? t : kv_row<kPerm>(P, bh, t);
+    part = __fadd_rn(part, half_bits_to_float(__ldg(src + static_cast<int64_t>(tr) * st[1]), P.fp16));
+  }
+  (kQ ? P.qpart : P.kpart)[(static_cast<int64_t>(bh) * P.nb + j) * 128 + d] = part;
 }
 
 // Channel means: the block sums in block order, then one division by S.
+template <bool kQ = false>
 __global__ void __launch_bounds__(128) k_mean_final_kernel(const __grid_constant__ PrepParams P) {
   const int bh = blockIdx.x, d = threadIdx.x;
-  const float* part = P.kpart + static_cast<int64_t>(bh) * P.nb * 128 + d;
+  const float* part = (kQ ? P.qpart : P.kpart) + static_cast<int64_t>(bh) * P.nb * 128 + d;
   float total = 0.0f;
   for (int j = 0; j < P.nb; ++j) total = __fadd_rn(total, part[j * 128]);
-  P.kmean[bh * 128 + d] = __fdiv_rn(total, static_cast<float>(P.S));
+  (kQ ? P.qmean : P.kmean)[bh * 128 + d] = __fdiv_rn(total, static_cast<float>(P.S));
+}
+
+// Q smoothing: key t's bias beta_t = mu_q . dec(code_t) from this thread's
+// 64 channels (words w, channels 64 half ..), summed with the other half's
+// thread (the neighbouring lane), written as the BF16 row
+// (hi, lo, hi, lo, 0, ..., 0), hi = bf16(beta), lo = bf16(beta - hi).
+__device__ __forceinline__ void write_key_bias(const PrepParams& P, int bh, int t, int half, const uint32_t* w) {
+  const float* mu = P.qmean + bh * 128 + half * 64;
+  float acc = 0.0f;
+#pragma unroll
+  for (int g = 0; g < 16; ++g) {
+    float dq[4];
+    dec4(w[g], dq);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc = fmaf(__ldg(mu + 4 * g + e), dq[e], acc);
+  }
+  acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 1);
+  if (half == 0) {
+    const __nv_bfloat16 hi = __float2bfloat16_rn(acc);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(acc - __bfloat162float(hi));
+    const uint32_t hl = static_cast<uint32_t>(__bfloat16_as_ushort(hi)) |
+                        (static_cast<uint32_t>(__bfloat16_as_ushort(lo)) << 16);
+    uint4* dst = reinterpret_cast<uint4*>(P.kbias + (static_cast<int64_t>(bh) * P.S_pad + t) * 16);
+    dst[0] = make_uint4(hl, hl, 0u, 0u);
+    dst[1] = make_uint4(0u, 0u, 0u, 0u);
+  }
 }
 
 // V-Smooth ("VC-Attention" summary, "V-Smooth"), first pass: per 128-token
@@ -217,10 +261,10 @@ __global__ void __launch_bounds__(256) prepare_qk_kernel(const __grid_constant__
     for (int i = 0; i < 8; ++i) x[i] = make_uint4(0, 0, 0, 0);
   }
 
-  if ((kOpt & kPrepSmoothK) && which == 1) {
-    // Smoothed K: the centred values fl(x - mean) set the block amax and are
-    // quantised; rows past S stay zero (no code, no part of the amax).
-    const float* mu = P.kmean + bh * 128 + half * 64;
+  if (((kOpt & kPrepSmoothK) && which == 1) || ((kOpt & kPrepSmoothQ) && which == 0)) {
+    // Smoothed K (or Q): the centred values fl(x - mean) set the block amax
+    // and are quantised; rows past S stay zero (no code, no part of the amax).
+    const float* mu = (which == 0 ? P.qmean : P.kmean) + bh * 128 + half * 64;
     float c[64];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -237,13 +281,15 @@ __global__ void __launch_bounds__(256) prepare_qk_kernel(const __grid_constant__
     for (int e = 0; e < 64; ++e) m = fmaxf(m, fabsf(c[e]));
     const float amax = __uint_as_float(block_max_u32(__float_as_uint(m), red));
     const QScale sc = scale_from_amax(amax);
-    if (tid == 0) P.sk[bh * P.nb + j] = sc.s;
+    if (tid == 0) (which == 0 ? P.sq : P.sk)[bh * P.nb + j] = sc.s;
     uint32_t w[16];
 #pragma unroll
     for (int g = 0; g < 16; ++g) w[g] = quant4(c[4 * g], c[4 * g + 1], c[4 * g + 2], c[4 * g + 3], sc.r);
-    uint4* d4 = reinterpret_cast<uint4*>(P.kc + (static_cast<int64_t>(bh) * P.S_pad + t) * 128 + half * 64);
+    uint4* d4 = reinterpret_cast<uint4*>((which == 0 ? P.qc : P.kc) + (static_cast<int64_t>(bh) * P.S_pad + t) * 128 +
+                                         half * 64);
 #pragma unroll
     for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    if ((kOpt & kPrepSmoothQ) && which == 1) write_key_bias(P, bh, t, half, w);
     return;
   }
 
@@ -278,6 +324,7 @@ __global__ void __launch_bounds__(256) prepare_qk_kernel(const __grid_constant__
   uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
   for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+  if ((kOpt & kPrepSmoothQ) && which == 1) write_key_bias(P, bh, t, half, w);
 }
 
 // One 128-token block of V.  512 threads: warp w owns channels 8w..8w+7,

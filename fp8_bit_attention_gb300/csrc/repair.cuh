@@ -16,8 +16,9 @@
 //      (its code recomputed exactly as prepare does), take amax|R| ->
 //      s_r = amax/448;
 //   4. write the residual codes E4M3(R * 448/amax) transposed (dvt), gather
-//      the selected quantised keys (k_sel) and the scale of each key's block
-//      (sk_sel), zero-padding up to n_pad.
+//      the selected quantised keys (k_sel), the scale of each key's block
+//      (sk_sel) and, with Q smoothing, each key's bias row (kb_sel),
+//      zero-padding up to n_pad.
 #pragma once
 
 #include <cstdint>
@@ -40,6 +41,10 @@ struct RepairParams {
   uint8_t* dvt;
   float* sk_sel;
   float* sr;
+  // Q smoothing (both NULL when off): the key bias rows [B*H][S_pad][16] of
+  // the preparation, and those of the selected keys [B*H][n_pad][16].
+  const uint16_t* kbias;
+  uint16_t* kb_sel;
 };
 
 constexpr int kRepairThreads = 1024;
@@ -182,6 +187,12 @@ __global__ void __launch_bounds__(kRepairThreads, 1) repair_prepare_kernel(const
       dvt[static_cast<int64_t>(4 * lane + e) * P.n_pad + i] = static_cast<uint8_t>(codes >> (8 * e));
     reinterpret_cast<uint32_t*>(ksel + static_cast<int64_t>(i) * 128)[lane] = kw;
     if (lane == 0) sksel[i] = skv;
+    if (P.kb_sel != nullptr && lane < 8) {
+      const uint32_t bw = i < P.n ? __ldg(reinterpret_cast<const uint32_t*>(
+                                        P.kbias + (static_cast<int64_t>(bh) * P.S_pad + clamp_token(idx[i], P.S)) * 16) + lane)
+                                  : 0u;
+      reinterpret_cast<uint32_t*>(P.kb_sel + (static_cast<int64_t>(bh) * P.n_pad + i) * 16)[lane] = bw;
+    }
   }
 }
 

@@ -86,7 +86,10 @@ typedef struct {
  *   perm  [B,H,S]          grouping only (else NULL): the token order of k, vt
  *                          and vmean (row t is input token perm[t]); the
  *                          caller's array, which must outlive the struct's use
- *                          (q keeps its order, so O does too) */
+ *                          (q keeps its order, so O does too)
+ *   kbias [B,H,S_pad,16]   Q smoothing only (else NULL): BF16 bits, key t's
+ *                          row (hi, lo, hi, lo, 0 x 12) with hi + lo ~ beta_t =
+ *                          mu_q . dec(k_t) (rows >= S zero) */
 typedef struct {
   int64_t B, S, H, nb, S_pad;
   uint8_t* q;
@@ -99,6 +102,7 @@ typedef struct {
   float* energy;
   uint16_t* vmean;
   const int32_t* perm;
+  uint16_t* kbias;
 } ovc_prepared;
 
 /* V residual repair set written by ovc_prepare_v_repair (n_pad = 128*ceil(n/128)):
@@ -106,7 +110,9 @@ typedef struct {
  *   k_sel  [B,H,n_pad,128] their quantised keys (zero padded)
  *   dvt    [B,H,128,n_pad] their quantised V residuals, transposed
  *   sk_sel [B,H,n_pad]     the key scale of each selected token's block
- *   sr     [B,H]           FP32 residual scale, amax|R_sel|/448 */
+ *   sr     [B,H]           FP32 residual scale, amax|R_sel|/448
+ *   kb_sel [B,H,n_pad,16]  Q smoothing only (else NULL): the selected keys'
+ *                          bias rows (as ovc_prepared.kbias, zero padded) */
 typedef struct {
   int64_t B, S, H, n, n_pad;
   int32_t* idx;
@@ -114,6 +120,7 @@ typedef struct {
   uint8_t* dvt;
   float* sk_sel;
   float* sr;
+  uint16_t* kb_sel;
 } ovc_repair;
 
 /* Bytes of workspace ovc_prepare needs for these dimensions (0 if invalid). */
@@ -137,19 +144,20 @@ ovc_status ovc_attention(const ovc_prepared* p, float softmax_scale, const ovc_o
                          void* stream);
 
 /* ovc_attention / ovc_attention_v_repair (r may be NULL) with a kernel
- * variant and, for short sequences, split key ranges.
+ * variant and, on request, split key ranges.
  *
- * Split key ranges (nsplit): the per-tile schedule (S < 32768) launches one
- * CTA per pair of 128-row query blocks; when those fill the SMs badly (224
- * tiles on 152 SMs run as two full waves), each tile's key blocks are cut
- * into nsplit contiguous ranges [s nb/nsplit, (s+1) nb/nsplit), each run as
- * its own online softmax (own reference, own row sum, mid-window order within
- * the range), and a merge pass combines them: with M = max m8_s and
- * w_s = l_s 2^((m8_s - M)/8), O = sum w_s O_s / sum w_s.  The partial results
- * live in caller workspace (ovc_attention_workspace_bytes).
- *   nsplit     0: automatic (1 without workspace, with a repair set or on the
- *              persistent schedule); 1..16: forced (<= nb; > 1 needs
- *              workspace and no repair set).
+ * Split key ranges (nsplit > 1; opt-in, never chosen by the library): each
+ * pair of 128-row query blocks has its key blocks cut into nsplit contiguous
+ * ranges [s nb/nsplit, (s+1) nb/nsplit), each run as its own online softmax
+ * (own reference, own row sum, mid-window order within the range), and a
+ * merge pass combines them: with M = max m8_s and w_s = l_s 2^((m8_s - M)/8),
+ * O = sum w_s O_s / sum w_s.  Because every range takes its ExpCast bytes
+ * against its own reference, this is a different computation from the
+ * method's single pass: results differ from ovc_attention's (both lie within
+ * the ExpCast error of exact attention).  The partial results live in caller
+ * workspace (ovc_attention_workspace_bytes).
+ *   nsplit     0 or 1: no split (the method; identical to ovc_attention);
+ *              2..16 (<= nb): forced split, needs workspace and no repair set.
  *   workspace  device memory, 256-byte aligned, at least
  *              ovc_attention_workspace_bytes(p, nsplit) bytes; may be NULL
  *              when no split is made.  Calls that share it must not overlap.
@@ -179,15 +187,9 @@ ovc_status ovc_attention_ex(const ovc_prepared* p, const ovc_repair* r, float so
                             const ovc_output* o, uint32_t flags, int32_t nsplit, void* workspace,
                             size_t workspace_bytes, void* stream);
 
-/* Workspace bytes ovc_attention_ex needs for nsplit ranges (nsplit = 0: the
- * automatic choice on the current device).  0 when no split is made, or for
- * invalid arguments. */
+/* Workspace bytes ovc_attention_ex needs for nsplit ranges: 0 when no split
+ * is made (nsplit 0 or 1) or for invalid arguments. */
 size_t ovc_attention_workspace_bytes(const ovc_prepared* p, int32_t nsplit);
-
-/* The number of key ranges the automatic choice (nsplit = 0) makes for these
- * dimensions on the current device: 1 for S >= 32768 (persistent schedule),
- * for invalid dimensions or without a usable device. */
-int32_t ovc_attention_auto_split(int64_t B, int64_t S, int64_t H);
 
 /* Bytes of workspace ovc_prepare_v_repair needs (0 if invalid).  budget in (0,1]. */
 size_t ovc_repair_workspace_bytes(int64_t B, int64_t S, int64_t H, float budget);
@@ -253,12 +255,12 @@ ovc_status ovc_attention_probe(const ovc_prepared* p, const ovc_repair* r, float
  * that loads the library holds until the process exits.
  *   out: filled in by the caller: B, S, H, nb = ceil(S/128), S_pad = 128*nb,
  *        and the output buffers q, k, vt (16-byte aligned), sq, sk, sv, vamax,
- *        energy (4-byte aligned), in the layouts of ovc_prepared; vmean and
- *        perm must be NULL.  The struct is then usable with ovc_attention and
+ *        energy (4-byte aligned), in the layouts of ovc_prepared; vmean,
+ *        perm and kbias must be NULL.  The struct is then usable with ovc_attention and
  *        ovc_prepare_v_repair like one filled by ovc_prepare.
  * Errors: OVC_ERR_SCRATCH_LIMIT if B*H > OVC_NOALLOC_MAX_HEADS (nothing is
- * launched); OVC_ERR_INVALID_ARG for a NULL or misaligned buffer, a vmean or
- * perm that is not NULL, or dimensions that do not match the inputs.
+ * launched); OVC_ERR_INVALID_ARG for a NULL or misaligned buffer, a vmean,
+ * perm or kbias that is not NULL, or dimensions that do not match the inputs.
  * The first call on a device looks up the array's device address on that
  * device (cudaGetSymbolAddress); make that first call before any stream
  * capture.  Every call shares the one array, which keeps the last call's
@@ -289,11 +291,24 @@ ovc_status ovc_prepare_noalloc(const ovc_tensor* q, const ovc_tensor* k, const o
  *     restored means M'_b = bf16(mu_b r) go to vmean.  Attention adds M'_b,
  *     weighted by each row's block row sum, back into O.  Not combinable with
  *     repair (no energies) or with split key ranges.
+ *   OVC_PREPARE_SMOOTH_Q  Q smoothing -- optional, off in ovc_prepare (same
+ *     prior art as K smoothing).  Per (b,h) Q's channel means mu_q over the
+ *     sequence (FP32, summed as K's) are subtracted before Q is quantised,
+ *     so Q's block scales lose the channel offset.  That moves every score
+ *     of key t by mu_q . k_t, which is not the same for all keys, so it is
+ *     added back: each key gets the bias beta_t = mu_q . dec(k_t) (its
+ *     quantised code, decoded), stored as a BF16 (hi, lo) pair in
+ *     ovc_prepared.kbias, and attention adds s_k beta_t to the key's
+ *     scores through one BF16 MMA per key block (the score is then the
+ *     product of mu_q + s_q dec(q') with s_k dec(k_t)).  Combines with K
+ *     smoothing, grouping, repair and split key ranges; not with V-Smooth.
  * ovc_prepare_workspace_bytes_ex gives the workspace for the same flags
- * (0 for unknown flags or unsupported shapes); unknown flags make
- * ovc_prepare_ex return OVC_ERR_INVALID_ARG.  Otherwise as ovc_prepare. */
+ * (0 for unknown flags, SMOOTH_Q with V_SMOOTH, or unsupported shapes);
+ * such flags make ovc_prepare_ex return OVC_ERR_INVALID_ARG.  Otherwise as
+ * ovc_prepare. */
 #define OVC_PREPARE_SMOOTH_K 1u
 #define OVC_PREPARE_V_SMOOTH 2u
+#define OVC_PREPARE_SMOOTH_Q 4u
 size_t ovc_prepare_workspace_bytes_ex(int64_t B, int64_t S, int64_t H, int64_t D, uint32_t flags);
 
 /* V-Smooth's grouping ("VC-Attention" summary, "V-Smooth": online k-means
@@ -305,6 +320,9 @@ size_t ovc_prepare_workspace_bytes_ex(int64_t B, int64_t S, int64_t H, int64_t D
  * lists the tokens ordered by (cluster, index).  Pass perm to
  * ovc_prepare_grouped so that V-Smooth's 128-token blocks hold similar
  * values.  Workspace: ovc_vsmooth_group_workspace_bytes (256-byte aligned).
+ * After the call the workspace begins with the state of the last assignment
+ * step, for inspection: the centroids it used, FP32 [B,H,C,128] at offset 0,
+ * then its labels, int32 [B,H,S], at the next multiple of 256 bytes.
  * Asynchronous on `stream`. */
 size_t ovc_vsmooth_group_workspace_bytes(int64_t B, int64_t S, int64_t H, int32_t clusters);
 ovc_status ovc_vsmooth_group(const ovc_tensor* v, int32_t clusters, int32_t iters, void* workspace,

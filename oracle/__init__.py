@@ -75,7 +75,7 @@ def lib():
             L.ovc_oracle_k_mean.restype = None
             L.ovc_oracle_k_mean.argtypes = [P, ctypes.c_int, i64, i64, i64, i64, i64, i64, P]
             L.ovc_oracle_vsmooth_v.restype = None
-            L.ovc_oracle_vsmooth_v.argtypes = [P, ctypes.c_int, i64, i64, i64, i64, i64, i64, P, P, P, P]
+            L.ovc_oracle_vsmooth_v.argtypes = [P, ctypes.c_int, i64, i64, i64, i64, i64, i64, P, P, P]
             L.ovc_oracle_kmeans_group.restype = ctypes.c_int
             L.ovc_oracle_kmeans_group.argtypes = [P, ctypes.c_int, i64, i64, i64, i64, i64, i64, i64, i64, P, P, P]
             L.ovc_oracle_quantize_v.restype = None
@@ -88,14 +88,14 @@ def lib():
             L.ovc_oracle_repair_quantize.argtypes = [P, ctypes.c_int, i64, i64, i64, i64, i64, i64, P, P, P,
                                                      i64, P, P]
             L.ovc_oracle_block_codes.restype = None
-            L.ovc_oracle_block_codes.argtypes = [P, ctypes.c_float, P, P, i64, i64, d, d, d, d, ctypes.c_int, P]
+            L.ovc_oracle_block_codes.argtypes = [P, ctypes.c_float, P, P, P, i64, i64, d, d, d, d, ctypes.c_int, P]
             L.ovc_oracle_attention_rows.restype = ctypes.c_int
             L.ovc_oracle_attention_rows.argtypes = (
-                [P, P, P, P, P, P, i64, i64, i64, P, P, P, i64, P, P, P, i64, d, d, d, d,
+                [P, P, P, P, P, P, i64, i64, i64, P, P, P, i64, P, P, P, P, i64, d, d, d, d,
                  ctypes.c_int, ctypes.c_int, ctypes.c_int, i64, P, P, P, P, i64, P, P, ctypes.c_int])
             L.ovc_oracle_attention_exact_rows.restype = ctypes.c_int
             L.ovc_oracle_attention_exact_rows.argtypes = (
-                [P, P, P, i64, i64, P, P, i64, d, d, ctypes.c_int, ctypes.c_int, i64, P, P,
+                [P, P, P, P, i64, i64, P, P, i64, d, d, ctypes.c_int, ctypes.c_int, i64, P, P,
                  ctypes.c_int])
             _lib = L
     return _lib
@@ -182,8 +182,8 @@ def _bf16_view(x: np.ndarray):
 
 
 def k_mean(x: np.ndarray, fp16: bool = False) -> np.ndarray:
-    """Channel means of K over the sequence, [B,H,128] float32 (K smoothing;
-    FP32 block sums in token order, then over blocks, then / S)."""
+    """Channel means of K (or Q) over the sequence, [B,H,128] float32 (K and
+    Q smoothing; FP32 block sums in token order, then over blocks, then / S)."""
     x, sb, ss, sh = _bf16_view(x)
     B, S, H, _ = x.shape
     mean = np.zeros((B, H, 128), np.float32)
@@ -222,26 +222,27 @@ def quantize_v(v: np.ndarray, fp16: bool = False):
 
 def vsmooth_v(v: np.ndarray, fp16: bool = False):
     """V-Smooth of V -> (codes token-major [B,H,S_pad,128], sv [B,H],
-    mu [B,H,nb,128] block means (BF16 values), mprime [B,H,nb,128] = bf16(mu r))."""
+    mu [B,H,nb,128] block means (BF16 values, held as float32)); token t of
+    block b is restored as sv * dec(code_t) + mu_b."""
     v, sb, ss, sh = _bf16_view(v)
     B, S, H, _ = v.shape
     nb = (S + 127) // 128
     codes = np.zeros((B, H, nb * 128, 128), np.uint8)
     sv = np.zeros((B, H), np.float32)
     mu = np.zeros((B, H, nb, 128), np.float32)
-    mprime = np.zeros((B, H, nb, 128), np.float32)
-    lib().ovc_oracle_vsmooth_v(_ptr(v), int(fp16), B, S, H, sb, ss, sh, _ptr(codes), _ptr(sv), _ptr(mu), _ptr(mprime))
-    return codes, sv, mu, mprime
+    lib().ovc_oracle_vsmooth_v(_ptr(v), int(fp16), B, S, H, sb, ss, sh, _ptr(codes), _ptr(sv), _ptr(mu))
+    return codes, sv, mu
 
 
 def kmeans_group(v: np.ndarray, clusters: int, iters: int, fp16: bool = False):
-    """V-Smooth grouping of V [B,S,H,128] bits -> (labels [B,H,S] int32,
-    centroids used by the last assignment [B,H,C,128], perm [B,H,S] int32:
-    the token at position t' of the grouped order is perm[t'])."""
+    """V-Smooth grouping of V [B,S,H,128] bits (Lloyd's k-means in double)
+    -> (labels [B,H,S] int32, centroids used by the last assignment
+    [B,H,C,128] float64, perm [B,H,S] int32: the token at position t' of the
+    grouped order is perm[t'])."""
     v, sb, ss, sh = _bf16_view(v)
     B, S, H, _ = v.shape
     labels = np.zeros((B, H, S), np.int32)
-    cent = np.zeros((B, H, clusters, 128), np.float32)
+    cent = np.zeros((B, H, clusters, 128), np.float64)
     perm = np.zeros((B, H, S), np.int32)
     rc = lib().ovc_oracle_kmeans_group(_ptr(v), int(fp16), B, S, H, sb, ss, sh, int(clusters), int(iters),
                                        _ptr(labels), _ptr(cent), _ptr(perm))
@@ -295,13 +296,18 @@ class Prepared:
     """The oracle's own quantised tensors for one (Q, K, V) triple."""
 
     def __init__(self, q, k, v, fp16: bool = False, smooth_k: bool = False, v_smooth: bool = False,
-                 perm: np.ndarray | None = None):
+                 perm: np.ndarray | None = None, smooth_q: bool = False):
         """q, k, v: uint16 bits [B,S,H,128] of BF16 inputs, or of FP16 ones if
         fp16.  smooth_k: subtract K's channel means before quantising K.
         v_smooth: V-Smooth (block means subtracted, residual quantised, means
         restored through the row sums); no residual energies then.  perm
         [B,H,S]: V-Smooth's grouping -- keys and values are taken in this
-        token order (queries are not)."""
+        token order (queries are not).  smooth_q: Q smoothing -- Q's channel
+        means mu_q are subtracted before quantising Q, and every score of key
+        t gains s_k beta_t with beta_t = mu_q . dec(K^_t) (kbias [B,H,S],
+        float64), so that a score is the exact product of mu_q + s_q dec(Q^')
+        with s_k dec(K^_t) (VC-Attention summary, "Why attention is the video
+        bottleneck": Q/K smoothing of the prior low-bit kernels)."""
         if perm is not None:
             k = permute_tokens(k, perm)
             v = permute_tokens(v, perm)
@@ -309,11 +315,18 @@ class Prepared:
         self.nb = (self.S + 127) // 128
         self.fp16 = bool(fp16)
         self.kmean = k_mean(k, fp16) if smooth_k else None
-        self.qc, self.sq = quantize_blocks(q, fp16)
+        self.qmean = k_mean(q, fp16) if smooth_q else None
+        self.qc, self.sq = quantize_blocks(q, fp16, self.qmean)
         self.kc, self.sk = quantize_blocks(k, fp16, self.kmean)
-        self.vmu = self.vmean = None
+        self.kbias = None
+        if smooth_q:
+            tab = e4m3_table()
+            kdec = tab[self.kc[:, :, :self.S, :]]                       # [B,H,S,128] double
+            self.kbias = np.ascontiguousarray(
+                np.einsum("bhtd,bhd->bht", kdec, self.qmean.astype(np.float64)))
+        self.vmu = None
         if v_smooth:
-            self.vc, self.sv, self.vmu, self.vmean = vsmooth_v(v, fp16)
+            self.vc, self.sv, self.vmu = vsmooth_v(v, fp16)
             self.energy = None
         else:
             self.vc, self.sv, self.energy = quantize_v(v, fp16)
@@ -353,7 +366,7 @@ def attention_rows(prep: Prepared, rows_bh, rows_s, *, sm=None, repair: Repair |
         nrep = 0
     rc = lib().ovc_oracle_attention_rows(
         _ptr(prep.qc), _ptr(prep.sq), _ptr(prep.kc), _ptr(prep.sk), _ptr(prep.vc), _ptr(prep.sv),
-        prep.B, prep.S, prep.H, _ptr(ridx), _ptr(rdc), _ptr(rsr), nrep, _ptr(prep.vmean),
+        prep.B, prep.S, prep.H, _ptr(ridx), _ptr(rdc), _ptr(rsr), nrep, _ptr(prep.vmu), _ptr(prep.kbias),
         _ptr(rows_bh), _ptr(rows_s), n, c0, beta, tau, sm, int(mid_window), int(snap), int(cast),
         int(nsplit), _ptr(out), _ptr(m8), _ptr(l), _ptr(nres), dump_block, _ptr(codes), _ptr(dm8),
         nthreads or default_threads())
@@ -385,15 +398,18 @@ def block_codes(prep: Prepared, bh: int, s: int, j: int, m8: float, *, sm=None,
     kc = np.ascontiguousarray(prep.kc.reshape(B * H, -1, 128)[bh])
     sk = np.ascontiguousarray(prep.sk.reshape(B * H, -1)[bh])
     sq = float(prep.sq.reshape(B * H, -1)[bh, s // 128])
+    kb = None if prep.kbias is None else np.ascontiguousarray(prep.kbias.reshape(B * H, -1)[bh])
     codes = np.zeros(128, np.uint8)
-    lib().ovc_oracle_block_codes(_ptr(qrow), sq, _ptr(kc), _ptr(sk), prep.S, j, float(m8),
+    lib().ovc_oracle_block_codes(_ptr(qrow), sq, _ptr(kc), _ptr(sk), _ptr(kb), prep.S, j, float(m8),
                                  c0, beta, sm, int(cast), _ptr(codes))
     return codes
 
 
 def attention_exact_rows(q, k, v, rows_bh, rows_s, *, sm=None, tau=TAU, mid_window=True,
-                         snap=True, nsplit=1, nthreads=None):
-    """Online-softmax skeleton with exact exp2 on raw inputs [BH,S,128] (double)."""
+                         snap=True, nsplit=1, kbias=None, nthreads=None):
+    """Online-softmax skeleton with exact exp2 on raw inputs [BH,S,128]
+    (double); kbias [BH,S] (optional) is added to every score of its key
+    before the softmax scale."""
     q = np.ascontiguousarray(q, dtype=np.float64)
     k = np.ascontiguousarray(k, dtype=np.float64)
     v = np.ascontiguousarray(v, dtype=np.float64)
@@ -404,8 +420,11 @@ def attention_exact_rows(q, k, v, rows_bh, rows_s, *, sm=None, tau=TAU, mid_wind
     sm = 1.0 / np.sqrt(128.0) if sm is None else float(sm)
     out = np.zeros((n, 128), np.float64)
     nres = np.zeros(n, np.int32)
+    if kbias is not None:
+        kbias = np.ascontiguousarray(kbias, dtype=np.float64)
+        assert kbias.shape == (BH, S)
     rc = lib().ovc_oracle_attention_exact_rows(
-        _ptr(q), _ptr(k), _ptr(v), BH, S, _ptr(rows_bh), _ptr(rows_s), n, tau, sm,
+        _ptr(q), _ptr(k), _ptr(v), _ptr(kbias), BH, S, _ptr(rows_bh), _ptr(rows_s), n, tau, sm,
         int(mid_window), int(snap), int(nsplit), _ptr(out), _ptr(nres), nthreads or default_threads())
     if rc != 0:
         raise ValueError(f"oracle attention_exact_rows failed ({rc})")

@@ -231,6 +231,7 @@ struct HeadView {
   const double* kscale = nullptr;  // [nb]
   const double* V = nullptr;       // value values, unscaled
   double vscale = 1.0;
+  const double* kbias = nullptr;   // Q smoothing: beta_t = mu_q . k_t per key (NULL: none)
   int64_t n_rep = 0;               // repair set
   const int32_t* rep_idx = nullptr;
   const double* dV = nullptr;      // [n_rep][128] decoded residual codes
@@ -320,9 +321,11 @@ void attend_row(const double* q, double qscale, const HeadView& hv, const Params
     const int64_t k0 = j * 128;
     const int64_t nk = std::min<int64_t>(128, hv.S - k0);   // tail block
     const double a = 8.0 * kLog2e * P.sm * qscale * hv.kscale[j];
+    const double ab = 8.0 * kLog2e * P.sm * hv.kscale[j];   // Q smoothing's bias term
     double bm = -INFINITY;
     for (int64_t c = 0; c < nk; ++c) {
       Z[c] = a * dot128(q, hv.K + (k0 + c) * 128);
+      if (hv.kbias) Z[c] += ab * hv.kbias[k0 + c];
       bm = std::max(bm, Z[c]);
     }
     maybe_rescale(bm, P, &m8, &l, O, nullptr, &nres);
@@ -351,6 +354,7 @@ void attend_row(const double* q, double qscale, const HeadView& hv, const Params
       const int64_t t = hv.rep_idx[r0 + c];
       const double a = 8.0 * kLog2e * P.sm * qscale * hv.kscale[t / 128];
       Z[c] = a * dot128(q, hv.K + t * 128);
+      if (hv.kbias) Z[c] += 8.0 * kLog2e * P.sm * hv.kscale[t / 128] * hv.kbias[t];
       bm = std::max(bm, Z[c]);
     }
     maybe_rescale(bm, P, &m8, &l, O, Orep, &nres_rep);   // never fires: keys already seen
@@ -551,13 +555,13 @@ void ovc_oracle_quantize_v(const uint16_t* v, int fp16, int64_t B, int64_t S, in
 //   mu_b  = bf16( fl( (sum of v_t over the block, FP32 in token order) / n_b ) )
 //   R_t   = fl(v_t - mu_b)
 //   one scale per head from amax |R| (as for V),  code_t = E4M3(fl(R_t r))
-//   M'_b  = bf16( fl(mu_b r) )   (the mean in the scale's units)
-// so that the value restored for token t is s (dec(code_t) + M'_b).  The
-// means cost 16 bits per 128 elements of a channel (0.125 bit per element,
-// as the summary states).
-//   codes [B,H,S_pad,128] token-major; sv [B,H]; mu, mprime [B,H,nb,128].
+// The value restored for token t is s dec(code_t) + mu_b, with mu_b as
+// stored: 16 bits per 128 elements of a channel (0.125 bit per element, as
+// the summary states).  The restore itself is exact here (attention_rows
+// adds mu_b / s in double before the final multiplication by s).
+//   codes [B,H,S_pad,128] token-major; sv [B,H]; mu [B,H,nb,128].
 void ovc_oracle_vsmooth_v(const uint16_t* v, int fp16, int64_t B, int64_t S, int64_t H, int64_t sb, int64_t ss,
-                          int64_t sh, uint8_t* codes, float* sv, float* mu, float* mprime) {
+                          int64_t sh, uint8_t* codes, float* sv, float* mu) {
   const Dims dm = make_dims(B, S, H);
   std::vector<float> R(static_cast<size_t>(S) * 128);
   for (int64_t b = 0; b < B; ++b)
@@ -581,11 +585,6 @@ void ovc_oracle_vsmooth_v(const uint16_t* v, int fp16, int64_t B, int64_t S, int
       }
       const Scale sc = scale_from_amax(amax);
       sv[bh] = sc.s;
-      for (int64_t j = 0; j < dm.nb; ++j)
-        for (int d = 0; d < 128; ++d) {
-          volatile float mr = mu[(bh * dm.nb + j) * 128 + d] * sc.r;
-          mprime[(bh * dm.nb + j) * 128 + d] = bf16_bits_to_float(bf16_from_double(static_cast<double>(mr)));
-        }
       uint8_t* out = codes + bh * dm.S_pad * 128;
       for (int64_t t = 0; t < dm.S_pad; ++t)
         for (int d = 0; d < 128; ++d) out[t * 128 + d] = t < S ? quantize_value(R[t * 128 + d], sc.r) : 0;
@@ -595,42 +594,21 @@ void ovc_oracle_vsmooth_v(const uint16_t* v, int fp16, int64_t B, int64_t S, int
 // V-Smooth's grouping step ([VC-summary "V-Smooth": online k-means clusters
 // each head's value tokens; keys and values are permuted together, which
 // leaves non-causal attention unchanged): Lloyd's k-means with C clusters and
-// `iters` iterations, then the tokens ordered by (cluster, index).
-// Arithmetic, all FP32 with every step rounded; the only fused operation is
-// the multiply-add of the dot product (one rounding, as fmaf):
+// `iters` assignment steps, then the tokens ordered by (cluster, index).  The
+// summary gives neither C, the iteration count nor the start; the reading
+// here is the plainest one, computed in double:
 //   start:   mu_c = x_(floor(c S / C)), c = 0..C-1
-//   assign:  n_c = sum_d mu_cd^2 (channel order, products rounded);
-//            dot(t, c) = 16 partial sums over channels 8k..8k+7: the first
-//            product rounded, then p_k <- fma(x_i, mu_i, p_k) left to right;
-//            then the pairwise tree p_k <- p_k + p_(k+w), w = 8..1;
-//            d(t, c) = n_c - 2 dot(t, c); the cluster with the smallest d,
+//   assign:  the cluster with the smallest squared distance sum_d (x_d - mu_cd)^2,
 //            ties to the lower c
-//   update:  mu_c = (sum of its tokens) / count, the sum taken per 128-token
-//            block in token order and then over the blocks in block order; a
-//            cluster with no token keeps its centroid
+//   update:  mu_c = mean of its tokens; a cluster with no token keeps its
+//            centroid
 // One iteration is assign then update; the labels returned are those of the
 // last assignment, and centroids [B,H,C,128] the centroids it used.
-float kmeans_dot(const float* x, const float* mu) {
-  float p[16];
-  for (int k = 0; k < 16; ++k) {
-    volatile float a = x[8 * k] * mu[8 * k];
-    for (int i = 1; i < 8; ++i) a = std::fma(x[8 * k + i], mu[8 * k + i], static_cast<float>(a));
-    p[k] = a;
-  }
-  for (int w = 8; w >= 1; w >>= 1)
-    for (int k = 0; k < w; ++k) {
-      volatile float q = p[k] + p[k + w];
-      p[k] = q;
-    }
-  return p[0];
-}
-
 int ovc_oracle_kmeans_group(const uint16_t* v, int fp16, int64_t B, int64_t S, int64_t H, int64_t sb, int64_t ss,
-                            int64_t sh, int64_t C, int64_t iters, int32_t* labels, float* centroids, int32_t* perm) {
+                            int64_t sh, int64_t C, int64_t iters, int32_t* labels, double* centroids, int32_t* perm) {
   if (C < 1 || C > S || iters < 1) return 1;
-  const Dims dm = make_dims(B, S, H);
-  std::vector<float> x(static_cast<size_t>(S) * 128), mu(static_cast<size_t>(C) * 128), nrm(C);
-  std::vector<float> sum(static_cast<size_t>(C) * 128), part(static_cast<size_t>(C) * 128);
+  std::vector<double> x(static_cast<size_t>(S) * 128), mu(static_cast<size_t>(C) * 128);
+  std::vector<double> sum(static_cast<size_t>(C) * 128);
   std::vector<int64_t> cnt(C);
   for (int64_t b = 0; b < B; ++b)
     for (int64_t h = 0; h < H; ++h) {
@@ -638,52 +616,33 @@ int ovc_oracle_kmeans_group(const uint16_t* v, int fp16, int64_t B, int64_t S, i
       for (int64_t t = 0; t < S; ++t)
         for (int d = 0; d < 128; ++d) x[t * 128 + d] = input_bits_to_float(v[b * sb + t * ss + h * sh + d], fp16);
       for (int64_t c = 0; c < C; ++c)
-        std::memcpy(&mu[c * 128], &x[(c * S / C) * 128], 128 * sizeof(float));
+        std::memcpy(&mu[c * 128], &x[(c * S / C) * 128], 128 * sizeof(double));
       int32_t* lab = labels + bh * S;
       for (int64_t it = 0; it < iters; ++it) {
-        for (int64_t c = 0; c < C; ++c) {
-          volatile float n = 0.0f;
-          for (int d = 0; d < 128; ++d) {
-            volatile float sq = mu[c * 128 + d] * mu[c * 128 + d];
-            n = n + sq;
-          }
-          nrm[c] = n;
-        }
-        if (it + 1 == iters) std::memcpy(centroids + bh * C * 128, mu.data(), C * 128 * sizeof(float));
+        if (it + 1 == iters) std::memcpy(centroids + bh * C * 128, mu.data(), C * 128 * sizeof(double));
         for (int64_t t = 0; t < S; ++t) {
-          float best = INFINITY;
+          double best = INFINITY;
           int32_t arg = 0;
           for (int64_t c = 0; c < C; ++c) {
-            const float dot = kmeans_dot(&x[t * 128], &mu[c * 128]);
-            volatile float dist = nrm[c] - 2.0f * dot;
+            double dist = 0.0;
+            for (int d = 0; d < 128; ++d) {
+              const double e = x[t * 128 + d] - mu[c * 128 + d];
+              dist += e * e;
+            }
             if (dist < best) best = dist, arg = static_cast<int32_t>(c);
           }
           lab[t] = arg;
         }
         if (it + 1 == iters) break;
-        std::fill(sum.begin(), sum.end(), 0.0f);
+        std::fill(sum.begin(), sum.end(), 0.0);
         std::fill(cnt.begin(), cnt.end(), 0);
-        for (int64_t j = 0; j < dm.nb; ++j) {
-          std::fill(part.begin(), part.end(), 0.0f);
-          for (int64_t t = j * 128; t < std::min(S, j * 128 + 128); ++t) {
-            const int64_t c = lab[t];
-            ++cnt[c];
-            for (int d = 0; d < 128; ++d) {
-              volatile float a = part[c * 128 + d] + x[t * 128 + d];
-              part[c * 128 + d] = a;
-            }
-          }
-          for (int64_t i = 0; i < C * 128; ++i) {
-            volatile float a = sum[i] + part[i];
-            sum[i] = a;
-          }
+        for (int64_t t = 0; t < S; ++t) {
+          ++cnt[lab[t]];
+          for (int d = 0; d < 128; ++d) sum[lab[t] * 128 + d] += x[t * 128 + d];
         }
         for (int64_t c = 0; c < C; ++c)
           if (cnt[c] > 0)
-            for (int d = 0; d < 128; ++d) {
-              volatile float m = sum[c * 128 + d] / static_cast<float>(cnt[c]);
-              mu[c * 128 + d] = m;
-            }
+            for (int d = 0; d < 128; ++d) mu[c * 128 + d] = sum[c * 128 + d] / static_cast<double>(cnt[c]);
       }
       // tokens ordered by (cluster, index)
       std::vector<int32_t> order(S);
@@ -746,8 +705,8 @@ void ovc_oracle_repair_quantize(const uint16_t* v, int fp16, int64_t B, int64_t 
 // (used to compare the device's P bytes under the device's own reference);
 // cast = 1 gives the exp-then-cast bytes.
 void ovc_oracle_block_codes(const uint8_t* qrow, float sq, const uint8_t* kcodes_head,
-                            const float* sk_head, int64_t S, int64_t j, double m8, double c0,
-                            double beta, double sm, int cast, uint8_t* codes) {
+                            const float* sk_head, const double* kbias_head, int64_t S, int64_t j, double m8,
+                            double c0, double beta, double sm, int cast, uint8_t* codes) {
   double q[128];
   for (int d = 0; d < 128; ++d) q[d] = e4m3_value(qrow[d]);
   Params P{c0, beta, 0.75, sm, 0, 1, 1, cast};
@@ -760,8 +719,10 @@ void ovc_oracle_block_codes(const uint8_t* qrow, float sq, const uint8_t* kcodes
     }
     double k[128];
     for (int d = 0; d < 128; ++d) k[d] = e4m3_value(kcodes_head[t * 128 + d]);
+    double Z = a * dot128(q, k);
+    if (kbias_head) Z += 8.0 * kLog2e * sm * static_cast<double>(sk_head[j]) * kbias_head[t];
     uint8_t code;
-    prob(a * dot128(q, k), m8, P, &code);
+    prob(Z, m8, P, &code);
     codes[c] = code;
   }
 }
@@ -770,9 +731,13 @@ void ovc_oracle_block_codes(const uint8_t* qrow, float sq, const uint8_t* kcodes
 // natural key order) for a list of query rows (b*H+h, s).  Inputs are the
 // oracle's own quantised tensors: qc/kc [B,H,S_pad,128], sq/sk [B,H,nb],
 // vc token-major [B,H,S_pad,128], sv [B,H].  Optional repair set: rep_idx
-// [B,H,n_rep], rep_dcodes [B,H,n_rep,128], sr [B,H].  vmean (V-Smooth, not
-// with repair): [B,H,nb,128] restored block means M'_b, added to every decoded
-// value of the block (the row-sum restore: sum_t p_t M'_b(t) = sum_b l_b M'_b).
+// [B,H,n_rep], rep_dcodes [B,H,n_rep,128], sr [B,H].  vmu (V-Smooth, not
+// with repair): [B,H,nb,128] block means mu_b in V's own units; token t of
+// block b is restored as s_v dec(code_t) + mu_b (the row-sum restore:
+// sum_t p_t mu_b(t) = sum_b l_b mu_b), in double.  kbias (Q smoothing, else
+// NULL): [B,H,S] beta_t = mu_q . dec(code_t), the per-key bias; each score of
+// key t gains 8 log2(e) sm s_k beta_t, so the score is the exact product of
+// the query mu_q + s_q dec(Q^') with the key s_k dec(K^_t).
 // Outputs per row: out
 // [nrows,128] (double), m8, l, nres [nrows,2] (main, repair).  If dump_codes
 // is given, the codes of key block dump_block are written per row
@@ -780,14 +745,15 @@ void ovc_oracle_block_codes(const uint8_t* qrow, float sq, const uint8_t* kcodes
 int ovc_oracle_attention_rows(const uint8_t* qc, const float* sq, const uint8_t* kc, const float* sk,
                               const uint8_t* vc, const float* sv, int64_t B, int64_t S, int64_t H,
                               const int32_t* rep_idx, const uint8_t* rep_dcodes, const float* sr,
-                              int64_t n_rep, const float* vmean, const int64_t* row_bh, const int64_t* row_s,
+                              int64_t n_rep, const float* vmu, const double* kbias, const int64_t* row_bh,
+                              const int64_t* row_s,
                               int64_t nrows, double c0, double beta, double tau, double sm,
                               int mid_window, int snap, int cast, int64_t nsplit, double* out, double* m8_out, double* l_out,
                               int32_t* nres_out, int64_t dump_block, uint8_t* dump_codes,
                               double* dump_m8, int nthreads) {
   const Dims dm = make_dims(B, S, H);
   const Params P{c0, beta, tau, sm, 0, mid_window, snap, cast};
-  if (nsplit < 1 || nsplit > dm.nb || (nsplit > 1 && n_rep > 0) || (vmean && n_rep > 0)) return 3;
+  if (nsplit < 1 || nsplit > dm.nb || (nsplit > 1 && n_rep > 0) || (vmu && n_rep > 0)) return 3;
   // Process the rows head by head so that one head's keys are decoded once.
   std::vector<int64_t> perm(nrows);
   for (int64_t i = 0; i < nrows; ++i) perm[i] = i;
@@ -805,7 +771,9 @@ int ovc_oracle_attention_rows(const uint8_t* qc, const float* sq, const uint8_t*
       for (int d = 0; d < 128; ++d) {
         K[t * 128 + d] = e4m3_value(kc[(bh * dm.S_pad + t) * 128 + d]);
         V[t * 128 + d] = e4m3_value(vc[(bh * dm.S_pad + t) * 128 + d]) +
-                         (vmean ? static_cast<double>(vmean[(bh * dm.nb + t / 128) * 128 + d]) : 0.0);
+                         (vmu ? static_cast<double>(vmu[(bh * dm.nb + t / 128) * 128 + d]) /
+                                    static_cast<double>(sv[bh])
+                              : 0.0);
       }
     ks.assign(sk + bh * dm.nb, sk + (bh + 1) * dm.nb);
     HeadView hv;
@@ -815,6 +783,7 @@ int ovc_oracle_attention_rows(const uint8_t* qc, const float* sq, const uint8_t*
     hv.kscale = ks.data();
     hv.V = V.data();
     hv.vscale = sv[bh];
+    hv.kbias = kbias ? kbias + bh * S : nullptr;
     if (n_rep > 0 && rep_idx) {
       dV.assign(n_rep * 128, 0.0);
       for (int64_t i = 0; i < n_rep * 128; ++i) dV[i] = e4m3_value(rep_dcodes[bh * n_rep * 128 + i]);
@@ -852,9 +821,10 @@ int ovc_oracle_attention_rows(const uint8_t* qc, const float* sq, const uint8_t*
 
 // The same online-softmax skeleton (traversal, lazy rescale, tail mask) on
 // raw double inputs with p = 2^((Z - m8)/8) exactly: must equal plain
-// softmax attention.  q/k/v: [BH,S,128]; rows as above.
-int ovc_oracle_attention_exact_rows(const double* q, const double* k, const double* v, int64_t BH,
-                                    int64_t S, const int64_t* row_bh, const int64_t* row_s,
+// softmax attention.  q/k/v: [BH,S,128]; rows as above; kbias (or NULL):
+// [BH,S] a per-key term added to every score (Q smoothing's bias).
+int ovc_oracle_attention_exact_rows(const double* q, const double* k, const double* v, const double* kbias,
+                                    int64_t BH, int64_t S, const int64_t* row_bh, const int64_t* row_s,
                                     int64_t nrows, double tau, double sm, int mid_window, int snap,
                                     int64_t nsplit, double* out, int32_t* nres_out, int nthreads) {
   const Dims dm = make_dims(1, S, 1);
@@ -874,6 +844,7 @@ int ovc_oracle_attention_exact_rows(const double* q, const double* k, const doub
     hv.K = k + bh * S * 128;
     hv.kscale = ones.data();
     hv.V = v + bh * S * 128;
+    hv.kbias = kbias ? kbias + bh * S : nullptr;
     RowResult rr;
     attend_row_split(q + (bh * S + s) * 128, 1.0, hv, P, nsplit, &rr, -1, nullptr, nullptr);
     std::memcpy(out + r * 128, rr.O, sizeof(rr.O));

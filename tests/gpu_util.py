@@ -23,12 +23,5 @@ def oracle_prep(q, k, v):
     return oracle.Prepared(W.bf16_bits(q), W.bf16_bits(k), W.bf16_bits(v))
 
 
-def n_auto(B, S, H):
-    """Key ranges the library chooses by itself for these dimensions on this
-    GPU; the oracle must run the same split to compare (1: no split)."""
-    import fp8_bit_attention_gb300 as ovc
-    return ovc.auto_split(B, S, H)
-
-
 def to_dev(*xs):
     return tuple(x.cuda() for x in xs)

@@ -114,9 +114,7 @@ def test_host_validation_rejects_bad_arguments(lib):
         assert lib.ovc_attention_workspace_bytes(ctypes.byref(p8), n) == want
     assert lib.ovc_attention_workspace_bytes(ctypes.byref(p8), 1) == 0
     assert lib.ovc_attention_workspace_bytes(ctypes.byref(p8), 9) == 0
-    if not torch.cuda.is_available():
-        assert lib.ovc_attention_workspace_bytes(ctypes.byref(p8), 0) == 0   # automatic needs a device
-        assert lib.ovc_attention_auto_split(1, 1000, 1) == 1
+    assert lib.ovc_attention_workspace_bytes(ctypes.byref(p8), 0) == 0   # 0: no split, never automatic
 
 
 def test_status_strings(lib):
@@ -168,7 +166,7 @@ def test_prepare_options_on_the_host(lib):
     assert smooth >= base + 56 * 574 * 128 * 4 + 56 * 128 * 4
     vsm = lib.ovc_prepare_workspace_bytes_ex(1, 73397, 56, 128, _abi.OVC_PREPARE_V_SMOOTH)
     assert vsm >= base + 56 * 574 * 128 * 4 + 56 * 128 * 576 * 2     # block means + M' tiles
-    assert lib.ovc_prepare_workspace_bytes_ex(1, 73397, 56, 128, 4) == 0        # unknown flag
+    assert lib.ovc_prepare_workspace_bytes_ex(1, 73397, 56, 128, 8) == 0        # unknown flag
     t = _abi.OvcTensor(0x1000, _abi.OVC_BF16, 1, 128, 1, 128, 128 * 128, 128, 128)
     out = _abi.OvcPrepared()
     st = lib.ovc_prepare_ex(ctypes.byref(t), ctypes.byref(t), ctypes.byref(t), 12, ctypes.c_void_p(0x100000),
@@ -200,3 +198,20 @@ def test_empty_inputs_give_an_empty_output_without_a_launch():
         assert o.shape == q.shape and o.dtype == torch.bfloat16 and o.numel() == 0
     with pytest.raises(ValueError):
         ovc.attention(torch.zeros((0, 4, 128)), torch.zeros((0, 5, 128)), torch.zeros((0, 4, 128)))
+
+
+def test_prepare_flag_workspaces(lib):
+    """Q smoothing adds its means and one 32-byte bias row per padded key;
+    it does not combine with V-Smooth; unknown flags size to 0."""
+    from fp8_bit_attention_gb300 import _abi
+    B, S, H = 1, 1000, 2
+    plain = lib.ovc_prepare_workspace_bytes_ex(B, S, H, 128, 0)
+    qs = lib.ovc_prepare_workspace_bytes_ex(B, S, H, 128, _abi.OVC_PREPARE_SMOOTH_Q)
+    assert qs >= plain + B * H * 1024 * 32 + B * H * 128 * 4
+    assert lib.ovc_prepare_workspace_bytes_ex(B, S, H, 128, _abi.OVC_PREPARE_SMOOTH_Q | _abi.OVC_PREPARE_V_SMOOTH) == 0
+    assert lib.ovc_prepare_workspace_bytes_ex(B, S, H, 128, 8) == 0
+    t = _abi.OvcTensor(0x1000, _abi.OVC_BF16, B, S, H, 128, S * H * 128, H * 128, 128)
+    out = _abi.OvcPrepared()
+    assert lib.ovc_prepare_ex(ctypes.byref(t), ctypes.byref(t), ctypes.byref(t),
+                              _abi.OVC_PREPARE_SMOOTH_Q | _abi.OVC_PREPARE_V_SMOOTH, ctypes.c_void_p(0x100000),
+                              1 << 30, ctypes.byref(out), None) == _abi.OVC_ERR_INVALID_ARG

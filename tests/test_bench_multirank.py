@@ -52,3 +52,36 @@ def test_single_process_defaults():
     w = W.WORKLOADS["small"]
     assert bench.rank_workload(w, 0) is w
     assert bench.max_over_ranks(3.5) == 3.5
+
+
+def _bench(args, extra_env=None, timeout=180):
+    import json
+    import subprocess
+    import sys
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    env.update(extra_env or {})
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), *args], capture_output=True, text=True,
+                       timeout=timeout, env=env, cwd=root)
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    return r.returncode, [json.loads(ln) for ln in lines], r.stderr
+
+
+def test_gpus_flag_starts_one_rank_per_gpu():
+    """`bench.py --gpus 2` run directly starts two ranks itself (through
+    torch.distributed.run); both join the process group and one line reports
+    n_gpus = 2."""
+    rc, lines, err = _bench(["--gpus", "2", "--dry-run"])
+    assert rc == 0, err
+    assert len(lines) == 1
+    assert lines[0]["n_gpus"] == 2 and lines[0]["ranks_joined"] == 2 and lines[0]["dry_run"] is True
+
+
+def test_gpus_flag_must_match_world_size():
+    rc, lines, err = _bench(["--gpus", "2", "--dry-run"],
+                            {"WORLD_SIZE": "3", "RANK": "0", "LOCAL_RANK": "0"})
+    assert rc != 0 and not lines
+    assert "WORLD_SIZE=3" in err
+    rc, lines, _ = _bench(["--dry-run"])
+    assert rc == 0 and lines[0]["n_gpus"] == 1

@@ -69,7 +69,7 @@ def test_full_size_sampled_parity(name):
                               ref.energy[0, 0].view(np.uint32))
         # sampled output rows
         rows = _sample_rows(S, nb, rng)
-        r = oracle.attention_rows(ref, np.zeros_like(rows), rows, nsplit=ovc.auto_split(B, S, H))
+        r = oracle.attention_rows(ref, np.zeros_like(rows), rows)
         got = o_cpu[b, rows, h, :]
         assert np.isfinite(got).all()
         assert rel_l2(got, r["out"]) <= TOL_REL_L2, (name, b, h)

@@ -14,7 +14,7 @@ import oracle
 import fp8_bit_attention_gb300 as ovc
 from fp8_bit_attention_gb300 import workloads as W
 
-from gpu_util import TOL_REL_L2, inputs, n_auto, oracle_prep, rel_l2, to_dev
+from gpu_util import TOL_REL_L2, inputs, oracle_prep, rel_l2, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -50,7 +50,7 @@ def test_prepare_bit_exact(B, H, S):
 @pytest.mark.parametrize("B,H,S", SHAPES)
 def test_attention_matches_oracle(B, H, S):
     q, k, v = inputs(B, H, S, seed=200 + S)
-    ref, _ = oracle.attention_full(oracle_prep(q, k, v), nsplit=n_auto(B, S, H))
+    ref, _ = oracle.attention_full(oracle_prep(q, k, v))
     o = ovc.attention(*to_dev(q, k, v))
     assert ovc.device_status() == 0
     got = o.float().cpu().numpy()
@@ -60,7 +60,7 @@ def test_attention_matches_oracle(B, H, S):
 
 def test_attention_3d_layout_and_strided_inputs():
     q, k, v = inputs(1, 2, 700, seed=301)
-    ref, _ = oracle.attention_full(oracle_prep(q, k, v), nsplit=n_auto(1, 700, 2))
+    ref, _ = oracle.attention_full(oracle_prep(q, k, v))
     qd, kd, vd = to_dev(q, k, v)
     o3 = ovc.attention(qd[0], kd[0], vd[0])                       # [S,H,128]
     assert rel_l2(o3.float().cpu().numpy(), ref[0]) <= TOL_REL_L2
@@ -85,7 +85,7 @@ def test_persistent_and_plain_schedules_agree_bitwise():
 
 def test_softmax_scale_argument():
     q, k, v = inputs(1, 1, 512, seed=303)
-    ref, _ = oracle.attention_full(oracle_prep(q, k, v), sm=0.05, nsplit=n_auto(1, 512, 1))
+    ref, _ = oracle.attention_full(oracle_prep(q, k, v), sm=0.05)
     o = ovc.attention(*to_dev(q, k, v), softmax_scale=0.05)
     assert rel_l2(o.float().cpu().numpy(), ref) <= TOL_REL_L2
 
@@ -144,7 +144,7 @@ def test_timeout_path_reports_and_recovers():
     prep = ovc.prepare(*to_dev(q, k, v))
     ovc.attention_probe(prep, skip_mma=True, wait_timeout_ns=20_000_000)
     assert ovc.device_status() == 5          # OVC_ERR_TIMEOUT, context still usable
-    ref, _ = oracle.attention_full(oracle_prep(q, k, v), nsplit=n_auto(1, 512, 1))
+    ref, _ = oracle.attention_full(oracle_prep(q, k, v))
     o = ovc.attention_prepared(prep)
     assert ovc.device_status() == 0
     assert rel_l2(o.float().cpu().numpy(), ref) <= TOL_REL_L2
@@ -206,7 +206,7 @@ def test_fp16_inputs_match_oracle(B, H, S):
     o = ovc.attention_prepared(prep).float().cpu().numpy()
     bh = np.repeat(np.arange(B * H), S)
     ss = np.tile(np.arange(S), B * H)
-    r = oracle.attention_rows(ref, bh, ss, nsplit=n_auto(B, S, H))["out"].reshape(B, H, S, 128).transpose(0, 2, 1, 3)
+    r = oracle.attention_rows(ref, bh, ss)["out"].reshape(B, H, S, 128).transpose(0, 2, 1, 3)
     assert rel_l2(o, r) <= TOL_REL_L2
     rep = ovc.prepare_v_repair(vd, prep, 0.02)
     rr = oracle.Repair(ref, 0.02)
@@ -236,7 +236,7 @@ def test_k_smoothing_matches_oracle(B, H, S, fp16):
     o = ovc.attention_prepared(prep).float().cpu().numpy()
     bh = np.repeat(np.arange(B * H), S)
     ss = np.tile(np.arange(S), B * H)
-    r = oracle.attention_rows(ref, bh, ss, nsplit=n_auto(B, S, H))["out"].reshape(B, H, S, 128).transpose(0, 2, 1, 3)
+    r = oracle.attention_rows(ref, bh, ss)["out"].reshape(B, H, S, 128).transpose(0, 2, 1, 3)
     assert rel_l2(o, r) <= TOL_REL_L2
     dev = ovc.attention(qd, kd, vd, smooth_k=True).cpu()
     host = ovc.attention(q.pin_memory(), k.pin_memory(), v.pin_memory(), smooth_k=True)
@@ -274,13 +274,13 @@ def test_attention_variants_match_oracle(flags, cast, natural, B, H, S):
     q, k, v = inputs(B, H, S, seed=600 + S)
     ref, _ = oracle.attention_full(oracle_prep(q, k, v), cast=cast, mid_window=not natural)
     prep = ovc.prepare(*to_dev(q, k, v))
-    o = ovc.attention_prepared(prep, flags=flags, nsplit=1)
+    o = ovc.attention_prepared(prep, flags=flags)
     assert ovc.device_status() == 0
     got = o.float().cpu().numpy()
     assert np.isfinite(got).all()
     assert rel_l2(got, ref) <= TOL_REL_L2
     if cast or (S + 127) // 128 > 1:              # one key block: both orders coincide
-        base = ovc.attention_prepared(prep, nsplit=1).float().cpu().numpy()
+        base = ovc.attention_prepared(prep).float().cpu().numpy()
         assert not np.array_equal(got, base)      # the variant really ran
 
 
@@ -322,7 +322,7 @@ def test_baseline_with_repair_and_schedules():
 
 def test_baseline_attention_entry_point():
     q, k, v = inputs(1, 2, 700, seed=801)
-    want, _ = oracle.attention_full(oracle_prep(q, k, v), cast=True, mid_window=False, nsplit=n_auto(1, 700, 2))
+    want, _ = oracle.attention_full(oracle_prep(q, k, v), cast=True, mid_window=False)
     o = ovc.baseline_attention(*to_dev(q, k, v))
     assert rel_l2(o.float().cpu().numpy(), want) <= TOL_REL_L2
 
@@ -358,23 +358,49 @@ def test_split_key_ranges_with_variants(flags, cast, natural):
     assert rel_l2(o.float().cpu().numpy(), want) <= TOL_REL_L2
 
 
-def test_auto_split_on_short_sequences_and_strided_output():
-    """Seven heads of 8192 tokens (224 tiles): the library splits on its own;
-    sampled rows match the oracle run with the same split; output strides
-    are honoured by the merge pass."""
+def test_default_entry_points_give_the_c_call_result_bit_for_bit():
+    """No entry point splits by itself: attention(), attention_prepared()
+    and the host-buffer path give ovc_attention's result bit for bit on
+    seven heads of 8192 tokens (224 tile pairs, too few for two full waves
+    of a GB300), whatever the GPU, and that result is the method's."""
+    import ctypes
+
+    from fp8_bit_attention_gb300 import _abi
     B, H, S = 1, 7, 8192
-    n = ovc.auto_split(B, S, H)
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    if sms == 152:
-        assert n == 2
-    assert ovc.auto_split(1, 73397, 56) == 1          # persistent schedule: never split
     q, k, v = inputs(B, H, S, seed=960)
+    qd, kd, vd = to_dev(q, k, v)
+    prep = ovc.prepare(qd, kd, vd)
+    o_c = torch.empty_like(qd)
+    od = _abi.OvcOutput(o_c.data_ptr(), o_c.stride(0), o_c.stride(1), o_c.stride(2))
+    assert _abi.lib().ovc_attention(ctypes.byref(prep.desc), 0.0, ctypes.byref(od),
+                                    ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)) == _abi.OVC_OK
+    assert torch.equal(ovc.attention_prepared(prep), o_c)
+    assert torch.equal(ovc.attention(qd, kd, vd), o_c)
+    host = ovc.attention(q.pin_memory(), k.pin_memory(), v.pin_memory())
+    assert torch.equal(host.view(torch.int16), o_c.cpu().view(torch.int16))
+    assert ovc.attention_workspace_bytes(prep, 0) == 0 and ovc.attention_workspace_bytes(prep, 1) == 0
+    assert ovc.device_status() == 0
+    ref = oracle_prep(q, k, v)
+    rng = np.random.default_rng(961)
+    rows = np.unique(np.concatenate([rng.integers(0, S, 40), [0, S - 1, 4096]]))
+    got = o_c.float().cpu().numpy()
+    for h in (0, H - 1):
+        r = oracle.attention_rows(ref, np.full_like(rows, h), rows)["out"]
+        assert rel_l2(got[0, rows, h], r) <= TOL_REL_L2
+
+
+def test_forced_split_into_a_strided_output():
+    """A split the caller asks for (n = 2 on seven heads of 8192 tokens)
+    matches the oracle run with the same split on sampled rows; the merge
+    pass honours the output strides."""
+    B, H, S, n = 1, 7, 8192, 2
+    q, k, v = inputs(B, H, S, seed=962)
     ref = oracle_prep(q, k, v)
     prep = ovc.prepare(*to_dev(q, k, v))
     big = torch.zeros((B, S, H, 256), dtype=torch.bfloat16, device="cuda")
-    ovc.attention_prepared(prep, out=big[..., 64:192])
+    ovc.attention_prepared(prep, out=big[..., 64:192], nsplit=n)
     assert ovc.device_status() == 0
-    rng = np.random.default_rng(961)
+    rng = np.random.default_rng(963)
     rows = np.unique(np.concatenate([rng.integers(0, S, 40), [0, S - 1, 4096]]))
     got = big.float().cpu().numpy()
     for h in (0, H - 1):
@@ -412,6 +438,18 @@ def _vsmooth_inputs(B, H, S, seed, offset=20.0):
     return q, k, v
 
 
+def _check_restored_means(prep, ref):
+    """The kernel restores the block means through a BF16 MMA operand, the
+    mean in V-scale units M' = bf16(mu_b / s_v) (as the product fl(mu_b r)).
+    The oracle keeps mu_b exact; M' must be that value within one BF16
+    rounding (2^-8 relative: 7 stored mantissa bits) plus the rounding of the
+    product."""
+    nb = ref.nb
+    mp = prep.v_means().float().cpu().numpy()[..., :nb].transpose(0, 1, 3, 2).astype(np.float64)
+    want = ref.vmu.astype(np.float64) / ref.sv.astype(np.float64)[:, :, None, None]
+    assert np.all(np.abs(mp - want) <= 2.0 ** -8 * np.abs(want) * (1 + 2.0 ** -20) + 1e-30)
+
+
 @pytest.mark.parametrize("B,H,S", [(1, 2, 1024), (1, 1, 1), (1, 2, 129), (2, 3, 300), (1, 2, 1000), (1, 1, 2300)])
 def test_v_smooth_prepare_bit_exact_and_attention(B, H, S):
     q, k, v = _vsmooth_inputs(B, H, S, seed=1100 + S)
@@ -421,9 +459,7 @@ def test_v_smooth_prepare_bit_exact_and_attention(B, H, S):
     assert np.array_equal(prep.vt_codes().cpu().numpy().transpose(0, 1, 3, 2), ref.vc)
     assert np.array_equal(prep.v_scales().cpu().numpy(), ref.sv)
     assert np.array_equal(prep.q_codes().cpu().numpy(), ref.qc) and np.array_equal(prep.k_codes().cpu().numpy(), ref.kc)
-    nb = (S + 127) // 128
-    mp = prep.v_means().float().cpu().numpy()[..., :nb].transpose(0, 1, 3, 2)
-    assert np.array_equal(mp, ref.vmean)
+    _check_restored_means(prep, ref)
     want, _ = oracle.attention_full(ref)
     o = ovc.attention_prepared(prep)
     assert ovc.device_status() == 0
@@ -468,23 +504,94 @@ def _clustered_inputs(B, H, S, seed, centres=6):
     return q, k, torch.from_numpy(v).to(torch.bfloat16)
 
 
+def _kmeans_dist(x, mu):
+    """Squared distances [S, C] in double, and the size of the FP32 error the
+    kernel's evaluation n_c - 2 x.mu may make in each (it sums 128 products
+    and 128 squares in FP32: below 128 ulps of the magnitudes involved)."""
+    d = ((x[:, None, :] - mu[None, :, :]) ** 2).sum(-1)
+    err = 2.0 ** -24 * 160 * ((mu ** 2).sum(-1)[None, :] + 2.0 * np.abs(x) @ np.abs(mu).T)
+    return d, err
+
+
+def _check_kmeans_step(x, labels, mu):
+    """labels: a nearest centroid of mu for every token, within the FP32
+    error bound of the two distances compared."""
+    d, err = _kmeans_dist(x, mu)
+    best = d.argmin(axis=1)
+    idx = np.arange(len(x))
+    assert np.all(d[idx, labels] - d[idx, best] <= err[idx, labels] + err[idx, best])
+
+
 @pytest.mark.parametrize("B,H,S,C,iters", [(1, 1, 1, 1, 1), (1, 2, 200, 7, 3), (2, 3, 300, 16, 4),
                                            (1, 2, 1000, 16, 4), (1, 1, 2300, 64, 2)])
-def test_grouping_bit_exact_and_grouped_v_smooth(B, H, S, C, iters):
+def test_grouping_is_lloyds_algorithm(B, H, S, C, iters):
+    """k-means labels have several correct answers at near ties, so the
+    GPU's grouping is checked for what Lloyd's algorithm fixes, step by step
+    on its own state (each run of i steps is the first i steps of a longer
+    one): the first centroids are the tokens floor(c S / C) exactly; every
+    assignment is a nearest centroid within the FP32 rounding bound; every
+    update is the members' mean within the FP32 summation bound (an empty
+    cluster keeps its centroid); the permutation is ordered by (label,
+    index).  The first assignment, made from the same centroids as the
+    oracle's, must agree with the oracle's wherever the choice is clear by
+    more than that bound."""
     q, k, v = _clustered_inputs(B, H, S, seed=1300 + S)
-    labels, _, perm_ref = oracle.kmeans_group(W.bf16_bits(v), C, iters)
-    qd, kd, vd = to_dev(q, k, v)
-    perm = ovc.group_v(vd, clusters=C, iters=iters)
-    torch.cuda.synchronize()
-    assert np.array_equal(perm.cpu().numpy(), perm_ref)
+    vd = v.cuda()
+    x_all = v.float().numpy().astype(np.float64)              # [B,S,H,128]
+    states = []
+    for i in range(1, iters + 1):
+        perm, labels, cent = ovc.group_v(vd, clusters=C, iters=i, return_state=True)
+        torch.cuda.synchronize()
+        states.append((perm.cpu().numpy(), labels.cpu().numpy().copy(), cent.cpu().numpy().astype(np.float64)))
+    lab1_ref, _, _ = oracle.kmeans_group(W.bf16_bits(v), C, 1)
+    nb = (S + 127) // 128
+    for b in range(B):
+        for h in range(H):
+            x = x_all[b, :, h, :]
+            start = x[(np.arange(C) * S) // C]
+            assert np.array_equal(states[0][2][b, h], start)
+            for i, (perm, labels, cent) in enumerate(states):
+                lab, mu = labels[b, h], cent[b, h]
+                _check_kmeans_step(x, lab, mu)
+                p = perm[b, h]
+                assert np.array_equal(np.sort(p), np.arange(S))
+                key = lab[p].astype(np.int64) * S + p
+                assert np.all(np.diff(key) > 0)
+                if i + 1 < len(states):
+                    nxt = states[i + 1][2][b, h]
+                    for c in range(C):
+                        m = lab == c
+                        if not m.any():
+                            assert np.array_equal(nxt[c], mu[c])
+                            continue
+                        mean = x[m].mean(axis=0)
+                        bound = 2.0 ** -24 * (m.sum() + nb + 4) * np.abs(x[m]).mean(axis=0) + 1e-30
+                        assert np.all(np.abs(nxt[c] - mean) <= bound), (i, c)
+            # the first step against the oracle's, where the choice is clear
+            d, err = _kmeans_dist(x, start)
+            srt = np.sort(d, axis=1)
+            margin = srt[:, 1] - srt[:, 0] if C > 1 else np.full(S, np.inf)
+            clear = margin > 2 * err.max(axis=1)
+            assert clear.mean() > 0.5
+            assert np.array_equal(states[0][1][b, h][clear], lab1_ref[b, h][clear])
+
+
+@pytest.mark.parametrize("B,H,S,C,iters", [(1, 2, 200, 7, 3), (2, 3, 300, 16, 4), (1, 1, 2300, 64, 2)])
+def test_grouped_v_smooth_prepare_bit_exact(B, H, S, C, iters):
+    """Preparation in a grouping order -- the oracle's own k-means order,
+    handed to the GPU -- gives the oracle's grouped V-Smooth tensors bit for
+    bit and its attention output within 5e-3."""
+    q, k, v = _clustered_inputs(B, H, S, seed=1300 + S)
+    _, _, perm_ref = oracle.kmeans_group(W.bf16_bits(v), C, iters)
     ref = oracle.Prepared(W.bf16_bits(q), W.bf16_bits(k), W.bf16_bits(v), v_smooth=True, perm=perm_ref)
+    qd, kd, vd = to_dev(q, k, v)
+    perm = torch.from_numpy(perm_ref).cuda()
     prep = ovc.prepare(qd, kd, vd, v_smooth=True, perm=perm)
     torch.cuda.synchronize()
     assert np.array_equal(prep.k_codes().cpu().numpy(), ref.kc) and np.array_equal(prep.k_scales().cpu().numpy(), ref.sk)
     assert np.array_equal(prep.vt_codes().cpu().numpy().transpose(0, 1, 3, 2), ref.vc)
     assert np.array_equal(prep.v_scales().cpu().numpy(), ref.sv)
-    nb = (S + 127) // 128
-    assert np.array_equal(prep.v_means().float().cpu().numpy()[..., :nb].transpose(0, 1, 3, 2), ref.vmean)
+    _check_restored_means(prep, ref)
     want, _ = oracle.attention_full(ref)
     o = ovc.attention_prepared(prep)
     assert ovc.device_status() == 0
@@ -515,8 +622,10 @@ def test_grouping_keeps_attention_and_lowers_v_smooth_error():
 
 
 def test_fp16_3d_inputs_through_grouping_v_smooth_and_split():
-    """FP16 [S,H,128] inputs: grouping permutation and grouped V-Smooth
-    preparation bit-exact, O within 5e-3; split key ranges on FP16 inputs."""
+    """FP16 [S,H,128] inputs: the grouping is Lloyd's algorithm on the FP16
+    values (first step checked), grouped V-Smooth preparation in the
+    oracle's order bit-exact, O within 5e-3; split key ranges on FP16
+    inputs."""
     B, H, S = 1, 2, 1100
     q, k, v = _clustered_inputs(B, H, S, seed=1500)
     q, k, v = (x.to(torch.float16) for x in (q, k, v))
@@ -524,9 +633,11 @@ def test_fp16_3d_inputs_through_grouping_v_smooth_and_split():
     _, _, perm_ref = oracle.kmeans_group(bits[2], 8, 3, fp16=True)
     ref = oracle.Prepared(*bits, fp16=True, v_smooth=True, perm=perm_ref)
     qd, kd, vd = (x[0].cuda() for x in (q, k, v))               # [S,H,128]
-    perm = ovc.group_v(vd, clusters=8, iters=3)
-    assert np.array_equal(perm.cpu().numpy(), perm_ref)
-    prep = ovc.prepare(qd, kd, vd, v_smooth=True, perm=perm)
+    _, lab, cent = ovc.group_v(vd, clusters=8, iters=1, return_state=True)
+    xv = v.float().numpy().astype(np.float64)
+    for h in range(H):
+        _check_kmeans_step(xv[0, :, h], lab[0, h].cpu().numpy(), cent[0, h].cpu().numpy().astype(np.float64))
+    prep = ovc.prepare(qd, kd, vd, v_smooth=True, perm=torch.from_numpy(perm_ref).cuda())
     torch.cuda.synchronize()
     assert np.array_equal(prep.vt_codes().cpu().numpy().transpose(0, 1, 3, 2), ref.vc)
     assert np.array_equal(prep.k_codes().cpu().numpy(), ref.kc)
@@ -679,3 +790,217 @@ def test_k_smoothing_with_repair(B, H, S, budget):
     o = ovc.attention_v_repair(prep, rep)
     assert ovc.device_status() == 0
     assert rel_l2(o.float().cpu().numpy(), want) <= TOL_REL_L2
+
+
+# ---- degenerate inputs and sharp rows ---------------------------------------
+def test_all_zero_blocks_and_heads():
+    """All-zero data takes the scale-1 path of the quantiser: a zero V head
+    (its output must be exactly 0), a zero K block (its scores are all 0), a
+    zero Q block (all its scores are 0: a uniform row), and a zero tail
+    block.  Prepared tensors bit-exact, O within 5e-3, the zero head's O
+    exactly 0."""
+    B, H, S = 1, 3, 700                      # nb = 6, tail block of 60 tokens
+    q, k, v = inputs(B, H, S, seed=2400)
+    v[0, :, 0] = 0                           # head 0: V all zero
+    k[0, 256:384, 1] = 0                     # head 1: K block 2 zero
+    q[0, 128:256, 1] = 0                     # head 1: Q block 1 zero
+    q[0, 640:, 2] = 0                        # head 2: the ragged tail block of Q, K and V zero
+    k[0, 640:, 2] = 0
+    v[0, 640:, 2] = 0
+    ref = oracle_prep(q, k, v)
+    prep = ovc.prepare(*to_dev(q, k, v))
+    torch.cuda.synchronize()
+    assert np.array_equal(prep.q_codes().cpu().numpy(), ref.qc)
+    assert np.array_equal(prep.k_codes().cpu().numpy(), ref.kc)
+    assert np.array_equal(prep.q_scales().cpu().numpy(), ref.sq)
+    assert np.array_equal(prep.k_scales().cpu().numpy(), ref.sk)
+    assert np.array_equal(prep.v_scales().cpu().numpy(), ref.sv)
+    assert np.array_equal(prep.vt_codes().cpu().numpy().transpose(0, 1, 3, 2), ref.vc)
+    assert np.array_equal(prep.energy().cpu().numpy().view(np.uint32), ref.energy.view(np.uint32))
+    assert ref.sv[0, 0] == 1.0 and ref.sk[0, 1, 2] == 1.0 and ref.sq[0, 1, 1] == 1.0 and ref.sq[0, 2, 5] == 1.0
+    want, _ = oracle.attention_full(ref)
+    o = ovc.attention_prepared(prep)
+    assert ovc.device_status() == 0
+    got = o.float().cpu().numpy()
+    assert not got[0, :, 0].any()
+    assert rel_l2(got, want) <= TOL_REL_L2
+    # the zero Q block's rows: every score is 0, so each row is the mean of V's rows
+    assert rel_l2(got[0, 128:256, 1], want[0, 128:256, 1]) <= TOL_REL_L2
+
+
+@pytest.mark.parametrize("sm,qb,kb", [(1.0, 2, 3), (2.5, 0, 4), (1.0, 5, 5)])
+def test_sharp_rows_p_codes_and_output(sm, qb, kb):
+    """A large softmax scale makes rows sharp: most codes are 0 or
+    subnormal and the reference moves late in the traversal.  P bytes are
+    within one code of the oracle's under the device's reference, and O is
+    within 5e-3."""
+    B, H, S = 1, 2, 700
+    q, k, v = inputs(B, H, S, seed=2500)
+    ref = oracle_prep(q, k, v)
+    prep = ovc.prepare(*to_dev(q, k, v))
+    bh = 1
+    o, codes, m8 = ovc.attention_probe(prep, softmax_scale=sm, dump=(bh, qb, kb))
+    assert ovc.device_status() == 0
+    codes, m8 = codes.cpu().numpy(), m8.cpu().numpy()
+    small = 0
+    for r in [r for r in range(128) if qb * 128 + r < S]:
+        want = oracle.block_codes(ref, bh, qb * 128 + r, kb, float(m8[r]), sm=sm)
+        assert np.abs(codes[r].astype(int) - want.astype(int)).max() <= 1
+        small += int((want < 8).sum())
+    assert small > 0.5 * 128 * min(128, S - qb * 128)       # the rows are sharp
+    want, res = oracle.attention_full(ref, sm=sm)
+    assert res["nres"][:, 0].max() >= 2                     # some rows rescale after the first block
+    assert rel_l2(o.float().cpu().numpy(), want) <= TOL_REL_L2
+
+
+def test_tail_block_codes_with_a_repair_set():
+    """The ragged last key block's P bytes, dumped from a call with a repair
+    set: within one code of the oracle's under the device reference, and 0
+    past the last key; the repaired output within 5e-3."""
+    B, H, S, budget = 1, 2, 1000, 0.02        # nb = 8, last block 104 keys
+    q, k, v = inputs(B, H, S, seed=2600)
+    ref = oracle_prep(q, k, v)
+    rr = oracle.Repair(ref, budget)
+    qd, kd, vd = to_dev(q, k, v)
+    prep = ovc.prepare(qd, kd, vd)
+    rep = ovc.prepare_v_repair(vd, prep, budget)
+    nb = (S + 127) // 128
+    for bh, qb in ((0, nb - 1), (1, 3)):
+        o, codes, m8 = ovc.attention_probe(prep, rep, dump=(bh, qb, nb - 1))
+        assert ovc.device_status() == 0
+        codes, m8 = codes.cpu().numpy(), m8.cpu().numpy()
+        rows = [r for r in range(128) if qb * 128 + r < S]
+        for r in rows:
+            want = oracle.block_codes(ref, bh, qb * 128 + r, nb - 1, float(m8[r]))
+            assert np.abs(codes[r].astype(int) - want.astype(int)).max() <= 1
+            assert not codes[r, S - (nb - 1) * 128:].any()
+    want, _ = oracle.attention_full(ref, repair=rr)
+    assert rel_l2(o.float().cpu().numpy(), want) <= TOL_REL_L2
+
+
+# ---- Q smoothing ---------------------------------------------------------------
+def _check_key_bias(prep, ref):
+    """The prepared key bias rows: (hi, lo, hi, lo, 0, ...) per key, zero
+    past S, and hi + lo the oracle's beta_t = mu_q . dec(k_t) within the FP32
+    rounding of a 128-term dot product plus the BF16 split (2^-16)."""
+    kb = prep.key_bias().float().cpu().numpy().astype(np.float64)       # [B,H,S_pad,16]
+    S = ref.S
+    assert np.array_equal(kb[..., 2], kb[..., 0]) and np.array_equal(kb[..., 3], kb[..., 1])
+    assert not kb[..., 4:].any() and not kb[:, :, S:].any()
+    beta = kb[:, :, :S, 0] + kb[:, :, :S, 1]
+    tab = oracle.e4m3_table()
+    mag = np.einsum("bhtd,bhd->bht", np.abs(tab[ref.kc[:, :, :S]]), np.abs(ref.qmean.astype(np.float64)))
+    assert np.all(np.abs(beta - ref.kbias) <= 2.0 ** -16 * np.abs(ref.kbias) + 2.0 ** -15 * mag + 1e-30)
+
+
+@pytest.mark.parametrize("B,H,S,fp16,smooth_k", [(1, 2, 1000, False, True), (2, 1, 300, True, False),
+                                                  (1, 1, 1, False, False), (1, 3, 129, False, True),
+                                                  (1, 2, 1024, False, False)])
+def test_q_smoothing_matches_oracle(B, H, S, fp16, smooth_k):
+    """prepare(smooth_q=True): Q codes and scales bit-exact (the channel means
+    are FP32 sums in a fixed order), the key bias rows within their rounding
+    bound, O within 5e-3 of the oracle's Q-smoothed attention, and both
+    schedules bit for bit."""
+    q, k, v = inputs(B, H, S, seed=2700 + S)
+    if fp16:
+        q, k, v = (x.to(torch.float16) for x in (q, k, v))
+    bits = [x.contiguous().view(torch.int16).numpy().view(np.uint16) for x in (q, k, v)]
+    ref = oracle.Prepared(*bits, fp16=fp16, smooth_k=smooth_k, smooth_q=True)
+    qd, kd, vd = to_dev(q, k, v)
+    prep = ovc.prepare(qd, kd, vd, smooth_k=smooth_k, smooth_q=True)
+    torch.cuda.synchronize()
+    assert np.array_equal(prep.q_codes().cpu().numpy(), ref.qc)
+    assert np.array_equal(prep.q_scales().cpu().numpy(), ref.sq)
+    assert np.array_equal(prep.k_codes().cpu().numpy(), ref.kc)
+    assert np.array_equal(prep.k_scales().cpu().numpy(), ref.sk)
+    assert np.array_equal(prep.vt_codes().cpu().numpy().transpose(0, 1, 3, 2), ref.vc)
+    _check_key_bias(prep, ref)
+    want, _ = oracle.attention_full(ref)
+    o = ovc.attention_prepared(prep)
+    assert ovc.device_status() == 0
+    got = o.float().cpu().numpy()
+    assert np.isfinite(got).all()
+    assert rel_l2(got, want) <= TOL_REL_L2
+    a, _, _ = ovc.attention_probe(prep, force_persistent=1)
+    b, _, _ = ovc.attention_probe(prep, force_persistent=-1)
+    assert torch.equal(a, b) and torch.equal(a, o)
+    if S > 1:                                   # without the bias the output is clearly another one
+        plain_q = oracle.Prepared(*bits, fp16=fp16, smooth_k=smooth_k)
+        assert rel_l2(got, oracle.attention_full(plain_q)[0]) < 0.5
+
+
+@pytest.mark.parametrize("S,qb,kb", [(1000, 3, 5), (1000, 7, 7), (300, 0, 2)])
+def test_q_smoothing_p_codes_under_device_reference(S, qb, kb):
+    q, k, v = inputs(1, 2, S, seed=2800 + S)
+    ref = oracle.Prepared(W.bf16_bits(q), W.bf16_bits(k), W.bf16_bits(v), smooth_q=True)
+    prep = ovc.prepare(*to_dev(q, k, v), smooth_q=True)
+    _, codes, m8 = ovc.attention_probe(prep, dump=(1, qb, kb))
+    codes, m8 = codes.cpu().numpy(), m8.cpu().numpy()
+    diffs = []
+    for r in [r for r in range(128) if qb * 128 + r < S]:
+        want = oracle.block_codes(ref, 1, qb * 128 + r, kb, float(m8[r]))
+        d = np.abs(codes[r].astype(int) - want.astype(int))
+        assert d.max() <= 1, (r, d.max())
+        diffs.append(d)
+    assert float(np.mean(np.concatenate(diffs) == 0)) > 0.99
+    assert ovc.device_status() == 0
+
+
+@pytest.mark.parametrize("budget", [0.02, 1.0])
+def test_q_smoothing_with_repair_split_and_variants(budget):
+    """Q smoothing with V residual repair (the selected keys carry their
+    bias rows), with split key ranges and with the exp-then-cast baseline."""
+    B, H, S = 1, 2, 1100
+    q, k, v = inputs(B, H, S, seed=2900)
+    ref = oracle.Prepared(W.bf16_bits(q), W.bf16_bits(k), W.bf16_bits(v), smooth_q=True, smooth_k=True)
+    rr = oracle.Repair(ref, budget)
+    qd, kd, vd = to_dev(q, k, v)
+    prep = ovc.prepare(qd, kd, vd, smooth_q=True, smooth_k=True)
+    rep = ovc.prepare_v_repair(vd, prep, budget)
+    torch.cuda.synchronize()
+    assert np.array_equal(rep.idx().cpu().numpy(), rr.idx)
+    n = rr.n
+    kbs = _abi_view_kb_sel(rep)
+    kbp = prep.key_bias()
+    for h in range(H):
+        assert torch.equal(kbs[0, h, :n], kbp[0, h, torch.from_numpy(rr.idx[0, h]).long().cuda()])
+    assert not kbs[0, :, n:].float().any()
+    want, _ = oracle.attention_full(ref, repair=rr)
+    o = ovc.attention_v_repair(prep, rep)
+    assert ovc.device_status() == 0
+    assert rel_l2(o.float().cpu().numpy(), want) <= TOL_REL_L2
+    if budget < 1.0:
+        want3, _ = oracle.attention_full(ref, nsplit=3)
+        assert rel_l2(ovc.attention_prepared(prep, nsplit=3).float().cpu().numpy(), want3) <= TOL_REL_L2
+        wantb, _ = oracle.attention_full(ref, cast=True, mid_window=False)
+        assert rel_l2(ovc.attention_prepared(prep, flags=3).float().cpu().numpy(), wantb) <= TOL_REL_L2
+    with pytest.raises(ValueError):
+        ovc.prepare(qd, kd, vd, smooth_q=True, v_smooth=True)
+    assert ovc.device_status() == 0
+
+
+def _abi_view_kb_sel(rep):
+    d = rep.desc
+    off = d.kb_sel - rep.workspace.data_ptr()
+    return rep.workspace[off:off + 32 * d.B * d.H * d.n_pad].view(torch.bfloat16).view(d.B, d.H, d.n_pad, 16)
+
+
+def test_q_smoothing_lowers_error_on_biased_queries():
+    """On the workloads' per-channel Q/K bias, smoothing Q as well as K
+    brings the GPU output closer to exact softmax attention."""
+    B, H, S = 1, 2, 2048
+    q, k, v = inputs(B, H, S, seed=3000)
+    qf, kf, vf = (x.to(torch.float64).numpy() for x in (q, k, v))
+    rows = np.arange(0, S, 13)
+    errs = []
+    for sq in (False, True):
+        o = ovc.attention(*to_dev(q, k, v), smooth_k=True, smooth_q=sq).double().cpu().numpy()
+        num = den = 0.0
+        for h in range(H):
+            s = (qf[0, rows, h] @ kf[0, :, h].T) / math.sqrt(128.0)
+            p = np.exp(s - s.max(axis=1, keepdims=True))
+            ex = (p @ vf[0, :, h]) / p.sum(axis=1, keepdims=True)
+            num += np.sum((o[0, rows, h] - ex) ** 2)
+            den += np.sum(ex ** 2)
+        errs.append(math.sqrt(num / den))
+    assert errs[1] < 0.95 * errs[0], errs

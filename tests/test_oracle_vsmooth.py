@@ -4,7 +4,7 @@ mean is added back through the row sums that online softmax keeps).
 
 * The block mean is the mean: the residuals of a block sum to ~0 (up to the
   BF16 rounding of the mean).
-* Reconstruction: s (dec(code) + M'_b) equals v within the E4M3 rounding of
+* Reconstruction: s dec(code) + mu_b equals v within the E4M3 rounding of
   the residual plus the BF16 rounding of the mean.
 * With values whose blocks are constant powers of two, both V-Smooth and the
   plain per-head V quantisation reproduce V exactly, so the two attention
@@ -39,7 +39,7 @@ def test_residuals_of_a_block_sum_to_zero(S):
     rng = np.random.default_rng(S)
     v = rng.standard_normal((1, S, 2, 128)) * 3 + rng.standard_normal((1, 1, 2, 128)) * 5
     vb = _bf16(v)
-    codes, sv, mu, mp = oracle.vsmooth_v(_bits(vb))
+    codes, sv, mu = oracle.vsmooth_v(_bits(vb))
     x = vb.float().numpy()
     for h in range(2):
         for j, (t0, t1) in enumerate(_blocks(S)):
@@ -55,16 +55,18 @@ def test_reconstruction_within_rounding_bounds():
     S = 700
     v = rng.standard_t(3, (1, S, 2, 128)) + 4.0 * rng.standard_normal((1, S // 128 + 1, 2, 128)).repeat(128, 1)[:, :S]
     vb = _bf16(v)
-    codes, sv, mu, mp = oracle.vsmooth_v(_bits(vb))
+    codes, sv, mu = oracle.vsmooth_v(_bits(vb))
     tab = oracle.e4m3_table()
     x = vb.float().numpy()
     for h in range(2):
         s = float(sv[0, h])
-        rec = s * (tab[codes[0, h, :S]] + np.repeat(mp[0, h], 128, axis=0)[:S])
-        R = np.abs(x[0, :, h, :] - np.repeat(mu[0, h], 128, axis=0)[:S])
+        mub = np.repeat(mu[0, h], 128, axis=0)[:S].astype(np.float64)
+        rec = s * tab[codes[0, h, :S]] + mub
+        R = np.abs(x[0, :, h, :] - mub)
         # E4M3 keeps 3 mantissa bits: half an ulp is <= 2^-4 of |R| (normal
-        # range) or 2^-10 s (subnormal); the mean's BF16 rounding is 2^-9 |mu|
-        bound = 2.0 ** -4 * R + 2.0 ** -10 * s + 2.0 ** -8 * np.abs(np.repeat(mu[0, h], 128, axis=0)[:S]) + 1e-6
+        # range) or 2^-10 s (subnormal); the residual is taken against the
+        # stored mean, so the mean adds no error of its own
+        bound = 2.0 ** -4 * R + 2.0 ** -10 * s + 1e-6
         assert np.all(np.abs(rec - x[0, :, h, :]) <= bound)
     # the residual's amax sets the scale: some code is the largest, 126 (448)
     assert (codes & 0x7F).max() == 126
@@ -73,8 +75,8 @@ def test_reconstruction_within_rounding_bounds():
 def test_exact_values_give_the_plain_result():
     """Blocks of constant values +-7 * 2^k with amax 28: the plain per-head
     scale s = 28/448 = 2^-4 and r = 16 are exact and every value is an E4M3
-    code times s, and V-Smooth's residual is exactly 0 (s = 1, M' = mean),
-    so both paths reconstruct V exactly."""
+    code times s, and V-Smooth's residual is exactly 0 (s = 1, mu_b = the
+    block's value), so both paths reconstruct V exactly."""
     rng = np.random.default_rng(7)
     S = 600
     nb = (S + 127) // 128
@@ -115,7 +117,7 @@ def test_v_smooth_cuts_the_error_of_block_offsets():
     tab = oracle.e4m3_table()
     x = vb.float().numpy()[0, :, 0, :]
     rec_plain = plain.sv[0, 0] * tab[plain.vc[0, 0, :S]]
-    rec_smooth = smooth.sv[0, 0] * (tab[smooth.vc[0, 0, :S]] + np.repeat(smooth.vmean[0, 0], 128, axis=0)[:S])
+    rec_smooth = smooth.sv[0, 0] * tab[smooth.vc[0, 0, :S]] + np.repeat(smooth.vmu[0, 0], 128, axis=0)[:S]
     ev_plain = np.linalg.norm(rec_plain - x) / np.linalg.norm(x)
     ev_smooth = np.linalg.norm(rec_smooth - x) / np.linalg.norm(x)
     assert ev_smooth < 0.1 * ev_plain, (ev_smooth, ev_plain)
