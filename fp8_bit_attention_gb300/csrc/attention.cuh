@@ -94,9 +94,7 @@ struct AttnParams {
   int32_t n_rep, n_rep_pad, rep_blocks;
   const float* sk_sel;
   const float* sr;
-  // Q smoothing: each key's bias tile rides with its key block (TMA) and one
-  // BF16 MMA per block adds beta_j / s_q to the scores (0: off)
-  int32_t qbias;
+
   // probe
   int64_t dump_bh, dump_qb, dump_kb;
   uint8_t* dump_codes;
@@ -178,7 +176,10 @@ constexpr int kVarExpThenCast = 1;   // p byte = E4M3(ex2(...)) on the MUFU
 constexpr int kVarNaturalOrder = 2;  // key blocks 0, 1, ..., nb-1
 constexpr int kVarSplit = 4;         // split key ranges (nsplit > 1): partial results for merge_kernel
 constexpr int kVarVSmooth = 8;       // V-Smooth: block means restored through the block row sums
-constexpr int kNumVariants = 9;      // 0-7, and 8 (V-Smooth with ExpCast, mid-window, no split)
+constexpr int kVarQBias = 16;        // Q smoothing: the key bias added to the scores by one BF16 MMA
+// Instantiated: 0-7, 8 (V-Smooth with ExpCast, mid-window, no split), 16-23
+// (Q smoothing with each of 0-7); indexed by the variant bits.
+constexpr int kNumVariants = 24;
 
 // Key block visited at step i of a range of n blocks starting at b0 (the
 // whole sequence, or one split range): cyclic from the range's middle block,
@@ -439,7 +440,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         mbar_init(smem_addr(&sm.m_full[r]), 1);
         mbar_init(smem_addr(&sm.m_empty[r]), 1);
       }
-    if (!(kVar & kVarVSmooth) && P.qbias)
+    if (kVar & kVarQBias)
       for (int t = 0; t < 2; ++t) mbar_init(smem_addr(&sm.a_full[t]), 128);
     sm.abort = 0;
     sm.zero = 0;
@@ -481,7 +482,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (!ok) break;
           }
           const uint32_t kbar = smem_addr(&sm.k_full[stage]), vbar = smem_addr(&sm.v_full[stage]);
-          const bool qbias = !(kVar & kVarVSmooth) && P.qbias;
+          constexpr bool qbias = (kVar & kVarQBias) != 0;
           mbar_arrive_expect_tx(kbar, qbias ? kTile + kBiasTile : kTile);
           mbar_arrive_expect_tx(vbar, kTile);
           if (i < uc.nbu) {
@@ -542,7 +543,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const uint64_t qd0 = sw128_desc(smem_addr(sm.q[0])), qd1 = sw128_desc(smem_addr(sm.q[1]));
       // Q smoothing: after S_t = Q_t K^T, one BF16 MMA adds (1/s_q)(beta_j)
       // from the tile's A operand and the stage's key bias rows.
-      const bool qbias = !(kVar & kVarVSmooth) && P.qbias;
+      constexpr bool qbias = (kVar & kVarQBias) != 0;
       uint64_t abd0 = 0, abd1 = 0;
       if (qbias) {
         abd0 = sw32_desc(smem_addr(sm.ab[0]));
@@ -698,7 +699,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       float kf = -INFINITY;                     // reference m8 = kf + frac(c0+beta)
       float l = 0.0f;
       const bool dump_tile = (P.dump_codes != nullptr) && tc.bh == P.dump_bh && qb == P.dump_qb && store;
-      if (!(kVar & kVarVSmooth) && P.qbias) {
+      if (kVar & kVarQBias) {
         // Q smoothing: this row of the tile's A operand, the BF16 pair
         // (hi, lo) of 1/s_q twice, (hi, hi, lo, lo, 0, 0, 0, 0) in every
         // 16-byte chunk (the same in every row and chunk, so the 32-byte
@@ -809,6 +810,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (rescale) tmem_scale_row128(tO, f);
         tmem_wait_st();
         tc_fence_before();
+        // One arrival per warp once all its lanes' stores are done: 128
+        // arrivals would queue on the one barrier the MMA warp is waiting on.
         mbar_arrive(smem_addr(&sm.p_full[t]));
         // The row sum waits until the codes are on their way to the tensor core.
         if (main_blk && !lsum_done) {

@@ -27,10 +27,14 @@ __device__ unsigned int g_status;
 
 namespace {
 
-// Every instantiation of the attention kernel, indexed by its variant bits.
+// Every instantiation of the attention kernel, indexed by its variant bits
+// (NULL where no combination exists).
 const decltype(&attention_kernel<0>) kAttentionKernels[kNumVariants] = {
-    attention_kernel<0>, attention_kernel<1>, attention_kernel<2>, attention_kernel<3>, attention_kernel<4>,
-    attention_kernel<5>, attention_kernel<6>, attention_kernel<7>, attention_kernel<kVarVSmooth>};
+    attention_kernel<0>, attention_kernel<1>, attention_kernel<2>, attention_kernel<3>,
+    attention_kernel<4>, attention_kernel<5>, attention_kernel<6>, attention_kernel<7>,
+    attention_kernel<kVarVSmooth>, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+    attention_kernel<16>, attention_kernel<17>, attention_kernel<18>, attention_kernel<19>,
+    attention_kernel<20>, attention_kernel<21>, attention_kernel<22>, attention_kernel<23>};
 
 constexpr int kMaxDevices = 64;
 constexpr uint32_t kPrepareFlags = OVC_PREPARE_SMOOTH_K | OVC_PREPARE_V_SMOOTH | OVC_PREPARE_SMOOTH_Q;
@@ -61,9 +65,11 @@ ovc_status device_state(DeviceState** out) {
     d.sms = sms;
     if (d.supported) {
       for (int v = 0; v < kNumVariants; ++v)
-        if (cudaFuncSetAttribute(kAttentionKernels[v], cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(v == kVarVSmooth ? kAttnSmemBytesVSmooth : kAttnSmemBytesQBias)) !=
-            cudaSuccess)
+        if (kAttentionKernels[v] != nullptr &&
+            cudaFuncSetAttribute(kAttentionKernels[v], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(v == kVarVSmooth ? kAttnSmemBytesVSmooth
+                                                                   : (v & kVarQBias) ? kAttnSmemBytesQBias
+                                                                                     : kAttnSmemBytes)) != cudaSuccess)
           return OVC_ERR_CUDA;
       if (cudaFuncSetAttribute(kmeans_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(kmeans_partial_smem())) != cudaSuccess)
@@ -216,10 +222,12 @@ GroupLayout group_layout(int64_t B, int64_t S, int64_t H, int64_t C) {
 }
 
 struct RepLayout {
-  size_t idx, k_sel, dvt, sk_sel, sr, kb_sel, total;
+  size_t idx, k_sel, dvt, sk_sel, sr, kb_sel, hist, cnt, ramax, total;
 };
 
-RepLayout rep_layout(int64_t B, int64_t H, int64_t n) {
+int64_t repair_chunks(int64_t S) { return (S + kRepairChunk - 1) / kRepairChunk; }
+
+RepLayout rep_layout(int64_t B, int64_t S, int64_t H, int64_t n) {
   const int64_t n_pad = (n + 127) / 128 * 128, BH = B * H;
   RepLayout L{};
   size_t off = 0;
@@ -234,6 +242,10 @@ RepLayout rep_layout(int64_t B, int64_t H, int64_t n) {
   L.sk_sel = take(static_cast<size_t>(BH) * n_pad * 4);
   L.sr = take(static_cast<size_t>(BH) * 4);
   L.kb_sel = take(static_cast<size_t>(BH) * n_pad * 32);   // used with Q smoothing only
+  // selection scratch: digit histograms, per-chunk counts, residual amax
+  L.hist = take(static_cast<size_t>(BH) * 4 * 256 * 4);
+  L.cnt = take(static_cast<size_t>(BH) * repair_chunks(S) * 2 * 4);
+  L.ramax = take(static_cast<size_t>(BH) * 4);
   L.total = off;
   return L;
 }
@@ -353,7 +365,6 @@ ovc_status run_attention(const ovc_prepared* p, const ovc_repair* r, float softm
   P.sq = p->sq;
   P.sk = p->sk;
   P.sv = p->sv;
-  P.qbias = qbias ? 1 : 0;
   P.o = static_cast<uint16_t*>(o->ptr);
   P.os[0] = o->stride_b;
   P.os[1] = o->stride_s;
@@ -387,7 +398,8 @@ ovc_status run_attention(const ovc_prepared* p, const ovc_repair* r, float softm
   const int64_t grid = persistent ? (nunits < dev->sms ? nunits : dev->sms) : nunits;
   static_assert(OVC_ATTN_EXP_THEN_CAST == kVarExpThenCast && OVC_ATTN_NATURAL_ORDER == kVarNaturalOrder,
                 "flag bits select the kernel variant");
-  const int variant = vsmooth ? kVarVSmooth : static_cast<int>(flags | (ns > 1 ? kVarSplit : 0));
+  const int variant =
+      vsmooth ? kVarVSmooth : static_cast<int>(flags | (ns > 1 ? kVarSplit : 0) | (qbias ? kVarQBias : 0));
   const size_t smem = vsmooth ? kAttnSmemBytesVSmooth : (qbias ? kAttnSmemBytesQBias : kAttnSmemBytes);
   kAttentionKernels[variant]<<<static_cast<unsigned>(grid), kAttnThreads, smem, static_cast<cudaStream_t>(stream)>>>(
       mq, mk, mv, mks, mdv, mvm, mkb, mkbs, P);
@@ -560,7 +572,7 @@ size_t ovc_attention_workspace_bytes(const ovc_prepared* p, int32_t nsplit) {
 
 size_t ovc_repair_workspace_bytes(int64_t B, int64_t S, int64_t H, float budget) {
   if (!dims_ok(B, S, H) || !(budget > 0.0f) || budget > 1.0f) return 0;
-  return rep_layout(B, H, repair_n(S, budget)).total;
+  return rep_layout(B, S, H, repair_n(S, budget)).total;
 }
 
 ovc_status ovc_prepare_v_repair(const ovc_tensor* v, const ovc_prepared* p, float budget, void* workspace,
@@ -575,7 +587,7 @@ ovc_status ovc_prepare_v_repair(const ovc_tensor* v, const ovc_prepared* p, floa
   if (!(budget > 0.0f) || budget > 1.0f) return OVC_ERR_INVALID_ARG;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return OVC_ERR_INVALID_ARG;
   const int64_t n = repair_n(p->S, budget);
-  const RepLayout L = rep_layout(p->B, p->H, n);
+  const RepLayout L = rep_layout(p->B, p->S, p->H, n);
   if (workspace_bytes < L.total) return OVC_ERR_WORKSPACE_TOO_SMALL;
   DeviceState* dev = nullptr;
   ovc_status st = device_state(&dev);
@@ -619,8 +631,26 @@ ovc_status ovc_prepare_v_repair(const ovc_tensor* v, const ovc_prepared* p, floa
   P.sr = r.sr;
   P.kbias = p->kbias;
   P.kb_sel = r.kb_sel;
-  repair_prepare_kernel<<<static_cast<unsigned>(p->B * p->H), kRepairThreads, 0,
-                          static_cast<cudaStream_t>(stream)>>>(P);
+  P.hist = reinterpret_cast<uint32_t*>(ws + L.hist);
+  P.cnt = reinterpret_cast<uint32_t*>(ws + L.cnt);
+  P.ramax = reinterpret_cast<uint32_t*>(ws + L.ramax);
+  P.nchunk = static_cast<int32_t>(repair_chunks(p->S));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the histograms and the amax accumulate: clear them (the counts are written whole)
+  if (cudaMemsetAsync(ws + L.hist, 0, L.cnt - L.hist, s) != cudaSuccess ||
+      cudaMemsetAsync(ws + L.ramax, 0, static_cast<size_t>(p->B * p->H) * 4, s) != cudaSuccess)
+    return OVC_ERR_CUDA;
+  const dim3 gsel(static_cast<unsigned>(P.nchunk), static_cast<unsigned>(p->B * p->H));
+  repair_hist_kernel<0><<<gsel, kRepairThreads, 0, s>>>(P);
+  repair_hist_kernel<1><<<gsel, kRepairThreads, 0, s>>>(P);
+  repair_hist_kernel<2><<<gsel, kRepairThreads, 0, s>>>(P);
+  repair_hist_kernel<3><<<gsel, kRepairThreads, 0, s>>>(P);
+  repair_count_kernel<<<gsel, kRepairThreads, 0, s>>>(P);
+  repair_scatter_kernel<<<gsel, kRepairThreads, 0, s>>>(P);
+  const unsigned tok = static_cast<unsigned>((r.n + kRepairTokensPerCta - 1) / kRepairTokensPerCta);
+  const unsigned pad = static_cast<unsigned>((r.n_pad + kRepairTokensPerCta - 1) / kRepairTokensPerCta);
+  repair_amax_kernel<<<dim3(tok, static_cast<unsigned>(p->B * p->H)), kRepairThreads, 0, s>>>(P);
+  repair_write_kernel<<<dim3(pad, static_cast<unsigned>(p->B * p->H)), kRepairThreads, 0, s>>>(P);
   st = launch_status();
   if (st == OVC_OK) *out = r;
   return st;

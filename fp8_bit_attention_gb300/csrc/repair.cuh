@@ -6,19 +6,28 @@
 // Open-VC Attention", "What happened": quantised residuals are added only to
 // the V tokens worst by energy.
 //
-// One CTA (1024 threads) per (batch, head):
-//   1. radix-select (4 passes of 8 bits over the FP32 energy bits, which order
-//      like the values because energies are >= 0) the n-th largest energy T;
-//   2. compact, in index order, every token with energy > T and the first
-//      (n - #greater) tokens with energy == T -> idx ascending (ties go to the
-//      lower index, exactly as a stable sort by energy would);
-//   3. recompute each selected token's FP32 residual R = v - s_v*dec(code)
-//      (its code recomputed exactly as prepare does), take amax|R| ->
-//      s_r = amax/448;
-//   4. write the residual codes E4M3(R * 448/amax) transposed (dvt), gather
-//      the selected quantised keys (k_sel), the scale of each key's block
-//      (sk_sel) and, with Q smoothing, each key's bias row (kb_sel),
-//      zero-padding up to n_pad.
+// Per (batch, head): select the n tokens with the largest FP32 residual
+// energy (ties to the lower index), list them in ascending order, quantise
+// their FP32 residuals R = v - s_v dec(code) with one scale per head
+// s_r = amax|R_sel| / 448, and gather their keys.  The work is spread over a
+// grid of (4096-token chunk, head) CTAs so that every SM takes part:
+//   repair_hist_kernel (4 launches)  radix select of the n-th largest energy
+//       T, 8 bits a pass from the top (FP32 bits of non-negative values order
+//       like the values); each CTA histograms its chunk of the keys that
+//       match the digits chosen so far into a global per-head histogram.  The
+//       digits chosen so far are re-derived from the earlier passes'
+//       histograms by every CTA (a 256-bin walk), so no launch is spent on it;
+//   repair_count_kernel              per chunk: keys > T and keys == T;
+//   repair_scatter_kernel            ordered compaction: every key > T and
+//       the first (n - #greater) keys == T, in index order, each CTA writing
+//       its chunk's keys at the offset the earlier chunks' counts give;
+//   repair_amax_kernel               a warp per selected token: its residual
+//       recomputed in FP32 (the code recomputed exactly as prepare does),
+//       amax folded into the head's maximum;
+//   repair_write_kernel              a warp per slot of the padded set: the
+//       residual codes E4M3(R * 448/amax) transposed (dvt), the selected
+//       quantised keys (k_sel), the scale of each key's block (sk_sel) and,
+//       with Q smoothing, each key's bias row (kb_sel); zero padding to n_pad.
 #pragma once
 
 #include <cstdint>
@@ -45,18 +54,127 @@ struct RepairParams {
   // the preparation, and those of the selected keys [B*H][n_pad][16].
   const uint16_t* kbias;
   uint16_t* kb_sel;
+  // Scratch (caller workspace, zeroed before the first pass): hist
+  // [B*H][4][256] digit counts of each pass, cnt [B*H][nchunk][2] (keys > T,
+  // keys == T) of each chunk, ramax [B*H] residual amax bits.
+  uint32_t* hist;
+  uint32_t* cnt;
+  uint32_t* ramax;
+  int32_t nchunk;
 };
 
-constexpr int kRepairThreads = 1024;
+constexpr int kRepairChunk = 4096;    // tokens per CTA in the selection kernels
+constexpr int kRepairThreads = 256;
+constexpr int kRepairTokensPerCta = kRepairThreads / 32;   // a warp per selected token
 
 // Selected indices are always in [0, S); the clamp only keeps a corrupted
 // workspace from turning into an out-of-bounds read.
 __device__ __forceinline__ int clamp_token(int t, int S) { return t < 0 ? 0 : (t >= S ? S - 1 : t); }
 
+// The digits of T chosen by passes 0 .. npass-1: walking each pass's
+// histogram from the top, the digit where the running count reaches the
+// number still to take.  prefix/mask: the digits so far; remaining: how many
+// keys with that prefix are still to take.
+struct RadixState {
+  uint32_t prefix, mask, remaining;
+};
+
+__device__ __forceinline__ RadixState radix_state(const uint32_t* hist_bh, int npass, uint32_t n) {
+  RadixState st{0u, 0u, n};
+  for (int p = 0; p < npass; ++p) {
+    const uint32_t* h = hist_bh + p * 256;
+    uint32_t cum = 0;
+    int d = 255;
+    for (; d > 0; --d) {
+      const uint32_t c = h[d];
+      if (cum + c >= st.remaining) break;
+      cum += c;
+    }
+    const int shift = 24 - 8 * p;
+    st.prefix |= static_cast<uint32_t>(d) << shift;
+    st.mask |= 255u << shift;
+    st.remaining -= cum;
+  }
+  return st;
+}
+
+// One radix pass over a chunk of one head's energies.
+template <int kPass>
+__global__ void __launch_bounds__(kRepairThreads) repair_hist_kernel(const __grid_constant__ RepairParams P) {
+  __shared__ uint32_t h[kRepairThreads / 32][256];
+  __shared__ RadixState st;
+  const int bh = blockIdx.y, chunk = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < (kRepairThreads / 32) * 256; i += kRepairThreads) (&h[0][0])[i] = 0u;
+  uint32_t* hist_bh = P.hist + static_cast<int64_t>(bh) * 4 * 256;
+  if (threadIdx.x == 0) st = radix_state(hist_bh, kPass, static_cast<uint32_t>(P.n));
+  __syncthreads();
+  const uint32_t prefix = st.prefix, mask = st.mask;
+  constexpr int shift = 24 - 8 * kPass;
+  const uint32_t* key = reinterpret_cast<const uint32_t*>(P.energy + static_cast<int64_t>(bh) * P.S);
+  const int t0 = chunk * kRepairChunk, t1 = min(P.S, t0 + kRepairChunk);
+  for (int tb = t0; tb < t1; tb += kRepairThreads) {
+    const int t = tb + threadIdx.x;
+    const uint32_t k = t < t1 ? __ldg(key + t) : 0u;
+    const bool in = t < t1 && (k & mask) == prefix;
+    const uint32_t bin = in ? (k >> shift) & 255u : 256u;
+    // warp-aggregated: one shared-memory atomic per distinct bin of the warp
+    const uint32_t peers = __match_any_sync(0xFFFFFFFFu, bin);
+    if (in && lane == __ffs(peers) - 1) atomicAdd(&h[warp][bin], static_cast<uint32_t>(__popc(peers)));
+  }
+  __syncthreads();
+  for (int b = threadIdx.x; b < 256; b += kRepairThreads) {
+    uint32_t c = 0;
+#pragma unroll
+    for (int w = 0; w < kRepairThreads / 32; ++w) c += h[w][b];
+    if (c) atomicAdd(hist_bh + kPass * 256 + b, c);
+  }
+}
+
+// Keys above T and keys equal to T in each chunk.
+__global__ void __launch_bounds__(kRepairThreads) repair_count_kernel(const __grid_constant__ RepairParams P) {
+  __shared__ uint32_t red[2][kRepairThreads / 32];
+  __shared__ RadixState st;
+  const int bh = blockIdx.y, chunk = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) st = radix_state(P.hist + static_cast<int64_t>(bh) * 4 * 256, 4, static_cast<uint32_t>(P.n));
+  __syncthreads();
+  const uint32_t T = st.prefix;
+  const uint32_t* key = reinterpret_cast<const uint32_t*>(P.energy + static_cast<int64_t>(bh) * P.S);
+  const int t0 = chunk * kRepairChunk, t1 = min(P.S, t0 + kRepairChunk);
+  uint32_t gt = 0, eq = 0;
+  for (int t = t0 + threadIdx.x; t < t1; t += kRepairThreads) {
+    const uint32_t k = __ldg(key + t);
+    gt += k > T;
+    eq += k == T;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    gt += __shfl_xor_sync(0xFFFFFFFFu, gt, o);
+    eq += __shfl_xor_sync(0xFFFFFFFFu, eq, o);
+  }
+  if (lane == 0) {
+    red[0][warp] = gt;
+    red[1][warp] = eq;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t g = 0, e = 0;
+    for (int w = 0; w < kRepairThreads / 32; ++w) {
+      g += red[0][w];
+      e += red[1][w];
+    }
+    uint32_t* c = P.cnt + (static_cast<int64_t>(bh) * P.nchunk + chunk) * 2;
+    c[0] = g;
+    c[1] = e;
+  }
+}
+
 // Exclusive prefix sum over the CTA; returns this thread's offset and writes
 // the CTA total to *total.
 __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t x, uint32_t* red, uint32_t* total) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int kWarps = kRepairThreads / 32;
   uint32_t inc = x;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -66,21 +184,63 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t x, uint32_t* r
   if (lane == 31) red[warp] = inc;
   __syncthreads();
   if (warp == 0) {
-    const uint32_t wv = red[lane];
+    const uint32_t wv = lane < kWarps ? red[lane] : 0u;
     uint32_t winc = wv;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, winc, o);
       if (lane >= o) winc += y;
     }
-    red[lane] = winc - wv;            // exclusive offset of each warp
-    if (lane == 31) red[32] = winc;   // CTA total
+    if (lane < kWarps) red[lane] = winc - wv;   // exclusive offset of each warp
+    if (lane == 31) red[32] = winc;             // CTA total
   }
   __syncthreads();
   const uint32_t off = red[warp] + inc - x;
   *total = red[32];
   __syncthreads();
   return off;
+}
+
+// Ordered compaction of one chunk: every key > T, and keys == T while the
+// head's count of equal keys taken stays below the number needed.
+__global__ void __launch_bounds__(kRepairThreads) repair_scatter_kernel(const __grid_constant__ RepairParams P) {
+  __shared__ uint32_t red[33];
+  __shared__ RadixState st;
+  __shared__ uint32_t base[2];
+  const int bh = blockIdx.y, chunk = blockIdx.x;
+  if (threadIdx.x == 0) {
+    st = radix_state(P.hist + static_cast<int64_t>(bh) * 4 * 256, 4, static_cast<uint32_t>(P.n));
+    // Offsets of this chunk: the keys taken and the keys == T seen before it.
+    const uint32_t* c = P.cnt + static_cast<int64_t>(bh) * P.nchunk * 2;
+    uint32_t out = 0, eq = 0;
+    for (int i = 0; i < chunk; ++i) {
+      const uint32_t g = c[2 * i], e = c[2 * i + 1];
+      const uint32_t e_taken = eq >= st.remaining ? 0u : min(e, st.remaining - eq);
+      out += g + e_taken;
+      eq += e;
+    }
+    base[0] = out;
+    base[1] = eq;
+  }
+  __syncthreads();
+  const uint32_t T = st.prefix, need_eq = st.remaining;
+  uint32_t base_out = base[0], base_eq = base[1];
+  const uint32_t* key = reinterpret_cast<const uint32_t*>(P.energy + static_cast<int64_t>(bh) * P.S);
+  int32_t* idx = P.idx + static_cast<int64_t>(bh) * P.n;
+  const int t0 = chunk * kRepairChunk, t1 = min(P.S, t0 + kRepairChunk);
+  for (int tb = t0; tb < t1; tb += kRepairThreads) {
+    const int t = tb + threadIdx.x;
+    const uint32_t k = t < t1 ? __ldg(key + t) : 0u;
+    const uint32_t gt = (t < t1 && k > T) ? 1u : 0u;
+    const uint32_t eq = (t < t1 && k == T) ? 1u : 0u;
+    uint32_t tot_eq, tot_take;
+    const uint32_t eq_rank = base_eq + block_exclusive_scan(eq, red, &tot_eq);
+    const uint32_t take = gt | (eq & (eq_rank < need_eq ? 1u : 0u));
+    const uint32_t pos = base_out + block_exclusive_scan(take, red, &tot_take);
+    if (take && pos < static_cast<uint32_t>(P.n)) idx[pos] = t;
+    base_eq += tot_eq;
+    base_out += tot_take;
+  }
 }
 
 // Residual of four consecutive channels of token t, recomputed in FP32.
@@ -97,103 +257,50 @@ __device__ __forceinline__ void residual4(const RepairParams& P, int b, int h, i
   for (int i = 0; i < 4; ++i) R[i] = __fsub_rn(x[i], __fmul_rn(sv, dq[i]));
 }
 
-__global__ void __launch_bounds__(kRepairThreads, 1) repair_prepare_kernel(const __grid_constant__ RepairParams P) {
-  __shared__ uint32_t hist[256];
-  __shared__ uint32_t red[33];
-  __shared__ uint32_t s_digit, s_remaining;
-  const int bh = blockIdx.x;
+// amax |R| over the selected tokens, per head.
+__global__ void __launch_bounds__(kRepairThreads) repair_amax_kernel(const __grid_constant__ RepairParams P) {
+  const int bh = blockIdx.y;
+  const int i = blockIdx.x * kRepairTokensPerCta + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (i >= P.n) return;
   const int b = bh / P.H, h = bh % P.H;
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
-  const uint32_t* key = reinterpret_cast<const uint32_t*>(P.energy + static_cast<int64_t>(bh) * P.S);
-  int32_t* idx = P.idx + static_cast<int64_t>(bh) * P.n;
-
-  // 1. radix select of the n-th largest key
-  uint32_t prefix = 0, mask = 0, remaining = static_cast<uint32_t>(P.n);
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    if (tid < 256) hist[tid] = 0;
-    __syncthreads();
-    for (int t = tid; t < P.S; t += kRepairThreads) {
-      const uint32_t k = __ldg(key + t);
-      if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1u);
-    }
-    __syncthreads();
-    if (tid == 0) {
-      uint32_t cum = 0;
-      int d = 255;
-      for (; d > 0; --d) {
-        if (cum + hist[d] >= remaining) break;
-        cum += hist[d];
-      }
-      s_digit = static_cast<uint32_t>(d);
-      s_remaining = remaining - cum;
-    }
-    __syncthreads();
-    prefix |= s_digit << shift;
-    mask |= 255u << shift;
-    remaining = s_remaining;
-    __syncthreads();
-  }
-  const uint32_t T = prefix;
-  const uint32_t need_eq = remaining;   // how many keys equal to T are taken
-
-  // 2. ordered compaction
-  uint32_t base_eq = 0, base_out = 0;
-  for (int c0 = 0; c0 < P.S; c0 += kRepairThreads) {
-    const int t = c0 + tid;
-    const uint32_t k = t < P.S ? __ldg(key + t) : 0u;
-    const uint32_t gt = (t < P.S && k > T) ? 1u : 0u;
-    const uint32_t eq = (t < P.S && k == T) ? 1u : 0u;
-    uint32_t tot_eq, tot_take;
-    const uint32_t eq_rank = base_eq + block_exclusive_scan(eq, red, &tot_eq);
-    const uint32_t take = gt | (eq & (eq_rank < need_eq ? 1u : 0u));
-    const uint32_t pos = base_out + block_exclusive_scan(take, red, &tot_take);
-    if (take && pos < static_cast<uint32_t>(P.n)) idx[pos] = t;
-    base_eq += tot_eq;
-    base_out += tot_take;
-  }
-  __syncthreads();
-
-  // 3. residual scale over the selected tokens
   const QScale vsc = scale_from_amax(__uint_as_float(P.vamax[bh]));
-  float amax = 0.0f;
-  for (int i = warp; i < P.n; i += kRepairThreads / 32) {
-    float R[4];
-    residual4(P, b, h, clamp_token(idx[i], P.S), 4 * lane, vsc.s, vsc.r, R);
+  float R[4];
+  residual4(P, b, h, clamp_token(P.idx[static_cast<int64_t>(bh) * P.n + i], P.S), 4 * lane, vsc.s, vsc.r, R);
+  float m = fmaxf(fmaxf(fabsf(R[0]), fabsf(R[1])), fmaxf(fabsf(R[2]), fabsf(R[3])));
 #pragma unroll
-    for (int e = 0; e < 4; ++e) amax = fmaxf(amax, fabsf(R[e]));
-  }
-  const float ramax = __uint_as_float(block_max_u32(__float_as_uint(amax), red));
-  const QScale rsc = scale_from_amax(ramax);
-  if (tid == 0) P.sr[bh] = rsc.s;
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  if (lane == 0) atomicMax(P.ramax + bh, __float_as_uint(m));
+}
 
-  // 4. residual codes (transposed), gathered keys and their block scales
-  uint8_t* dvt = P.dvt + static_cast<int64_t>(bh) * 128 * P.n_pad;
-  uint8_t* ksel = P.k_sel + static_cast<int64_t>(bh) * P.n_pad * 128;
-  float* sksel = P.sk_sel + static_cast<int64_t>(bh) * P.n_pad;
-  for (int i = warp; i < P.n_pad; i += kRepairThreads / 32) {
-    uint32_t codes = 0, kw = 0;
-    float skv = 0.0f;
-    if (i < P.n) {
-      const int t = clamp_token(idx[i], P.S);
-      float R[4];
-      residual4(P, b, h, t, 4 * lane, vsc.s, vsc.r, R);
-      codes = quant4(R[0], R[1], R[2], R[3], rsc.r);
-      kw = __ldg(reinterpret_cast<const uint32_t*>(P.kc + (static_cast<int64_t>(bh) * P.S_pad + t) * 128) + lane);
-      skv = P.sk[bh * P.nb + t / 128];
-    }
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-      dvt[static_cast<int64_t>(4 * lane + e) * P.n_pad + i] = static_cast<uint8_t>(codes >> (8 * e));
-    reinterpret_cast<uint32_t*>(ksel + static_cast<int64_t>(i) * 128)[lane] = kw;
-    if (lane == 0) sksel[i] = skv;
-    if (P.kb_sel != nullptr && lane < 8) {
-      const uint32_t bw = i < P.n ? __ldg(reinterpret_cast<const uint32_t*>(
-                                        P.kbias + (static_cast<int64_t>(bh) * P.S_pad + clamp_token(idx[i], P.S)) * 16) + lane)
-                                  : 0u;
-      reinterpret_cast<uint32_t*>(P.kb_sel + (static_cast<int64_t>(bh) * P.n_pad + i) * 16)[lane] = bw;
-    }
+// Residual codes (transposed), gathered keys, their block scales and bias
+// rows, for slot i of the padded repair set.
+__global__ void __launch_bounds__(kRepairThreads) repair_write_kernel(const __grid_constant__ RepairParams P) {
+  const int bh = blockIdx.y;
+  const int i = blockIdx.x * kRepairTokensPerCta + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  const QScale rsc = scale_from_amax(__uint_as_float(P.ramax[bh]));
+  if (blockIdx.x == 0 && threadIdx.x == 0) P.sr[bh] = rsc.s;
+  if (i >= P.n_pad) return;
+  const int b = bh / P.H, h = bh % P.H;
+  uint32_t codes = 0, kw = 0, bw = 0;
+  float skv = 0.0f;
+  if (i < P.n) {
+    const QScale vsc = scale_from_amax(__uint_as_float(P.vamax[bh]));
+    const int t = clamp_token(P.idx[static_cast<int64_t>(bh) * P.n + i], P.S);
+    float R[4];
+    residual4(P, b, h, t, 4 * lane, vsc.s, vsc.r, R);
+    codes = quant4(R[0], R[1], R[2], R[3], rsc.r);
+    kw = __ldg(reinterpret_cast<const uint32_t*>(P.kc + (static_cast<int64_t>(bh) * P.S_pad + t) * 128) + lane);
+    skv = P.sk[bh * P.nb + t / 128];
+    if (P.kb_sel != nullptr && lane < 8)
+      bw = __ldg(reinterpret_cast<const uint32_t*>(P.kbias + (static_cast<int64_t>(bh) * P.S_pad + t) * 16) + lane);
   }
+  uint8_t* dvt = P.dvt + static_cast<int64_t>(bh) * 128 * P.n_pad;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) dvt[static_cast<int64_t>(4 * lane + e) * P.n_pad + i] = static_cast<uint8_t>(codes >> (8 * e));
+  reinterpret_cast<uint32_t*>(P.k_sel + (static_cast<int64_t>(bh) * P.n_pad + i) * 128)[lane] = kw;
+  if (lane == 0) P.sk_sel[static_cast<int64_t>(bh) * P.n_pad + i] = skv;
+  if (P.kb_sel != nullptr && lane < 8)
+    reinterpret_cast<uint32_t*>(P.kb_sel + (static_cast<int64_t>(bh) * P.n_pad + i) * 16)[lane] = bw;
 }
 
 }  // namespace ovc
