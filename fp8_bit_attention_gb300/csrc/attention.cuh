@@ -406,6 +406,37 @@ __device__ __forceinline__ void tmem_scale_row128(uint32_t taddr, float f) {
   tmem_wait_st();
 }
 
+// MMA issue, by lane 0 alone (W = false) or by the whole converged MMA warp
+// with one elected lane (W = true; every wait then becomes a warp vote).  The
+// method's kernel runs fastest with lane-0 issue (72.2 against 73.0 ms at
+// S = 73397, H = 56); the Q-smoothing variants, whose QK^T adds a BF16 MMA,
+// with warp issue (75.0 against 78.3 ms).
+template <bool W>
+__device__ __forceinline__ bool issue_vote(bool ok) {
+  if constexpr (W) return __all_sync(0xFFFFFFFFu, ok);
+  return ok;
+}
+template <bool W>
+__device__ __forceinline__ void issue_f8_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+  if constexpr (W) mma_f8_ss_w(d, a, b, id, acc);
+  else mma_f8_ss(d, a, b, id, acc);
+}
+template <bool W>
+__device__ __forceinline__ void issue_f8_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t id, uint32_t acc) {
+  if constexpr (W) mma_f8_ts_w(d, a, b, id, acc);
+  else mma_f8_ts(d, a, b, id, acc);
+}
+template <bool W>
+__device__ __forceinline__ void issue_bf16_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+  if constexpr (W) mma_bf16_ss_w(d, a, b, id, acc);
+  else mma_bf16_ss(d, a, b, id, acc);
+}
+template <bool W>
+__device__ __forceinline__ void issue_commit(uint32_t bar) {
+  if constexpr (W) tc_commit_w(bar);
+  else tc_commit(bar);
+}
+
 template <int kVar>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -527,7 +558,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA
-    if (lane == 0 && !P.skip_mma) {
+    constexpr bool kW = (kVar & kVarQBias) != 0;   // issue style, see issue_vote
+    if ((kW || lane == 0) && !P.skip_mma) {
       uint32_t kv_iter = 0, q_iter = 0, sp0 = 0, sp1 = 0, mrun = 0;
       bool ok = true, issued = false;
       // V-Smooth: O_t += L_t M'^T for a run's 16 blocks, L_t the BF16 row
@@ -553,35 +585,35 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const UnitCoord ucm = unit_coord<kVar>(P, u);
         const int nbu = ucm.nbu, b0 = ucm.b0;
         const int nblk = nbu + P.rep_blocks;
-        ok = mbar_wait(smem_addr(&sm.q_full), q_iter & 1, tmo, abort_flag);
+        ok = issue_vote<kW>(mbar_wait(smem_addr(&sm.q_full), q_iter & 1, tmo, abort_flag));
         if (!ok) break;
         if (qbias) {
-          ok = mbar_wait(smem_addr(&sm.a_full[0]), q_iter & 1, tmo, abort_flag) &&
-               mbar_wait(smem_addr(&sm.a_full[1]), q_iter & 1, tmo, abort_flag);
+          ok = issue_vote<kW>(mbar_wait(smem_addr(&sm.a_full[0]), q_iter & 1, tmo, abort_flag) &&
+                              mbar_wait(smem_addr(&sm.a_full[1]), q_iter & 1, tmo, abort_flag));
           if (!ok) break;
         }
         // Scores of the first block for both query tiles.
         {
           const uint32_t stage = kv_iter % kStages;
-          ok = mbar_wait(smem_addr(&sm.k_full[stage]), (kv_iter / kStages) & 1, tmo, abort_flag);
+          ok = issue_vote<kW>(mbar_wait(smem_addr(&sm.k_full[stage]), (kv_iter / kStages) & 1, tmo, abort_flag));
           if (!ok) break;
           tc_fence_after();
           const uint64_t kd = sw128_desc(smem_addr(sm.k[stage]));
           const uint64_t kbd = qbias ? sw32_desc(smem_addr(sm.kb[stage])) : 0;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) mma_f8_ss(tS0, qd0 + 2 * kk, kd + 2 * kk, kIdesc, kk > 0);
-          if (qbias) mma_bf16_ss(tS0, abd0, kbd, kIdescBf16, 1u);
-          tc_commit(smem_addr(&sm.s_full[0]));
+          for (int kk = 0; kk < 4; ++kk) issue_f8_ss<kW>(tS0, qd0 + 2 * kk, kd + 2 * kk, kIdesc, kk > 0);
+          if (qbias) issue_bf16_ss<kW>(tS0, abd0, kbd, kIdescBf16, 1u);
+          issue_commit<kW>(smem_addr(&sm.s_full[0]));
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) mma_f8_ss(tS1, qd1 + 2 * kk, kd + 2 * kk, kIdesc, kk > 0);
-          if (qbias) mma_bf16_ss(tS1, abd1, kbd, kIdescBf16, 1u);
-          tc_commit(smem_addr(&sm.s_full[1]));
+          for (int kk = 0; kk < 4; ++kk) issue_f8_ss<kW>(tS1, qd1 + 2 * kk, kd + 2 * kk, kIdesc, kk > 0);
+          if (qbias) issue_bf16_ss<kW>(tS1, abd1, kbd, kIdescBf16, 1u);
+          issue_commit<kW>(smem_addr(&sm.s_full[1]));
           issued = true;
         }
         for (int i = 0; i < nblk; ++i) {
           const uint32_t stage = kv_iter % kStages;
           trace_mark(P, 2, kv_iter, 0);
-          ok = mbar_wait(smem_addr(&sm.v_full[stage]), (kv_iter / kStages) & 1, tmo, abort_flag);
+          ok = issue_vote<kW>(mbar_wait(smem_addr(&sm.v_full[stage]), (kv_iter / kStages) & 1, tmo, abort_flag));
           if (!ok) break;
           const uint64_t vd = sw128_desc(smem_addr(sm.v[stage]));
           const bool last = (i + 1 == nblk);
@@ -598,20 +630,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (i + 1 == nbu) fl |= 2u;
           }
           // ---- query tile 0: O0 += P0 V, then the next block's S0
-          ok = mbar_wait(smem_addr(&sm.p_full[0]), sp0, tmo, abort_flag);
+          ok = issue_vote<kW>(mbar_wait(smem_addr(&sm.p_full[0]), sp0, tmo, abort_flag));
           if (!ok) break;
           trace_mark(P, 2, kv_iter, 1);
           sp0 ^= 1;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_f8_ts(tO0, tS0 + 8 * kk, vd + 2 * kk, kIdesc, (i > 0 || kk > 0) ? 1u : 0u);
+            issue_f8_ts<kW>(tO0, tS0 + 8 * kk, vd + 2 * kk, kIdesc, (i > 0 || kk > 0) ? 1u : 0u);
           if (kVar & kVarVSmooth) {
 #pragma unroll
             for (uint32_t b = 0; b < 2; ++b)
               if (fl & (1u << b)) {
                 const uint32_t r = mrun - 2 + b;
-                ok = mbar_wait(smem_addr(&sm.m_full[r & 1]), (r >> 1) & 1, tmo, abort_flag);
+                ok = issue_vote<kW>(mbar_wait(smem_addr(&sm.m_full[r & 1]), (r >> 1) & 1, tmo, abort_flag));
                 if (!ok) break;
                 tc_fence_after();
                 mean_mma(tO0, tS0 + 32 + 16 * b, r & 1);
@@ -620,45 +652,45 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           }
           uint64_t kd_next = 0;
           if (!last) {
-            ok = mbar_wait(smem_addr(&sm.k_full[nstage]), ((kv_iter + 1) / kStages) & 1, tmo, abort_flag);
+            ok = issue_vote<kW>(mbar_wait(smem_addr(&sm.k_full[nstage]), ((kv_iter + 1) / kStages) & 1, tmo, abort_flag));
             if (!ok) break;
             tc_fence_after();
             kd_next = sw128_desc(smem_addr(sm.k[nstage]));
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) mma_f8_ss(tS0, qd0 + 2 * kk, kd_next + 2 * kk, kIdesc, kk > 0);
-            if (qbias) mma_bf16_ss(tS0, abd0, sw32_desc(smem_addr(sm.kb[nstage])), kIdescBf16, 1u);
-            tc_commit(smem_addr(&sm.s_full[0]));
+            for (int kk = 0; kk < 4; ++kk) issue_f8_ss<kW>(tS0, qd0 + 2 * kk, kd_next + 2 * kk, kIdesc, kk > 0);
+            if (qbias) issue_bf16_ss<kW>(tS0, abd0, sw32_desc(smem_addr(sm.kb[nstage])), kIdescBf16, 1u);
+            issue_commit<kW>(smem_addr(&sm.s_full[0]));
           } else {
-            tc_commit(smem_addr(&sm.o_full[0]));
+            issue_commit<kW>(smem_addr(&sm.o_full[0]));
           }
           // ---- query tile 1
           trace_mark(P, 2, kv_iter, 2);
-          ok = mbar_wait(smem_addr(&sm.p_full[1]), sp1, tmo, abort_flag);
+          ok = issue_vote<kW>(mbar_wait(smem_addr(&sm.p_full[1]), sp1, tmo, abort_flag));
           if (!ok) break;
           trace_mark(P, 2, kv_iter, 3);
           sp1 ^= 1;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_f8_ts(tO1, tS1 + 8 * kk, vd + 2 * kk, kIdesc, (i > 0 || kk > 0) ? 1u : 0u);
+            issue_f8_ts<kW>(tO1, tS1 + 8 * kk, vd + 2 * kk, kIdesc, (i > 0 || kk > 0) ? 1u : 0u);
           if (kVar & kVarVSmooth) {
 #pragma unroll
             for (uint32_t b = 0; b < 2; ++b)
               if (fl & (1u << b)) {
                 const uint32_t r = mrun - 2 + b;
                 mean_mma(tO1, tS1 + 32 + 16 * b, r & 1);
-                tc_commit(smem_addr(&sm.m_empty[r & 1]));
+                issue_commit<kW>(smem_addr(&sm.m_empty[r & 1]));
               }
           }
-          tc_commit(smem_addr(&sm.kv_empty[stage]));
+          issue_commit<kW>(smem_addr(&sm.kv_empty[stage]));
           if (!last) {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) mma_f8_ss(tS1, qd1 + 2 * kk, kd_next + 2 * kk, kIdesc, kk > 0);
-            if (qbias) mma_bf16_ss(tS1, abd1, sw32_desc(smem_addr(sm.kb[nstage])), kIdescBf16, 1u);
-            tc_commit(smem_addr(&sm.s_full[1]));
+            for (int kk = 0; kk < 4; ++kk) issue_f8_ss<kW>(tS1, qd1 + 2 * kk, kd_next + 2 * kk, kIdesc, kk > 0);
+            if (qbias) issue_bf16_ss<kW>(tS1, abd1, sw32_desc(smem_addr(sm.kb[nstage])), kIdescBf16, 1u);
+            issue_commit<kW>(smem_addr(&sm.s_full[1]));
           } else {
-            tc_commit(smem_addr(&sm.o_full[1]));
-            tc_commit(smem_addr(&sm.q_empty));
+            issue_commit<kW>(smem_addr(&sm.o_full[1]));
+            issue_commit<kW>(smem_addr(&sm.q_empty));
           }
           ++kv_iter;
         }
@@ -667,7 +699,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (!ok) record_abort(sm, P);
       if (issued) {
         // Every MMA issued so far has completed once this barrier flips.
-        tc_commit(smem_addr(&sm.drain));
+        issue_commit<kW>(smem_addr(&sm.drain));
         mbar_wait(smem_addr(&sm.drain), 0, kDrainNs, &sm.zero);
       }
     }
