@@ -71,44 +71,74 @@ constexpr int kRepairTokensPerCta = kRepairThreads / 32;   // a warp per selecte
 // workspace from turning into an out-of-bounds read.
 __device__ __forceinline__ int clamp_token(int t, int S) { return t < 0 ? 0 : (t >= S ? S - 1 : t); }
 
-// The digits of T chosen by passes 0 .. npass-1: walking each pass's
-// histogram from the top, the digit where the running count reaches the
-// number still to take.  prefix/mask: the digits so far; remaining: how many
-// keys with that prefix are still to take.
+// The digits of T chosen by passes 0 .. npass-1: the digit of a pass is the
+// highest d at which the keys with a larger digit number fewer than those
+// still to take, and those with digit >= d at least as many.  prefix/mask:
+// the digits so far; remaining: how many keys with that prefix are still to
+// take.  Called by every thread of the CTA (kRepairThreads); each pass's
+// histogram is staged in shared memory and warp 0 finds the digit with a
+// suffix sum over its lanes (lane l holds bins 255-8l .. 248-8l).
 struct RadixState {
   uint32_t prefix, mask, remaining;
 };
 
 __device__ __forceinline__ RadixState radix_state(const uint32_t* hist_bh, int npass, uint32_t n) {
-  RadixState st{0u, 0u, n};
+  __shared__ uint32_t bins[256];
+  __shared__ RadixState st;
+  if (threadIdx.x == 0) st = RadixState{0u, 0u, n};
+  __syncthreads();
   for (int p = 0; p < npass; ++p) {
-    const uint32_t* h = hist_bh + p * 256;
-    uint32_t cum = 0;
-    int d = 255;
-    for (; d > 0; --d) {
-      const uint32_t c = h[d];
-      if (cum + c >= st.remaining) break;
-      cum += c;
+    for (int b = threadIdx.x; b < 256; b += kRepairThreads) bins[b] = hist_bh[p * 256 + b];
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      const int lane = threadIdx.x;
+      const uint32_t remaining = st.remaining;
+      uint32_t c[8], tot = 0;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        c[k] = bins[255 - 8 * lane - k];
+        tot += c[k];
+      }
+      uint32_t incl = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const uint32_t excl = incl - tot;   // keys in the bins above this lane's
+      // the lane whose bins hold the cut; the last lane takes it if none does
+      // (its lowest bin, digit 0, then holds the remaining keys)
+      const unsigned hit = __ballot_sync(0xFFFFFFFFu, excl < remaining && remaining <= incl);
+      const int owner = hit ? __ffs(hit) - 1 : 31;
+      if (lane == owner) {
+        uint32_t cum = excl;
+        int d = 255 - 8 * lane;
+        for (int k = 0; k < 8; ++k, --d) {
+          if (d == 0 || cum + c[k] >= remaining) break;
+          cum += c[k];
+        }
+        const int shift = 24 - 8 * p;
+        st.prefix |= static_cast<uint32_t>(d) << shift;
+        st.mask |= 255u << shift;
+        st.remaining = remaining - cum;
+      }
     }
-    const int shift = 24 - 8 * p;
-    st.prefix |= static_cast<uint32_t>(d) << shift;
-    st.mask |= 255u << shift;
-    st.remaining -= cum;
+    __syncthreads();
   }
-  return st;
+  const RadixState r = st;
+  __syncthreads();
+  return r;
 }
 
 // One radix pass over a chunk of one head's energies.
 template <int kPass>
 __global__ void __launch_bounds__(kRepairThreads) repair_hist_kernel(const __grid_constant__ RepairParams P) {
   __shared__ uint32_t h[kRepairThreads / 32][256];
-  __shared__ RadixState st;
   const int bh = blockIdx.y, chunk = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < (kRepairThreads / 32) * 256; i += kRepairThreads) (&h[0][0])[i] = 0u;
   uint32_t* hist_bh = P.hist + static_cast<int64_t>(bh) * 4 * 256;
-  if (threadIdx.x == 0) st = radix_state(hist_bh, kPass, static_cast<uint32_t>(P.n));
-  __syncthreads();
+  const RadixState st = radix_state(hist_bh, kPass, static_cast<uint32_t>(P.n));
   const uint32_t prefix = st.prefix, mask = st.mask;
   constexpr int shift = 24 - 8 * kPass;
   const uint32_t* key = reinterpret_cast<const uint32_t*>(P.energy + static_cast<int64_t>(bh) * P.S);
@@ -134,12 +164,9 @@ __global__ void __launch_bounds__(kRepairThreads) repair_hist_kernel(const __gri
 // Keys above T and keys equal to T in each chunk.
 __global__ void __launch_bounds__(kRepairThreads) repair_count_kernel(const __grid_constant__ RepairParams P) {
   __shared__ uint32_t red[2][kRepairThreads / 32];
-  __shared__ RadixState st;
   const int bh = blockIdx.y, chunk = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) st = radix_state(P.hist + static_cast<int64_t>(bh) * 4 * 256, 4, static_cast<uint32_t>(P.n));
-  __syncthreads();
-  const uint32_t T = st.prefix;
+  const uint32_t T = radix_state(P.hist + static_cast<int64_t>(bh) * 4 * 256, 4, static_cast<uint32_t>(P.n)).prefix;
   const uint32_t* key = reinterpret_cast<const uint32_t*>(P.energy + static_cast<int64_t>(bh) * P.S);
   const int t0 = chunk * kRepairChunk, t1 = min(P.S, t0 + kRepairChunk);
   uint32_t gt = 0, eq = 0;
@@ -205,11 +232,10 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t x, uint32_t* r
 // head's count of equal keys taken stays below the number needed.
 __global__ void __launch_bounds__(kRepairThreads) repair_scatter_kernel(const __grid_constant__ RepairParams P) {
   __shared__ uint32_t red[33];
-  __shared__ RadixState st;
   __shared__ uint32_t base[2];
   const int bh = blockIdx.y, chunk = blockIdx.x;
+  const RadixState st = radix_state(P.hist + static_cast<int64_t>(bh) * 4 * 256, 4, static_cast<uint32_t>(P.n));
   if (threadIdx.x == 0) {
-    st = radix_state(P.hist + static_cast<int64_t>(bh) * 4 * 256, 4, static_cast<uint32_t>(P.n));
     // Offsets of this chunk: the keys taken and the keys == T seen before it.
     const uint32_t* c = P.cnt + static_cast<int64_t>(bh) * P.nchunk * 2;
     uint32_t out = 0, eq = 0;
