@@ -94,6 +94,10 @@ struct AttnParams {
   int32_t n_rep, n_rep_pad, rep_blocks;
   const float* sk_sel;
   const float* sr;
+  // Always 1.  The ExpCast threads branch on it before adding up a block's
+  // row sum: the compiler cannot drop the branch, so it cannot lift the sum
+  // above the P store's wait and the hand-over to fill their latency.
+  int32_t rowsum_gate;
 
   // probe
   int64_t dump_bh, dump_qb, dump_kb;
@@ -143,8 +147,23 @@ struct AttnSmem {
   alignas(1024) uint8_t ab[2][kBiasTile];         // per query tile: 128 rows of (hi, lo) parts of 1/s_q
 };
 
+// Repair variants only: the per-column multipliers of the repair blocks
+// (8 log2e sm s_q s_k of each selected key, scaled as the byte step takes
+// them), written by the tile's own 128 threads one block ahead into one of
+// two buffers, each with a barrier of 128 arrivals.  It takes the place of
+// the V-Smooth tail, which the repair variants never use, from the first
+// 16-byte boundary there (the multipliers are read as float4).
+struct alignas(16) RepairTail {
+  float ksc[2][2][128];      // [tile][buffer][column]
+  uint64_t ksc_full[2][2];   // [tile][buffer]
+};
+constexpr size_t kRepairTailOffset = (offsetof(AttnSmem, m_full) + 15) / 16 * 16;
+
 // Dynamic shared memory of a launch, + 1024 bytes of alignment slack.
 constexpr size_t kAttnSmemBytes = offsetof(AttnSmem, m_full) + 1024;
+constexpr size_t kAttnSmemBytesRepair = kRepairTailOffset + sizeof(RepairTail) + 1024;
+static_assert(kRepairTailOffset + sizeof(RepairTail) <= offsetof(AttnSmem, a_full),
+              "the repair tail fits in the V-Smooth tail");
 constexpr size_t kAttnSmemBytesVSmooth = offsetof(AttnSmem, a_full) + 1024;
 constexpr size_t kAttnSmemBytesQBias = sizeof(AttnSmem) + 1024;
 static_assert(kAttnSmemBytesQBias <= 232448, "shared memory per CTA");
@@ -177,9 +196,11 @@ constexpr int kVarNaturalOrder = 2;  // key blocks 0, 1, ..., nb-1
 constexpr int kVarSplit = 4;         // split key ranges (nsplit > 1): partial results for merge_kernel
 constexpr int kVarVSmooth = 8;       // V-Smooth: block means restored through the block row sums
 constexpr int kVarQBias = 16;        // Q smoothing: the key bias added to the scores by one BF16 MMA
+constexpr int kVarRepair = 32;       // V residual repair: the selected keys' blocks follow each unit's own
 // Instantiated: 0-7, 8 (V-Smooth with ExpCast, mid-window, no split), 16-23
-// (Q smoothing with each of 0-7); indexed by the variant bits.
-constexpr int kNumVariants = 24;
+// (Q smoothing with each of 0-7), 32-35 and 48-51 (repair with 0-3 and
+// 16-19: never split, never V-Smooth); indexed by the variant bits.
+constexpr int kNumVariants = 52;
 
 // Key block visited at step i of a range of n blocks starting at b0 (the
 // whole sequence, or one split range): cyclic from the range's middle block,
@@ -266,16 +287,16 @@ __device__ __forceinline__ float codes_sum(const uint32_t* w) {
 }
 
 // Same, with one multiplier per column (repair blocks: each selected key
-// keeps the scale of the block it came from) and no row sum.
-__device__ __forceinline__ void expcast_block_cols(const uint32_t* s, const float4* ksel, float c8sq256,
-                                                   float cs, uint32_t* w) {
+// keeps the scale of the block it came from, so as_c = a_c / 256 comes from
+// shared memory, four columns a load) and no row sum.
+__device__ __forceinline__ void expcast_block_cols(const uint32_t* s, const float4* as4, float cs, uint32_t* w) {
 #pragma unroll
   for (int g = 0; g < 32; ++g) {
-    const float4 k4 = __ldg(ksel + g);
-    const uint32_t u0 = expcast_code(s[4 * g + 0], c8sq256 * k4.x, cs);
-    const uint32_t u1 = expcast_code(s[4 * g + 1], c8sq256 * k4.y, cs);
-    const uint32_t u2 = expcast_code(s[4 * g + 2], c8sq256 * k4.z, cs);
-    const uint32_t u3 = expcast_code(s[4 * g + 3], c8sq256 * k4.w, cs);
+    const float4 a4 = as4[g];
+    const uint32_t u0 = expcast_code(s[4 * g + 0], a4.x, cs);
+    const uint32_t u1 = expcast_code(s[4 * g + 1], a4.y, cs);
+    const uint32_t u2 = expcast_code(s[4 * g + 2], a4.z, cs);
+    const uint32_t u3 = expcast_code(s[4 * g + 3], a4.w, cs);
     w[g] = __byte_perm(__byte_perm(u0, u1, 0x0040), __byte_perm(u2, u3, 0x0040), 0x5410);
   }
 }
@@ -316,13 +337,12 @@ __device__ __forceinline__ void cast_words(const uint32_t* s, float ac, float cc
   for (int g = 0; g < 32; ++g) w[g] = cast_word<false>(s[4 * g], s[4 * g + 1], s[4 * g + 2], s[4 * g + 3], ac, ac, ac, ac, cc);
 }
 
-__device__ __forceinline__ void cast_block_cols(const uint32_t* s, const float4* ksel, float c8sq8, float cc,
-                                                uint32_t* w) {
+// Per-column multipliers ac_c = a_c / 8 from shared memory (repair blocks).
+__device__ __forceinline__ void cast_block_cols(const uint32_t* s, const float4* ac4, float cc, uint32_t* w) {
 #pragma unroll
   for (int g = 0; g < 32; ++g) {
-    const float4 k4 = __ldg(ksel + g);
-    w[g] = cast_word<true>(s[4 * g], s[4 * g + 1], s[4 * g + 2], s[4 * g + 3], c8sq8 * k4.x, c8sq8 * k4.y,
-                     c8sq8 * k4.z, c8sq8 * k4.w, cc);
+    const float4 a4 = ac4[g];
+    w[g] = cast_word<true>(s[4 * g], s[4 * g + 1], s[4 * g + 2], s[4 * g + 3], a4.x, a4.y, a4.z, a4.w, cc);
   }
 }
 
@@ -451,6 +471,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int lane = threadIdx.x & 31;
   const volatile int* abort_flag = &sm.abort;
   const uint64_t tmo = P.timeout_ns;
+  constexpr bool kRep = (kVar & kVarRepair) != 0;
+  RepairTail& rt = *reinterpret_cast<RepairTail*>(reinterpret_cast<uint8_t*>(&sm) + kRepairTailOffset);
 
   if (warp == kProducerWarp && lane == 0) {
     mbar_init(smem_addr(&sm.q_full), 1);
@@ -473,6 +495,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
     if (kVar & kVarQBias)
       for (int t = 0; t < 2; ++t) mbar_init(smem_addr(&sm.a_full[t]), 128);
+    if (kRep)
+      for (int t = 0; t < 2; ++t)
+        for (int b = 0; b < 2; ++b) mbar_init(smem_addr(&rt.ksc_full[t][b]), 128);
     sm.abort = 0;
     sm.zero = 0;
     fence_mbar_init();
@@ -498,7 +523,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       for (int u = blockIdx.x; u < P.nunits && ok; u += gridDim.x) {
         const UnitCoord uc = unit_coord<kVar>(P, u);
         const TileCoord& tc = uc.tc;
-        const int nblk = uc.nbu + P.rep_blocks;
+        const int nblk = uc.nbu + (kRep ? P.rep_blocks : 0);
         if (q_iter > 0) ok = mbar_wait(smem_addr(&sm.q_empty), (q_iter - 1) & 1, tmo, abort_flag);
         if (!ok) break;
         const uint32_t qbar = smem_addr(&sm.q_full);
@@ -516,7 +541,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           constexpr bool qbias = (kVar & kVarQBias) != 0;
           mbar_arrive_expect_tx(kbar, qbias ? kTile + kBiasTile : kTile);
           mbar_arrive_expect_tx(vbar, kTile);
-          if (i < uc.nbu) {
+          if (!kRep || i < uc.nbu) {
             const int j = key_block<kVar>(i, uc.b0, uc.nbu);
             tma_load_2d(smem_addr(sm.k[stage]), &tm_k, kbar, 0, tc.bh * P.S_pad + j * 128);
             if (qbias) tma_load_2d(smem_addr(sm.kb[stage]), &tm_kb, kbar, 0, tc.bh * P.S_pad + j * 128);
@@ -584,7 +609,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       for (int u = blockIdx.x; u < P.nunits && ok; u += gridDim.x) {
         const UnitCoord ucm = unit_coord<kVar>(P, u);
         const int nbu = ucm.nbu, b0 = ucm.b0;
-        const int nblk = nbu + P.rep_blocks;
+        const int nblk = nbu + (kRep ? P.rep_blocks : 0);
         ok = issue_vote<kW>(mbar_wait(smem_addr(&sm.q_full), q_iter & 1, tmo, abort_flag));
         if (!ok) break;
         if (qbias) {
@@ -714,6 +739,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const uint32_t tS = tmem + lane_off + t * 128;
     const uint32_t tO = tmem + lane_off + 256 + t * 128;
     uint32_t blk_count = 0, tile_count = 0;
+    uint32_t rep_count = 0;                     // repair blocks started (all units): buffer and parity
     const int trole = (wq == 0) ? t : -1;
     bool ok = true;
     if (kVar & kVarVSmooth) {
@@ -723,7 +749,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     for (int u = blockIdx.x; u < P.nunits && ok; u += gridDim.x) {
       const UnitCoord uc = unit_coord<kVar>(P, u);
       const TileCoord& tc = uc.tc;
-      const int nblk = uc.nbu + P.rep_blocks;
       const int qb = t ? tc.qb1 : tc.qb0;
       const bool store = (t == 0) || tc.has1;
       const float sq = P.sq[tc.bh * P.nb + qb];
@@ -750,9 +775,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       // Key scale of the current block, loaded one block ahead.
       float sk_next = __ldg(P.sk + tc.bh * P.nb + key_block<kVar>(0, uc.b0, uc.nbu));
-      for (int i = 0; i < nblk; ++i) {
-        const bool main_blk = i < uc.nbu;
-        const int j = main_blk ? key_block<kVar>(i, uc.b0, uc.nbu) : 0;
+      for (int i = 0; i < uc.nbu; ++i) {
+        const int j = key_block<kVar>(i, uc.b0, uc.nbu);
         const float skj = sk_next;
         if (i + 1 < uc.nbu) sk_next = __ldg(P.sk + tc.bh * P.nb + key_block<kVar>(i + 1, uc.b0, uc.nbu));
         const uint32_t gi = blk_count;
@@ -766,64 +790,45 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         uint32_t w[32];
         float f = 1.0f;
         bool rescale = false;
-        if (main_blk) {
-          const int valid = P.S - j * 128;
-          const float a = c8sq * skj;
-          const float as = expcast_scale_a(a);
-          float mx = tmem_load_row128_max(tS, s);
-          if (valid < 128) {       // ragged tail block: mask, then a software max
-#pragma unroll
-            for (int c = 0; c < 128; ++c)
-              if (c >= valid) s[c] = 0xFF800000u;  // -inf: excluded from max, code 0
-            mx = rowmax128(s);
-          }
-          const float bm8 = mx * a;
-          const bool need = bm8 > kf + (kFrac + kLazy);
-          if (__any_sync(0xFFFFFFFFu, need)) {
-            const float kn = need ? ceilf(bm8 - kFrac) : kf;
-            f = need ? exp2f((kf - kn) * 0.125f) : 1.0f;
-            l *= f;
-            kf = kn;
-            rescale = i > 0;
-            if ((kVar & kVarVSmooth) && rescale) {
-              // Row sums not yet added to O change units with it.
-#pragma unroll
-              for (int c = 0; c < 16; ++c) sm.lbuf[t][c][row] *= f;
-            }
-          }
-          if (trole >= 0) trace_mark(P, trole, gi, 3);
-          if (kVar & kVarExpThenCast)
-            cast_words(s, a * 0.125f, (64.0f - kFrac - kf) * 0.125f, w);
-          else
-            expcast_words<0, 32>(s, as, expcast_scale_c(kCodeBase - kf), w);
-          if (dump_tile && j == P.dump_kb) {
-            uint4* d = reinterpret_cast<uint4*>(P.dump_codes + row * 128);
-#pragma unroll
-            for (int g = 0; g < 8; ++g) d[g] = make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
-            P.dump_m8[row] = kf + kFrac;
-          }
-        } else {
-          tmem_load_row128(tS, s);
-          const int r = i - uc.nbu;
-          const int valid = P.n_rep - r * 128;
+        const int valid = P.S - j * 128;
+        const float a = c8sq * skj;
+        const float as = expcast_scale_a(a);
+        float mx = tmem_load_row128_max(tS, s);
+        if (valid < 128) {       // ragged tail block: mask, then a software max
 #pragma unroll
           for (int c = 0; c < 128; ++c)
-            if (c >= valid) s[c] = 0xFF800000u;
-          const float4* ks = reinterpret_cast<const float4*>(
-              P.sk_sel + static_cast<int64_t>(tc.bh) * P.n_rep_pad + r * 128);
-          if (kVar & kVarExpThenCast)
-            cast_block_cols(s, ks, c8sq * 0.125f, (64.0f - kFrac - kf) * 0.125f, w);
-          else
-            expcast_block_cols(s, ks, expcast_scale_a(c8sq), expcast_scale_c(kCodeBase - kf), w);
-          if (r == 0) {
-            f = P.sv[tc.bh] / P.sr[tc.bh];
-            rescale = true;
+            if (c >= valid) s[c] = 0xFF800000u;  // -inf: excluded from max, code 0
+          mx = rowmax128(s);
+        }
+        const float bm8 = mx * a;
+        const bool need = bm8 > kf + (kFrac + kLazy);
+        if (__any_sync(0xFFFFFFFFu, need)) {
+          const float kn = need ? ceilf(bm8 - kFrac) : kf;
+          f = need ? exp2f((kf - kn) * 0.125f) : 1.0f;
+          l *= f;
+          kf = kn;
+          rescale = i > 0;
+          if ((kVar & kVarVSmooth) && rescale) {
+            // Row sums not yet added to O change units with it.
+#pragma unroll
+            for (int c = 0; c < 16; ++c) sm.lbuf[t][c][row] *= f;
           }
+        }
+        if (trole >= 0) trace_mark(P, trole, gi, 3);
+        if (kVar & kVarExpThenCast)
+          cast_words(s, a * 0.125f, (64.0f - kFrac - kf) * 0.125f, w);
+        else
+          expcast_words<0, 32>(s, as, expcast_scale_c(kCodeBase - kf), w);
+        if (dump_tile && j == P.dump_kb) {
+          uint4* d = reinterpret_cast<uint4*>(P.dump_codes + row * 128);
+#pragma unroll
+          for (int g = 0; g < 8; ++g) d[g] = make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
+          P.dump_m8[row] = kf + kFrac;
         }
         if (trole >= 0) trace_mark(P, trole, gi, 4);
         tmem_st32(tS, w);
         bool lsum_done = false;
-        if ((kVar & kVarVSmooth) && main_blk) {
+        if (kVar & kVarVSmooth) {
           // V-Smooth: a block that starts a run hands the previous run's row
           // sums to the mean MMA (columns 32-47 of S_t); the unit's last block
           // adds its own row sum first and hands its run over too (48-63).
@@ -842,16 +847,68 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (rescale) tmem_scale_row128(tO, f);
         tmem_wait_st();
         tc_fence_before();
-        // One arrival per warp once all its lanes' stores are done: 128
-        // arrivals would queue on the one barrier the MMA warp is waiting on.
+        // Every thread arrives once its own P stores are done (128 arrivals).
         mbar_arrive(smem_addr(&sm.p_full[t]));
         // The row sum waits until the codes are on their way to the tensor core.
-        if (main_blk && !lsum_done) {
+        if (!lsum_done && P.rowsum_gate) {
           const float lbi = codes_sum(w);
           l += lbi;
           if (kVar & kVarVSmooth) sm.lbuf[t][j & 15][row] = lbi;
         }
         if (trole >= 0) trace_mark(P, trole, gi, 6);
+      }
+      if (kRep && ok) {
+        // The repair blocks, after the row's final reference is known: codes
+        // against it with each selected key's own multiplier, no max, no row
+        // sum; the first one changes O's units from s_v to s_r.  Multiplier
+        // r + 1 is written while block r runs, into the other buffer; a buffer
+        // is written again only after every thread of the tile has arrived for
+        // the block after its last reader, so no thread still reads it.
+        const float* sk_sel = P.sk_sel + static_cast<int64_t>(tc.bh) * P.n_rep_pad + row;
+        // a selected key's multiplier: this times its block scale
+        const float rep_base = (kVar & kVarExpThenCast) ? c8sq * 0.125f : expcast_scale_a(c8sq);
+        float sk_rep = __ldg(sk_sel);
+        rt.ksc[t][rep_count & 1][row] = rep_base * sk_rep;
+        mbar_arrive(smem_addr(&rt.ksc_full[t][rep_count & 1]));
+        for (int r = 0; r < P.rep_blocks; ++r) {
+          const uint32_t rc = rep_count++;
+          const bool more = r + 1 < P.rep_blocks;
+          if (more) sk_rep = __ldg(sk_sel + (r + 1) * 128);
+          const uint32_t gi = blk_count;
+          if (trole >= 0) trace_mark(P, trole, gi, 0);
+          ok = __all_sync(0xFFFFFFFFu,
+                          mbar_wait(smem_addr(&sm.s_full[t]), blk_count & 1, tmo, abort_flag) &&
+                              mbar_wait(smem_addr(&rt.ksc_full[t][rc & 1]), (rc >> 1) & 1, tmo, abort_flag));
+          ++blk_count;
+          if (!ok) break;
+          if (trole >= 0) trace_mark(P, trole, gi, 1);
+          tc_fence_after();
+          uint32_t s[128];
+          uint32_t w[32];
+          tmem_load_row128(tS, s);
+          if (!more) {   // only the set's last block holds padding columns
+            const int valid = P.n_rep - r * 128;
+#pragma unroll
+            for (int c = 0; c < 128; ++c)
+              if (c >= valid) s[c] = 0xFF800000u;
+          }
+          const float4* ks = reinterpret_cast<const float4*>(rt.ksc[t][rc & 1]);
+          if (kVar & kVarExpThenCast)
+            cast_block_cols(s, ks, (64.0f - kFrac - kf) * 0.125f, w);
+          else
+            expcast_block_cols(s, ks, expcast_scale_c(kCodeBase - kf), w);
+          if (trole >= 0) trace_mark(P, trole, gi, 4);
+          tmem_st32(tS, w);
+          if (r == 0) tmem_scale_row128(tO, P.sv[tc.bh] / P.sr[tc.bh]);
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(smem_addr(&sm.p_full[t]));
+          if (more) {
+            rt.ksc[t][rep_count & 1][row] = rep_base * sk_rep;
+            mbar_arrive(smem_addr(&rt.ksc_full[t][rep_count & 1]));
+          }
+          if (trole >= 0) trace_mark(P, trole, gi, 6);
+        }
       }
       if (!ok) break;
       ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&sm.o_full[t]), tile_count & 1, tmo, abort_flag));
@@ -886,7 +943,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         continue;
       }
       // Epilogue: O = scale * O_acc / l, BF16, one 256-byte row per thread.
-      const float scale = (P.rep_blocks > 0 ? P.sr[tc.bh] : P.sv[tc.bh]) / l;
+      const float scale = (kRep ? P.sr[tc.bh] : P.sv[tc.bh]) / l;
       const int b = tc.bh / P.H, h = tc.bh - b * P.H;
       uint16_t* orow = P.o + b * P.os[0] + static_cast<int64_t>(q_row) * P.os[1] + h * P.os[2];
 #pragma unroll 1

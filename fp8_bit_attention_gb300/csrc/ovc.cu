@@ -34,7 +34,19 @@ const decltype(&attention_kernel<0>) kAttentionKernels[kNumVariants] = {
     attention_kernel<4>, attention_kernel<5>, attention_kernel<6>, attention_kernel<7>,
     attention_kernel<kVarVSmooth>, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
     attention_kernel<16>, attention_kernel<17>, attention_kernel<18>, attention_kernel<19>,
-    attention_kernel<20>, attention_kernel<21>, attention_kernel<22>, attention_kernel<23>};
+    attention_kernel<20>, attention_kernel<21>, attention_kernel<22>, attention_kernel<23>,
+    nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+    attention_kernel<32>, attention_kernel<33>, attention_kernel<34>, attention_kernel<35>,
+    nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+    attention_kernel<48>, attention_kernel<49>, attention_kernel<50>, attention_kernel<51>};
+
+// Dynamic shared memory of each variant's launch.
+size_t attn_smem_bytes(int variant) {
+  if (variant == kVarVSmooth) return kAttnSmemBytesVSmooth;
+  if (variant & kVarQBias) return kAttnSmemBytesQBias;
+  if (variant & kVarRepair) return kAttnSmemBytesRepair;
+  return kAttnSmemBytes;
+}
 
 constexpr int kMaxDevices = 64;
 constexpr uint32_t kPrepareFlags = OVC_PREPARE_SMOOTH_K | OVC_PREPARE_V_SMOOTH | OVC_PREPARE_SMOOTH_Q;
@@ -67,9 +79,7 @@ ovc_status device_state(DeviceState** out) {
       for (int v = 0; v < kNumVariants; ++v)
         if (kAttentionKernels[v] != nullptr &&
             cudaFuncSetAttribute(kAttentionKernels[v], cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(v == kVarVSmooth ? kAttnSmemBytesVSmooth
-                                                                   : (v & kVarQBias) ? kAttnSmemBytesQBias
-                                                                                     : kAttnSmemBytes)) != cudaSuccess)
+                                 static_cast<int>(attn_smem_bytes(v))) != cudaSuccess)
           return OVC_ERR_CUDA;
       if (cudaFuncSetAttribute(kmeans_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(kmeans_partial_smem())) != cudaSuccess)
@@ -342,6 +352,7 @@ ovc_status run_attention(const ovc_prepared* p, const ovc_repair* r, float softm
   }
 
   AttnParams P{};
+  P.rowsum_gate = 1;
   P.B = static_cast<int32_t>(p->B);
   P.S = static_cast<int32_t>(p->S);
   P.H = static_cast<int32_t>(p->H);
@@ -398,9 +409,10 @@ ovc_status run_attention(const ovc_prepared* p, const ovc_repair* r, float softm
   const int64_t grid = persistent ? (nunits < dev->sms ? nunits : dev->sms) : nunits;
   static_assert(OVC_ATTN_EXP_THEN_CAST == kVarExpThenCast && OVC_ATTN_NATURAL_ORDER == kVarNaturalOrder,
                 "flag bits select the kernel variant");
-  const int variant =
-      vsmooth ? kVarVSmooth : static_cast<int>(flags | (ns > 1 ? kVarSplit : 0) | (qbias ? kVarQBias : 0));
-  const size_t smem = vsmooth ? kAttnSmemBytesVSmooth : (qbias ? kAttnSmemBytesQBias : kAttnSmemBytes);
+  const int variant = vsmooth ? kVarVSmooth
+                              : static_cast<int>(flags | (ns > 1 ? kVarSplit : 0) | (qbias ? kVarQBias : 0) |
+                                                 (r ? kVarRepair : 0));
+  const size_t smem = attn_smem_bytes(variant);
   kAttentionKernels[variant]<<<static_cast<unsigned>(grid), kAttnThreads, smem, static_cast<cudaStream_t>(stream)>>>(
       mq, mk, mv, mks, mdv, mvm, mkb, mkbs, P);
   if (ns > 1) {
