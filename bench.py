@@ -494,7 +494,8 @@ def run_ours(a):
         te = statistics.median(times_e2e)
         te = max_over_ranks(te, dist, dev)
         e2e = {"value": world * flop / te / 1e12, "unit": "TFLOP/s", "ms_per_step": te * 1e3,
-               "calls": "median of 5 attention(q, k, v) calls on pinned host tensors",
+               "calls": "median of 5 attention(q, k, v) calls on pinned host tensors: the C-ABI call "
+                        "ovc_attention_host streams head chunks through the GPU, every copy inside the call",
                "h2d_bytes_per_step": 3 * q.numel() * q.element_size(),
                "d2h_bytes_per_step": o_host.numel() * o_host.element_size()}
 

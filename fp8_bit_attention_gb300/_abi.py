@@ -51,6 +51,11 @@ class OvcRepair(ctypes.Structure):
                 ("kb_sel", c_ptr)]
 
 
+class OvcHostIO(ctypes.Structure):
+    _fields_ = [("q", c_ptr), ("k", c_ptr), ("v", c_ptr), ("o", c_ptr), ("dtype", c_i32),
+                ("B", c_i64), ("S", c_i64), ("H", c_i64)]
+
+
 class OvcProbe(ctypes.Structure):
     _fields_ = [("dump_bh", c_i64), ("dump_qblock", c_i64), ("dump_kblock", c_i64),
                 ("dump_codes", c_ptr), ("dump_m8", c_ptr), ("wait_timeout_ns", ctypes.c_uint64),
@@ -84,8 +89,11 @@ SIGNATURES = {
     "ovc_vsmooth_group": (c_i32, [P(OvcTensor), c_i32, c_i32, c_ptr, ctypes.c_size_t, c_ptr, c_ptr]),
     "ovc_prepare_grouped": (c_i32, [P(OvcTensor), P(OvcTensor), P(OvcTensor), c_ptr, ctypes.c_uint32, c_ptr,
                                     ctypes.c_size_t, P(OvcPrepared), c_ptr]),
-    "ovc_memcpy2d": (c_i32, [c_ptr, ctypes.c_size_t, c_ptr, ctypes.c_size_t, ctypes.c_size_t,
-                             ctypes.c_size_t, c_ptr]),
+    "ovc_attention_host": (c_i32, [P(OvcHostIO), ctypes.c_float, ctypes.c_uint32, ctypes.c_float, c_ptr, c_i32,
+                                   c_ptr, ctypes.c_size_t]),
+    "ovc_attention_host_workspace_bytes": (ctypes.c_size_t, [c_i64, c_i64, c_i64, c_i32, ctypes.c_uint32,
+                                                             ctypes.c_float]),
+    "ovc_host_chunk_plan": (c_i32, [c_i64, c_i64, c_i32, c_ptr, c_i32]),
 }
 
 _lock = threading.Lock()

@@ -385,44 +385,20 @@ def device_status(stream=None) -> int:
     return int(lib().ovc_get_device_status(ctypes.c_void_p(_stream_handle(stream))))
 
 
-def memcpy2d(dst_ptr: int, dpitch: int, src_ptr: int, spitch: int, width: int, height: int,
-             stream=None) -> None:
-    """Strided asynchronous copy (``ovc_memcpy2d``) on ``stream`` (default: current)."""
-    check(lib().ovc_memcpy2d(dst_ptr, dpitch, src_ptr, spitch, width, height, _stream_handle(stream)),
-          "ovc_memcpy2d")
-
-
 def head_chunks(H: int, chunk_heads=None, tiles_per_head: int | None = None,
                 sms: int | None = None) -> list[tuple[int, int]]:
-    """Head ranges of the host-buffer path.
+    """Head ranges [h0, h1) of the host-buffer path.
 
     chunk_heads: an int (equal chunks of that many heads), a sequence of chunk
-    sizes summing to H, or None for the default plan.  The first chunk's copy
-    in and the last chunk's copy out are the only copies that no computation
-    hides, so the default ramps: e and 2e heads first, 2e and e last, with
-    e = H/56 rounded (at least 1).  A chunk's attention takes about five
-    times as long as the copy of as many heads (73397 tokens on a GB300), so
-    each chunk still hides the next one's copy; hence also h <= 10 e below.
-    The chunks between take h heads each, h in [H/8, min(H/4, 10 e)] chosen
-    so that h * tiles_per_head fills whole waves of `sms` CTAs best, the
-    larger h on a tie (fewer chunks; with 287 tile pairs per head on 152 SMs,
-    9 heads make exactly 17 waves); without those figures, about a quarter
-    of H."""
+    sizes summing to H, or None for the library's default plan
+    (``ovc_host_chunk_plan``: a ramp of small chunks at both ends, and chunks
+    between whose tile pairs fill whole waves of `sms` CTAs best)."""
     if chunk_heads is None:
-        e = max(1, int(round(H / 56)))
-        if H < 12:
-            return head_chunks(H, max(1, -(-H // 4)))
-        mid = H - 6 * e
-        h = max(1, -(-H // 4))
-        if tiles_per_head and sms:
-            def waste(n):
-                t = n * tiles_per_head
-                return (-(-t // sms) * sms) / t
-            # at most 10 e heads: the 2e-head chunk before must hide its copy
-            hi = max(2, min(H // 4, 10 * e))
-            h = min(range(max(1, min(H // 8, hi)), hi + 1), key=lambda n: (round(waste(n), 4), -n))
-        sizes = [e, 2 * e] + [h] * (mid // h) + ([mid % h] if mid % h else []) + [2 * e, e]
-        return head_chunks(H, sizes)
+        buf = (ctypes.c_int32 * 64)()
+        n = lib().ovc_host_chunk_plan(int(H), int(tiles_per_head or 0), int(sms or 0), buf, 64)
+        if n < 1:
+            raise ValueError(f"no chunk plan for H = {H}")
+        return head_chunks(H, list(buf[:n]))
     if isinstance(chunk_heads, int):
         n = max(1, chunk_heads)
         return [(h0, min(H, h0 + n)) for h0 in range(0, H, n)]
@@ -444,13 +420,10 @@ def _attention_device(q, k, v, softmax_scale, repair_budget, out, smooth_k=False
 
 
 def _attention_host(q, k, v, softmax_scale, repair_budget, out, dev, chunk_heads, smooth_k=False, smooth_q=False):
-    """Host-resident inputs streamed through the GPU in head chunks.
-
-    Every head is computed independently (its V scale, residual ranking and
-    attention involve that head alone), so the result equals a single
-    whole-tensor call bit for bit.  Chunk c+1 is copied in while chunk c is
-    prepared and attended, and chunk c-1's output is copied out meanwhile:
-    the copies (bound by the host link) hide behind the attention kernels."""
+    """Host-resident inputs and output: ``ovc_attention_host`` streams them
+    through `dev` in head chunks (copies overlapping the neighbouring chunks'
+    computation) and returns once O is in `out`.  This function only checks
+    the tensors, computes the chunk plan and provides the device workspace."""
     q4, k4, v4 = (_as4d(x) for x in (q, k, v))
     if k4.shape != q4.shape or v4.shape != q4.shape:
         raise ValueError("q, k and v must have the same shape")
@@ -468,72 +441,21 @@ def _attention_host(q, k, v, softmax_scale, repair_budget, out, dev, chunk_heads
     nb = -(-S // 128)
     chunks = head_chunks(H, chunk_heads, tiles_per_head=B * (-(-nb // 2)),
                          sms=torch.cuda.get_device_properties(dev).multi_processor_count)
-    hmax = max(h1 - h0 for h0, h1 in chunks)
-    # Chunks alternate between two compute streams, so that a chunk's
-    # preparation and first CTAs can start on the SMs that the previous
-    # chunk's last, partly filled wave leaves idle.
-    comps = [torch.cuda.current_stream(dev), torch.cuda.Stream(dev)]
-    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    # Two sets of staging buffers: chunk c uses set c % 2.
-    n_el = B * S * hmax * D
-    stage_in = [[torch.empty(n_el, dtype=q4.dtype, device=dev) for _ in range(3)] for _ in range(2)]
-    stage_out = [torch.empty(n_el, dtype=torch.bfloat16, device=dev) for _ in range(2)]
-    # The staging buffers come from the caching allocator on the current
-    # stream (comps[0]); a block freed by work still pending there may be
-    # handed out, so the other streams start only after that work.
-    for s in (s_in, s_out, comps[1]):
-        s.wait_stream(comps[0])
-    in_free = [None, None]      # compute has consumed the set's inputs
-    out_free = [None, None]     # the set's output has been copied out
-    try:
-        _stream_chunks(q4, k4, v4, o4, chunks, stage_in, stage_out, in_free, out_free, comps, s_in, s_out,
-                       softmax_scale, repair_budget, smooth_k, smooth_q)
-    finally:
-        # The staging buffers die with this frame: let every stream finish with them.
-        s_out.synchronize()
-        s_in.synchronize()
-        for cs in comps:
-            cs.synchronize()
+    sizes = [h1 - h0 for h0, h1 in chunks]
+    flags = _prep_flags(smooth_k, False, smooth_q)
+    budget = float(repair_budget or 0.0)
+    nbytes = lib().ovc_attention_host_workspace_bytes(B, S, max(sizes), _DTYPES[q4.dtype], flags, budget)
+    if nbytes == 0:
+        raise ValueError("unsupported arguments for the host-buffer path")
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    io = _abi.OvcHostIO(q4.data_ptr(), k4.data_ptr(), v4.data_ptr(), o4.data_ptr(), _DTYPES[q4.dtype], B, S, H)
+    arr = (ctypes.c_int32 * len(sizes))(*sizes)
+    # The workspace comes from the caching allocator on the current stream;
+    # the call's own streams must not start before work pending there is done.
+    torch.cuda.current_stream(dev).synchronize()
+    check(lib().ovc_attention_host(ctypes.byref(io), float(softmax_scale or 0.0), flags, budget, arr, len(sizes),
+                                   ctypes.c_void_p(ws.data_ptr()), nbytes), "ovc_attention_host")
     return out
-
-
-def _stream_chunks(q4, k4, v4, o4, chunks, stage_in, stage_out, in_free, out_free, comps, s_in, s_out,
-                   softmax_scale, repair_budget, smooth_k, smooth_q):
-    B, S, H, D = q4.shape
-    el = q4.element_size()
-    for c, (h0, h1) in enumerate(chunks):
-        hc, st = h1 - h0, c % 2
-        ins = [buf[:B * S * hc * D].view(B, S, hc, D) for buf in stage_in[st]]
-        with torch.cuda.stream(s_in):
-            if in_free[st] is not None:
-                s_in.wait_event(in_free[st])
-            for src, dst in zip((q4, k4, v4), ins):
-                memcpy2d(dst.data_ptr(), hc * D * el, src.data_ptr() + h0 * D * el, H * D * el,
-                         hc * D * el, B * S, s_in)
-            ready = torch.cuda.Event()
-            ready.record(s_in)
-        comp = comps[st]             # staging set st and compute stream st go together
-        with torch.cuda.stream(comp):
-            comp.wait_event(ready)
-            prep = prepare(*ins, smooth_k=smooth_k, smooth_q=smooth_q)
-            rep = prepare_v_repair(ins[2], prep, repair_budget) if repair_budget else None
-            in_free[st] = torch.cuda.Event()
-            in_free[st].record(comp)
-            if out_free[st] is not None:
-                comp.wait_event(out_free[st])
-            ob = stage_out[st][:B * S * hc * D].view(B, S, hc, D)
-            if rep is not None:
-                attention_v_repair(prep, rep, softmax_scale=softmax_scale, out=ob)
-            else:
-                attention_prepared(prep, softmax_scale=softmax_scale, out=ob)
-            done = torch.cuda.Event()
-            done.record(comp)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(done)
-            memcpy2d(o4.data_ptr() + h0 * D * 2, H * D * 2, ob.data_ptr(), hc * D * 2, hc * D * 2,
-                     B * S, s_out)
-            out_free[st] = torch.cuda.Event()
-            out_free[st].record(s_out)
 
 
 def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, softmax_scale: float | None = None,

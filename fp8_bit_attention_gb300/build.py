@@ -7,7 +7,8 @@ import subprocess
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 SRC = os.path.join(PKG, "csrc", "ovc.cu")
-HEADERS = [os.path.join(PKG, "csrc", f) for f in ("ptx.cuh", "prepare.cuh", "attention.cuh", "repair.cuh", "group.cuh")]
+HEADERS = [os.path.join(PKG, "csrc", f) for f in ("ptx.cuh", "prepare.cuh", "attention.cuh", "repair.cuh", "group.cuh",
+                                                          "host_stream.cuh")]
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD_DIR, "libovc.so")

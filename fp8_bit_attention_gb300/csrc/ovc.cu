@@ -760,17 +760,9 @@ ovc_status ovc_vsmooth_group(const ovc_tensor* v, int32_t clusters, int32_t iter
   return launch_status();
 }
 
-ovc_status ovc_memcpy2d(void* dst, size_t dpitch, const void* src, size_t spitch, size_t width,
-                        size_t height, void* stream) {
-  if (width == 0 || height == 0) return OVC_OK;
-  if (!dst || !src || width > dpitch || width > spitch) return OVC_ERR_INVALID_ARG;
-  return cudaMemcpy2DAsync(dst, dpitch, src, spitch, width, height, cudaMemcpyDefault,
-                           static_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? OVC_OK
-             : OVC_ERR_CUDA;
-}
-
 }  // extern "C"
+
+#include "host_stream.cuh"
 
 // ---------------------------------------------------------------------------
 // ovc_prepare_noalloc: ovc_prepare for callers that cannot allocate.  The

@@ -339,21 +339,71 @@ ovc_status ovc_prepare_grouped(const ovc_tensor* q, const ovc_tensor* k, const o
 ovc_status ovc_prepare_ex(const ovc_tensor* q, const ovc_tensor* k, const ovc_tensor* v, uint32_t flags,
                           void* workspace, size_t workspace_bytes, ovc_prepared* out, void* stream);
 
-/* Strided asynchronous copy (cudaMemcpy2DAsync, direction inferred from the
- * pointers) -- no counterpart in the pages; infrastructure for the host-buffer
- * path of the Python binding, which streams host-resident [B,S,H,128] inputs
- * through the GPU in head chunks so that the copies overlap the previous
- * chunk's attention.  A head range [h0,h1) of such a tensor is height = B*S
- * rows of width = (h1-h0)*128*elem_bytes bytes, spitch = H*128*elem_bytes
- * apart.
- *   dst, src: host or device pointers; host memory must be pinned for the
- *             copy to be asynchronous (pageable memory still copies
- *             correctly, synchronously).  width <= dpitch and width <= spitch.
- *   stream:   a cudaStream_t (NULL: the legacy default stream).
- * Returns OVC_OK (also when width or height is 0), OVC_ERR_INVALID_ARG, or
- * OVC_ERR_CUDA if the copy could not be enqueued. */
-ovc_status ovc_memcpy2d(void* dst, size_t dpitch, const void* src, size_t spitch, size_t width,
-                        size_t height, void* stream);
+/* The whole call for inputs and output in HOST memory -- the pages' API takes
+ * device tensors; this entry point serves callers whose tensors live on the
+ * host (no counterpart in the pages).  Q, K, V and O are streamed through the
+ * current device in chunks of whole heads: while one chunk is prepared and
+ * attended, the next chunk's inputs are copied in and the previous chunk's
+ * output is copied out, so the copies (bound by the host link) hide behind
+ * the attention kernels.  Every head is computed on its own (its V scale,
+ * residual ranking and attention involve that head alone), so the result
+ * equals ovc_prepare_ex + (ovc_prepare_v_repair +) ovc_attention_ex over all
+ * heads at once, bit for bit.
+ *   io            host pointers q, k, v (contiguous [B,S,H,128] of dtype
+ *                 OVC_BF16 or OVC_FP16) and o (contiguous BF16 [B,S,H,128]).
+ *                 Pinned (page-locked) memory lets the copies run
+ *                 asynchronously at full speed; pageable memory gives the
+ *                 same result, more slowly.
+ *   softmax_scale <= 0 selects 1/sqrt(128).
+ *   prep_flags    OR of OVC_PREPARE_SMOOTH_K and OVC_PREPARE_SMOOTH_Q.
+ *   repair_budget 0 for none, else in (0, 1] as for ovc_prepare_v_repair.
+ *   chunk_sizes   nchunks head counts, each >= 1, summing to H, in head order
+ *                 (ovc_host_chunk_plan gives the default plan).
+ *   workspace     device memory, 256-byte aligned, at least
+ *                 ovc_attention_host_workspace_bytes(B, S, largest chunk, ...)
+ *                 bytes: two sets of staging buffers, preparations and repair
+ *                 sets (chunk c uses set c % 2).
+ * Synchronous: the call creates its own streams (two for compute, one for
+ * each copy direction), and returns once O is complete in host memory and
+ * every stream has finished with the workspace, also after an error.
+ * Returns OVC_ERR_INVALID_ARG, OVC_ERR_UNSUPPORTED (dtype),
+ * OVC_ERR_WORKSPACE_TOO_SMALL, any error of the calls it makes, or
+ * OVC_ERR_CUDA if a copy, stream or event call fails.  Device-side timeouts
+ * are reported by ovc_get_device_status() as for every other call. */
+typedef struct {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  int32_t dtype;                    /* OVC_BF16 or OVC_FP16 (q, k, v); o is BF16 */
+  int64_t B, S, H;
+} ovc_host_io;
+
+ovc_status ovc_attention_host(const ovc_host_io* io, float softmax_scale, uint32_t prep_flags,
+                              float repair_budget, const int32_t* chunk_sizes, int32_t nchunks,
+                              void* workspace, size_t workspace_bytes);
+
+/* Workspace bytes of ovc_attention_host whose largest chunk has
+ * max_chunk_heads heads (0 for invalid arguments). */
+size_t ovc_attention_host_workspace_bytes(int64_t B, int64_t S, int64_t max_chunk_heads, int32_t dtype,
+                                          uint32_t prep_flags, float repair_budget);
+
+/* The default head-chunk plan of ovc_attention_host, a host-only
+ * computation: writes the chunk sizes (in head order) to sizes[0..n) and
+ * returns n, or -1 if H < 1 or more than max_chunks sizes would be needed.
+ * The first chunk's copy in and the last chunk's copy out are the only
+ * copies no computation hides, so the plan ramps: e and 2e heads first, 2e
+ * and e last, e = H/56 rounded (half to even, at least 1).  A chunk's
+ * attention takes about five times as long as the copy of as many heads
+ * (73397 tokens on a GB300), so each chunk still hides the next one's copy;
+ * hence also h <= 10 e below.  The chunks between take h heads each, h in
+ * [H/8, min(H/4, 10 e)] chosen so that h * tiles_per_head fills whole waves
+ * of `sms` CTAs best (filled / used slots compared to four decimals, the
+ * larger h on a tie); with tiles_per_head or sms <= 0, h = ceil(H/4).  Fewer
+ * than 12 heads: equal chunks of ceil(H/4).  tiles_per_head = B * ceil(nb/2)
+ * for the attention kernel's pairs of 128-row query blocks (nb = ceil(S/128));
+ * sms = the device's SM count. */
+int32_t ovc_host_chunk_plan(int64_t H, int64_t tiles_per_head, int32_t sms, int32_t* sizes, int32_t max_chunks);
 
 #ifdef __cplusplus
 }

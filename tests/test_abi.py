@@ -131,13 +131,82 @@ def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
         _abi.lib()
 
 
-def test_memcpy2d_validates_on_the_host(lib):
+def _host_io(B=1, S=300, H=4, dtype=0, ptr=0x1000):
     from fp8_bit_attention_gb300 import _abi
-    assert lib.ovc_memcpy2d(0x1000, 64, 0x2000, 64, 0, 10, None) == _abi.OVC_OK        # nothing to copy
-    assert lib.ovc_memcpy2d(0x1000, 64, 0x2000, 64, 16, 0, None) == _abi.OVC_OK
-    assert lib.ovc_memcpy2d(0x1000, 32, 0x2000, 64, 64, 1, None) == _abi.OVC_ERR_INVALID_ARG  # width > dpitch
-    assert lib.ovc_memcpy2d(0x1000, 64, 0x2000, 32, 64, 1, None) == _abi.OVC_ERR_INVALID_ARG  # width > spitch
-    assert lib.ovc_memcpy2d(None, 64, 0x2000, 64, 64, 1, None) == _abi.OVC_ERR_INVALID_ARG
+    return _abi.OvcHostIO(ptr, ptr, ptr, ptr, dtype, B, S, H)
+
+
+def test_attention_host_validates_on_the_host(lib):
+    """Every argument check of the host-buffer call runs before it touches a device."""
+    import ctypes
+    from fp8_bit_attention_gb300 import _abi
+    sizes = (ctypes.c_int32 * 2)(1, 3)
+    need = lib.ovc_attention_host_workspace_bytes(1, 300, 3, 0, 0, 0.0)
+    assert need > 0
+    ws = 0x10000
+    call = lambda io, fl=0, bud=0.0, sz=sizes, n=2, w=ws, nbytes=need: lib.ovc_attention_host(
+        ctypes.byref(io) if io is not None else None, 0.0, fl, bud, sz, n, w, nbytes)
+    assert call(None) == _abi.OVC_ERR_INVALID_ARG
+    assert call(_host_io(ptr=0)) == _abi.OVC_ERR_INVALID_ARG                 # null host pointers
+    assert call(_host_io(dtype=7)) == _abi.OVC_ERR_UNSUPPORTED
+    assert call(_host_io(S=0)) == _abi.OVC_ERR_INVALID_ARG
+    assert call(_host_io(H=5)) == _abi.OVC_ERR_INVALID_ARG                   # sizes sum to 4, not 5
+    assert call(_host_io(), sz=(ctypes.c_int32 * 2)(0, 4)) == _abi.OVC_ERR_INVALID_ARG
+    assert call(_host_io(), sz=None) == _abi.OVC_ERR_INVALID_ARG
+    assert call(_host_io(), n=0) == _abi.OVC_ERR_INVALID_ARG
+    assert call(_host_io(), fl=_abi.OVC_PREPARE_V_SMOOTH) == _abi.OVC_ERR_INVALID_ARG
+    assert call(_host_io(), fl=8) == _abi.OVC_ERR_INVALID_ARG
+    assert call(_host_io(), bud=1.5) == _abi.OVC_ERR_INVALID_ARG
+    assert call(_host_io(), bud=-0.1) == _abi.OVC_ERR_INVALID_ARG
+    assert call(_host_io(), w=None) == _abi.OVC_ERR_INVALID_ARG
+    assert call(_host_io(), w=ws + 16) == _abi.OVC_ERR_INVALID_ARG          # not 256-byte aligned
+    assert call(_host_io(), nbytes=need - 1) == _abi.OVC_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_attention_host_workspace_bytes(lib):
+    """Two sets of: Q, K, V staging, a preparation, a repair set, an output staging."""
+    from fp8_bit_attention_gb300 import _abi
+    al = lambda x: (x + 255) // 256 * 256
+    for B, S, hmax, flags, bud in ((1, 73397, 9, 0, 0.0), (2, 300, 3, _abi.OVC_PREPARE_SMOOTH_K, 0.02),
+                                   (1, 1, 1, _abi.OVC_PREPARE_SMOOTH_Q, 1.0)):
+        chunk = al(B * S * hmax * 128 * 2)
+        prep = al(lib.ovc_prepare_workspace_bytes_ex(B, S, hmax, 128, flags))
+        rep = al(lib.ovc_repair_workspace_bytes(B, S, hmax, bud)) if bud > 0 else 0
+        want = 2 * (3 * chunk + prep + rep + chunk)
+        for dtype in (_abi.OVC_BF16, _abi.OVC_FP16):
+            assert lib.ovc_attention_host_workspace_bytes(B, S, hmax, dtype, flags, bud) == want
+    assert lib.ovc_attention_host_workspace_bytes(1, 300, 3, 5, 0, 0.0) == 0             # dtype
+    assert lib.ovc_attention_host_workspace_bytes(1, 300, 3, 0, _abi.OVC_PREPARE_V_SMOOTH, 0.0) == 0
+    assert lib.ovc_attention_host_workspace_bytes(1, 300, 3, 0, 0, 2.0) == 0             # budget
+    assert lib.ovc_attention_host_workspace_bytes(1, 0, 3, 0, 0, 0.0) == 0
+
+
+def test_host_chunk_plan_follows_its_rule(lib):
+    """ovc_host_chunk_plan against its documented rule, restated here."""
+    import ctypes
+    for H in list(range(1, 40)) + [56, 57, 84, 112, 200]:
+        for tph, sms in ((0, 0), (287, 152), (1, 152), (144, 148), (18, 152)):
+            buf = (ctypes.c_int32 * 128)()
+            n = lib.ovc_host_chunk_plan(H, tph, sms, buf, 128)
+            sizes = list(buf[:n])
+            assert n >= 1 and sum(sizes) == H and min(sizes) >= 1
+            if H < 12:
+                q = -(-H // 4)
+                assert sizes == [q] * (H // q) + ([H % q] if H % q else [])
+                continue
+            e = max(1, round(H / 56))
+            if tph and sms:
+                hi = max(2, min(H // 4, 10 * e))
+                lo = max(1, min(H // 8, hi))
+                waste = lambda c: round(-(-c * tph // sms) * sms / (c * tph), 4)
+                h = min(range(lo, hi + 1), key=lambda c: (waste(c), -c))
+            else:
+                h = -(-H // 4)
+            mid = H - 6 * e
+            assert sizes == [e, 2 * e] + [h] * (mid // h) + ([mid % h] if mid % h else []) + [2 * e, e]
+    buf = (ctypes.c_int32 * 3)()
+    assert lib.ovc_host_chunk_plan(56, 287, 152, buf, 3) == -1       # needs 10 sizes
+    assert lib.ovc_host_chunk_plan(0, 287, 152, buf, 3) == -1
 
 
 def test_head_chunks_cover_every_head_once():

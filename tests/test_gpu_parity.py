@@ -186,6 +186,37 @@ def test_host_buffer_path_streams_head_chunks_bit_exactly(B, H, S, chunk, budget
     assert ovc.device_status() == 0
 
 
+@pytest.mark.parametrize("B,H,S,dtype,smooth,budget,sizes", [
+    (1, 5, 900, torch.bfloat16, (False, False), None, [1, 3, 1]),
+    (2, 4, 333, torch.float16, (True, True), 0.03, [4]),
+    (1, 6, 129, torch.bfloat16, (True, False), 1.0, [2, 2, 1, 1]),
+])
+def test_c_abi_host_call_matches_device_call(B, H, S, dtype, smooth, budget, sizes):
+    """ovc_attention_host called directly through the C ABI (host pointers,
+    caller workspace, explicit chunk sizes) against the device call with the
+    same options, bit for bit."""
+    import ctypes
+    from fp8_bit_attention_gb300 import _abi
+    q, k, v = (x.to(dtype) for x in inputs(B, H, S, seed=71 + S))
+    qd, kd, vd = to_dev(q, k, v)
+    want = ovc.attention(qd, kd, vd, repair_budget=budget, smooth_k=smooth[0], smooth_q=smooth[1]).cpu()
+    qp, kp, vp = (x.contiguous().pin_memory() for x in (q, k, v))
+    o = torch.full((B, S, H, 128), float("nan"), dtype=torch.bfloat16).pin_memory()
+    flags = (_abi.OVC_PREPARE_SMOOTH_K if smooth[0] else 0) | (_abi.OVC_PREPARE_SMOOTH_Q if smooth[1] else 0)
+    dt = _abi.OVC_FP16 if dtype == torch.float16 else _abi.OVC_BF16
+    lib = _abi.lib()
+    nbytes = lib.ovc_attention_host_workspace_bytes(B, S, max(sizes), dt, flags, float(budget or 0.0))
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    torch.cuda.synchronize()
+    io = _abi.OvcHostIO(qp.data_ptr(), kp.data_ptr(), vp.data_ptr(), o.data_ptr(), dt, B, S, H)
+    arr = (ctypes.c_int32 * len(sizes))(*sizes)
+    st = lib.ovc_attention_host(ctypes.byref(io), 0.0, flags, float(budget or 0.0), arr, len(sizes),
+                                ctypes.c_void_p(ws.data_ptr()), nbytes)
+    assert st == _abi.OVC_OK
+    assert ovc.device_status() == 0
+    assert torch.equal(o.view(torch.int16), want.view(torch.int16))
+
+
 @pytest.mark.parametrize("B,H,S", [(1, 2, 1000), (2, 1, 300)])
 def test_fp16_inputs_match_oracle(B, H, S):
     """FP16 inputs ("Open VC Attention" catalogue entry: FP16 or BF16):
