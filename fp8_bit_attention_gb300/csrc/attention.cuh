@@ -427,10 +427,11 @@ __device__ __forceinline__ void tmem_scale_row128(uint32_t taddr, float f) {
 }
 
 // MMA issue, by lane 0 alone (W = false) or by the whole converged MMA warp
-// with one elected lane (W = true; every wait then becomes a warp vote).  The
-// method's kernel runs fastest with lane-0 issue (72.2 against 73.0 ms at
-// S = 73397, H = 56); the Q-smoothing variants, whose QK^T adds a BF16 MMA,
-// with warp issue (75.0 against 78.3 ms).
+// with one elected lane (W = true; every wait then becomes a warp vote).
+// Issued from a converged warp, a tcgen05.commit costs the tensor pipe
+// nothing; issued by one lane of a diverged warp, each costs about as much
+// as an MMA.  Warp issue is used by every variant but V-Smooth, whose MMA
+// warp also runs the mean MMAs' run bookkeeping.
 template <bool W>
 __device__ __forceinline__ bool issue_vote(bool ok) {
   if constexpr (W) return __all_sync(0xFFFFFFFFu, ok);
@@ -583,7 +584,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA
-    constexpr bool kW = (kVar & kVarQBias) != 0;   // issue style, see issue_vote
+    constexpr bool kW = (kVar & kVarVSmooth) == 0;   // issue style, see issue_vote
     if ((kW || lane == 0) && !P.skip_mma) {
       uint32_t kv_iter = 0, q_iter = 0, sp0 = 0, sp1 = 0, mrun = 0;
       bool ok = true, issued = false;
