@@ -774,6 +774,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         fence_proxy_async_smem();
         mbar_arrive(smem_addr(&sm.a_full[t]));
       }
+      // Repair: a selected key's multiplier is rep_base times its block scale.
+      const float rep_base = (kVar & kVarExpThenCast) ? c8sq * 0.125f : expcast_scale_a(c8sq);
+      if (kRep) {
+        // The first repair block's multipliers are written now, so that the
+        // key scale's load waits alongside the unit's first scores instead of
+        // after its last main block.  The buffer was last read in the repair
+        // block before last, which every thread of the tile finished before
+        // arriving for the last one (this thread waited for that).
+        rt.ksc[t][rep_count & 1][row] =
+            rep_base * __ldg(P.sk_sel + static_cast<int64_t>(tc.bh) * P.n_rep_pad + row);
+        mbar_arrive(smem_addr(&rt.ksc_full[t][rep_count & 1]));
+      }
       // Key scale of the current block, loaded one block ahead.
       float sk_next = __ldg(P.sk + tc.bh * P.nb + key_block<kVar>(0, uc.b0, uc.nbu));
       for (int i = 0; i < uc.nbu; ++i) {
@@ -865,12 +877,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // r + 1 is written while block r runs, into the other buffer; a buffer
         // is written again only after every thread of the tile has arrived for
         // the block after its last reader, so no thread still reads it.
+        // (Block 0's were written at the start of the unit.)
         const float* sk_sel = P.sk_sel + static_cast<int64_t>(tc.bh) * P.n_rep_pad + row;
-        // a selected key's multiplier: this times its block scale
-        const float rep_base = (kVar & kVarExpThenCast) ? c8sq * 0.125f : expcast_scale_a(c8sq);
-        float sk_rep = __ldg(sk_sel);
-        rt.ksc[t][rep_count & 1][row] = rep_base * sk_rep;
-        mbar_arrive(smem_addr(&rt.ksc_full[t][rep_count & 1]));
+        float sk_rep = 0.0f;
         for (int r = 0; r < P.rep_blocks; ++r) {
           const uint32_t rc = rep_count++;
           const bool more = r + 1 < P.rep_blocks;
