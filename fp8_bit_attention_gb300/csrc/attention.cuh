@@ -655,6 +655,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
             if (i + 1 == nbu) fl |= 2u;
           }
+          // The next block's K (loaded stages ahead) is waited for here, while
+          // the warp would wait for P anyway: a wait on a completed barrier
+          // still takes a round trip, which between P.V and QK^T sits on the
+          // tiles' chain (68.8 against 70.8 ms at S = 73397, H = 56).  The
+          // V-Smooth variant keeps it between them (82.1 against 83.7 ms).
+          constexpr bool kEarlyK = (kVar & kVarVSmooth) == 0;
+          uint64_t kd_next = 0;
+          if (kEarlyK && !last) {
+            ok = issue_vote<kW>(mbar_wait(smem_addr(&sm.k_full[nstage]), ((kv_iter + 1) / kStages) & 1, tmo, abort_flag));
+            if (!ok) break;
+            kd_next = sw128_desc(smem_addr(sm.k[nstage]));
+          }
           // ---- query tile 0: O0 += P0 V, then the next block's S0
           ok = issue_vote<kW>(mbar_wait(smem_addr(&sm.p_full[0]), sp0, tmo, abort_flag));
           if (!ok) break;
@@ -676,12 +688,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
               }
             if (!ok) break;
           }
-          uint64_t kd_next = 0;
           if (!last) {
-            ok = issue_vote<kW>(mbar_wait(smem_addr(&sm.k_full[nstage]), ((kv_iter + 1) / kStages) & 1, tmo, abort_flag));
-            if (!ok) break;
-            tc_fence_after();
-            kd_next = sw128_desc(smem_addr(sm.k[nstage]));
+            if (!kEarlyK) {
+              ok = issue_vote<kW>(mbar_wait(smem_addr(&sm.k_full[nstage]), ((kv_iter + 1) / kStages) & 1, tmo, abort_flag));
+              if (!ok) break;
+              tc_fence_after();
+              kd_next = sw128_desc(smem_addr(sm.k[nstage]));
+            }
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) issue_f8_ss<kW>(tS0, qd0 + 2 * kk, kd_next + 2 * kk, kIdesc, kk > 0);
             if (qbias) issue_bf16_ss<kW>(tS0, abd0, sw32_desc(smem_addr(sm.kb[nstage])), kIdescBf16, 1u);
@@ -886,9 +899,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           if (more) sk_rep = __ldg(sk_sel + (r + 1) * 128);
           const uint32_t gi = blk_count;
           if (trole >= 0) trace_mark(P, trole, gi, 0);
+          // The multipliers (written a block ahead) first, so that this wait's
+          // round trip overlaps the scores' computation.
           ok = __all_sync(0xFFFFFFFFu,
-                          mbar_wait(smem_addr(&sm.s_full[t]), blk_count & 1, tmo, abort_flag) &&
-                              mbar_wait(smem_addr(&rt.ksc_full[t][rc & 1]), (rc >> 1) & 1, tmo, abort_flag));
+                          mbar_wait(smem_addr(&rt.ksc_full[t][rc & 1]), (rc >> 1) & 1, tmo, abort_flag) &&
+                              mbar_wait(smem_addr(&sm.s_full[t]), blk_count & 1, tmo, abort_flag));
           ++blk_count;
           if (!ok) break;
           if (trole >= 0) trace_mark(P, trole, gi, 1);
