@@ -412,16 +412,32 @@ __device__ __forceinline__ void flush_row_sums(float* lb, uint32_t taddr) {
   tmem_st16(taddr, r);
 }
 
-// O row *= f in tensor memory (one 128-column row per thread).
+// O row *= f in tensor memory (one 128-column row per thread).  kBatched:
+// all four 32-column loads in flight at once (one TMEM round trip), then the
+// products stored back; else one chunk at a time.  The two give the same
+// values; which is faster depends on the variant's schedule (S = 73397,
+// H = 56: the method's kernel 67.6 batched against 68.7 ms; the V-Smooth
+// kernel 82.0 chunked against 84.8; the repair and Q-smoothing kernels no
+// faster batched).
+template <bool kBatched>
 __device__ __forceinline__ void tmem_scale_row128(uint32_t taddr, float f) {
-#pragma unroll 1
-  for (int c = 0; c < 128; c += 32) {
-    uint32_t r[32];
-    tmem_ld32(taddr + c, r);
-    tmem_wait_ld32(r);
+  if constexpr (kBatched) {
+    uint32_t r[128];
+    tmem_load_row128(taddr, r);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * f);
-    tmem_st32(taddr + c, r);
+    for (int i = 0; i < 128; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * f);
+#pragma unroll
+    for (int c = 0; c < 128; c += 32) tmem_st32(taddr + c, r + c);
+  } else {
+#pragma unroll 1
+    for (int c = 0; c < 128; c += 32) {
+      uint32_t r[32];
+      tmem_ld32(taddr + c, r);
+      tmem_wait_ld32(r);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * f);
+      tmem_st32(taddr + c, r);
+    }
   }
   tmem_wait_st();
 }
@@ -870,7 +886,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         // O is stable here (every earlier MMA of this tile has completed) and
         // the next P.V waits for this thread's arrival below.
-        if (rescale) tmem_scale_row128(tO, f);
+        if (rescale) tmem_scale_row128<(kVar & (kVarRepair | kVarVSmooth | kVarQBias)) == 0>(tO, f);
         tmem_wait_st();
         tc_fence_before();
         // Every thread arrives once its own P stores are done (128 arrivals).
@@ -924,7 +940,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             expcast_block_cols(s, ks, expcast_scale_c(kCodeBase - kf), w);
           if (trole >= 0) trace_mark(P, trole, gi, 4);
           tmem_st32(tS, w);
-          if (r == 0) tmem_scale_row128(tO, P.sv[tc.bh] / P.sr[tc.bh]);
+          if (r == 0) tmem_scale_row128<false>(tO, P.sv[tc.bh] / P.sr[tc.bh]);
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(smem_addr(&sm.p_full[t]));
