@@ -541,13 +541,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const UnitCoord uc = unit_coord<kVar>(P, u);
         const TileCoord& tc = uc.tc;
         const int nblk = uc.nbu + (kRep ? P.rep_blocks : 0);
-        if (q_iter > 0) ok = mbar_wait(smem_addr(&sm.q_empty), (q_iter - 1) & 1, tmo, abort_flag);
-        if (!ok) break;
-        const uint32_t qbar = smem_addr(&sm.q_full);
-        mbar_arrive_expect_tx(qbar, 2 * kTile);
-        tma_load_2d(smem_addr(sm.q[0]), &tm_q, qbar, 0, tc.bh * P.S_pad + tc.qb0 * 128);
-        tma_load_2d(smem_addr(sm.q[1]), &tm_q, qbar, 0, tc.bh * P.S_pad + tc.qb1 * 128);
-        ++q_iter;
         for (int i = 0; i < nblk; ++i) {
           const uint32_t stage = kv_iter % kStages, round = kv_iter / kStages;
           if (kv_iter >= kStages) {
@@ -582,6 +575,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             tma_load_2d(smem_addr(sm.v[stage]), &tm_dv, vbar, r * 128, tc.bh * 128);
           }
           ++kv_iter;
+          if (i == 0) {
+            // The unit's Q after its first K/V block, whose stage the previous
+            // unit frees blocks earlier than its last P.V frees Q; then the
+            // next unit's Q is pulled into L2 for its own load.
+            if (q_iter > 0) ok = mbar_wait(smem_addr(&sm.q_empty), (q_iter - 1) & 1, tmo, abort_flag);
+            if (!ok) break;
+            const uint32_t qbar = smem_addr(&sm.q_full);
+            mbar_arrive_expect_tx(qbar, 2 * kTile);
+            tma_load_2d(smem_addr(sm.q[0]), &tm_q, qbar, 0, tc.bh * P.S_pad + tc.qb0 * 128);
+            tma_load_2d(smem_addr(sm.q[1]), &tm_q, qbar, 0, tc.bh * P.S_pad + tc.qb1 * 128);
+            ++q_iter;
+            if (u + static_cast<int>(gridDim.x) < P.nunits) {
+              const TileCoord tn = unit_coord<kVar>(P, u + static_cast<int>(gridDim.x)).tc;
+              tma_prefetch_l2_2d(&tm_q, 0, tn.bh * P.S_pad + tn.qb0 * 128);
+              tma_prefetch_l2_2d(&tm_q, 0, tn.bh * P.S_pad + tn.qb1 * 128);
+            }
+          }
         }
       }
       if (!ok) {
@@ -952,6 +962,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
       }
       if (!ok) break;
+      const float s_out = (kRep ? P.sr : P.sv)[tc.bh];   // loaded while O completes
       ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&sm.o_full[t]), tile_count & 1, tmo, abort_flag));
       ++tile_count;
       if (!ok) break;
@@ -983,21 +994,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (store && q_row < P.S) P.part_ml[prow] = make_float2(kf + kFrac, l);
         continue;
       }
-      // Epilogue: O = scale * O_acc / l, BF16, one 256-byte row per thread.
-      const float scale = (kRep ? P.sr[tc.bh] : P.sv[tc.bh]) / l;
+      // Epilogue: O = scale * O_acc / l, BF16, one 256-byte row per thread;
+      // the row comes out of TMEM in one round trip.
+      const float scale = s_out / l;
       const int b = tc.bh / P.H, h = tc.bh - b * P.H;
       uint16_t* orow = P.o + b * P.os[0] + static_cast<int64_t>(q_row) * P.os[1] + h * P.os[2];
-#pragma unroll 1
-      for (int c = 0; c < 128; c += 32) {
-        uint32_t r[32];
-        tmem_ld32(tO + c, r);
-        tmem_wait_ld32(r);
-        if (store && q_row < P.S) {
+      uint32_t r[128];
+      tmem_load_row128(tO, r);
+      if (store && q_row < P.S) {
+#pragma unroll
+        for (int c = 0; c < 128; c += 32) {
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            __nv_bfloat162 v2 = __floats2bfloat162_rn(__uint_as_float(r[2 * e]) * scale,
-                                                      __uint_as_float(r[2 * e + 1]) * scale);
+            __nv_bfloat162 v2 = __floats2bfloat162_rn(__uint_as_float(r[c + 2 * e]) * scale,
+                                                      __uint_as_float(r[c + 2 * e + 1]) * scale);
             pk[e] = *reinterpret_cast<uint32_t*>(&v2);
           }
           uint4* dst = reinterpret_cast<uint4*>(orow + c);

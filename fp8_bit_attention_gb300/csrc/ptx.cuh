@@ -71,6 +71,14 @@ __device__ __forceinline__ void tma_prefetch_map(const void* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Pull a tile of a tensor map into L2 ahead of its load (no shared memory,
+// no barrier; coordinates inside the tensor).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const void* map, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* map, uint32_t bar, int32_t x,
                                             int32_t y) {
   asm volatile(
