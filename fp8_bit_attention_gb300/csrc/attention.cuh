@@ -197,10 +197,11 @@ constexpr int kVarSplit = 4;         // split key ranges (nsplit > 1): partial r
 constexpr int kVarVSmooth = 8;       // V-Smooth: block means restored through the block row sums
 constexpr int kVarQBias = 16;        // Q smoothing: the key bias added to the scores by one BF16 MMA
 constexpr int kVarRepair = 32;       // V residual repair: the selected keys' blocks follow each unit's own
+constexpr int kVarDump = 64;         // the probe's P-byte dump (test hook; kept out of the other kernels,
+                                     // whose block loop runs faster without its code)
 // Instantiated: 0-7, 8 (V-Smooth with ExpCast, mid-window, no split), 16-23
 // (Q smoothing with each of 0-7), 32-35 and 48-51 (repair with 0-3 and
-// 16-19: never split, never V-Smooth); indexed by the variant bits.
-constexpr int kNumVariants = 52;
+// 16-19: never split, never V-Smooth), and dump variants of 0-3, 16 and 32.
 
 // Key block visited at step i of a range of n blocks starting at b0 (the
 // whole sequence, or one split range): cyclic from the range's middle block,
@@ -346,19 +347,21 @@ __device__ __forceinline__ void cast_block_cols(const uint32_t* s, const float4*
   }
 }
 
-// Maximum of 128 FP32 values: eight independent 3-input chains, then a tree.
-__device__ __forceinline__ float rowmax128(const uint32_t* s) {
-  float m[8];
-#pragma unroll
-  for (int k = 0; k < 8; ++k) m[k] = fmaxf(__uint_as_float(s[k]), __uint_as_float(s[k + 8]));
-#pragma unroll
-  for (int c = 16; c < 128; c += 16)
-#pragma unroll
-    for (int k = 0; k < 8; ++k) m[k] = fmax3(m[k], __uint_as_float(s[c + k]), __uint_as_float(s[c + 8 + k]));
-  return fmax3(fmax3(m[0], m[1], m[2]), fmax3(m[3], m[4], m[5]), fmaxf(m[6], m[7]));
+// Ragged tail block (keys >= S): this row's columns [valid, 128) of S set
+// to -inf in tensor memory, by a short loop of stores, before the scores are
+// loaded; the max-reducing load then skips them and the byte step gives them
+// code 0.  A rolled loop keeps the hot block loop small (it runs at most once
+// per tile).
+__device__ __forceinline__ void tmem_mask_tail(uint32_t taddr, int valid) {
+  constexpr uint32_t kNegInf = 0xFF800000u;
+  int c = valid;
+#pragma unroll 1
+  for (; c < 128 && (c & 31) != 0; ++c) tmem_st1(taddr + static_cast<uint32_t>(c), kNegInf);
+#pragma unroll 1
+  for (; c < 128; c += 32) tmem_fill32(taddr + static_cast<uint32_t>(c), kNegInf);
+  tmem_wait_st();
 }
 
-// 128 scores and their maximum (four max-reducing loads).
 __device__ __forceinline__ float tmem_load_row128_max(uint32_t taddr, uint32_t* s) {
   float m0, m1, m2, m3;
   tmem_ld32_max(taddr + 0, s, m0);
@@ -795,7 +798,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const float c8sq = P.c8 * sq;
       float kf = -INFINITY;                     // reference m8 = kf + frac(c0+beta)
       float l = 0.0f;
-      const bool dump_tile = (P.dump_codes != nullptr) && tc.bh == P.dump_bh && qb == P.dump_qb && store;
+      const bool dump_tile = (kVar & kVarDump) && tc.bh == P.dump_bh && qb == P.dump_qb && store;
       if (kVar & kVarQBias) {
         // Q smoothing: this row of the tile's A operand, the BF16 pair
         // (hi, lo) of 1/s_q twice, (hi, hi, lo, lo, 0, 0, 0, 0) in every
@@ -845,13 +848,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int valid = P.S - j * 128;
         const float a = c8sq * skj;
         const float as = expcast_scale_a(a);
-        float mx = tmem_load_row128_max(tS, s);
-        if (valid < 128) {       // ragged tail block: mask, then a software max
-#pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (c >= valid) s[c] = 0xFF800000u;  // -inf: excluded from max, code 0
-          mx = rowmax128(s);
-        }
+        if (valid < 128) tmem_mask_tail(tS, valid);
+        const float mx = tmem_load_row128_max(tS, s);
         const float bm8 = mx * a;
         const bool need = bm8 > kf + (kFrac + kLazy);
         if (__any_sync(0xFFFFFFFFu, need)) {
@@ -871,7 +869,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           cast_words(s, a * 0.125f, (64.0f - kFrac - kf) * 0.125f, w);
         else
           expcast_words<0, 32>(s, as, expcast_scale_c(kCodeBase - kf), w);
-        if (dump_tile && j == P.dump_kb) {
+        if ((kVar & kVarDump) && dump_tile && j == P.dump_kb) {
           uint4* d = reinterpret_cast<uint4*>(P.dump_codes + row * 128);
 #pragma unroll
           for (int g = 0; g < 8; ++g) d[g] = make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
@@ -936,13 +934,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           tc_fence_after();
           uint32_t s[128];
           uint32_t w[32];
+          if (!more) tmem_mask_tail(tS, P.n_rep - r * 128);   // only the set's last block has padding
           tmem_load_row128(tS, s);
-          if (!more) {   // only the set's last block holds padding columns
-            const int valid = P.n_rep - r * 128;
-#pragma unroll
-            for (int c = 0; c < 128; ++c)
-              if (c >= valid) s[c] = 0xFF800000u;
-          }
           const float4* ks = reinterpret_cast<const float4*>(rt.ksc[t][rc & 1]);
           if (kVar & kVarExpThenCast)
             cast_block_cols(s, ks, (64.0f - kFrac - kf) * 0.125f, w);

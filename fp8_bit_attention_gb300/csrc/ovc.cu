@@ -27,21 +27,32 @@ __device__ unsigned int g_status;
 
 namespace {
 
-// Every instantiation of the attention kernel, indexed by its variant bits
-// (NULL where no combination exists).
-const decltype(&attention_kernel<0>) kAttentionKernels[kNumVariants] = {
-    attention_kernel<0>, attention_kernel<1>, attention_kernel<2>, attention_kernel<3>,
-    attention_kernel<4>, attention_kernel<5>, attention_kernel<6>, attention_kernel<7>,
-    attention_kernel<kVarVSmooth>, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
-    attention_kernel<16>, attention_kernel<17>, attention_kernel<18>, attention_kernel<19>,
-    attention_kernel<20>, attention_kernel<21>, attention_kernel<22>, attention_kernel<23>,
-    nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
-    attention_kernel<32>, attention_kernel<33>, attention_kernel<34>, attention_kernel<35>,
-    nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
-    attention_kernel<48>, attention_kernel<49>, attention_kernel<50>, attention_kernel<51>};
+// The instantiations of the attention kernel, by variant bits: 0-7, 8
+// (V-Smooth), 16-23 (Q smoothing), 32-35 and 48-51 (repair), and the
+// P-byte dump of the probe call with the method, the baseline variants, Q
+// smoothing and repair (64-67, 80, 96).
+using AttnKernelFn = decltype(&attention_kernel<0>);
+constexpr int kAttnVariantIds[] = {0,  1,  2,  3,  4,  5,  6,  7,  8,  16, 17, 18, 19, 20, 21, 22, 23,
+                                   32, 33, 34, 35, 48, 49, 50, 51, 64, 65, 66, 67, 80, 96};
+
+AttnKernelFn attention_kernel_for(int variant) {
+  switch (variant) {
+#define OVC_K(n) \
+  case n:        \
+    return attention_kernel<n>;
+    OVC_K(0) OVC_K(1) OVC_K(2) OVC_K(3) OVC_K(4) OVC_K(5) OVC_K(6) OVC_K(7) OVC_K(8)
+    OVC_K(16) OVC_K(17) OVC_K(18) OVC_K(19) OVC_K(20) OVC_K(21) OVC_K(22) OVC_K(23)
+    OVC_K(32) OVC_K(33) OVC_K(34) OVC_K(35) OVC_K(48) OVC_K(49) OVC_K(50) OVC_K(51)
+    OVC_K(64) OVC_K(65) OVC_K(66) OVC_K(67) OVC_K(80) OVC_K(96)
+#undef OVC_K
+    default:
+      return nullptr;
+  }
+}
 
 // Dynamic shared memory of each variant's launch.
 size_t attn_smem_bytes(int variant) {
+  variant &= ~kVarDump;
   if (variant == kVarVSmooth) return kAttnSmemBytesVSmooth;
   if (variant & kVarQBias) return kAttnSmemBytesQBias;
   if (variant & kVarRepair) return kAttnSmemBytesRepair;
@@ -76,9 +87,8 @@ ovc_status device_state(DeviceState** out) {
     d.supported = (major == 10 && minor == 3);
     d.sms = sms;
     if (d.supported) {
-      for (int v = 0; v < kNumVariants; ++v)
-        if (kAttentionKernels[v] != nullptr &&
-            cudaFuncSetAttribute(kAttentionKernels[v], cudaFuncAttributeMaxDynamicSharedMemorySize,
+      for (const int v : kAttnVariantIds)
+        if (cudaFuncSetAttribute(attention_kernel_for(v), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(attn_smem_bytes(v))) != cudaSuccess)
           return OVC_ERR_CUDA;
       if (cudaFuncSetAttribute(kmeans_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -409,11 +419,14 @@ ovc_status run_attention(const ovc_prepared* p, const ovc_repair* r, float softm
   const int64_t grid = persistent ? (nunits < dev->sms ? nunits : dev->sms) : nunits;
   static_assert(OVC_ATTN_EXP_THEN_CAST == kVarExpThenCast && OVC_ATTN_NATURAL_ORDER == kVarNaturalOrder,
                 "flag bits select the kernel variant");
-  const int variant = vsmooth ? kVarVSmooth
-                              : static_cast<int>(flags | (ns > 1 ? kVarSplit : 0) | (qbias ? kVarQBias : 0) |
-                                                 (r ? kVarRepair : 0));
+  const int variant = (vsmooth ? kVarVSmooth
+                                 : static_cast<int>(flags | (ns > 1 ? kVarSplit : 0) | (qbias ? kVarQBias : 0) |
+                                                    (r ? kVarRepair : 0))) |
+                      (P.dump_codes != nullptr ? kVarDump : 0);
+  const AttnKernelFn kernel = attention_kernel_for(variant);
+  if (kernel == nullptr) return OVC_ERR_INVALID_ARG;   // a P-byte dump with a variant that has none
   const size_t smem = attn_smem_bytes(variant);
-  kAttentionKernels[variant]<<<static_cast<unsigned>(grid), kAttnThreads, smem, static_cast<cudaStream_t>(stream)>>>(
+  kernel<<<static_cast<unsigned>(grid), kAttnThreads, smem, static_cast<cudaStream_t>(stream)>>>(
       mq, mk, mv, mks, mdv, mvm, mkb, mkbs, P);
   if (ns > 1) {
     const int64_t rows = BH * p->S;
