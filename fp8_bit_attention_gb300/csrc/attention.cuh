@@ -419,9 +419,9 @@ __device__ __forceinline__ void flush_row_sums(float* lb, uint32_t taddr) {
 // all four 32-column loads in flight at once (one TMEM round trip), then the
 // products stored back; else one chunk at a time.  The two give the same
 // values; which is faster depends on the variant's schedule (S = 73397,
-// H = 56: the method's kernel 67.6 batched against 68.7 ms; the V-Smooth
-// kernel 82.0 chunked against 84.8; the repair and Q-smoothing kernels no
-// faster batched).
+// H = 56: the method's kernel 67.6 batched against 68.7 ms, the Q-smoothing
+// kernel 67.8 against 69.6; the V-Smooth kernel 82.0 chunked against 84.8;
+// the repair kernels 18% slower batched).
 template <bool kBatched>
 __device__ __forceinline__ void tmem_scale_row128(uint32_t taddr, float f) {
   if constexpr (kBatched) {
@@ -894,7 +894,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         // O is stable here (every earlier MMA of this tile has completed) and
         // the next P.V waits for this thread's arrival below.
-        if (rescale) tmem_scale_row128<(kVar & (kVarRepair | kVarVSmooth | kVarQBias)) == 0>(tO, f);
+        if (rescale) tmem_scale_row128<(kVar & (kVarRepair | kVarVSmooth)) == 0>(tO, f);
         tmem_wait_st();
         tc_fence_before();
         // Every thread arrives once its own P stores are done (128 arrivals).
