@@ -256,15 +256,29 @@ __device__ __forceinline__ float expcast_scale_c(float c) {   // c = c0 + beta -
   return c * (1.0f / 256.0f);
 }
 
+// Two codes: each score's saturating FMA, then the rounding FMA of both at
+// once on a packed FP32 pair (two independently rounded FMAs, the same bits
+// as two scalar ones, in one instruction).
+__device__ __forceinline__ void expcast_code2(uint32_t s0, uint32_t s1, float as, float cs, uint32_t& u0,
+                                              uint32_t& u1) {
+  constexpr uint64_t k256x2 = 0x4380000043800000ull;     // (256, 256)
+  constexpr uint64_t kMagicx2 = 0x4B4000004B400000ull;   // (1.5 * 2^23, 1.5 * 2^23)
+  const float t0 = fma_sat(__uint_as_float(s0), as, cs);
+  const float t1 = fma_sat(__uint_as_float(s1), as, cs);
+  uint64_t t, r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(t) : "f"(t0), "f"(t1));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(t), "l"(k256x2), "l"(kMagicx2));
+  asm("mov.b64 {%0, %1}, %2;" : "=r"(u0), "=r"(u1) : "l"(r));
+}
+
 // Codes of the scores s[4 G0 .. 4 (G0 + NG)) into the words w[G0 .. G0 + NG).
 template <int G0, int NG>
 __device__ __forceinline__ void expcast_words(const uint32_t* s, float as, float cs, uint32_t* w) {
 #pragma unroll
   for (int g = G0; g < G0 + NG; ++g) {
-    const uint32_t u0 = expcast_code(s[4 * g + 0], as, cs);
-    const uint32_t u1 = expcast_code(s[4 * g + 1], as, cs);
-    const uint32_t u2 = expcast_code(s[4 * g + 2], as, cs);
-    const uint32_t u3 = expcast_code(s[4 * g + 3], as, cs);
+    uint32_t u0, u1, u2, u3;
+    expcast_code2(s[4 * g + 0], s[4 * g + 1], as, cs, u0, u1);
+    expcast_code2(s[4 * g + 2], s[4 * g + 3], as, cs, u2, u3);
     w[g] = __byte_perm(__byte_perm(u0, u1, 0x0040), __byte_perm(u2, u3, 0x0040), 0x5410);
   }
 }
