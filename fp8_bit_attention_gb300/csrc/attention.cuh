@@ -66,7 +66,6 @@ constexpr uint32_t kIdesc = idesc_e4m3_f32(128, 128);
 constexpr uint32_t kIdescBf16 = idesc_bf16_f32(128, 128);
 constexpr uint32_t kMeanTile = 128 * 16 * 2;               // bytes of one M' tile: 128 channels x 16 blocks BF16
 constexpr uint32_t kBiasTile = 128 * 16 * 2;               // bytes of one Q-smoothing operand tile: 128 rows x 16 BF16
-constexpr float kMagic = 12582912.0f;                       // 1.5 * 2^23
 // ExpCast constants: c0 = 120 (stored value 2^8 p), beta = -0.35, tau = 0.75.
 constexpr float kCodeBase = 119.0f;                         // floor(c0 + beta)
 constexpr float kFrac = 0.65f;                              // frac(c0 + beta)
@@ -242,29 +241,26 @@ __device__ __forceinline__ UnitCoord unit_coord(const AttnParams& P, int u) {
 // It produces 32 packed words of codes (bytes in key order); codes_sum adds
 // up their decoded values for the row sum.
 // ---------------------------------------------------------------------------
-// One ExpCast code in the low byte of the result.  The inputs are scaled by
-// 1/256 (as = a/256, cs = (c0+beta-m8)/256): a saturating FMA clamps the code
-// at 0, and a second FMA by 256 adding 1.5*2^23 rounds it to the integer in
-// the low mantissa bits (the code's upper end, 126, is kept by the lazy
-// rescale threshold).
-__device__ __forceinline__ uint32_t expcast_code(uint32_t s, float as, float cs) {
-  return __float_as_uint(fmaf(fma_sat(__uint_as_float(s), as, cs), 256.0f, kMagic));
-}
-
 __device__ __forceinline__ float expcast_scale_a(float a) { return a * (1.0f / 256.0f); }
 __device__ __forceinline__ float expcast_scale_c(float c) {   // c = c0 + beta - m8 (an integer)
   return c * (1.0f / 256.0f);
 }
 
-// Two codes: each score's saturating FMA, then the rounding FMA of both at
-// once on a packed FP32 pair (two independently rounded FMAs, the same bits
-// as two scalar ones, in one instruction).
-__device__ __forceinline__ void expcast_code2(uint32_t s0, uint32_t s1, float as, float cs, uint32_t& u0,
-                                              uint32_t& u1) {
+// Two ExpCast codes, each in the low byte of its result.  The inputs are
+// scaled by 1/256 (as = a/256, cs = (c0+beta-m8)/256): a saturating FMA per
+// score clamps the code at 0, and an FMA by 256 adding 1.5*2^23 rounds it to
+// the integer in the low mantissa bits (the code's upper end, 126, is kept
+// by the lazy rescale threshold).  The rounding FMA of the two runs as one
+// packed FP32-pair FMA: two independently rounded results, the same bits as
+// two scalar FMAs, in one instruction (the saturating FMA has no packed
+// form).  as0, as1: the two scores' multipliers, equal except in the repair
+// blocks.
+__device__ __forceinline__ void expcast_code2(uint32_t s0, uint32_t s1, float as0, float as1, float cs,
+                                              uint32_t& u0, uint32_t& u1) {
   constexpr uint64_t k256x2 = 0x4380000043800000ull;     // (256, 256)
   constexpr uint64_t kMagicx2 = 0x4B4000004B400000ull;   // (1.5 * 2^23, 1.5 * 2^23)
-  const float t0 = fma_sat(__uint_as_float(s0), as, cs);
-  const float t1 = fma_sat(__uint_as_float(s1), as, cs);
+  const float t0 = fma_sat(__uint_as_float(s0), as0, cs);
+  const float t1 = fma_sat(__uint_as_float(s1), as1, cs);
   uint64_t t, r;
   asm("mov.b64 %0, {%1, %2};" : "=l"(t) : "f"(t0), "f"(t1));
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(t), "l"(k256x2), "l"(kMagicx2));
@@ -277,8 +273,8 @@ __device__ __forceinline__ void expcast_words(const uint32_t* s, float as, float
 #pragma unroll
   for (int g = G0; g < G0 + NG; ++g) {
     uint32_t u0, u1, u2, u3;
-    expcast_code2(s[4 * g + 0], s[4 * g + 1], as, cs, u0, u1);
-    expcast_code2(s[4 * g + 2], s[4 * g + 3], as, cs, u2, u3);
+    expcast_code2(s[4 * g + 0], s[4 * g + 1], as, as, cs, u0, u1);
+    expcast_code2(s[4 * g + 2], s[4 * g + 3], as, as, cs, u2, u3);
     w[g] = __byte_perm(__byte_perm(u0, u1, 0x0040), __byte_perm(u2, u3, 0x0040), 0x5410);
   }
 }
@@ -308,10 +304,9 @@ __device__ __forceinline__ void expcast_block_cols(const uint32_t* s, const floa
 #pragma unroll
   for (int g = 0; g < 32; ++g) {
     const float4 a4 = as4[g];
-    const uint32_t u0 = expcast_code(s[4 * g + 0], a4.x, cs);
-    const uint32_t u1 = expcast_code(s[4 * g + 1], a4.y, cs);
-    const uint32_t u2 = expcast_code(s[4 * g + 2], a4.z, cs);
-    const uint32_t u3 = expcast_code(s[4 * g + 3], a4.w, cs);
+    uint32_t u0, u1, u2, u3;
+    expcast_code2(s[4 * g + 0], s[4 * g + 1], a4.x, a4.y, cs, u0, u1);
+    expcast_code2(s[4 * g + 2], s[4 * g + 3], a4.z, a4.w, cs, u2, u3);
     w[g] = __byte_perm(__byte_perm(u0, u1, 0x0040), __byte_perm(u2, u3, 0x0040), 0x5410);
   }
 }
