@@ -539,5 +539,5 @@ def flops(B: int, S: int, H: int, D: int = 128) -> float:
 
 __all__ = ["Prepared", "Repair", "OvcError", "CapturedAttention", "prepare", "attention_prepared", "attention_workspace_bytes",
            "group_v", "prepare_v_repair",
-           "attention_v_repair", "attention_probe", "device_status", "attention", "memcpy2d",
+           "attention_v_repair", "attention_probe", "device_status", "attention",
            "head_chunks", "prepare_workspace_bytes", "repair_workspace_bytes", "flops"]
