@@ -305,7 +305,9 @@ def run_reference(a):
         return
     w = W.WORKLOADS[a.workload]
     q, k, v = W.generate(w)
-    rows = 64
+    # The main arm's cpu_baseline sample: the head's quantisation (about
+    # 1.5 s on 16 cores) stays a minor part of each step.
+    rows = 2048
     for _ in range(a.warmup):
         cpu_baseline(w, q, k, v, rows=rows)
     vals, times = [], []
