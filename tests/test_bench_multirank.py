@@ -85,3 +85,24 @@ def test_gpus_flag_must_match_world_size():
     assert "WORLD_SIZE=3" in err
     rc, lines, _ = _bench(["--dry-run"])
     assert rc == 0 and lines[0]["n_gpus"] == 1
+
+
+def test_reference_arm_prints_its_line():
+    """--impl reference times the CPU oracle on a bounded sample and prints
+    one JSON line with the main arm's metric, its own cpu_baseline and an
+    e2e entry with no host<->device bytes."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--workload", "small",
+                        "--steps", "1", "--warmup", "0"], capture_output=True, text=True, timeout=600, env=env,
+                       cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC
+    assert line["value"] > 0 and line["unit"] == "TFLOP/s" and line["higher_is_better"] is True
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    assert line["config"]["workload"] == "small"
