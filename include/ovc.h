@@ -227,7 +227,10 @@ const char* ovc_status_string(ovc_status s);
  * schedule, -1 = one CTA per tile, 0 = automatic.  trace, if not NULL and
  * the library was built with -DOVC_TRACE=1, receives per-role SM clock
  * stamps of the first 64 blocks of CTA 0 (pipeline analysis; ignored
- * otherwise).  r may be NULL. */
+ * otherwise).  r may be NULL.  The dump runs in separate kernel builds
+ * (the production kernels carry no dump code): it is available with the
+ * method's kernel, the OVC_ATTN_* variants, Q smoothing and repair; asked
+ * for with V-Smooth, the call returns OVC_ERR_INVALID_ARG. */
 typedef struct {
   int64_t dump_bh, dump_qblock, dump_kblock;
   uint8_t* dump_codes;
