@@ -229,8 +229,10 @@ const char* ovc_status_string(ovc_status s);
  * stamps of the first 64 blocks of CTA 0 (pipeline analysis; ignored
  * otherwise).  r may be NULL.  The dump runs in separate kernel builds
  * (the production kernels carry no dump code): it is available with the
- * method's kernel, the OVC_ATTN_* variants, Q smoothing and repair; asked
- * for with V-Smooth, the call returns OVC_ERR_INVALID_ARG. */
+ * method's kernel and its OVC_ATTN_* variants, and with Q smoothing or a
+ * repair set on the method's kernel.  Other combinations (V-Smooth; Q
+ * smoothing or repair together with OVC_ATTN_* flags or with each other)
+ * return OVC_ERR_INVALID_ARG. */
 typedef struct {
   int64_t dump_bh, dump_qblock, dump_kblock;
   uint8_t* dump_codes;
