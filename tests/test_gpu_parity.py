@@ -521,7 +521,23 @@ def test_v_smooth_persistent_schedule_and_rejections():
         ovc.attention_prepared(prep, nsplit=2)
     with pytest.raises(ovc.OvcError):
         ovc.attention_prepared(prep, flags=1)
+    with pytest.raises(ovc.OvcError):          # no P-byte dump build of the V-Smooth kernel
+        ovc.attention_probe(prep, dump=(0, 1, 2))
     assert ovc.device_status() == 0
+
+
+def test_p_byte_dump_builds_give_the_production_output():
+    """The probe's P-byte dump runs in separate kernel builds; with the dump
+    on, the output must still be the production kernel's, within the
+    tolerance (the same arithmetic, compiled separately)."""
+    q, k, v = inputs(1, 2, 1000, seed=3100)
+    qd, kd, vd = to_dev(q, k, v)
+    prep = ovc.prepare(qd, kd, vd)
+    o = ovc.attention_prepared(prep).float()
+    od, codes, m8 = ovc.attention_probe(prep, dump=(1, 3, 5))
+    assert ovc.device_status() == 0
+    assert rel_l2(od.float().cpu().numpy(), o.cpu().numpy()) <= 1e-3
+    assert int(codes.max()) <= 126 and bool(torch.isfinite(m8).all())
 
 
 # ---- V-Smooth grouping --------------------------------------------------------
